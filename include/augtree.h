@@ -1,0 +1,217 @@
+/*
+ * augtree.h - C ABI of exact, differentiable shared-prompt tree attention on one GPU.
+ *
+ * Method: AugTree, "Splitting Prompt Prefill from Response Replay for
+ * Context-Parallel Long-Context LLM Post-Training".
+ *   - Sec. 2.1 / 3.1: a replay tree T = (P, {R_i}, i = 1..G): one shared prompt and
+ *     G sibling response branches.  A batch holds several trees ("groups").
+ *   - Sec. 2.2: attention O = softmax(Q K^T / sqrt(D_h) + M) V, tiled over Q and KV
+ *     blocks with an online softmax state.
+ *   - Sec. 3.2, Eq. 1: a response token t of branch i sees all prompt keys and the
+ *     keys of its own branch up to and including itself; never a sibling's keys.
+ *     Prompt tokens see earlier prompt tokens (causal prefill) and no response keys.
+ *   - Sec. 3.2, Eq. 2: the prompt K/V gradient is the sum over all G branches,
+ *     accumulated and then propagated through the prompt-prefill graph.
+ *   - Sec. 3.3: partial online-softmax states merge associatively.
+ *   - Sec. 3.4: replay units with work weights, balanced largest-first.
+ *
+ * Data layout ("THD", row-major, contiguous, all tensors on the current device):
+ *   prompt  Q, O, dQ, dO : [total_prompt, Hq,  D]     prompt  K, V, dK, dV : [total_prompt, Hkv, D]
+ *   response Q, O, dQ, dO: [total_resp,   Hq,  D]     response K, V, dK, dV: [total_resp,   Hkv, D]
+ *   lse (log-sum-exp of the scaled scores, natural log, fp32): [Hq, tokens]
+ * Groups are contiguous in the prompt arrays and in the response arrays; the
+ * branches of one group are contiguous in the response arrays.  Query head h uses
+ * KV head floor(h / (Hq / Hkv)).  Element type: all of Q, K, V, O, dO, dQ, dK, dV
+ * have the plan's dtype (fp32 or bf16); lse, the prompt-gradient sums and every
+ * workspace are fp32.  Computation is fp32 accumulation in both modes.
+ *
+ * Ownership: the caller owns every tensor and every workspace.  A plan owns only its
+ * device copies of the descriptors and work queues (allocated by augtree_plan_create,
+ * freed by augtree_plan_destroy).  The compute calls allocate nothing.
+ *
+ * Execution: compute calls are asynchronous on the given stream (0 = legacy default
+ * stream) of the plan's device.  They validate arguments on the host and return an
+ * error code; no exception, abort or device trap is ever raised.  A CUDA launch
+ * failure is reported as AUGTREE_ERR_CUDA.
+ */
+#ifndef AUGTREE_H
+#define AUGTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  AUGTREE_OK = 0,
+  AUGTREE_ERR_INVALID_ARG = 1,          /* null pointer, bad offsets, bad sizes            */
+  AUGTREE_ERR_UNSUPPORTED = 2,          /* dtype, head_dim not in {64,128}, Hq % Hkv != 0 */
+  AUGTREE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below augtree_plan_workspace_bytes    */
+  AUGTREE_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed           */
+  AUGTREE_ERR_DEVICE_CHECK = 5,         /* a kernel reported a failed internal check      */
+  AUGTREE_ERR_TIMEOUT = 6,              /* a bounded device-side wait gave up             */
+  AUGTREE_ERR_CAPACITY = 7              /* an output buffer is too small (schedule export)*/
+} augtree_status;
+
+typedef enum { AUGTREE_FP32 = 0, AUGTREE_BF16 = 1 } augtree_dtype;
+
+/* Kernel family: SIMT fp32-FMA kernels (any dtype; the only family for fp32) or the
+ * tcgen05 tensor-core kernels (bf16 only).  AUTO picks tensor cores for bf16. */
+typedef enum { AUGTREE_KERNEL_AUTO = 0, AUGTREE_KERNEL_SIMT = 1, AUGTREE_KERNEL_TC = 2 } augtree_kernel;
+
+/* Operations, used to select a work queue or a workspace size. */
+typedef enum {
+  AUGTREE_OP_PREFILL_FWD = 0,
+  AUGTREE_OP_REPLAY_FWD = 1,
+  AUGTREE_OP_REPLAY_BWD = 2,
+  AUGTREE_OP_PREFILL_BWD = 3
+} augtree_op;
+
+/* Ragged group / branch descriptors (host memory, read during plan creation only).
+ *   prompt_off  [n_groups+1]   prompt token offsets; group g owns prompt rows
+ *                              [prompt_off[g], prompt_off[g+1]); prompt_off[0] = 0.
+ *   branch_begin[n_groups+1]   group g owns branches [branch_begin[g], branch_begin[g+1]);
+ *                              branch_begin[0] = 0, branch_begin[n_groups] = n_branches.
+ *   resp_off    [n_branches+1] response token offsets; branch b owns response rows
+ *                              [resp_off[b], resp_off[b+1]); resp_off[0] = 0.
+ * All three must be non-decreasing.  Empty prompts, empty branches and groups
+ * without branches are allowed. */
+typedef struct {
+  const int32_t* prompt_off;
+  const int32_t* branch_begin;
+  const int32_t* resp_off;
+  int32_t n_groups;
+  int32_t n_branches;
+} augtree_desc;
+
+typedef struct {
+  int32_t hq;            /* query heads                                         */
+  int32_t hkv;           /* key/value heads; hq % hkv == 0 (MHA, GQA, MQA)       */
+  int32_t head_dim;      /* 64 or 128                                           */
+  int32_t dtype;         /* augtree_dtype                                       */
+  float softmax_scale;   /* 0 => 1/sqrt(head_dim) (Sec. 2.2)                    */
+  int32_t num_sms;       /* balancing width of the work queues; 0 => device SMs */
+  int32_t kernel;        /* augtree_kernel                                      */
+  int32_t reserved;      /* must be 0                                           */
+} augtree_config;
+
+typedef struct augtree_plan augtree_plan;
+
+/* ---- Work queues ------------------------------------------------------------------
+ * Every compute call walks a queue of work items, AUGTREE_ITEM_WORDS int32 each:
+ *   [0] kind   [1] group   [2] tile   [3] head   [4] split   [5] cost   [6] a   [7] b
+ * Tile sizes: BM query rows per query tile, BN keys per KV tile (augtree_tile_sizes).
+ * Let, for group g, L_P its prompt length, p0 its first prompt row, L_R the total
+ * length of its branches, r0 their first response row, r = Hq/Hkv.
+ *
+ *  kind 0 PREFILL_Q (prefill_fwd): query tile `tile` of the prompt, rows
+ *    [p0 + tile*BM, min(p0 + (tile+1)*BM, p0 + L_P)), query head `head`.
+ *    a = number of prompt KV tiles = ceil((row_end - p0) / BN), b = 0, cost = a.
+ *  kind 1 REPLAY_Q (replay_fwd): query tile `tile` of the group's concatenated
+ *    branches, rows [r0 + tile*BM, min(r0 + (tile+1)*BM, r0 + L_R)) (a tile may span
+ *    branches), query head `head`.  a = ceil(L_P / BN) prompt KV tiles (dense);
+ *    b = ceil((row_end - branch_start(first row)) / BN) own KV tiles starting at the
+ *    first row's branch start; cost = a + b.
+ *  kind 2 PROMPT_KV (replay_bwd): prompt KV tile `tile` (keys [p0 + tile*BN, ...)),
+ *    KV head `head`, split `split`: response query tiles [a, b) of the group, each
+ *    for the r query heads of the KV head.  cost = (b - a) * r.
+ *  kind 3 RESP_KV (replay_bwd): response KV tile `tile` (keys [r0 + tile*BN, ...)),
+ *    KV head `head`: response query tiles [a, b) where a = floor(tile*BN/BM) and b
+ *    covers the end of the branch holding the tile's last key.  cost = (b - a) * r.
+ *  kind 4 PREFILL_KV (prefill_bwd): prompt KV tile `tile`, KV head `head`: prompt
+ *    query tiles [a, b) = [floor(tile*BN/BM), ceil(L_P/BM)).  cost = (b - a) * r.
+ *
+ * Split rule (replay_bwd, atomic-free split-K of the prompt dK/dV, Eq. 2): let
+ * U = sum of the costs of all replay_bwd items before splitting, T = max(r,
+ * ceil(U / (2 * num_sms))), nq = ceil(L_R / BM).  A group with L_P > 0 and L_R > 0
+ * gets s = min(64, max(1, ceil(nq*r / T))) splits of C = ceil(nq / s) query tiles
+ * (then s = ceil(nq / C)); split k covers query tiles [k*C, min((k+1)*C, nq)).
+ *
+ * Order: items are sorted by cost descending, then by (group, tile, kind, split,
+ * head) ascending - the largest-first greedy balancing of replay units (Sec. 3.4);
+ * thread blocks take items in this order.
+ */
+#define AUGTREE_ITEM_WORDS 8
+
+/* Tile sizes BM (query rows) and BN (keys) the plan's kernels use for an op. */
+augtree_status augtree_tile_sizes(const augtree_config* cfg, int32_t op, int32_t* bm, int32_t* bn);
+
+/* Host-only schedule build, no GPU needed: writes the work queue of `op` for the
+ * given descriptors and config (cfg->num_sms must be > 0) into out[cap_items *
+ * AUGTREE_ITEM_WORDS]; *n_items receives the item count.  Returns
+ * AUGTREE_ERR_CAPACITY (with *n_items set) when cap_items is too small. */
+augtree_status augtree_schedule_build(const augtree_desc* desc, const augtree_config* cfg,
+                                      int32_t op, int32_t* out, size_t cap_items,
+                                      size_t* n_items);
+
+/* ---- Plans ------------------------------------------------------------------------ */
+
+/* Validates the descriptors and config, builds all four work queues on the host and
+ * copies them with the descriptors to the current device (synchronously).
+ * *out receives the plan; free it with augtree_plan_destroy. */
+augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_config* cfg,
+                                   augtree_plan** out);
+augtree_status augtree_plan_destroy(augtree_plan* plan);
+
+/* Workspace bytes each compute call needs (0 allowed: pass ws = NULL). */
+augtree_status augtree_plan_workspace_bytes(const augtree_plan* plan, int32_t op, size_t* bytes);
+
+/* Copy of the plan's work queue for `op` to host memory (for bit-exact checks). */
+augtree_status augtree_schedule_export(const augtree_plan* plan, int32_t op, int32_t* host_out,
+                                       size_t cap_items, size_t* n_items);
+
+/* ---- Compute (device pointers; stream = cudaStream_t) ----------------------------- */
+
+/* Prompt prefill (Sec. 3.2): causal self-attention of every group's prompt.
+ * In: qp [P,Hq,D], kp/vp [P,Hkv,D].  Out: op [P,Hq,D], lse_p [Hq,P]. */
+augtree_status augtree_prefill_fwd(const augtree_plan* plan, const void* qp, const void* kp,
+                                   const void* vp, void* op, float* lse_p, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* Response replay (Sec. 3.2-3.3, Eq. 1): each response row attends to all prompt keys
+ * of its group (dense) and to its own branch's keys up to itself (causal); the two
+ * partial states are merged in one online softmax.
+ * In: qr [R,Hq,D], kp/vp [P,Hkv,D], kr/vr [R,Hkv,D].  Out: or_ [R,Hq,D], lse_r [Hq,R]. */
+augtree_status augtree_replay_fwd(const augtree_plan* plan, const void* qr, const void* kp,
+                                  const void* vp, const void* kr, const void* vr, void* or_,
+                                  float* lse_r, void* ws, size_t ws_bytes, void* stream);
+
+/* Replay backward.  In: forward inputs, or_, lse_r, dor [R,Hq,D].
+ * Out: dqr [R,Hq,D], dkr/dvr [R,Hkv,D] (plan dtype), and the fp32 prompt-gradient sums
+ * over all branches dkp_sum/dvp_sum [P,Hkv,D] (Eq. 2; overwritten, not accumulated).
+ * Split-K partials of the prompt sums are reduced in a fixed order (no atomics). */
+augtree_status augtree_replay_bwd(const augtree_plan* plan, const void* qr, const void* kp,
+                                  const void* vp, const void* kr, const void* vr,
+                                  const void* or_, const float* lse_r, const void* dor,
+                                  void* dqr, void* dkr, void* dvr, float* dkp_sum,
+                                  float* dvp_sum, void* ws, size_t ws_bytes, void* stream);
+
+/* Prefill backward: causal backward of the prompt with dop [P,Hq,D], plus the replay
+ * sums: dkp = dK_prefill + dkp_acc, dvp = dV_prefill + dvp_acc (dkp_acc / dvp_acc
+ * nullable => 0).  Out: dqp [P,Hq,D], dkp/dvp [P,Hkv,D] in the plan dtype. */
+augtree_status augtree_prefill_bwd(const augtree_plan* plan, const void* qp, const void* kp,
+                                   const void* vp, const void* op, const float* lse_p,
+                                   const void* dop, const float* dkp_acc, const float* dvp_acc,
+                                   void* dqp, void* dkp, void* dvp, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* State merge (+) of Sec. 3.3 in (O, lse) form, fp32:
+ *   lse = log(exp(lse_a) + exp(lse_b)),  o = exp(lse_a - lse) oa + exp(lse_b - lse) ob.
+ * oa/ob/o [rows, h, d], lse_a/lse_b/lse [h, rows].  (0, -inf) is the identity; two
+ * -inf inputs give o = 0, lse = -inf.  o may alias oa or ob; lse may alias lse_a or
+ * lse_b. */
+augtree_status augtree_lse_merge(int64_t rows, int32_t h, int32_t d, const float* oa,
+                                 const float* lse_a, const float* ob, const float* lse_b,
+                                 float* o, float* lse, void* stream);
+
+const char* augtree_status_string(augtree_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t augtree_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AUGTREE_H */

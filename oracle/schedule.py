@@ -1,0 +1,128 @@
+"""Reference builder of the tile work queues (bit-exact target of the library's).
+
+TEST INFRASTRUCTURE ONLY: imported by tests, never by the library.
+
+AugTree paper, Sec. 3.4: the response paths of a tree become bounded replay units,
+each with a work estimate from its query length and its valid Q-KV tile count, and
+units are assigned to lanes so that the most loaded lane is as light as possible
+("largest-first greedy balancing" when the exact subset DP is not used).  On one GPU
+a lane is a thread block: a unit is a (query tile, head) item in the forward and a
+(KV tile, KV head, split) item in the backward, its weight is its number of valid
+tile interactions, and blocks take items in order of decreasing weight.
+
+The item encoding, split rule and tie-break order are the library contract written
+out below in plain Python loops; the comparison with the library is bit for bit.
+"""
+from __future__ import annotations
+
+from typing import List, Tuple
+
+import numpy as np
+
+PREFILL_Q, REPLAY_Q, PROMPT_KV, RESP_KV, PREFILL_KV = 0, 1, 2, 3, 4
+OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD = 0, 1, 2, 3
+MAX_SPLIT = 64
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def _groups(offsets):
+    prompt_off, branch_begin, resp_off = [list(map(int, x)) for x in offsets]
+    out = []
+    for g in range(len(prompt_off) - 1):
+        p0, p1 = prompt_off[g], prompt_off[g + 1]
+        b0, b1 = branch_begin[g], branch_begin[g + 1]
+        starts = [resp_off[b] for b in range(b0, b1)]
+        ends = [resp_off[b + 1] for b in range(b0, b1)]
+        r0, r1 = resp_off[b0], resp_off[b1]
+        out.append(dict(p0=p0, lp=p1 - p0, r0=r0, lr=r1 - r0, starts=starts, ends=ends))
+    return out
+
+
+def _branch_of(grp, row: int) -> int:
+    """Index (within the group) of the branch holding global response row `row`;
+    empty branches are skipped."""
+    for i, (s, e) in enumerate(zip(grp["starts"], grp["ends"])):
+        if s <= row < e:
+            return i
+    raise ValueError("row outside the group's branches")
+
+
+def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -> np.ndarray:
+    """Work queue of `op` as an int32 array [n_items, 8]:
+    kind, group, tile, head, split, cost, a, b."""
+    r = hq // hkv
+    groups = _groups(offsets)
+    items: List[Tuple[int, ...]] = []
+    if op == OP_PREFILL_FWD:
+        for g, grp in enumerate(groups):
+            for t in range(_cdiv(grp["lp"], bm)):
+                row_end = min(grp["p0"] + (t + 1) * bm, grp["p0"] + grp["lp"])
+                a = _cdiv(row_end - grp["p0"], bn)
+                for h in range(hq):
+                    items.append((PREFILL_Q, g, t, h, 0, a, a, 0))
+    elif op == OP_REPLAY_FWD:
+        for g, grp in enumerate(groups):
+            a = _cdiv(grp["lp"], bn)
+            for t in range(_cdiv(grp["lr"], bm)):
+                row_begin = grp["r0"] + t * bm
+                row_end = min(row_begin + bm, grp["r0"] + grp["lr"])
+                bstart = grp["starts"][_branch_of(grp, row_begin)]
+                b = _cdiv(row_end - bstart, bn)
+                for h in range(hq):
+                    items.append((REPLAY_Q, g, t, h, 0, a + b, a, b))
+    elif op == OP_REPLAY_BWD:
+        # Unsplit costs first, to fix the split target.
+        total = 0
+        resp_items = []
+        for g, grp in enumerate(groups):
+            nq = _cdiv(grp["lr"], bm)
+            nkp = _cdiv(grp["lp"], bn) if nq > 0 else 0
+            total += nkp * nq * r * hkv
+            for j in range(_cdiv(grp["lr"], bn)):
+                k_lo = grp["r0"] + j * bn
+                k_hi = min(k_lo + bn, grp["r0"] + grp["lr"])
+                e = grp["ends"][_branch_of(grp, k_hi - 1)]
+                qa = (k_lo - grp["r0"]) // bm
+                qb = _cdiv(e - grp["r0"], bm)
+                resp_items.append((g, j, qa, qb))
+                total += (qb - qa) * r * hkv
+        target = max(r, _cdiv(total, 2 * num_sms))
+        for g, grp in enumerate(groups):
+            nq = _cdiv(grp["lr"], bm)
+            if grp["lp"] == 0 or nq == 0:
+                continue
+            s = min(MAX_SPLIT, max(1, _cdiv(nq * r, target)))
+            c = _cdiv(nq, s)
+            s = _cdiv(nq, c)
+            for j in range(_cdiv(grp["lp"], bn)):
+                for k in range(s):
+                    qa, qb = k * c, min((k + 1) * c, nq)
+                    for h in range(hkv):
+                        items.append((PROMPT_KV, g, j, h, k, (qb - qa) * r, qa, qb))
+        for (g, j, qa, qb) in resp_items:
+            for h in range(hkv):
+                items.append((RESP_KV, g, j, h, 0, (qb - qa) * r, qa, qb))
+    elif op == OP_PREFILL_BWD:
+        for g, grp in enumerate(groups):
+            nq = _cdiv(grp["lp"], bm)
+            for j in range(_cdiv(grp["lp"], bn)):
+                qa = (j * bn) // bm
+                for h in range(hkv):
+                    items.append((PREFILL_KV, g, j, h, 0, (nq - qa) * r, qa, nq))
+    else:
+        raise ValueError(op)
+    # Largest first; ties by (group, tile, kind, split, head).
+    items.sort(key=lambda it: (-it[5], it[1], it[2], it[0], it[4], it[3]))
+    return np.array(items, dtype=np.int32).reshape(-1, 8)
+
+
+def splits_per_group(queue: np.ndarray, n_groups: int) -> List[int]:
+    """Number of prompt-KV splits of each group in a replay_bwd queue."""
+    s = [1] * n_groups
+    for it in queue:
+        if it[0] == PROMPT_KV:
+            s[it[1]] = max(s[it[1]], int(it[4]) + 1)
+    return s

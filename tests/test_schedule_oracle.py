@@ -1,0 +1,176 @@
+"""Pins of the reference work-queue builder (CPU only).
+
+The queues are the on-chip form of the paper's replay units and largest-first greedy
+balancing (AugTree, Sec. 3.4): every valid Q-KV tile interaction implied by Eq. 1
+(Sec. 3.2) must be evaluated exactly once, no item may carry an empty tile, and items
+come in order of decreasing weight.  These properties are checked here by brute force
+over the (query row, key) pairs of small ragged trees, independently of the
+builder's own loops.
+"""
+import numpy as np
+import pytest
+
+from oracle import schedule as S
+import workloads as W
+
+
+def valid_pairs(tree):
+    """Brute force: per group, the sets of valid (query, key) pairs, in global row
+    indices, split by (query side, key side): pp (prompt->prompt), rp (response ->
+    prompt), rr (response -> response)."""
+    out = []
+    p_base = r_base = 0
+    for lp, bl in zip(tree.prompt_lens, tree.branch_lens):
+        pp = {(p_base + i, p_base + j) for i in range(lp) for j in range(i + 1)}
+        rp, rr = set(), set()
+        rb = r_base
+        for li in bl:
+            for t in range(li):
+                rp |= {(rb + t, p_base + j) for j in range(lp)}
+                rr |= {(rb + t, rb + j) for j in range(t + 1)}
+            rb += li
+        out.append(dict(pp=pp, rp=rp, rr=rr, p0=p_base, lp=lp, r0=r_base, lr=sum(bl)))
+        p_base += lp
+        r_base += sum(bl)
+    return out
+
+
+def check_order(q):
+    keys = [(-int(it[5]), int(it[1]), int(it[2]), int(it[0]), int(it[4]), int(it[3])) for it in q]
+    assert keys == sorted(keys)
+
+
+TREES = [
+    W.Tree([5], [[3, 4]]),
+    W.Tree([70, 33], [[1, 60, 25], [40]]),
+    W.Tree([0, 41], [[30, 20], [0, 57]]),
+    W.Tree([64, 2, 30], [[], [31], [1, 1, 1, 17]]),
+    W.Tree([130], [[9] * 7 + [65]]),
+]
+TILES = [(4, 4), (8, 4), (4, 8), (16, 16), (8, 16)]
+
+
+@pytest.mark.parametrize("ti", range(len(TREES)))
+@pytest.mark.parametrize("bm,bn", TILES)
+@pytest.mark.parametrize("hq,hkv", [(4, 2), (2, 2)])
+def test_forward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv):
+    tree = TREES[ti]
+    groups = valid_pairs(tree)
+    offs = tree.offsets()
+    for op, kind, side in ((S.OP_PREFILL_FWD, S.PREFILL_Q, "pp"), (S.OP_REPLAY_FWD, S.REPLAY_Q, None)):
+        q = S.build(offs, hq, hkv, op, bm, bn, num_sms=3)
+        check_order(q)
+        covered = {}
+        for it in q:
+            k, g, tile, h, split, cost, a, b = map(int, it)
+            assert k == kind and split == 0
+            grp = groups[g]
+            if op == S.OP_PREFILL_FWD:
+                rows = range(grp["p0"] + tile * bm, min(grp["p0"] + (tile + 1) * bm, grp["p0"] + grp["lp"]))
+                tiles = [("p", grp["p0"] + j * bn) for j in range(a)]
+                assert b == 0 and cost == a
+            else:
+                rows = range(grp["r0"] + tile * bm, min(grp["r0"] + (tile + 1) * bm, grp["r0"] + grp["lr"]))
+                first = rows[0]
+                # own-branch keys start at the first row's branch start (brute force)
+                bstart = min(y for (rr, y) in grp["rr"] if rr == first)
+                tiles = [("p", grp["p0"] + j * bn) for j in range(a)] + \
+                        [("r", bstart + j * bn) for j in range(b)]
+                assert cost == a + b
+            assert len(rows) > 0
+            for (side_k, k0) in tiles:
+                keys = range(k0, k0 + bn)
+                hit = 0
+                for row in rows:
+                    for key in keys:
+                        if op == S.OP_PREFILL_FWD:
+                            ok = (row, key) in grp["pp"]
+                        else:
+                            ok = (row, key) in (grp["rp"] if side_k == "p" else grp["rr"])
+                        if ok:
+                            assert (side_k, row, key, h) not in covered, "pair covered twice"
+                            covered[(side_k, row, key, h)] = 1
+                            hit += 1
+                assert hit > 0, "empty KV tile in an item"
+        # every valid pair, every head
+        for grp in groups:
+            for h in range(hq):
+                if op == S.OP_PREFILL_FWD:
+                    for (row, key) in grp["pp"]:
+                        assert ("p", row, key, h) in covered
+                else:
+                    for (row, key) in grp["rp"]:
+                        assert ("p", row, key, h) in covered
+                    for (row, key) in grp["rr"]:
+                        assert ("r", row, key, h) in covered
+
+
+@pytest.mark.parametrize("ti", range(len(TREES)))
+@pytest.mark.parametrize("bm,bn", TILES)
+@pytest.mark.parametrize("hq,hkv,sms", [(4, 2, 1), (4, 2, 64), (2, 2, 2), (8, 1, 1)])
+def test_backward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv, sms):
+    tree = TREES[ti]
+    groups = valid_pairs(tree)
+    offs = tree.offsets()
+    r = hq // hkv
+    for op in (S.OP_REPLAY_BWD, S.OP_PREFILL_BWD):
+        q = S.build(offs, hq, hkv, op, bm, bn, num_sms=sms)
+        check_order(q)
+        covered = set()
+        split_ranges = {}
+        for it in q:
+            kind, g, tile, hk, split, cost, a, b = map(int, it)
+            grp = groups[g]
+            assert cost == (b - a) * r and b > a
+            if kind == S.PREFILL_KV:
+                assert op == S.OP_PREFILL_BWD
+                k0, rows0, rows1, pairs, side = grp["p0"], grp["p0"], grp["p0"] + grp["lp"], grp["pp"], "pp"
+            elif kind == S.PROMPT_KV:
+                assert op == S.OP_REPLAY_BWD
+                k0, rows0, rows1, pairs, side = grp["p0"], grp["r0"], grp["r0"] + grp["lr"], grp["rp"], "rp"
+                split_ranges.setdefault((g, tile, hk), []).append((split, a, b))
+            else:
+                assert kind == S.RESP_KV and op == S.OP_REPLAY_BWD and split == 0
+                k0, rows0, rows1, pairs, side = grp["r0"], grp["r0"], grp["r0"] + grp["lr"], grp["rr"], "rr"
+            keys = range(k0 + tile * bn, min(k0 + (tile + 1) * bn, k0 + (grp["lp"] if side != "rr" else grp["lr"])))
+            assert len(keys) > 0
+            for qt in range(a, b):
+                rows = range(rows0 + qt * bm, min(rows0 + (qt + 1) * bm, rows1))
+                hit = 0
+                for row in rows:
+                    for key in keys:
+                        if (row, key) in pairs:
+                            for h in range(hk * r, (hk + 1) * r):
+                                assert (side, row, key, h) not in covered
+                                covered.add((side, row, key, h))
+                            hit += 1
+                assert hit > 0, "empty query tile in an item"
+        for grp in groups:
+            sides = ("pp",) if op == S.OP_PREFILL_BWD else ("rp", "rr")
+            for side in sides:
+                for (row, key) in grp[side]:
+                    for h in range(hq):
+                        assert (side, row, key, h) in covered
+        # splits of one prompt KV tile partition the group's query tiles, in order
+        for (g, tile, hk), lst in split_ranges.items():
+            lst.sort()
+            assert [s for s, _, _ in lst] == list(range(len(lst)))
+            assert lst[0][1] == 0 and all(lst[i][2] == lst[i + 1][1] for i in range(len(lst) - 1))
+            assert lst[-1][2] == -(-groups[g]["lr"] // bm)
+
+
+def test_lpt_order_meets_the_list_scheduling_bound():
+    """Items are taken largest first (Sec. 3.4).  Any list schedule on m lanes has
+    makespan <= total/m + largest item; LPT order must also be non-increasing."""
+    import heapq
+    tree = W.Tree([300, 20], [[37, 200, 5, 90], [400, 3]])
+    offs = tree.offsets()
+    for op in (S.OP_PREFILL_FWD, S.OP_REPLAY_FWD, S.OP_REPLAY_BWD, S.OP_PREFILL_BWD):
+        q = S.build(offs, 4, 2, op, 16, 16, num_sms=4)
+        costs = [int(c) for c in q[:, 5]]
+        assert costs == sorted(costs, reverse=True)
+        m = 8
+        lanes = [0] * m
+        for c in costs:
+            heapq.heappush(lanes, heapq.heappop(lanes) + c)
+        assert max(lanes) <= sum(costs) / m + max(costs)
