@@ -1,0 +1,376 @@
+"""Benchmark of exact shared-prompt tree attention, forward + backward, on GB300.
+
+One step = the whole hot path over one batch of seeded synthetic replay trees: prompt
+prefill forward, response replay forward, replay backward (prompt K/V gradient summed
+over all branches, split-K reduced without atomics) and prefill backward.  The
+schedule (work queues) of a batch is built once, on the host, ahead of the step, the
+way a planner prepares a batch while the GPU runs the previous one.
+
+Metric: useful TFLOP/s of fwd+bwd, counting only non-redundant tree FLOPs:
+4*D*Hq*N forward + 10*D*Hq*N backward, N = exact count of valid (query, key) pairs
+with the prompt counted once.  Also tokens/s (unique tree tokens) and the fraction of
+the measured dense-BF16 tensor peak.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (the path has no
+exchange step on one batch); value = all ranks' work / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+DEFAULT_WORKLOAD = "prompt_heavy"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    self.rows.append(parts)
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def useful_flops(w):
+    return w.useful_flops(True, True)
+
+
+# ---------------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample of the workload's structure.
+# ---------------------------------------------------------------------------------
+def oracle_sample(w):
+    """A down-scaled sample with the same structure: the first group, prompt and
+    branch lengths scaled by 1/8, one KV head and its query heads... bounded to a few
+    seconds of fp64 work.  Returns (workload, description)."""
+    import workloads as W
+    lp = max(1, w.tree.prompt_lens[0] // 16)
+    bl = [max(1, x // 16) for x in w.tree.branch_lens[0]]
+    tree = W.Tree([lp], [bl])
+    r = w.hq // w.hkv
+    sample = W.custom(tree, hq=r, hkv=1, d=w.d, dtype=w.dtype, seed=w.seed, scale=w.scale, name=w.name + "_sample")
+    desc = (f"group 0 of {w.name} with prompt and branch lengths /16 (L_P={lp}, G={len(bl)}, "
+            f"sum L_i={sum(bl)}), one KV head with its {r} query heads, D={w.d}; fp64 numpy oracle "
+            f"(tree-direct form), fwd+bwd; rate = useful FLOPs of the sample / time")
+    return sample, desc
+
+
+def time_oracle(w, min_seconds=10.0, max_reps=50):
+    from oracle import attention as A
+    import workloads as W
+    sample, desc = oracle_sample(w)
+    t = {n: W.tensor_rows_np(sample, n) for n in W.TENSORS}
+    flops = useful_flops(sample)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        A.tree_attention_direct(t, sample.tree.offsets(), A.default_scale(sample.d))
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    rate = flops * reps / el / 1e12
+    return rate, desc, el / reps
+
+
+def threads_used():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return int(max(x.get("num_threads", 1) for x in info))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import shared_prompt_tree_gb300 as at
+    import workloads as W
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.workload(args.workload)
+    kernel = {"auto": at.KERNEL_AUTO, "simt": at.KERNEL_SIMT, "tc": at.KERNEL_TC}[args.kernel]
+    dt = at.BF16 if w.dtype == "bf16" else at.FP32
+    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt, kernel=kernel)
+    t = {n: W.tensor_torch(w, n, dev) for n in W.TENSORS}
+    stream = torch.cuda.current_stream()
+    tdt = torch.bfloat16 if dt == at.BF16 else torch.float32
+    f32 = torch.float32
+    o_p, o_r = torch.empty_like(t["q_p"]), torch.empty_like(t["q_r"])
+    lse_p = torch.empty(w.hq, w.tree.total_prompt, dtype=f32, device=dev)
+    lse_r = torch.empty(w.hq, w.tree.total_resp, dtype=f32, device=dev)
+    dq_p, dk_p, dv_p = (torch.empty_like(t[n]) for n in ("q_p", "k_p", "v_p"))
+    dq_r, dk_r, dv_r = (torch.empty_like(t[n]) for n in ("q_r", "k_r", "v_r"))
+    dkp_sum = torch.empty(t["k_p"].shape, dtype=f32, device=dev)
+    dvp_sum = torch.empty(t["v_p"].shape, dtype=f32, device=dev)
+    ws_r = torch.empty(max(1, plan.workspace_bytes(at.OP_REPLAY_BWD)), dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(max(1, plan.workspace_bytes(at.OP_PREFILL_BWD)), dtype=torch.uint8, device=dev)
+
+    n_ev = 5
+    def step(evs=None):
+        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
+        rec(0)
+        at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, stream=stream)
+        rec(1)
+        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, stream=stream)
+        rec(2)
+        at.augtree_replay_bwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, t["do_r"],
+                              dq_r, dk_r, dv_r, dkp_sum, dvp_sum, ws_r, stream=stream)
+        rec(3)
+        at.augtree_prefill_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], dkp_sum, dvp_sum,
+                               dq_p, dk_p, dv_p, ws_p, stream=stream)
+        rec(4)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        import torch.distributed as dist
+        x = torch.tensor([ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        ms = float(x.item())
+    per_call = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(n_ev - 1)]
+                         for k in range(args.steps)]).mean(0)
+    ms_step = ms / args.steps
+
+    # e2e through the public API with host buffers: H2D of the step's inputs from
+    # pinned memory, the step, D2H of its results (outputs and all gradients).
+    host_in = {n: t[n].cpu().pin_memory() for n in W.TENSORS}
+    outs = [o_p, o_r, lse_p, lse_r, dq_p, dk_p, dv_p, dq_r, dk_r, dv_r]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in outs)
+    e_steps = max(1, min(args.steps, 5))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        for n in W.TENSORS:
+            t[n].copy_(host_in[n], non_blocking=True)
+        step()
+        for x, hx in zip(outs, host_out):
+            hx.copy_(x, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if world > 1:
+        import torch.distributed as dist
+        x = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        e2e_ms = float(x.item())
+
+    flops = useful_flops(w)
+    tokens = w.tokens
+    tflops = flops * world / (ms_step * 1e-3) / 1e12
+    pk, pk_kind = peaks()
+    names = ["prefill_fwd", "replay_fwd", "replay_bwd", "prefill_bwd"]
+    n_pairs_prompt = sum(lp * (lp + 1) // 2 for lp in w.tree.prompt_lens)
+    n_pairs = w.tree.pair_count()
+    per_flops = [4 * w.d * w.hq * n_pairs_prompt, 4 * w.d * w.hq * (n_pairs - n_pairs_prompt),
+                 10 * w.d * w.hq * (n_pairs - n_pairs_prompt), 10 * w.d * w.hq * n_pairs_prompt]
+    dom = int(np.argmax(per_call))
+    ach = per_flops[dom] / (per_call[dom] * 1e-3) / 1e12
+    peak_s = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    launches_per_step = count_launches(plan, at)
+
+    result = {
+        "metric": "tree-attn fwd+bwd useful TFLOP/s & tokens/s; % of GB300 BF16 tensor peak",
+        "value": round(tflops, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if dt == at.BF16 else "fp32",
+        "data": "synthetic (seeded counter-hash N(0,1) values, bf16-rounded)",
+        "config": {"workload": w.name, "groups": w.tree.n_groups, "prompt_lens": w.tree.prompt_lens[:4],
+                   "branches": w.tree.n_branches, "total_prompt": w.tree.total_prompt,
+                   "total_resp": w.tree.total_resp, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
+                   "parallelism": f"replicas x{world}", "kernel_family": args.kernel,
+                   "l2": "inputs larger than L2 (no flush)"},
+        "tokens_per_s": round(tokens * world / (ms_step * 1e-3), 1),
+        "flattened_tokens_per_s": round(w.tree.flattened_tokens() * world / (ms_step * 1e-3), 1),
+        "pct_of_bf16_peak": round(100.0 * tflops / world / pk["bf16_tflops"], 2),
+        "per_call_ms": {n: round(float(x), 4) for n, x in zip(names, per_call)},
+        "per_call_tflops": {n: round(f / (x * 1e-3) / 1e12, 2) for n, f, x in zip(names, per_flops, per_call)},
+        "roofline": {"bound": "tensor", "kernel": names[dom], "achieved": round(ach, 2), "peak": peak_s,
+                     "unit": "TFLOP/s", "frac": round(ach / peak_s, 4), "traffic": None,
+                     "peak_kind": f"bf16 dense sustained ({pk_kind})"},
+        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, per = time_oracle(w, min_seconds=args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads_used(),
+                                  "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def count_launches(plan, at):
+    """Kernels one step launches: prefill fwd 1, replay fwd 1, replay bwd 4
+    (preprocess, main, split reduce, dQ convert), prefill bwd 3."""
+    n = 0
+    n += 1 if plan.schedule(at.OP_PREFILL_FWD).shape[0] else 0
+    n += 1 if plan.schedule(at.OP_REPLAY_FWD).shape[0] else 0
+    n += (1 if plan.total_resp else 0) + (1 if plan.schedule(at.OP_REPLAY_BWD).shape[0] else 0) \
+        + (1 if plan.total_prompt else 0) + (1 if plan.total_resp else 0)
+    n += 3 if plan.total_prompt else 0
+    return n
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle, as it stands, on the host cores.  Each step
+    is a bounded sample of the workload (see oracle_sample)."""
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return
+    import workloads as W
+    from oracle import attention as A
+    w = W.workload(args.workload)
+    sample, desc = oracle_sample(w)
+    t = {n: W.tensor_rows_np(sample, n) for n in W.TENSORS}
+    flops = useful_flops(sample)
+    for _ in range(args.warmup):
+        A.tree_attention_direct(t, sample.tree.offsets(), A.default_scale(sample.d))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        A.tree_attention_direct(t, sample.tree.offsets(), A.default_scale(sample.d))
+    el = time.perf_counter() - t0
+    rate = flops * args.steps / el / 1e12
+    res = {"impl": "reference", "metric": "tree-attn fwd+bwd useful TFLOP/s & tokens/s; % of GB300 BF16 tensor peak",
+           "value": round(rate, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": {"workload": w.name, "sample": desc},
+           "cpu_baseline": {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads_used(), "kind": "oracle",
+                            "sample": desc},
+           "e2e": {"value": round(rate, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+// Memory-bound kernels of the path: the backward preprocess (Delta and the zeroed fp32
+// dQ accumulator), the dQ conversion, the fixed-order split-K reduction of the prompt
+// K/V gradient (Eq. 2), and the partial-state merge of Sec. 3.3.
+//
+// AugTree paper, Sec. 3.2 (Eq. 2: the prompt K/V gradient is the sum over branches,
+// "exact many-to-one gradient aggregation") and Sec. 3.3 (partial online-softmax
+// states S = (m, l, O_acc) merge associatively; here in (O, lse) form).
+#include <cmath>
+
+#include "common.cuh"
+
+namespace augtree {
+namespace {
+
+// One warp per (row, head): Delta = sum_d dO * O in fp32; also zeroes the fp32 dQ
+// accumulator row.  delta layout [Hq, rows].
+template <typename T>
+__global__ void preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO, int64_t rows, int hq, int d,
+                                  float* __restrict__ delta, float* __restrict__ dq_acc) {
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows * hq) return;
+  const int64_t row = warp / hq;
+  const int h = (int)(warp % hq);
+  const int64_t base = warp * d;
+  float acc = 0.f;
+  for (int c = lane; c < d; c += 32) acc += to_f32(o[base + c]) * to_f32(dO[base + c]);
+  acc = warp_sum(acc);
+  if (lane == 0) delta[(int64_t)h * rows + row] = acc;
+  for (int c = lane; c < d; c += 32) dq_acc[base + c] = 0.f;
+}
+
+template <typename T>
+__global__ void convert_kernel(const float* __restrict__ src, T* __restrict__ dst, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = from_f32<T>(src[i]);
+}
+
+// Per prompt row (one block per row, Hkv*D columns): groups with several splits sum
+// their partials in ascending split order; groups without prompt-KV items (no
+// responses) get zeros; single-split groups were written in place by the backward.
+__global__ void split_reduce_kernel(const GroupInfo* __restrict__ groups, const SplitInfo* __restrict__ splits,
+                                    int n_groups, int cols, const float* __restrict__ dk_part,
+                                    const float* __restrict__ dv_part, float* __restrict__ dk_sum,
+                                    float* __restrict__ dv_sum, int total_prompt) {
+  const int row = blockIdx.x;
+  if (row >= total_prompt) return;
+  // group of this row: binary search over p0
+  int lo = 0, hi = n_groups - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (groups[mid].p0 <= row) lo = mid; else hi = mid - 1;
+  }
+  // skip empty groups that share p0 with the holder
+  int g = lo;
+  while (g > 0 && groups[g].lp == 0) --g;
+  while (g < n_groups && !(groups[g].p0 <= row && row < groups[g].p0 + groups[g].lp)) ++g;
+  if (g >= n_groups) return;
+  const SplitInfo s = splits[g];
+  const int64_t out = (int64_t)row * cols;
+  if (s.nsplit == 1) return;
+  if (s.nsplit == 0) {
+    for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+      dk_sum[out + c] = 0.f;
+      dv_sum[out + c] = 0.f;
+    }
+    return;
+  }
+  const int lp = groups[g].lp;
+  const int64_t local = row - groups[g].p0;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+    float ak = 0.f, av = 0.f;
+    for (int k = 0; k < s.nsplit; ++k) {
+      const int64_t pr = (s.part_row0 + (int64_t)k * lp + local) * cols + c;
+      ak += dk_part[pr];
+      av += dv_part[pr];
+    }
+    dk_sum[out + c] = ak;
+    dv_sum[out + c] = av;
+  }
+}
+
+// (O, lse) merge, one thread per (row, head) pair looping over d.
+__global__ void lse_merge_kernel(int64_t rows, int h, int d, const float* __restrict__ oa,
+                                 const float* __restrict__ la, const float* __restrict__ ob,
+                                 const float* __restrict__ lb, float* __restrict__ o, float* __restrict__ l) {
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows * h) return;
+  const int64_t row = warp / h;
+  const int head = (int)(warp % h);
+  const int64_t li = (int64_t)head * rows + row;
+  const float a = la[li], b = lb[li];
+  const float m = fmaxf(a, b);
+  float wa = 0.f, wb = 0.f, lse = -INFINITY;
+  if (m != -INFINITY) {
+    const float ea = (a == -INFINITY) ? 0.f : expf(a - m);
+    const float eb = (b == -INFINITY) ? 0.f : expf(b - m);
+    const float s = ea + eb;
+    lse = m + logf(s);
+    wa = ea / s;
+    wb = eb / s;
+  }
+  const int64_t base = warp * d;
+  for (int c = lane; c < d; c += 32) {
+    const float x = oa[base + c], y = ob[base + c];
+    o[base + c] = wa * x + wb * y;
+  }
+  __syncwarp();
+  if (lane == 0) l[li] = lse;
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d, float* delta,
+                              float* dq_acc, cudaStream_t st) {
+  const int64_t warps = rows * hq;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (warps + 7) / 8;
+  if (dtype == AUGTREE_BF16)
+    preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, st>>>(
+        (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, rows, hq, d, delta, dq_acc);
+  else
+    preprocess_kernel<float><<<(unsigned)blocks, threads, 0, st>>>((const float*)o, (const float*)dO, rows, hq, d,
+                                                                   delta, dq_acc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int dtype, int64_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (n + threads - 1) / threads;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (dtype == AUGTREE_BF16)
+    convert_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, st>>>(dq_acc, (__nv_bfloat16*)dq, n);
+  else
+    convert_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(dq_acc, (float*)dq, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, const float* dv_part, float* dk_sum,
+                                float* dv_sum, cudaStream_t st) {
+  if (p->total_prompt == 0 || p->n_groups == 0) return cudaSuccess;
+  const int cols = p->cfg.hkv * p->cfg.head_dim;
+  split_reduce_kernel<<<p->total_prompt, 256, 0, st>>>(p->groups_d, p->splits_d, p->n_groups, cols, dk_part, dv_part,
+                                                       dk_sum, dv_sum, p->total_prompt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(int64_t rows, int h, int d, const float* oa, const float* la, const float* ob,
+                             const float* lb, float* o, float* l, cudaStream_t st) {
+  const int64_t warps = rows * h;
+  const int64_t blocks = (warps + 7) / 8;
+  lse_merge_kernel<<<(unsigned)blocks, 256, 0, st>>>(rows, h, d, oa, la, ob, lb, o, l);
+  return cudaGetLastError();
+}
+
+}  // namespace augtree

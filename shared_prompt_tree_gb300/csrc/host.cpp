@@ -1,0 +1,592 @@
+// Host side of the C ABI: descriptor validation, the largest-first work queues, plans,
+// workspace layout and the dispatch of the compute calls to their kernels.
+//
+// AugTree, "Splitting Prompt Prefill from Response Replay for Context-Parallel
+// Long-Context LLM Post-Training":
+//   Sec. 3.1        replay tree T = (P, {R_i}) per group (the ragged descriptors);
+//   Sec. 3.2        prefill once, replay many; Eq. 1 valid KV context; Eq. 2 prompt
+//                   K/V gradient summed over all branches;
+//   Sec. 3.4        bounded replay units with work weights, largest-first greedy
+//                   balancing (the work queues built here; thread blocks are the lanes).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+using namespace augtree;
+
+namespace {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Grp {
+  int64_t p0, lp, r0, lr;
+  std::vector<int64_t> starts, ends;  // branch row ranges (global response rows)
+};
+
+bool read_groups(const std::vector<int32_t>& po, const std::vector<int32_t>& bb,
+                 const std::vector<int32_t>& ro, std::vector<Grp>& out) {
+  const int ng = (int)po.size() - 1;
+  out.resize(ng);
+  for (int g = 0; g < ng; ++g) {
+    Grp& G = out[g];
+    G.p0 = po[g];
+    G.lp = (int64_t)po[g + 1] - po[g];
+    G.r0 = ro[bb[g]];
+    G.lr = (int64_t)ro[bb[g + 1]] - ro[bb[g]];
+    for (int b = bb[g]; b < bb[g + 1]; ++b) {
+      G.starts.push_back(ro[b]);
+      G.ends.push_back(ro[b + 1]);
+    }
+  }
+  return true;
+}
+
+// Index (within the group) of the non-empty branch holding global response row `row`.
+int branch_of(const Grp& G, int64_t row) {
+  auto it = std::upper_bound(G.starts.begin(), G.starts.end(), row);
+  int i = (int)(it - G.starts.begin()) - 1;
+  while (i >= 0 && !(G.starts[i] <= row && row < G.ends[i])) --i;  // skip empty branches
+  return i;
+}
+
+struct Item {
+  int32_t w[AUGTREE_ITEM_WORDS];
+};
+
+augtree_status validate_desc(const augtree_desc* d, std::vector<int32_t>& po, std::vector<int32_t>& bb,
+                             std::vector<int32_t>& ro) {
+  if (!d || !d->prompt_off || !d->branch_begin || !d->resp_off) return AUGTREE_ERR_INVALID_ARG;
+  if (d->n_groups < 0 || d->n_branches < 0) return AUGTREE_ERR_INVALID_ARG;
+  po.assign(d->prompt_off, d->prompt_off + d->n_groups + 1);
+  bb.assign(d->branch_begin, d->branch_begin + d->n_groups + 1);
+  ro.assign(d->resp_off, d->resp_off + d->n_branches + 1);
+  if (po[0] != 0 || bb[0] != 0 || ro[0] != 0) return AUGTREE_ERR_INVALID_ARG;
+  if (bb[d->n_groups] != d->n_branches) return AUGTREE_ERR_INVALID_ARG;
+  for (int g = 0; g < d->n_groups; ++g)
+    if (po[g + 1] < po[g] || bb[g + 1] < bb[g]) return AUGTREE_ERR_INVALID_ARG;
+  for (int b = 0; b < d->n_branches; ++b)
+    if (ro[b + 1] < ro[b]) return AUGTREE_ERR_INVALID_ARG;
+  return AUGTREE_OK;
+}
+
+augtree_status validate_cfg(const augtree_config* c, bool need_sms) {
+  if (!c) return AUGTREE_ERR_INVALID_ARG;
+  if (c->hq <= 0 || c->hkv <= 0 || c->reserved != 0) return AUGTREE_ERR_INVALID_ARG;
+  if (c->num_sms < 0 || (need_sms && c->num_sms == 0)) return AUGTREE_ERR_INVALID_ARG;
+  if (!(c->softmax_scale >= 0.0f) || std::isinf(c->softmax_scale)) return AUGTREE_ERR_INVALID_ARG;
+  if (c->hq % c->hkv != 0) return AUGTREE_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return AUGTREE_ERR_UNSUPPORTED;
+  if (c->dtype != AUGTREE_FP32 && c->dtype != AUGTREE_BF16) return AUGTREE_ERR_UNSUPPORTED;
+  if (c->kernel < AUGTREE_KERNEL_AUTO || c->kernel > AUGTREE_KERNEL_TC) return AUGTREE_ERR_INVALID_ARG;
+  if (c->kernel == AUGTREE_KERNEL_TC && (c->dtype != AUGTREE_BF16 || c->head_dim != 128))
+    return AUGTREE_ERR_UNSUPPORTED;
+  return AUGTREE_OK;
+}
+
+int resolve_family(const augtree_config* c) {
+  if (c->kernel == AUGTREE_KERNEL_SIMT) return AUGTREE_KERNEL_SIMT;
+  if (c->kernel == AUGTREE_KERNEL_TC) return AUGTREE_KERNEL_TC;
+  return (c->dtype == AUGTREE_BF16 && c->head_dim == 128) ? AUGTREE_KERNEL_TC : AUGTREE_KERNEL_SIMT;
+}
+
+void tiles_for(int family, int op, int* bm, int* bn) {
+  if (family == AUGTREE_KERNEL_TC) {
+    // Forward: 128 query rows x 128 keys per tile; backward: 128 keys x 64 query rows.
+    *bn = 128;
+    *bm = (op == AUGTREE_OP_PREFILL_FWD || op == AUGTREE_OP_REPLAY_FWD) ? 128 : 64;
+  } else {
+    *bm = 64;
+    *bn = 64;
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+namespace augtree {
+
+augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int32_t>& bb,
+                           const std::vector<int32_t>& ro, int hq, int hkv, int op, int bm, int bn,
+                           int num_sms, std::vector<int32_t>& out) {
+  std::vector<Grp> groups;
+  read_groups(po, bb, ro, groups);
+  const int r = hq / hkv;
+  std::vector<Item> items;
+  auto push = [&](int kind, int g, int64_t tile, int head, int split, int64_t cost, int64_t a, int64_t b) {
+    Item it;
+    it.w[0] = kind; it.w[1] = g; it.w[2] = (int32_t)tile; it.w[3] = head;
+    it.w[4] = split; it.w[5] = (int32_t)cost; it.w[6] = (int32_t)a; it.w[7] = (int32_t)b;
+    items.push_back(it);
+  };
+  const int ng = (int)groups.size();
+  if (op == AUGTREE_OP_PREFILL_FWD) {
+    for (int g = 0; g < ng; ++g) {
+      const Grp& G = groups[g];
+      for (int64_t t = 0; t < cdiv(G.lp, bm); ++t) {
+        int64_t row_end = std::min(G.p0 + (t + 1) * bm, G.p0 + G.lp);
+        int64_t a = cdiv(row_end - G.p0, bn);
+        for (int h = 0; h < hq; ++h) push(K_PREFILL_Q, g, t, h, 0, a, a, 0);
+      }
+    }
+  } else if (op == AUGTREE_OP_REPLAY_FWD) {
+    for (int g = 0; g < ng; ++g) {
+      const Grp& G = groups[g];
+      int64_t a = cdiv(G.lp, bn);
+      for (int64_t t = 0; t < cdiv(G.lr, bm); ++t) {
+        int64_t row_begin = G.r0 + t * bm;
+        int64_t row_end = std::min(row_begin + bm, G.r0 + G.lr);
+        int64_t bstart = G.starts[branch_of(G, row_begin)];
+        int64_t b = cdiv(row_end - bstart, bn);
+        for (int h = 0; h < hq; ++h) push(K_REPLAY_Q, g, t, h, 0, a + b, a, b);
+      }
+    }
+  } else if (op == AUGTREE_OP_REPLAY_BWD) {
+    // Costs before splitting fix the split target.
+    int64_t total = 0;
+    struct RI { int g; int64_t j, qa, qb; };
+    std::vector<RI> resp;
+    for (int g = 0; g < ng; ++g) {
+      const Grp& G = groups[g];
+      int64_t nq = cdiv(G.lr, bm);
+      int64_t nkp = nq > 0 ? cdiv(G.lp, bn) : 0;
+      total += nkp * nq * r * hkv;
+      for (int64_t j = 0; j < cdiv(G.lr, bn); ++j) {
+        int64_t k_lo = G.r0 + j * bn;
+        int64_t k_hi = std::min(k_lo + bn, G.r0 + G.lr);
+        int64_t e = G.ends[branch_of(G, k_hi - 1)];
+        int64_t qa = (k_lo - G.r0) / bm;
+        int64_t qb = cdiv(e - G.r0, bm);
+        resp.push_back({g, j, qa, qb});
+        total += (qb - qa) * r * hkv;
+      }
+    }
+    int64_t target = std::max<int64_t>(r, cdiv(total, 2 * (int64_t)num_sms));
+    for (int g = 0; g < ng; ++g) {
+      const Grp& G = groups[g];
+      int64_t nq = cdiv(G.lr, bm);
+      if (G.lp == 0 || nq == 0) continue;
+      int64_t s = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, cdiv(nq * r, target)));
+      int64_t c = cdiv(nq, s);
+      s = cdiv(nq, c);
+      for (int64_t j = 0; j < cdiv(G.lp, bn); ++j)
+        for (int64_t k = 0; k < s; ++k) {
+          int64_t qa = k * c, qb = std::min((k + 1) * c, nq);
+          for (int h = 0; h < hkv; ++h) push(K_PROMPT_KV, g, j, h, (int)k, (qb - qa) * r, qa, qb);
+        }
+    }
+    for (const RI& x : resp)
+      for (int h = 0; h < hkv; ++h) push(K_RESP_KV, x.g, x.j, h, 0, (x.qb - x.qa) * r, x.qa, x.qb);
+  } else if (op == AUGTREE_OP_PREFILL_BWD) {
+    for (int g = 0; g < ng; ++g) {
+      const Grp& G = groups[g];
+      int64_t nq = cdiv(G.lp, bm);
+      for (int64_t j = 0; j < cdiv(G.lp, bn); ++j) {
+        int64_t qa = (j * bn) / bm;
+        for (int h = 0; h < hkv; ++h) push(K_PREFILL_KV, g, j, h, 0, (nq - qa) * r, qa, nq);
+      }
+    }
+  } else {
+    return AUGTREE_ERR_INVALID_ARG;
+  }
+  // Largest first; ties by (group, tile, kind, split, head).  The key is unique per
+  // item, so the order is fully determined.
+  std::sort(items.begin(), items.end(), [](const Item& x, const Item& y) {
+    if (x.w[5] != y.w[5]) return x.w[5] > y.w[5];
+    if (x.w[1] != y.w[1]) return x.w[1] < y.w[1];
+    if (x.w[2] != y.w[2]) return x.w[2] < y.w[2];
+    if (x.w[0] != y.w[0]) return x.w[0] < y.w[0];
+    if (x.w[4] != y.w[4]) return x.w[4] < y.w[4];
+    return x.w[3] < y.w[3];
+  });
+  out.resize(items.size() * AUGTREE_ITEM_WORDS);
+  if (!items.empty()) std::memcpy(out.data(), items.data(), items.size() * sizeof(Item));
+  return AUGTREE_OK;
+}
+
+BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
+  BwdWorkspace w;
+  const size_t hq = p->cfg.hq, hkv = p->cfg.hkv, d = p->cfg.head_dim, R = p->total_resp;
+  w.delta_off = 0;
+  w.dq_off = align256(hq * R * 4);
+  w.dkpart_off = w.dq_off + align256(R * hq * d * 4);
+  w.dvpart_off = w.dkpart_off + align256((size_t)p->part_rows * hkv * d * 4);
+  w.total = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
+  return w;
+}
+
+BwdWorkspace prefill_bwd_ws(const augtree_plan* p) {
+  BwdWorkspace w;
+  const size_t hq = p->cfg.hq, d = p->cfg.head_dim, P = p->total_prompt;
+  w.delta_off = 0;
+  w.dq_off = align256(hq * P * 4);
+  w.dkpart_off = w.dvpart_off = w.dq_off + align256(P * hq * d * 4);
+  w.total = w.dkpart_off;
+  return w;
+}
+
+Geometry geometry(const augtree_plan* p) {
+  Geometry g;
+  g.groups = p->groups_d;
+  g.row_bstart = p->row_bstart_d;
+  g.splits = p->splits_d;
+  g.hq = p->cfg.hq;
+  g.hkv = p->cfg.hkv;
+  g.d = p->cfg.head_dim;
+  g.total_prompt = p->total_prompt;
+  g.total_resp = p->total_resp;
+  g.scale = p->cfg.softmax_scale > 0.f ? p->cfg.softmax_scale : 1.0f / std::sqrt((float)p->cfg.head_dim);
+  g.scale_log2 = g.scale * 1.4426950408889634f;
+  return g;
+}
+
+}  // namespace augtree
+
+// =====================================================================================
+// C ABI
+// =====================================================================================
+extern "C" {
+
+const char* augtree_status_string(augtree_status s) {
+  switch (s) {
+    case AUGTREE_OK: return "ok";
+    case AUGTREE_ERR_INVALID_ARG: return "invalid argument";
+    case AUGTREE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case AUGTREE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case AUGTREE_ERR_CUDA: return "CUDA error";
+    case AUGTREE_ERR_DEVICE_CHECK: return "device-side check failed";
+    case AUGTREE_ERR_TIMEOUT: return "device-side wait timed out";
+    case AUGTREE_ERR_CAPACITY: return "output capacity too small";
+  }
+  return "unknown status";
+}
+
+int32_t augtree_version(void) { return 100; }
+
+augtree_status augtree_tile_sizes(const augtree_config* cfg, int32_t op, int32_t* bm, int32_t* bn) {
+  augtree_status st = validate_cfg(cfg, false);
+  if (st != AUGTREE_OK) return st;
+  if (!bm || !bn || op < 0 || op > 3) return AUGTREE_ERR_INVALID_ARG;
+  int m, n;
+  tiles_for(resolve_family(cfg), op, &m, &n);
+  *bm = m;
+  *bn = n;
+  return AUGTREE_OK;
+}
+
+augtree_status augtree_schedule_build(const augtree_desc* desc, const augtree_config* cfg, int32_t op,
+                                      int32_t* out, size_t cap_items, size_t* n_items) {
+  std::vector<int32_t> po, bb, ro;
+  augtree_status st = validate_desc(desc, po, bb, ro);
+  if (st != AUGTREE_OK) return st;
+  if ((st = validate_cfg(cfg, true)) != AUGTREE_OK) return st;
+  if (!n_items || op < 0 || op > 3 || (cap_items > 0 && !out)) return AUGTREE_ERR_INVALID_ARG;
+  int bm, bn;
+  tiles_for(resolve_family(cfg), op, &bm, &bn);
+  std::vector<int32_t> q;
+  try {
+    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, bm, bn, cfg->num_sms, q);
+  } catch (const std::bad_alloc&) {
+    return AUGTREE_ERR_CAPACITY;
+  }
+  if (st != AUGTREE_OK) return st;
+  *n_items = q.size() / AUGTREE_ITEM_WORDS;
+  if (*n_items > cap_items) return AUGTREE_ERR_CAPACITY;
+  if (!q.empty()) std::memcpy(out, q.data(), q.size() * sizeof(int32_t));
+  return AUGTREE_OK;
+}
+
+augtree_status augtree_plan_destroy(augtree_plan* p) {
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != p->device) cudaSetDevice(p->device);
+  cudaFree(p->groups_d);
+  cudaFree(p->row_bstart_d);
+  cudaFree(p->row_bend_d);
+  cudaFree(p->splits_d);
+  cudaFree(p->err_d);
+  for (int i = 0; i < 4; ++i) cudaFree(p->queue_d[i]);
+  if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+  delete p;
+  return AUGTREE_OK;
+}
+
+augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_config* cfg, augtree_plan** out) {
+  if (!out) return AUGTREE_ERR_INVALID_ARG;
+  *out = nullptr;
+  std::vector<int32_t> po, bb, ro;
+  augtree_status st = validate_desc(desc, po, bb, ro);
+  if (st != AUGTREE_OK) return st;
+  if ((st = validate_cfg(cfg, false)) != AUGTREE_OK) return st;
+  augtree_plan* p = new (std::nothrow) augtree_plan();
+  if (!p) return AUGTREE_ERR_CUDA;
+  p->cfg = *cfg;
+  p->groups_d = nullptr;
+  p->err_d = nullptr;
+  p->row_bstart_d = nullptr;
+  p->row_bend_d = nullptr;
+  p->splits_d = nullptr;
+  for (int i = 0; i < 4; ++i) p->queue_d[i] = nullptr;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return AUGTREE_ERR_CUDA;
+  }
+  if (p->cfg.num_sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess || sms <= 0) {
+      delete p;
+      return AUGTREE_ERR_CUDA;
+    }
+    p->cfg.num_sms = sms;
+  }
+  p->family = resolve_family(cfg);
+  p->n_groups = desc->n_groups;
+  p->n_branches = desc->n_branches;
+  p->total_prompt = po[desc->n_groups];
+  p->total_resp = ro[desc->n_branches];
+  std::vector<Grp> groups;
+  read_groups(po, bb, ro, groups);
+  p->groups_h.resize(p->n_groups);
+  for (int g = 0; g < p->n_groups; ++g)
+    p->groups_h[g] = GroupInfo{(int32_t)groups[g].p0, (int32_t)groups[g].lp, (int32_t)groups[g].r0,
+                               (int32_t)groups[g].lr};
+  std::vector<int32_t> bstart(std::max(1, p->total_resp)), bend(std::max(1, p->total_resp));
+  for (int b = 0; b < p->n_branches; ++b)
+    for (int32_t row = ro[b]; row < ro[b + 1]; ++row) {
+      bstart[row] = ro[b];
+      bend[row] = ro[b + 1];
+    }
+  for (int op = 0; op < 4; ++op) {
+    tiles_for(p->family, op, &p->bm[op], &p->bn[op]);
+    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, p->bm[op], p->bn[op], p->cfg.num_sms, p->queue_h[op]);
+    if (st != AUGTREE_OK) {
+      delete p;
+      return st;
+    }
+    p->n_items[op] = p->queue_h[op].size() / AUGTREE_ITEM_WORDS;
+  }
+  // Forward tensor-core units pair consecutive items: heads h, h+1 (h even) of one
+  // query tile share their KV head when Hq/Hkv is even.  The sort order puts the Hq
+  // items of a (group, tile) next to each other, so pairs are checked, not assumed.
+  for (int op = 0; op < 4; ++op) {
+    p->paired[op] = 0;
+    if (p->family != AUGTREE_KERNEL_TC || op > AUGTREE_OP_REPLAY_FWD) continue;
+    const int r = cfg->hq / cfg->hkv;
+    bool ok = (cfg->hq % 2 == 0) && (r % 2 == 0) && (p->n_items[op] % 2 == 0);
+    for (size_t i = 0; ok && i + 1 < p->n_items[op]; i += 2) {
+      const int32_t* a = &p->queue_h[op][i * AUGTREE_ITEM_WORDS];
+      const int32_t* b = a + AUGTREE_ITEM_WORDS;
+      ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 2 == 0 && b[3] == a[3] + 1;
+    }
+    p->paired[op] = ok ? 1 : 0;
+  }
+  // Split-K bookkeeping from the replay backward queue.
+  p->splits_h.assign(std::max(1, p->n_groups), SplitInfo{0, 0, 0});
+  for (size_t i = 0; i < p->n_items[AUGTREE_OP_REPLAY_BWD]; ++i) {
+    const int32_t* it = &p->queue_h[AUGTREE_OP_REPLAY_BWD][i * AUGTREE_ITEM_WORDS];
+    if (it[0] == K_PROMPT_KV) p->splits_h[it[1]].nsplit = std::max(p->splits_h[it[1]].nsplit, it[4] + 1);
+  }
+  p->part_rows = 0;
+  for (int g = 0; g < p->n_groups; ++g) {
+    SplitInfo& s = p->splits_h[g];
+    s.part_row0 = p->part_rows;
+    if (s.nsplit > 1) p->part_rows += (int64_t)s.nsplit * p->groups_h[g].lp;
+  }
+  // Device copies.
+  auto up = [&](void** dst, const void* src, size_t bytes) -> bool {
+    if (bytes == 0) bytes = 16;
+    if (cudaMalloc(dst, bytes) != cudaSuccess) return false;
+    return cudaMemcpy(*dst, src, bytes, cudaMemcpyHostToDevice) == cudaSuccess;
+  };
+  bool ok = true;
+  std::vector<int32_t> pad(4, 0);
+  ok = ok && up((void**)&p->groups_d, p->groups_h.empty() ? (const void*)pad.data() : p->groups_h.data(),
+                p->groups_h.size() * sizeof(GroupInfo));
+  ok = ok && up((void**)&p->row_bstart_d, bstart.data(), bstart.size() * sizeof(int32_t));
+  ok = ok && up((void**)&p->row_bend_d, bend.data(), bend.size() * sizeof(int32_t));
+  ok = ok && up((void**)&p->err_d, pad.data(), sizeof(uint32_t));
+  ok = ok && up((void**)&p->splits_d, p->splits_h.data(), p->splits_h.size() * sizeof(SplitInfo));
+  for (int op = 0; op < 4 && ok; ++op)
+    ok = up((void**)&p->queue_d[op], p->queue_h[op].empty() ? (const void*)pad.data() : p->queue_h[op].data(),
+            p->queue_h[op].size() * sizeof(int32_t));
+  if (!ok) {
+    cudaGetLastError();
+    augtree_plan_destroy(p);
+    return AUGTREE_ERR_CUDA;
+  }
+  *out = p;
+  return AUGTREE_OK;
+}
+
+augtree_status augtree_plan_workspace_bytes(const augtree_plan* p, int32_t op, size_t* bytes) {
+  if (!p || !bytes) return AUGTREE_ERR_INVALID_ARG;
+  switch (op) {
+    case AUGTREE_OP_PREFILL_FWD:
+    case AUGTREE_OP_REPLAY_FWD: *bytes = 0; return AUGTREE_OK;
+    case AUGTREE_OP_REPLAY_BWD: *bytes = replay_bwd_ws(p).total; return AUGTREE_OK;
+    case AUGTREE_OP_PREFILL_BWD: *bytes = prefill_bwd_ws(p).total; return AUGTREE_OK;
+  }
+  return AUGTREE_ERR_INVALID_ARG;
+}
+
+augtree_status augtree_schedule_export(const augtree_plan* p, int32_t op, int32_t* host_out, size_t cap_items,
+                                       size_t* n_items) {
+  if (!p || !n_items || op < 0 || op > 3) return AUGTREE_ERR_INVALID_ARG;
+  *n_items = p->n_items[op];
+  if (p->n_items[op] > cap_items) return AUGTREE_ERR_CAPACITY;
+  if (p->n_items[op] == 0) return AUGTREE_OK;
+  if (!host_out) return AUGTREE_ERR_INVALID_ARG;
+  // Read back the device copy: the export shows what the kernels walk.
+  if (cudaMemcpy(host_out, p->queue_d[op], p->n_items[op] * AUGTREE_ITEM_WORDS * sizeof(int32_t),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return AUGTREE_ERR_CUDA;
+  return AUGTREE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+augtree_status check_device(const augtree_plan* p) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return AUGTREE_ERR_CUDA;
+  return cur == p->device ? AUGTREE_OK : AUGTREE_ERR_INVALID_ARG;
+}
+
+augtree_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AUGTREE_OK : AUGTREE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+augtree_status augtree_prefill_fwd(const augtree_plan* p, const void* qp, const void* kp, const void* vp, void* op,
+                                   float* lse_p, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_prompt > 0 && (!qp || !kp || !vp || !op || !lse_p)) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  if (p->n_items[AUGTREE_OP_PREFILL_FWD] == 0) return AUGTREE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (p->family == AUGTREE_KERNEL_TC)
+    return from_cuda(tc_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s));
+  return from_cuda(simt_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s));
+}
+
+augtree_status augtree_replay_fwd(const augtree_plan* p, const void* qr, const void* kp, const void* vp,
+                                  const void* kr, const void* vr, void* or_, float* lse_r, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_resp > 0 && (!qr || !kr || !vr || !or_ || !lse_r)) return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_resp > 0 && p->total_prompt > 0 && (!kp || !vp)) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  if (p->n_items[AUGTREE_OP_REPLAY_FWD] == 0) return AUGTREE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (p->family == AUGTREE_KERNEL_TC)
+    return from_cuda(tc_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s));
+  return from_cuda(simt_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s));
+}
+
+augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const void* kp, const void* vp,
+                                  const void* kr, const void* vr, const void* or_, const float* lse_r,
+                                  const void* dor, void* dqr, void* dkr, void* dvr, float* dkp_sum,
+                                  float* dvp_sum, void* ws, size_t ws_bytes, void* stream) {
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_resp > 0 && (!qr || !kr || !vr || !or_ || !lse_r || !dor || !dqr || !dkr || !dvr))
+    return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_prompt > 0 && (!dkp_sum || !dvp_sum)) return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_resp > 0 && p->total_prompt > 0 && (!kp || !vp)) return AUGTREE_ERR_INVALID_ARG;
+  BwdWorkspace w = replay_bwd_ws(p);
+  if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
+  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = (char*)ws;
+  float* delta = (float*)(base + w.delta_off);
+  float* dq_acc = (float*)(base + w.dq_off);
+  float* dk_part = (float*)(base + w.dkpart_off);
+  float* dv_part = (float*)(base + w.dvpart_off);
+  const int dt = p->cfg.dtype;
+  cudaError_t e = cudaSuccess;
+  if (p->total_resp > 0)
+    e = launch_preprocess(or_, dor, dt, p->total_resp, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
+  if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0) {
+    if (p->family == AUGTREE_KERNEL_TC)
+      e = tc_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
+                 dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
+    else
+      e = simt_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
+                   dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
+  }
+  if (e == cudaSuccess && p->total_prompt > 0) e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
+  if (e == cudaSuccess && p->total_resp > 0)
+    e = launch_dq_convert(dq_acc, dqr, dt, (int64_t)p->total_resp * p->cfg.hq * p->cfg.head_dim, s);
+  return from_cuda(e);
+}
+
+augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const void* kp, const void* vp,
+                                   const void* op, const float* lse_p, const void* dop, const float* dkp_acc,
+                                   const float* dvp_acc, void* dqp, void* dkp, void* dvp, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_prompt > 0 && (!qp || !kp || !vp || !op || !lse_p || !dop || !dqp || !dkp || !dvp))
+    return AUGTREE_ERR_INVALID_ARG;
+  if ((dkp_acc == nullptr) != (dvp_acc == nullptr)) return AUGTREE_ERR_INVALID_ARG;
+  BwdWorkspace w = prefill_bwd_ws(p);
+  if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
+  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  if (p->total_prompt == 0) return AUGTREE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = (char*)ws;
+  float* delta = (float*)(base + w.delta_off);
+  float* dq_acc = (float*)(base + w.dq_off);
+  const int dt = p->cfg.dtype;
+  cudaError_t e = launch_preprocess(op, dop, dt, p->total_prompt, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
+  if (e == cudaSuccess && p->n_items[AUGTREE_OP_PREFILL_BWD] > 0) {
+    if (p->family == AUGTREE_KERNEL_TC)
+      e = tc_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
+                 nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
+    else
+      e = simt_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
+                   nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
+  }
+  if (e == cudaSuccess)
+    e = launch_dq_convert(dq_acc, dqp, dt, (int64_t)p->total_prompt * p->cfg.hq * p->cfg.head_dim, s);
+  return from_cuda(e);
+}
+
+augtree_status augtree_plan_check(const augtree_plan* p, void* stream) {
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return AUGTREE_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpy(&w, p->err_d, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return AUGTREE_ERR_CUDA;
+  if (w != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(p->err_d, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return AUGTREE_ERR_CUDA;
+    return (w & 1u) ? AUGTREE_ERR_TIMEOUT : AUGTREE_ERR_DEVICE_CHECK;
+  }
+  return AUGTREE_OK;
+}
+
+augtree_status augtree_lse_merge(int64_t rows, int32_t h, int32_t d, const float* oa, const float* lse_a,
+                                 const float* ob, const float* lse_b, float* o, float* lse, void* stream) {
+  if (rows < 0 || h <= 0 || d <= 0) return AUGTREE_ERR_INVALID_ARG;
+  if (rows == 0) return AUGTREE_OK;
+  if (!oa || !lse_a || !ob || !lse_b || !o || !lse) return AUGTREE_ERR_INVALID_ARG;
+  return from_cuda(launch_lse_merge(rows, h, d, oa, lse_a, ob, lse_b, o, lse, (cudaStream_t)stream));
+}
+
+}  // extern "C"

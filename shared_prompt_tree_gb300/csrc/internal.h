@@ -1,0 +1,111 @@
+// Internal declarations shared by the host library and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/augtree.h"
+
+namespace augtree {
+
+enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3, K_PREFILL_KV = 4 };
+constexpr int kMaxSplit = 64;
+
+// Per-group geometry on the device: first prompt row, prompt length, first response
+// row, total response length of the group's branches.
+struct GroupInfo {
+  int32_t p0, lp, r0, lr;
+};
+
+// Per-group split-K bookkeeping of the replay backward (prompt dK/dV partials).
+struct SplitInfo {
+  int32_t nsplit;     // 0: group has no prompt-KV items; 1: written in place; >1: partials
+  int32_t pad;
+  int64_t part_row0;  // first row of the group's partial block in the workspace
+};
+
+// Pointers a kernel needs to interpret queue items.
+struct Geometry {
+  const GroupInfo* groups;    // [n_groups]
+  const int32_t* row_bstart;  // [total_resp] first response row of each row's branch
+  const SplitInfo* splits;    // [n_groups] (replay backward only)
+  int32_t hq, hkv, d;
+  int32_t total_prompt, total_resp;
+  float scale;                // softmax scale s
+  float scale_log2;           // s * log2(e)
+};
+
+}  // namespace augtree
+
+struct augtree_plan {
+  augtree_config cfg;
+  int device;
+  int family;  // AUGTREE_KERNEL_SIMT or AUGTREE_KERNEL_TC
+  int32_t n_groups, n_branches, total_prompt, total_resp;
+  int32_t bm[4], bn[4];
+  std::vector<augtree::GroupInfo> groups_h;
+  std::vector<augtree::SplitInfo> splits_h;
+  int64_t part_rows;  // rows of split partials (per dK and per dV), over all groups
+  std::vector<int32_t> queue_h[4];
+  size_t n_items[4];
+  // device copies
+  augtree::GroupInfo* groups_d;
+  int32_t* row_bstart_d;
+  int32_t* row_bend_d;  // [total_resp] one past the last response row of each row's branch
+  augtree::SplitInfo* splits_d;
+  int32_t* queue_d[4];
+  int paired[4];      // forward tensor-core units take two items (two heads of one KV head)
+  uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
+};
+
+namespace augtree {
+
+// Work-queue build shared by augtree_schedule_build and augtree_plan_create.
+augtree_status build_queue(const std::vector<int32_t>& prompt_off, const std::vector<int32_t>& branch_begin,
+                           const std::vector<int32_t>& resp_off, int hq, int hkv, int op, int bm, int bn,
+                           int num_sms, std::vector<int32_t>& out);
+
+// Workspace layout of the backward calls.
+struct BwdWorkspace {
+  size_t delta_off, dq_off, dkpart_off, dvpart_off, total;
+};
+BwdWorkspace replay_bwd_ws(const augtree_plan* p);
+BwdWorkspace prefill_bwd_ws(const augtree_plan* p);
+
+Geometry geometry(const augtree_plan* p);
+
+// 3-D TMA map over a [rows, heads, 128] bf16 tensor (box 64 x 1 x box_rows, 128-byte
+// swizzle, zero fill outside the tensor).
+bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads, int box_rows);
+
+// ---- launchers (return cudaGetLastError() of their launches) ---------------------
+// SIMT family (any dtype).
+cudaError_t simt_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
+                     const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);
+cudaError_t simt_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
+                     const void* kr, const void* vr, const float* lse, const void* dO,
+                     const float* delta, float* dq_acc, void* dk_out, void* dv_out,
+                     float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
+                     const float* dk_add, const float* dv_add, cudaStream_t st);
+// Tensor-core family (bf16).
+cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
+                   const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);
+cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
+                   const void* kr, const void* vr, const float* lse, const void* dO,
+                   const float* delta, float* dq_acc, void* dk_out, void* dv_out,
+                   float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
+                   const float* dk_add, const float* dv_add, cudaStream_t st);
+
+// Memory-bound helpers.
+cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d,
+                              float* delta, float* dq_acc, cudaStream_t st);
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int dtype, int64_t n, cudaStream_t st);
+cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, const float* dv_part,
+                                float* dk_sum, float* dv_sum, cudaStream_t st);
+cudaError_t launch_lse_merge(int64_t rows, int h, int d, const float* oa, const float* la,
+                             const float* ob, const float* lb, float* o, float* l, cudaStream_t st);
+
+}  // namespace augtree

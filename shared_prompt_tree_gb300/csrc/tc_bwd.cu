@@ -1,0 +1,473 @@
+// Tensor-core backward of tree attention on sm_103a (KV-stationary).
+//
+// AugTree paper, "Splitting Prompt Prefill from Response Replay ...":
+//   Sec. 3.2, Eq. 2  the prompt K/V gradient is the sum over all G branches of the
+//                    branch losses' gradients; it is accumulated and then sent back
+//                    through the prompt-prefill graph (prefill backward adds it);
+//   Sec. 3.3         MoveQ keeps prompt KV stationary and brings the queries of every
+//                    branch to it - on one GPU: a thread block owns one prompt K/V tile
+//                    and walks the response query tiles of all branches (split into a
+//                    few chunks when the prompt has few tiles; the chunks' partial sums
+//                    are reduced in a fixed order afterwards, no atomics).
+//
+// One thread block per work item: 128 keys of one KV head, query tiles [a, b) of 64
+// rows for each of the r query heads of that KV head.  Per query tile (keys are the
+// MMA M dimension, so P^T and dS^T come out with one key per TMEM lane):
+//   S^T  = K Q^T            (TMEM, fp32)   -> P^T  = exp2(s S^T log2e - lse)
+//   dP^T = V dO^T           (TMEM, fp32)   -> dS^T = P^T (dP^T - Delta)
+//   dV  += P^T dO           (A = P^T from TMEM, bf16)
+//   dK  += dS^T Q           (A = dS^T from TMEM, bf16)
+//   dQ^T = K^T dS^T         (B = dS^T from shared memory) -> fp32 reductions into the
+//                            dQ accumulator (one query row per instruction across d)
+// Warps: 0-3 softmax/dS (thread = key), 4-7 dQ epilogue (thread = head dim),
+//        8 TMA producer, 9 TMEM allocator + MMA issuer.
+// TMEM columns: S^T x2 [0,128) (P^T over it), dP^T [128,192) (dS^T over it),
+//               dQ^T [192,256), dV [256,384), dK [384,512).
+#include <cuda.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace augtree {
+namespace {
+
+using namespace tc;
+
+constexpr int BWD_THREADS = 320;
+constexpr int NQ = 2;                                   // Q/dO ring stages
+constexpr int KV_BLK = 128 * 128;                       // 128 rows x 64 dims bf16 = 16 KB
+constexpr int Q_BLK = 64 * 128;                         // 64 rows x 64 dims bf16 = 8 KB
+constexpr int K_OFF = 0;                                // 2 blocks
+constexpr int V_OFF = K_OFF + 2 * KV_BLK;               // 2 blocks
+constexpr int Q_OFF = V_OFF + 2 * KV_BLK;               // [NQ][2 blocks]
+constexpr int DO_OFF = Q_OFF + NQ * 2 * Q_BLK;          // [NQ][2 blocks]
+constexpr int DS_OFF = DO_OFF + NQ * 2 * Q_BLK;         // dS^T [128 keys x 64 q] bf16
+constexpr int ROWS_OFF = DS_OFF + KV_BLK;               // [NQ] x {lse2[64], delta[64]}
+constexpr int BAR_OFF = ROWS_OFF + NQ * 2 * 64 * 4;
+constexpr int BWD_SMEM = BAR_OFF + 256 + 1024;
+
+constexpr uint32_t T_ST = 0, T_DPT = 128, T_DQT = 192, T_DV = 256, T_DK = 384;
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t q_full[NQ];
+  uint64_t q_empty[NQ];
+  uint64_t s_full[2];
+  uint64_t dp_full;
+  uint64_t p_ready;
+  uint64_t ds_ready;
+  uint64_t dv_done;
+  uint64_t dk_done;
+  uint64_t dq_full;
+  uint64_t dq_free;
+  uint64_t acc_done;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2, Geometry geo,
+    const int32_t* __restrict__ queue, const int32_t* __restrict__ row_bend, int bm, int bn,
+    const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dq_acc,
+    __nv_bfloat16* __restrict__ dk_out, __nv_bfloat16* __restrict__ dv_out, float* __restrict__ dk_part,
+    float* __restrict__ dv_part, float* __restrict__ dk_sum, float* __restrict__ dv_sum,
+    const float* __restrict__ dk_add, const float* __restrict__ dv_add, uint32_t* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + BAR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const WorkItem it = load_item(queue, blockIdx.x);
+  const GroupInfo G = geo.groups[it.group];
+  const int r = geo.hq / geo.hkv;
+  const int kvh = it.head;
+  const bool resp_keys = it.kind == K_RESP_KV;
+  const bool prefill = it.kind == K_PREFILL_KV;
+  const int64_t kbase = resp_keys ? G.r0 : G.p0;
+  const int64_t key0 = kbase + (int64_t)it.tile * bn;
+  const int64_t key_end = min(key0 + (int64_t)bn, kbase + (int64_t)(resp_keys ? G.lr : G.lp));
+  const int64_t qbase = prefill ? G.p0 : G.r0;
+  const int64_t q_end = qbase + (prefill ? G.lp : G.lr);
+  const int64_t q_rows_total = prefill ? geo.total_prompt : geo.total_resp;
+  const int nqt = it.b - it.a;
+  const int n_iter = nqt * r;
+  // iteration i: query head kvh*r + i / nqt, query tile a + i % nqt
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(&bars->q_full[i], 1 + 32);
+      mbar_init(&bars->q_empty[i], 1);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, 128);
+    mbar_init(&bars->ds_ready, 128);
+    mbar_init(&bars->dv_done, 1);
+    mbar_init(&bars->dk_done, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->acc_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(resp_keys ? &tm_k2 : &tm_k);
+    prefetch_tmap(resp_keys ? &tm_v2 : &tm_v);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    bool ok = true;
+    if (lane == 0) {
+      const CUtensorMap* km = resp_keys ? &tm_k2 : &tm_k;
+      const CUtensorMap* vm = resp_keys ? &tm_v2 : &tm_v;
+      mbar_expect_tx(&bars->kv_full, 4 * KV_BLK);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_3d(smem + K_OFF + kb * KV_BLK, km, &bars->kv_full, kb * 64, kvh, (int)key0);
+        tma_load_3d(smem + V_OFF + kb * KV_BLK, vm, &bars->kv_full, kb * 64, kvh, (int)key0);
+      }
+    }
+    for (int i = 0; i < n_iter; ++i) {
+      const int stage = i % NQ, use = i / NQ;
+      if (lane == 0) ok = mbar_wait(&bars->q_empty[stage], (use & 1) ^ 1, err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int h = kvh * r + i / nqt;
+      const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
+      if (lane == 0) {
+        mbar_expect_tx(&bars->q_full[stage], 4 * Q_BLK);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * Q_BLK, &tm_q, &bars->q_full[stage], kb * 64, h, (int)row0);
+          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * Q_BLK, &tm_do, &bars->q_full[stage], kb * 64, h,
+                      (int)row0);
+        }
+      }
+      float* rows = reinterpret_cast<float*>(smem + ROWS_OFF) + stage * 128;
+      for (int c = lane; c < 64; c += 32) {
+        const int64_t row = row0 + c;
+        const bool v = row < q_end;
+        rows[c] = v ? lse[(int64_t)h * q_rows_total + row] * 1.4426950408889634f : 0.f;
+        rows[64 + c] = v ? delta[(int64_t)h * q_rows_total + row] : 0.f;
+      }
+      mbar_arrive(&bars->q_full[stage]);
+      issued = i + 1;
+    }
+    if (lane == 0) {
+      // Never leave a copy in flight.
+      mbar_wait(&bars->kv_full, 0, err);
+      for (int i = max(0, issued - NQ); i < issued; ++i) mbar_wait(&bars->q_full[i % NQ], (i / NQ) & 1, err);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);    // K Q^T, V dO^T
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, 128, false, true);  // P^T dO, dS^T Q (B MN-major)
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // K^T dS^T
+      const uint32_t k_addr = smem_u32(smem + K_OFF), v_addr = smem_u32(smem + V_OFF);
+      const uint32_t ds_addr = smem_u32(smem + DS_OFF);
+      bool ok = mbar_wait(&bars->kv_full, 0, err);
+      tc_fence_after();
+      auto issue_s = [&](int i) {  // S^T(i) -> ST[i % 2]
+        const int stage = i % NQ;
+        const uint32_t q_addr = smem_u32(smem + Q_OFF + stage * 2 * Q_BLK);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = smem_desc_sw128(k_addr + (kk >> 2) * KV_BLK + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = smem_desc_sw128(q_addr + (kk >> 2) * Q_BLK + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + T_ST + (i & 1) * 64, a, b, id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[i & 1]);
+      };
+      auto issue_dp = [&](int i) {  // dP^T(i) -> DPT
+        const int stage = i % NQ;
+        const uint32_t do_addr = smem_u32(smem + DO_OFF + stage * 2 * Q_BLK);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = smem_desc_sw128(v_addr + (kk >> 2) * KV_BLK + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = smem_desc_sw128(do_addr + (kk >> 2) * Q_BLK + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + T_DPT, a, b, id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->dp_full);
+      };
+      if (ok && n_iter > 0) {
+        ok = mbar_wait(&bars->q_full[0], 0, err);
+        tc_fence_after();
+        if (ok) {
+          issue_s(0);
+          issue_dp(0);
+        }
+      }
+      for (int i = 0; ok && i < n_iter; ++i) {
+        const int stage = i % NQ;
+        // S^T(i+1) into the other S buffer, whose P^T(i-1) must have been consumed.
+        if (i + 1 < n_iter) {
+          if (!(ok = mbar_wait(&bars->q_full[(i + 1) % NQ], ((i + 1) / NQ) & 1, err))) break;
+          if (i >= 1 && !(ok = mbar_wait(&bars->dv_done, (i - 1) & 1, err))) break;
+          tc_fence_after();
+          issue_s(i + 1);
+        }
+        const uint32_t q_addr = smem_u32(smem + Q_OFF + stage * 2 * Q_BLK);
+        const uint32_t do_addr = smem_u32(smem + DO_OFF + stage * 2 * Q_BLK);
+        // dV += P^T dO
+        if (!(ok = mbar_wait(&bars->p_ready, i & 1, err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t b = smem_desc_sw128(do_addr + kk * 2048, Q_BLK, 1024);
+          mma_ts(tmem + T_DV, tmem + T_ST + (i & 1) * 64 + kk * 8, b, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars->dv_done);
+        // dK += dS^T Q
+        if (!(ok = mbar_wait(&bars->ds_ready, i & 1, err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t b = smem_desc_sw128(q_addr + kk * 2048, Q_BLK, 1024);
+          mma_ts(tmem + T_DK, tmem + T_DPT + kk * 8, b, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars->dk_done);
+        // dQ^T = K^T dS^T, once the epilogue has read dQ^T(i-1)
+        if (i >= 1 && !(ok = mbar_wait(&bars->dq_free, (i - 1) & 1, err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = smem_desc_sw128(k_addr + kk * 2048, KV_BLK, 1024);
+          const uint64_t b = smem_desc_sw128(ds_addr + kk * 2048, KV_BLK, 1024);
+          mma_ss(tmem + T_DQT, a, b, id_dq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->dq_full);
+        mma_commit(&bars->q_empty[stage]);
+        // dP^T(i+1) overwrites dS^T(i) in TMEM: wait for dK(i).
+        if (i + 1 < n_iter) {
+          if (!(ok = mbar_wait(&bars->dk_done, i & 1, err))) break;
+          tc_fence_after();
+          issue_dp(i + 1);
+        }
+      }
+      mma_commit(&bars->acc_done);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T and dS^T
+    const int t = warp * 32 + lane;  // key row / TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int64_t key = key0 + t;
+    const bool key_ok = key < key_end;
+    // valid query rows for this key: [q_lo, q_hi)
+    int64_t q_lo = qbase, q_hi = q_end;
+    if (prefill) q_lo = key;
+    if (resp_keys) {
+      q_lo = key;
+      const int64_t be = key_ok ? (int64_t)row_bend[key] : key;
+      q_hi = be < q_end ? be : q_end;
+    }
+    if (!key_ok) q_hi = q_lo;
+    const float sl2 = geo.scale_log2;
+    bool ok = true;
+    uint8_t* ds_row = smem + DS_OFF + t * 128;
+    for (int i = 0; i < n_iter; ++i) {
+      const int stage = i % NQ;
+      const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
+      const float* rows = reinterpret_cast<const float*>(smem + ROWS_OFF) + stage * 128;
+      // rows[] (lse, Delta) of this stage are published by the producer with q_full.
+      if (!(ok = mbar_wait(&bars->q_full[stage], (i / NQ) & 1, err))) break;
+      if (!(ok = mbar_wait(&bars->s_full[i & 1], (i >> 1) & 1, err))) break;
+      tc_fence_after();
+      uint32_t sraw[2][32];
+      tmem_ld32(tmem + lane_off + T_ST + (i & 1) * 64, sraw[0]);
+      tmem_ld32(tmem + lane_off + T_ST + (i & 1) * 64 + 32, sraw[1]);
+      tmem_ld_wait();
+      const int64_t lo64 = q_lo - row0, hi64 = q_hi - row0;
+      const int lo = lo64 < 0 ? 0 : (lo64 > 64 ? 64 : (int)lo64);
+      const int hi = hi64 < 0 ? 0 : (hi64 > 64 ? 64 : (int)hi64);  // exclusive
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float sv = __uint_as_float(sraw[c >> 5][c & 31]);
+        const float e = fast_exp2(fmaf(sv, sl2, -rows[c]));
+        p[c] = (c >= lo && c < hi) ? e : 0.f;
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      tmem_st32(tmem + lane_off + T_ST + (i & 1) * 64, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      // dS^T = P^T (dP^T - Delta)
+      if (!(ok = mbar_wait(&bars->dp_full, i & 1, err))) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + T_DPT, sraw[0]);
+      tmem_ld32(tmem + lane_off + T_DPT + 32, sraw[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float d0 = p[2 * c] * (__uint_as_float(sraw[(2 * c) >> 5][(2 * c) & 31]) - rows[64 + 2 * c]);
+        const float d1 = p[2 * c + 1] * (__uint_as_float(sraw[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - rows[65 + 2 * c]);
+        pk[c] = pack_bf16x2(d0, d1);
+      }
+      tmem_st32(tmem + lane_off + T_DPT, pk);
+      // shared-memory copy for dQ^T = K^T dS^T, once dQ^T(i-1) has read the last one
+      if (i >= 1 && !(ok = mbar_wait(&bars->dq_full, (i - 1) & 1, err))) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const int pos = ch ^ (t & 7);  // 128-byte swizzle: 16-byte chunk index ^ row % 8
+        *reinterpret_cast<uint4*>(ds_row + pos * 16) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_ready);
+    }
+    // dV, dK rows of this key
+    if (ok && mbar_wait(&bars->acc_done, 0, err) && n_iter > 0) {
+      tc_fence_after();
+      const int64_t off = (key * geo.hkv + kvh) * 128;
+      float* fk = nullptr;
+      float* fv = nullptr;
+      int64_t foff = off;
+      if (it.kind == K_PROMPT_KV) {
+        const SplitInfo s = geo.splits[it.group];
+        fk = dk_sum;
+        fv = dv_sum;
+        if (s.nsplit > 1) {
+          fk = dk_part;
+          fv = dv_part;
+          foff = ((s.part_row0 + (int64_t)it.split * G.lp + (key - G.p0)) * geo.hkv + kvh) * 128;
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t kv[32], vv[32];
+        tmem_ld32(tmem + lane_off + T_DK + c * 32, kv);
+        tmem_ld32(tmem + lane_off + T_DV + c * 32, vv);
+        tmem_ld_wait();
+        if (!key_ok) continue;
+        float a[32], b[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          a[i] = __uint_as_float(kv[i]) * geo.scale;
+          b[i] = __uint_as_float(vv[i]);
+        }
+        if (fk) {
+          float4* pk4 = reinterpret_cast<float4*>(fk + foff + c * 32);
+          float4* pv4 = reinterpret_cast<float4*>(fv + foff + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            pk4[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+            pv4[i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+          }
+        } else {
+          if (dk_add) {
+            const float4* ak = reinterpret_cast<const float4*>(dk_add + off + c * 32);
+            const float4* av = reinterpret_cast<const float4*>(dv_add + off + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = ak[i], y = av[i];
+              a[4 * i] += x.x; a[4 * i + 1] += x.y; a[4 * i + 2] += x.z; a[4 * i + 3] += x.w;
+              b[4 * i] += y.x; b[4 * i + 1] += y.y; b[4 * i + 2] += y.z; b[4 * i + 3] += y.w;
+            }
+          }
+          uint4* ok4 = reinterpret_cast<uint4*>(dk_out + off + c * 32);
+          uint4* ov4 = reinterpret_cast<uint4*>(dv_out + off + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            ok4[i] = make_uint4(pack_bf16x2(a[8 * i], a[8 * i + 1]), pack_bf16x2(a[8 * i + 2], a[8 * i + 3]),
+                                pack_bf16x2(a[8 * i + 4], a[8 * i + 5]), pack_bf16x2(a[8 * i + 6], a[8 * i + 7]));
+            ov4[i] = make_uint4(pack_bf16x2(b[8 * i], b[8 * i + 1]), pack_bf16x2(b[8 * i + 2], b[8 * i + 3]),
+                                pack_bf16x2(b[8 * i + 4], b[8 * i + 5]), pack_bf16x2(b[8 * i + 6], b[8 * i + 7]));
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ epilogue
+    const int w4 = warp - 4;
+    const int dcol = w4 * 32 + lane;  // head-dim index = TMEM lane of dQ^T
+    const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
+    for (int i = 0; i < n_iter; ++i) {
+      if (!mbar_wait(&bars->dq_full, i & 1, err)) break;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(tmem + lane_off + T_DQT, v[0]);
+      tmem_ld32(tmem + lane_off + T_DQT + 32, v[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      const int h = kvh * r + i / nqt;
+      const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
+      const int64_t n64 = q_end - row0;
+      const int n = n64 > 64 ? 64 : (int)n64;
+      float* base = dq_acc + (row0 * geo.hq + h) * 128 + dcol;
+      const int64_t stride = (int64_t)geo.hq * 128;
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (c < n) red_add_f32(base + c * stride, __uint_as_float(v[c >> 5][c & 31]) * geo.scale);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
+                   const void* vr, const float* lse, const void* dO, const float* delta, float* dq_acc,
+                   void* dk_out, void* dv_out, float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
+                   const float* dk_add, const float* dv_add, cudaStream_t st) {
+  const bool prefill = op == AUGTREE_OP_PREFILL_BWD;
+  const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
+  CUtensorMap mq, mdo, mk, mv, mk2, mv2;
+  if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, 64)) return cudaErrorInvalidValue;
+  if (!encode_rows_map(&mdo, dO, q_rows, p->cfg.hq, 64)) return cudaErrorInvalidValue;
+  const bool have_p = p->total_prompt > 0 && kp && vp;
+  const bool have_r = !prefill && p->total_resp > 0 && kr && vr;
+  if (have_p) {
+    if (!encode_rows_map(&mk, kp, p->total_prompt, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+    if (!encode_rows_map(&mv, vp, p->total_prompt, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+  }
+  if (have_r) {
+    if (!encode_rows_map(&mk2, kr, p->total_resp, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+    if (!encode_rows_map(&mv2, vr, p->total_resp, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+  }
+  if (!have_p) {
+    mk = have_r ? mk2 : mq;
+    mv = have_r ? mv2 : mq;
+  }
+  if (!have_r) {
+    mk2 = mk;
+    mv2 = mv;
+  }
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
+  if (e != cudaSuccess) return e;
+  tc_bwd_kernel<<<(unsigned)p->n_items[op], BWD_THREADS, BWD_SMEM, st>>>(
+      mq, mdo, mk, mv, mk2, mv2, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op], lse, delta,
+      dq_acc, (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, dk_part, dv_part, dk_sum, dv_sum, dk_add, dv_add,
+      p->err_d);
+  return cudaGetLastError();
+}
+
+}  // namespace augtree
