@@ -47,7 +47,8 @@ extern "C" {
 typedef enum {
   AUGTREE_OK = 0,
   AUGTREE_ERR_INVALID_ARG = 1,          /* null pointer, bad offsets, bad sizes            */
-  AUGTREE_ERR_UNSUPPORTED = 2,          /* dtype, head_dim not in {64,128}, Hq % Hkv != 0 */
+  AUGTREE_ERR_UNSUPPORTED = 2,          /* dtype, head_dim not in {64,128}, Hq % Hkv != 0,
+                                           tensor cores asked for other than bf16, D=128 */
   AUGTREE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below augtree_plan_workspace_bytes    */
   AUGTREE_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed           */
   AUGTREE_ERR_DEVICE_CHECK = 5,         /* a kernel reported a failed internal check      */
@@ -58,7 +59,8 @@ typedef enum {
 typedef enum { AUGTREE_FP32 = 0, AUGTREE_BF16 = 1 } augtree_dtype;
 
 /* Kernel family: SIMT fp32-FMA kernels (any dtype; the only family for fp32) or the
- * tcgen05 tensor-core kernels (bf16 only).  AUTO picks tensor cores for bf16. */
+ * tcgen05 tensor-core kernels (bf16 with head_dim 128 only).  AUTO picks tensor
+ * cores for bf16 with head_dim 128, SIMT otherwise. */
 typedef enum { AUGTREE_KERNEL_AUTO = 0, AUGTREE_KERNEL_SIMT = 1, AUGTREE_KERNEL_TC = 2 } augtree_kernel;
 
 /* Operations, used to select a work queue or a workspace size. */
@@ -205,6 +207,12 @@ augtree_status augtree_prefill_bwd(const augtree_plan* plan, const void* qp, con
 augtree_status augtree_lse_merge(int64_t rows, int32_t h, int32_t d, const float* oa,
                                  const float* lse_a, const float* ob, const float* lse_b,
                                  float* o, float* lse, void* stream);
+
+/* Synchronizes `stream`, then reads and clears the plan's device error word.  Returns
+ * AUGTREE_ERR_TIMEOUT if a kernel launched with this plan gave up on a bounded
+ * device-side wait (it then skipped the rest of its work item and exited cleanly),
+ * AUGTREE_ERR_DEVICE_CHECK for any other recorded device-side failure, else OK. */
+augtree_status augtree_plan_check(const augtree_plan* plan, void* stream);
 
 const char* augtree_status_string(augtree_status s);
 
