@@ -19,7 +19,8 @@
 //   warps 0-7   two softmax warpgroups, one per query head; thread i owns row i
 //               (TMEM lane i): masks, running max with lazy rescaling of O (only
 //               when the max grows by more than 2^8), P = exp2(...) as bf16 back
-//               into TMEM over S, and the final O / l and lse.
+//               into TMEM over S, the row sum l of those bf16 values, and the final
+//               O / l and lse.
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,384), O1 [384,512).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -259,8 +260,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
           for (int i = 0; i < 32; ++i) {
             const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sl2, -mu));
             const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sl2, -mu));
-            psum += p0 + p1;
             pk[i] = pack_bf16x2(p0, p1);
+            // The denominator sums the bf16 values the PV product uses, so numerator
+            // and denominator carry the same rounded weights.
+            psum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
           }
           tmem_st32(tS + c * 32, pk);
         }
