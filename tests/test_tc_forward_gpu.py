@@ -28,12 +28,14 @@ def test_tc_forward_matches_oracle(cuda_device, ti, hq, hkv):
 
 
 def test_tc_forward_large_scores(cuda_device):
-    """Values scaled by 4: scores spread over a wide range, so the running max moves
-    by more than the lazy-rescale threshold and O is rescaled in TMEM."""
-    w = W.custom(TREES[4], hq=4, hkv=2, d=128, dtype="bf16", seed=77, scale=4.0)
+    """Q, K and V scaled by 4: scores spread 16x wider, so the running max moves by
+    more than the lazy-rescale threshold and O is rescaled in TMEM.  O is linear in V,
+    so O / 4 is held to the bound stated for unit-variance values."""
+    sc = 4.0
+    w = W.custom(TREES[4], hq=4, hkv=2, d=128, dtype="bf16", seed=77, scale=sc)
     got = run_cuda_fwd(w, kernel=at.KERNEL_TC)
     ref = run_oracle_fwd(w)
     for k in ("o_p", "o_r"):
-        assert np.max(np.abs(got[k] - ref[k])) <= 1e-2, k
+        assert np.max(np.abs(got[k] - ref[k])) / sc <= 1e-2, k
     for k in ("lse_p", "lse_r"):
         assert np.max(np.abs(got[k] - ref[k]) / np.maximum(1.0, np.abs(ref[k]))) <= 1e-2, k
