@@ -106,6 +106,24 @@ def useful_flops(w):
     return w.useful_flops(True, True)
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (the identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, ms_local: float, world: int, device=None):
+    """Whole-job rate of N independent replicas: every rank's units over the slowest
+    rank's time.  Returns (rate in units/s, max-over-ranks ms)."""
+    ms = max_over_ranks(ms_local, device)
+    return units_per_rank * world / (ms * 1e-3), ms
+
+
 # ---------------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle on a bounded sample of the workload's structure.
 # ---------------------------------------------------------------------------------
@@ -168,6 +186,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.workload(args.workload)
+    if args.scale_down > 1:
+        w = scaled_down(w, args.scale_down)
     kernel = {"auto": at.KERNEL_AUTO, "simt": at.KERNEL_SIMT, "tc": at.KERNEL_TC}[args.kernel]
     dt = at.BF16 if w.dtype == "bf16" else at.FP32
     plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt, kernel=kernel)
@@ -221,12 +241,8 @@ def run_ours(args):
     end.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        import torch.distributed as dist
-        x = torch.tensor([ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        ms = float(x.item())
+    plan.check()  # raises if any kernel of the step gave up on a bounded wait
+    ms = max_over_ranks(start.elapsed_time(end), dev)
     per_call = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(n_ev - 1)]
                          for k in range(args.steps)]).mean(0)
     ms_step = ms / args.steps
@@ -250,12 +266,7 @@ def run_ours(args):
             hx.copy_(x, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    if world > 1:
-        import torch.distributed as dist
-        x = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        e2e_ms = float(x.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
 
     flops = useful_flops(w)
     tokens = w.tokens
@@ -313,6 +324,13 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def scaled_down(w, k):
+    """The workload's structure with every length divided by k (profiling cases)."""
+    import workloads as W
+    tree = W.Tree([max(1, x // k) for x in w.tree.prompt_lens], [[max(1, x // k) for x in b] for b in w.tree.branch_lens])
+    return W.custom(tree, w.hq, w.hkv, w.d, w.dtype, w.seed, w.scale, name=f"{w.name}/{k}")
+
+
 def count_launches(plan, at):
     """Kernels one step launches: prefill fwd 1, replay fwd 1, replay bwd 4
     (preprocess, main, split reduce, dQ convert), prefill bwd 3."""
@@ -365,6 +383,7 @@ def main():
     ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scale-down", type=int, default=1, help="divide every length by this (profiling only)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

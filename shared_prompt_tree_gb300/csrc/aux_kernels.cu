@@ -30,6 +30,56 @@ __global__ void preprocess_kernel(const T* __restrict__ o, const T* __restrict__
   for (int c = lane; c < d; c += 32) dq_acc[base + c] = 0.f;
 }
 
+// One block (4 warps) per (64-row query tile, head); tiles of all groups are numbered
+// consecutively (GroupInfo::tp0 / tr0).  Writes stats[h][tile] = {lse*log2e [64],
+// Delta [64]} with zeros for rows past the group's end, and zeroes the valid rows'
+// dQ accumulator for head h.
+__global__ void preprocess_tiled_kernel(const GroupInfo* __restrict__ groups, int n_groups, bool prompt_side,
+                                        int ntiles, const __nv_bfloat16* __restrict__ o,
+                                        const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
+                                        int64_t rows_total, int hq, float* __restrict__ stats,
+                                        float* __restrict__ dq_acc) {
+  const int tile = blockIdx.x;
+  const int h = blockIdx.y;
+  // group holding this tile: last group whose first tile is <= tile and that has tiles
+  int lo = 0, hi = n_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int t0 = prompt_side ? groups[mid].tp0 : groups[mid].tr0;
+    if (t0 <= tile) lo = mid; else hi = mid - 1;
+  }
+  const GroupInfo G = groups[lo];
+  const int64_t base = prompt_side ? G.p0 : G.r0;
+  const int64_t len = prompt_side ? G.lp : G.lr;
+  const int64_t row0 = base + (int64_t)(tile - (prompt_side ? G.tp0 : G.tr0)) * kStatRows;
+  float* out = stats + ((int64_t)h * ntiles + tile) * 2 * kStatRows;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < kStatRows; r += 4) {
+    const int64_t row = row0 + r;
+    float dl = 0.f, l2 = 0.f;
+    if (row < base + len) {
+      const int64_t off = (row * hq + h) * 128 + lane * 4;
+      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+      const uint2 b = *reinterpret_cast<const uint2*>(dO + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float2 x = __bfloat1622float2(a2[i]), y = __bfloat1622float2(b2[i]);
+        acc += x.x * y.x + x.y * y.y;
+      }
+      dl = warp_sum(acc);
+      l2 = lse[(int64_t)h * rows_total + row] * 1.4426950408889634f;
+      *reinterpret_cast<float4*>(dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (lane == 0) {
+      out[r] = l2;
+      out[kStatRows + r] = dl;
+    }
+  }
+}
+
 template <typename T>
 __global__ void convert_kernel(const float* __restrict__ src, T* __restrict__ dst, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
@@ -124,6 +174,18 @@ cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t 
   else
     preprocess_kernel<float><<<(unsigned)blocks, threads, 0, st>>>((const float*)o, (const float*)dO, rows, hq, d,
                                                                    delta, dq_acc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess_tiled(const augtree_plan* p, bool prompt_side, const void* o, const void* dO,
+                                    const float* lse, float* stats, float* dq_acc, cudaStream_t st) {
+  const int ntiles = prompt_side ? p->ntiles_p : p->ntiles_r;
+  if (ntiles == 0) return cudaSuccess;
+  dim3 grid(ntiles, p->cfg.hq);
+  preprocess_tiled_kernel<<<grid, 128, 0, st>>>(p->groups_d, p->n_groups, prompt_side, ntiles,
+                                                (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, lse,
+                                                prompt_side ? p->total_prompt : p->total_resp, p->cfg.hq, stats,
+                                                dq_acc);
   return cudaGetLastError();
 }
 

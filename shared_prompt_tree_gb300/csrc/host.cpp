@@ -207,11 +207,20 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   return AUGTREE_OK;
 }
 
+// Row statistics of the backward: SIMT kernels read Delta [Hq, rows]; tensor-core
+// kernels read tiles of {lse * log2(e), Delta} [Hq, tiles, 2 x 64] (one bulk copy each).
+static size_t stats_bytes(const augtree_plan* p, bool prompt_side) {
+  const size_t hq = p->cfg.hq;
+  if (p->family == AUGTREE_KERNEL_TC)
+    return hq * (size_t)(prompt_side ? p->ntiles_p : p->ntiles_r) * 2 * kStatRows * 4;
+  return hq * (size_t)(prompt_side ? p->total_prompt : p->total_resp) * 4;
+}
+
 BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
   BwdWorkspace w;
   const size_t hq = p->cfg.hq, hkv = p->cfg.hkv, d = p->cfg.head_dim, R = p->total_resp;
   w.delta_off = 0;
-  w.dq_off = align256(hq * R * 4);
+  w.dq_off = align256(stats_bytes(p, false));
   w.dkpart_off = w.dq_off + align256(R * hq * d * 4);
   w.dvpart_off = w.dkpart_off + align256((size_t)p->part_rows * hkv * d * 4);
   w.total = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
@@ -222,7 +231,7 @@ BwdWorkspace prefill_bwd_ws(const augtree_plan* p) {
   BwdWorkspace w;
   const size_t hq = p->cfg.hq, d = p->cfg.head_dim, P = p->total_prompt;
   w.delta_off = 0;
-  w.dq_off = align256(hq * P * 4);
+  w.dq_off = align256(stats_bytes(p, true));
   w.dkpart_off = w.dvpart_off = w.dq_off + align256(P * hq * d * 4);
   w.total = w.dkpart_off;
   return w;
@@ -353,7 +362,14 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   p->groups_h.resize(p->n_groups);
   for (int g = 0; g < p->n_groups; ++g)
     p->groups_h[g] = GroupInfo{(int32_t)groups[g].p0, (int32_t)groups[g].lp, (int32_t)groups[g].r0,
-                               (int32_t)groups[g].lr};
+                               (int32_t)groups[g].lr, 0, 0};
+  p->ntiles_p = p->ntiles_r = 0;
+  for (int g = 0; g < p->n_groups; ++g) {
+    p->groups_h[g].tp0 = p->ntiles_p;
+    p->groups_h[g].tr0 = p->ntiles_r;
+    p->ntiles_p += (int32_t)cdiv(p->groups_h[g].lp, kStatRows);
+    p->ntiles_r += (int32_t)cdiv(p->groups_h[g].lr, kStatRows);
+  }
   std::vector<int32_t> bstart(std::max(1, p->total_resp)), bend(std::max(1, p->total_resp));
   for (int b = 0; b < p->n_branches; ++b)
     for (int32_t row = ro[b]; row < ro[b + 1]; ++row) {
@@ -517,12 +533,14 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
   float* dv_part = (float*)(base + w.dvpart_off);
   const int dt = p->cfg.dtype;
   cudaError_t e = cudaSuccess;
+  const bool tc = p->family == AUGTREE_KERNEL_TC;
   if (p->total_resp > 0)
-    e = launch_preprocess(or_, dor, dt, p->total_resp, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
+    e = tc ? launch_preprocess_tiled(p, false, or_, dor, lse_r, delta, dq_acc, s)
+           : launch_preprocess(or_, dor, dt, p->total_resp, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
   if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0) {
-    if (p->family == AUGTREE_KERNEL_TC)
-      e = tc_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
-                 dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
+    if (tc)
+      e = tc_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dq_acc, dkr, dvr, dk_part, dv_part,
+                 dkp_sum, dvp_sum, nullptr, nullptr, s);
     else
       e = simt_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
                    dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
@@ -552,11 +570,13 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
   float* delta = (float*)(base + w.delta_off);
   float* dq_acc = (float*)(base + w.dq_off);
   const int dt = p->cfg.dtype;
-  cudaError_t e = launch_preprocess(op, dop, dt, p->total_prompt, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
+  const bool tc = p->family == AUGTREE_KERNEL_TC;
+  cudaError_t e = tc ? launch_preprocess_tiled(p, true, op, dop, lse_p, delta, dq_acc, s)
+                     : launch_preprocess(op, dop, dt, p->total_prompt, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
   if (e == cudaSuccess && p->n_items[AUGTREE_OP_PREFILL_BWD] > 0) {
-    if (p->family == AUGTREE_KERNEL_TC)
-      e = tc_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
-                 nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
+    if (tc)
+      e = tc_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dq_acc, dkp, dvp, nullptr,
+                 nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
     else
       e = simt_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
                    nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);

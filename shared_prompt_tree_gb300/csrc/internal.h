@@ -15,10 +15,14 @@ enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3,
 constexpr int kMaxSplit = 64;
 
 // Per-group geometry on the device: first prompt row, prompt length, first response
-// row, total response length of the group's branches.
+// row, total response length of the group's branches, and the group's first 64-row
+// query tile on the prompt side and on the response side in the tiled backward
+// row-statistics buffer (tensor-core family).
 struct GroupInfo {
   int32_t p0, lp, r0, lr;
+  int32_t tp0, tr0;
 };
+constexpr int kStatRows = 64;  // rows per tile of the backward row-statistics buffer
 
 // Per-group split-K bookkeeping of the replay backward (prompt dK/dV partials).
 struct SplitInfo {
@@ -58,6 +62,7 @@ struct augtree_plan {
   augtree::SplitInfo* splits_d;
   int32_t* queue_d[4];
   int paired[4];      // forward tensor-core units take two items (two heads of one KV head)
+  int32_t ntiles_p, ntiles_r;  // 64-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
 };
 
@@ -80,6 +85,8 @@ Geometry geometry(const augtree_plan* p);
 // 3-D TMA map over a [rows, heads, 128] bf16 tensor (box 64 x 1 x box_rows, 128-byte
 // swizzle, zero fill outside the tensor).
 bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads, int box_rows);
+// Same over a [rows, heads, 128] fp32 tensor, box 128 x 1 x box_rows, no swizzle.
+bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads, int box_rows);
 
 // ---- launchers (return cudaGetLastError() of their launches) ---------------------
 // SIMT family (any dtype).
@@ -94,14 +101,17 @@ cudaError_t simt_bwd(const augtree_plan* p, int op, const void* q, const void* k
 cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
                    const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);
 cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
-                   const void* kr, const void* vr, const float* lse, const void* dO,
-                   const float* delta, float* dq_acc, void* dk_out, void* dv_out,
+                   const void* kr, const void* vr, const float* stats, const void* dO, float* dq_acc, void* dk_out, void* dv_out,
                    float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
                    const float* dk_add, const float* dv_add, cudaStream_t st);
 
 // Memory-bound helpers.
 cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d,
                               float* delta, float* dq_acc, cudaStream_t st);
+// Tensor-core backward preprocess: per (64-row query tile, head) writes 512 bytes
+// {lse * log2(e) [64], Delta [64]} (zeros past the group's end) and zeroes dQ_acc.
+cudaError_t launch_preprocess_tiled(const augtree_plan* p, bool prompt_side, const void* o, const void* dO,
+                                    const float* lse, float* stats, float* dq_acc, cudaStream_t st);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int dtype, int64_t n, cudaStream_t st);
 cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, const float* dv_part,
                                 float* dk_sum, float* dv_sum, cudaStream_t st);

@@ -16,13 +16,16 @@
 //   S^T  = K Q^T            (TMEM, fp32)   -> P^T  = exp2(s S^T log2e - lse)
 //   dP^T = V dO^T           (TMEM, fp32)   -> dS^T = P^T (dP^T - Delta)
 //   dV  += P^T dO           (A = P^T from TMEM, bf16)
-//   dK  += dS^T Q           (A = dS^T from TMEM, bf16)
-//   dQ^T = K^T dS^T         (B = dS^T from shared memory) -> fp32 reductions into the
-//                            dQ accumulator (one query row per instruction across d)
+//   dK  += dS^T Q           (A = dS^T from shared memory, K-major)
+//   dQ^T = K^T dS^T         (B = the same dS^T tile, MN-major) -> staged in shared
+//                            memory as two [32 rows x 128 dims] fp32 halves, each
+//                            added to the dQ accumulator with one TMA bulk reduce-add
+// dS^T lives in two shared-memory buffers (128-byte swizzle), so dP^T(i+1) can be
+// computed as soon as dP^T(i) has been read out of TMEM.
 // Warps: 0-3 softmax/dS (thread = key), 4-7 dQ epilogue (thread = head dim),
 //        8 TMA producer, 9 TMEM allocator + MMA issuer.
-// TMEM columns: S^T x2 [0,128) (P^T over it), dP^T [128,192) (dS^T over it),
-//               dQ^T [192,256), dV [256,384), dK [384,512).
+// TMEM columns: S^T x2 [0,128) (P^T over it), dP^T [128,192), dQ^T [192,256),
+//               dV [256,384), dK [384,512).
 #include <cuda.h>
 
 #include <cmath>
@@ -36,15 +39,17 @@ namespace {
 using namespace tc;
 
 constexpr int BWD_THREADS = 320;
-constexpr int NQ = 2;                                   // Q/dO ring stages
+constexpr int NQ = 3;                                   // Q/dO ring stages
 constexpr int KV_BLK = 128 * 128;                       // 128 rows x 64 dims bf16 = 16 KB
 constexpr int Q_BLK = 64 * 128;                         // 64 rows x 64 dims bf16 = 8 KB
 constexpr int K_OFF = 0;                                // 2 blocks
 constexpr int V_OFF = K_OFF + 2 * KV_BLK;               // 2 blocks
 constexpr int Q_OFF = V_OFF + 2 * KV_BLK;               // [NQ][2 blocks]
 constexpr int DO_OFF = Q_OFF + NQ * 2 * Q_BLK;          // [NQ][2 blocks]
-constexpr int DS_OFF = DO_OFF + NQ * 2 * Q_BLK;         // dS^T [128 keys x 64 q] bf16
-constexpr int ROWS_OFF = DS_OFF + KV_BLK;               // [NQ] x {lse2[64], delta[64]}
+constexpr int DS_OFF = DO_OFF + NQ * 2 * Q_BLK;         // [2] dS^T [128 keys x 64 q] bf16
+constexpr int DQ_OFF = DS_OFF + 2 * KV_BLK;             // dQ half tile [32 q x 128 d] fp32
+constexpr int DQ_BYTES = 32 * 128 * 4;
+constexpr int ROWS_OFF = DQ_OFF + DQ_BYTES;             // [NQ] x {lse2[64], delta[64]}
 constexpr int BAR_OFF = ROWS_OFF + NQ * 2 * 64 * 4;
 constexpr int BWD_SMEM = BAR_OFF + 256 + 1024;
 
@@ -56,10 +61,13 @@ struct BwdBars {
   uint64_t q_empty[NQ];
   uint64_t s_full[2];
   uint64_t dp_full;
-  uint64_t p_ready;
-  uint64_t ds_ready;
+  uint64_t dp_free;
+  // Per-buffer signals: the softmax warps may run one query tile ahead of the MMA
+  // issuer, so a single barrier could complete two phases before its waiter looks.
+  uint64_t p_ready[2];
+  uint64_t ds_ready[2];
+  uint64_t ds_free[2];
   uint64_t dv_done;
-  uint64_t dk_done;
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t acc_done;
@@ -70,16 +78,34 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+// dQ tile [64 rows x 128 dims] fp32 in shared memory added to the global accumulator.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2, Geometry geo,
+    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2,
+    const __grid_constant__ CUtensorMap tm_dq, Geometry geo,
     const int32_t* __restrict__ queue, const int32_t* __restrict__ row_bend, int bm, int bn,
-    const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dq_acc,
+    const float* __restrict__ stats, int ntiles,
     __nv_bfloat16* __restrict__ dk_out, __nv_bfloat16* __restrict__ dv_out, float* __restrict__ dk_part,
     float* __restrict__ dv_part, float* __restrict__ dk_sum, float* __restrict__ dv_sum,
     const float* __restrict__ dk_add, const float* __restrict__ dv_add, uint32_t* __restrict__ err) {
@@ -107,16 +133,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < NQ; ++i) {
-      mbar_init(&bars->q_full[i], 1 + 32);
+      mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
     }
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, 128);
-    mbar_init(&bars->ds_ready, 128);
+    mbar_init(&bars->dp_free, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->p_ready[b], 128);
+      mbar_init(&bars->ds_ready[b], 128);
+      mbar_init(&bars->ds_free[b], 1);
+    }
     mbar_init(&bars->dv_done, 1);
-    mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->acc_done, 1);
@@ -128,6 +157,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     prefetch_tmap(&tm_do);
     prefetch_tmap(resp_keys ? &tm_k2 : &tm_k);
     prefetch_tmap(resp_keys ? &tm_v2 : &tm_v);
+    prefetch_tmap(&tm_dq);
   }
   __syncthreads();
   tc_fence_after();
@@ -146,29 +176,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         tma_load_3d(smem + V_OFF + kb * KV_BLK, vm, &bars->kv_full, kb * 64, kvh, (int)key0);
       }
     }
-    for (int i = 0; i < n_iter; ++i) {
+    const int tile_base = prefill ? G.tp0 : G.tr0;
+    for (int i = 0; i < n_iter && lane == 0; ++i) {
       const int stage = i % NQ, use = i / NQ;
-      if (lane == 0) ok = mbar_wait(&bars->q_empty[stage], (use & 1) ^ 1, err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!(ok = mbar_wait(&bars->q_empty[stage], (use & 1) ^ 1, err))) break;
       const int h = kvh * r + i / nqt;
-      const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
-      if (lane == 0) {
-        mbar_expect_tx(&bars->q_full[stage], 4 * Q_BLK);
-        for (int kb = 0; kb < 2; ++kb) {
-          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * Q_BLK, &tm_q, &bars->q_full[stage], kb * 64, h, (int)row0);
-          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * Q_BLK, &tm_do, &bars->q_full[stage], kb * 64, h,
-                      (int)row0);
-        }
+      const int qt = it.a + i % nqt;
+      const int64_t row0 = qbase + (int64_t)qt * bm;
+      mbar_expect_tx(&bars->q_full[stage], 4 * Q_BLK + 2 * kStatRows * 4);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * Q_BLK, &tm_q, &bars->q_full[stage], kb * 64, h, (int)row0);
+        tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * Q_BLK, &tm_do, &bars->q_full[stage], kb * 64, h, (int)row0);
       }
-      float* rows = reinterpret_cast<float*>(smem + ROWS_OFF) + stage * 128;
-      for (int c = lane; c < 64; c += 32) {
-        const int64_t row = row0 + c;
-        const bool v = row < q_end;
-        rows[c] = v ? lse[(int64_t)h * q_rows_total + row] * 1.4426950408889634f : 0.f;
-        rows[64 + c] = v ? delta[(int64_t)h * q_rows_total + row] : 0.f;
-      }
-      mbar_arrive(&bars->q_full[stage]);
+      // {lse * log2(e), Delta} of the tile's 64 rows: one 512-byte bulk copy.
+      bulk_load(smem + ROWS_OFF + stage * 2 * kStatRows * 4,
+                stats + ((int64_t)h * ntiles + tile_base + qt) * 2 * kStatRows, 2 * kStatRows * 4,
+                &bars->q_full[stage]);
       issued = i + 1;
     }
     if (lane == 0) {
@@ -183,12 +206,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       constexpr uint32_t id_acc = idesc_bf16_f32(128, 128, false, true);  // P^T dO, dS^T Q (B MN-major)
       constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // K^T dS^T
       const uint32_t k_addr = smem_u32(smem + K_OFF), v_addr = smem_u32(smem + V_OFF);
-      const uint32_t ds_addr = smem_u32(smem + DS_OFF);
+      const uint32_t ds_addr0 = smem_u32(smem + DS_OFF);
       bool ok = mbar_wait(&bars->kv_full, 0, err);
       tc_fence_after();
       auto issue_s = [&](int i) {  // S^T(i) -> ST[i % 2]
-        const int stage = i % NQ;
-        const uint32_t q_addr = smem_u32(smem + Q_OFF + stage * 2 * Q_BLK);
+        const uint32_t q_addr = smem_u32(smem + Q_OFF + (i % NQ) * 2 * Q_BLK);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t a = smem_desc_sw128(k_addr + (kk >> 2) * KV_BLK + (kk & 3) * 32, 16, 1024);
@@ -198,8 +220,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         mma_commit(&bars->s_full[i & 1]);
       };
       auto issue_dp = [&](int i) {  // dP^T(i) -> DPT
-        const int stage = i % NQ;
-        const uint32_t do_addr = smem_u32(smem + DO_OFF + stage * 2 * Q_BLK);
+        const uint32_t do_addr = smem_u32(smem + DO_OFF + (i % NQ) * 2 * Q_BLK);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t a = smem_desc_sw128(v_addr + (kk >> 2) * KV_BLK + (kk & 3) * 32, 16, 1024);
@@ -218,8 +239,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       }
       for (int i = 0; ok && i < n_iter; ++i) {
         const int stage = i % NQ;
-        // S^T(i+1) into the other S buffer, whose P^T(i-1) must have been consumed.
-        if (i + 1 < n_iter) {
+        const bool more = i + 1 < n_iter;
+        // S^T(i+1) into the other S buffer, once dV(i-1) has consumed its P^T(i-1).
+        if (more) {
           if (!(ok = mbar_wait(&bars->q_full[(i + 1) % NQ], ((i + 1) / NQ) & 1, err))) break;
           if (i >= 1 && !(ok = mbar_wait(&bars->dv_done, (i - 1) & 1, err))) break;
           tc_fence_after();
@@ -228,7 +250,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         const uint32_t q_addr = smem_u32(smem + Q_OFF + stage * 2 * Q_BLK);
         const uint32_t do_addr = smem_u32(smem + DO_OFF + stage * 2 * Q_BLK);
         // dV += P^T dO
-        if (!(ok = mbar_wait(&bars->p_ready, i & 1, err))) break;
+        if (!(ok = mbar_wait(&bars->p_ready[i & 1], (i >> 1) & 1, err))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -236,16 +258,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
           mma_ts(tmem + T_DV, tmem + T_ST + (i & 1) * 64 + kk * 8, b, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->dv_done);
-        // dK += dS^T Q
-        if (!(ok = mbar_wait(&bars->ds_ready, i & 1, err))) break;
+        // dP^T(i+1) as soon as dP^T(i) has been read out of TMEM
+        if (more) {
+          if (!(ok = mbar_wait(&bars->dp_free, i & 1, err))) break;
+          tc_fence_after();
+          issue_dp(i + 1);
+        }
+        // dK += dS^T Q ; dQ^T = K^T dS^T  (dS^T from shared-memory buffer i % 2)
+        if (!(ok = mbar_wait(&bars->ds_ready[i & 1], (i >> 1) & 1, err))) break;
         tc_fence_after();
+        const uint32_t ds_addr = ds_addr0 + (i & 1) * KV_BLK;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = smem_desc_sw128(ds_addr + kk * 32, 16, 1024);
           const uint64_t b = smem_desc_sw128(q_addr + kk * 2048, Q_BLK, 1024);
-          mma_ts(tmem + T_DK, tmem + T_DPT + kk * 8, b, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ss(tmem + T_DK, a, b, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bars->dk_done);
-        // dQ^T = K^T dS^T, once the epilogue has read dQ^T(i-1)
         if (i >= 1 && !(ok = mbar_wait(&bars->dq_free, (i - 1) & 1, err))) break;
         tc_fence_after();
 #pragma unroll
@@ -255,13 +283,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
           mma_ss(tmem + T_DQT, a, b, id_dq, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dq_full);
+        mma_commit(&bars->ds_free[i & 1]);
         mma_commit(&bars->q_empty[stage]);
-        // dP^T(i+1) overwrites dS^T(i) in TMEM: wait for dK(i).
-        if (i + 1 < n_iter) {
-          if (!(ok = mbar_wait(&bars->dk_done, i & 1, err))) break;
-          tc_fence_after();
-          issue_dp(i + 1);
-        }
       }
       mma_commit(&bars->acc_done);
     }
@@ -282,7 +305,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     if (!key_ok) q_hi = q_lo;
     const float sl2 = geo.scale_log2;
     bool ok = true;
-    uint8_t* ds_row = smem + DS_OFF + t * 128;
     for (int i = 0; i < n_iter; ++i) {
       const int stage = i % NQ;
       const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
@@ -298,35 +320,37 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       const int64_t lo64 = q_lo - row0, hi64 = q_hi - row0;
       const int lo = lo64 < 0 ? 0 : (lo64 > 64 ? 64 : (int)lo64);
       const int hi = hi64 < 0 ? 0 : (hi64 > 64 ? 64 : (int)hi64);  // exclusive
-      float p[64];
+      uint32_t pk[32];  // P^T as bf16 pairs: A operand of dV and the P factor of dS
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float sv = __uint_as_float(sraw[c >> 5][c & 31]);
-        const float e = fast_exp2(fmaf(sv, sl2, -rows[c]));
-        p[c] = (c >= lo && c < hi) ? e : 0.f;
+      for (int c = 0; c < 32; ++c) {
+        const int c0 = 2 * c, c1 = 2 * c + 1;
+        const float e0 = fast_exp2(fmaf(__uint_as_float(sraw[c0 >> 5][c0 & 31]), sl2, -rows[c0]));
+        const float e1 = fast_exp2(fmaf(__uint_as_float(sraw[c1 >> 5][c1 & 31]), sl2, -rows[c1]));
+        pk[c] = pack_bf16x2((c0 >= lo && c0 < hi) ? e0 : 0.f, (c1 >= lo && c1 < hi) ? e1 : 0.f);
       }
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
       tmem_st32(tmem + lane_off + T_ST + (i & 1) * 64, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_ready);
-      // dS^T = P^T (dP^T - Delta)
+      mbar_arrive(&bars->p_ready[i & 1]);
+      // dS^T = P^T (dP^T - Delta), with the same bf16 P the dV product uses
       if (!(ok = mbar_wait(&bars->dp_full, i & 1, err))) break;
       tc_fence_after();
       tmem_ld32(tmem + lane_off + T_DPT, sraw[0]);
       tmem_ld32(tmem + lane_off + T_DPT + 32, sraw[1]);
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->dp_free);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float d0 = p[2 * c] * (__uint_as_float(sraw[(2 * c) >> 5][(2 * c) & 31]) - rows[64 + 2 * c]);
-        const float d1 = p[2 * c + 1] * (__uint_as_float(sraw[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - rows[65 + 2 * c]);
+        const int c0 = 2 * c, c1 = 2 * c + 1;
+        const float p0 = __uint_as_float(pk[c] << 16), p1 = __uint_as_float(pk[c] & 0xFFFF0000u);
+        const float d0 = p0 * (__uint_as_float(sraw[c0 >> 5][c0 & 31]) - rows[64 + c0]);
+        const float d1 = p1 * (__uint_as_float(sraw[c1 >> 5][c1 & 31]) - rows[64 + c1]);
         pk[c] = pack_bf16x2(d0, d1);
       }
-      tmem_st32(tmem + lane_off + T_DPT, pk);
-      // shared-memory copy for dQ^T = K^T dS^T, once dQ^T(i-1) has read the last one
-      if (i >= 1 && !(ok = mbar_wait(&bars->dq_full, (i - 1) & 1, err))) break;
+      // dS^T row into buffer i % 2, once dK(i-2) and dQ^T(i-2) have read that buffer
+      if (i >= 2 && !(ok = mbar_wait(&bars->ds_free[i & 1], ((i >> 1) - 1) & 1, err))) break;
+      uint8_t* ds_row = smem + DS_OFF + (i & 1) * KV_BLK + t * 128;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         const int pos = ch ^ (t & 7);  // 128-byte swizzle: 16-byte chunk index ^ row % 8
@@ -334,9 +358,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       }
       fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_ready);
+      mbar_arrive(&bars->ds_ready[i & 1]);
     }
     // dV, dK rows of this key
     if (ok && mbar_wait(&bars->acc_done, 0, err) && n_iter > 0) {
@@ -362,39 +384,42 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         tmem_ld32(tmem + lane_off + T_DV + c * 32, vv);
         tmem_ld_wait();
         if (!key_ok) continue;
-        float a[32], b[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          a[i] = __uint_as_float(kv[i]) * geo.scale;
-          b[i] = __uint_as_float(vv[i]);
-        }
+        for (int i = 0; i < 32; ++i) kv[i] = __float_as_uint(__uint_as_float(kv[i]) * geo.scale);
         if (fk) {
           float4* pk4 = reinterpret_cast<float4*>(fk + foff + c * 32);
           float4* pv4 = reinterpret_cast<float4*>(fv + foff + c * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            pk4[i] = make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-            pv4[i] = make_float4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+            pk4[i] = make_float4(__uint_as_float(kv[4 * i]), __uint_as_float(kv[4 * i + 1]),
+                                 __uint_as_float(kv[4 * i + 2]), __uint_as_float(kv[4 * i + 3]));
+            pv4[i] = make_float4(__uint_as_float(vv[4 * i]), __uint_as_float(vv[4 * i + 1]),
+                                 __uint_as_float(vv[4 * i + 2]), __uint_as_float(vv[4 * i + 3]));
           }
         } else {
-          if (dk_add) {
-            const float4* ak = reinterpret_cast<const float4*>(dk_add + off + c * 32);
-            const float4* av = reinterpret_cast<const float4*>(dv_add + off + c * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 x = ak[i], y = av[i];
-              a[4 * i] += x.x; a[4 * i + 1] += x.y; a[4 * i + 2] += x.z; a[4 * i + 3] += x.w;
-              b[4 * i] += y.x; b[4 * i + 1] += y.y; b[4 * i + 2] += y.z; b[4 * i + 3] += y.w;
-            }
-          }
           uint4* ok4 = reinterpret_cast<uint4*>(dk_out + off + c * 32);
           uint4* ov4 = reinterpret_cast<uint4*>(dv_out + off + c * 32);
+          const float4* ak = reinterpret_cast<const float4*>(dk_add + off + c * 32);
+          const float4* av = reinterpret_cast<const float4*>(dv_add + off + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            ok4[i] = make_uint4(pack_bf16x2(a[8 * i], a[8 * i + 1]), pack_bf16x2(a[8 * i + 2], a[8 * i + 3]),
-                                pack_bf16x2(a[8 * i + 4], a[8 * i + 5]), pack_bf16x2(a[8 * i + 6], a[8 * i + 7]));
-            ov4[i] = make_uint4(pack_bf16x2(b[8 * i], b[8 * i + 1]), pack_bf16x2(b[8 * i + 2], b[8 * i + 3]),
-                                pack_bf16x2(b[8 * i + 4], b[8 * i + 5]), pack_bf16x2(b[8 * i + 6], b[8 * i + 7]));
+            float a[8], b[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              a[e] = __uint_as_float(kv[8 * i + e]);
+              b[e] = __uint_as_float(vv[8 * i + e]);
+            }
+            if (dk_add) {
+              const float4 x0 = ak[2 * i], x1 = ak[2 * i + 1], y0 = av[2 * i], y1 = av[2 * i + 1];
+              a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w;
+              a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
+              b[0] += y0.x; b[1] += y0.y; b[2] += y0.z; b[3] += y0.w;
+              b[4] += y1.x; b[5] += y1.y; b[6] += y1.z; b[7] += y1.w;
+            }
+            ok4[i] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                                pack_bf16x2(a[6], a[7]));
+            ov4[i] = make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]), pack_bf16x2(b[4], b[5]),
+                                pack_bf16x2(b[6], b[7]));
           }
         }
       }
@@ -404,25 +429,38 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     const int w4 = warp - 4;
     const int dcol = w4 * 32 + lane;  // head-dim index = TMEM lane of dQ^T
     const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
+    float* tile = reinterpret_cast<float*>(smem + DQ_OFF);
+    const bool leader = threadIdx.x == 128;
     for (int i = 0; i < n_iter; ++i) {
       if (!mbar_wait(&bars->dq_full, i & 1, err)) break;
       tc_fence_after();
-      uint32_t v[2][32];
-      tmem_ld32(tmem + lane_off + T_DQT, v[0]);
-      tmem_ld32(tmem + lane_off + T_DQT + 32, v[1]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
       const int h = kvh * r + i / nqt;
       const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
-      const int64_t n64 = q_end - row0;
-      const int n = n64 > 64 ? 64 : (int)n64;
-      float* base = dq_acc + (row0 * geo.hq + h) * 128 + dcol;
-      const int64_t stride = (int64_t)geo.hq * 128;
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c < n) red_add_f32(base + c * stride, __uint_as_float(v[c >> 5][c & 31]) * geo.scale);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + T_DQT + half * 32, v);
+        tmem_ld_wait();
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->dq_free);
+        }
+        // The staging buffer is free once the previous bulk reduce has read it.
+        if (leader) bulk_wait_read0();
+        named_bar(1, 128);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) tile[c * 128 + dcol] = __uint_as_float(v[c]) * geo.scale;
+        fence_proxy_async_smem();
+        named_bar(1, 128);
+        if (leader) {
+          // Rows past the group's end hold exact zeros (their dS^T columns are zero),
+          // and rows past the tensor's end are clipped by the copy.
+          tma_reduce_add_3d(&tm_dq, tile, 0, h, (int)(row0 + half * 32));
+          bulk_commit();
+        }
+      }
     }
+    if (leader) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -435,14 +473,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
 }  // namespace
 
 cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                   const void* vr, const float* lse, const void* dO, const float* delta, float* dq_acc,
+                   const void* vr, const float* stats, const void* dO, float* dq_acc,
                    void* dk_out, void* dv_out, float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
                    const float* dk_add, const float* dv_add, cudaStream_t st) {
   const bool prefill = op == AUGTREE_OP_PREFILL_BWD;
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
-  CUtensorMap mq, mdo, mk, mv, mk2, mv2;
+  CUtensorMap mq, mdo, mk, mv, mk2, mv2, mdq;
   if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, 64)) return cudaErrorInvalidValue;
   if (!encode_rows_map(&mdo, dO, q_rows, p->cfg.hq, 64)) return cudaErrorInvalidValue;
+  if (!encode_f32_rows_map(&mdq, dq_acc, q_rows, p->cfg.hq, 32)) return cudaErrorInvalidValue;
   const bool have_p = p->total_prompt > 0 && kp && vp;
   const bool have_r = !prefill && p->total_resp > 0 && kr && vr;
   if (have_p) {
@@ -464,8 +503,8 @@ cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp,
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
   if (e != cudaSuccess) return e;
   tc_bwd_kernel<<<(unsigned)p->n_items[op], BWD_THREADS, BWD_SMEM, st>>>(
-      mq, mdo, mk, mv, mk2, mv2, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op], lse, delta,
-      dq_acc, (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, dk_part, dv_part, dk_sum, dv_sum, dk_add, dv_add,
+      mq, mdo, mk, mv, mk2, mv2, mdq, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op], stats,
+      prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, dk_part, dv_part, dk_sum, dv_sum, dk_add, dv_add,
       p->err_d);
   return cudaGetLastError();
 }

@@ -233,23 +233,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
         const float mx = tmax * sl2;  // -inf stays -inf
         const bool need = (m != -INFINITY) && (mx > m + 8.0f);
         const float m_new = (m == -INFINITY) ? mx : (need ? mx : m);
-        if (__any_sync(0xffffffffu, need)) {
-          // O_s += P_s(j-1) V must be complete before O is rescaled.
-          if (!(ok = mbar_wait(&bars->o_done[s], (j - 1) & 1, err))) break;
-          tc_fence_after();
-          const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
-          tmem_st_wait();
-          l *= alpha;
-        }
+        const float alpha = need ? fast_exp2(m - m_new) : 1.f;
         m = m_new;
         const float mu = (m == -INFINITY) ? 0.f : m;
         float psum = 0.f;
@@ -268,7 +252,23 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
           tmem_st32(tS + c * 32, pk);
         }
         tmem_st_wait();
-        l += psum;
+        l = l * alpha + psum;
+        if (__any_sync(0xffffffffu, need)) {
+          // O_s += P_s(j-1) V must be complete before O is rescaled; PV(j) is issued
+          // only after p_full(j) below.
+          if (!(ok = mbar_wait(&bars->o_done[s], (j - 1) & 1, err))) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_st_wait();
+        }
         tc_fence_before();
         mbar_arrive(&bars->p_full[s]);
       }
@@ -331,6 +331,20 @@ bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads,
   cuuint32_t es[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over a [rows, heads, 128] fp32 tensor: box of 128 dims x 1 head x box_rows,
+// no swizzle (the dQ accumulator, written by bulk reduce-add).
+bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads, int box_rows) {
+  auto enc = get_encode();
+  if (!enc || !ptr || rows <= 0) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {128 * 4, (cuuint64_t)heads * 128 * 4};
+  cuuint32_t box[3] = {128, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -65,15 +65,17 @@ def test_full_size_sampled_rows_and_identities(cuda_device, name):
     rng = np.random.default_rng(1234)
     r = w.hq // w.hkv
     scale = A.default_scale(w.d)
-    # 1. sampled rows, two query heads each (first and last of a random KV head)
+    # 1. sampled rows, two query heads (first and last) of one of two sampled KV heads
+    kv_heads = sorted(set(int(x) for x in rng.integers(0, w.hkv, size=2)))
+    kv_cache = {kv: {n: W.tensor_rows_np(w, n, heads=[kv]) for n in ("k_p", "v_p", "k_r", "v_r")}
+                for kv in kv_heads}
     for kind, row in sample_rows(w, rng):
-        kv = int(rng.integers(0, w.hkv))
+        kv = kv_heads[int(rng.integers(0, len(kv_heads)))]
+        c = kv_cache[kv]
         heads = [kv * r, kv * r + r - 1]
         (pa, pb), (ra, rb) = A.row_key_set(kind, row, offs)
-        kk = np.concatenate([W.tensor_rows_np(w, "k_p", rows=np.arange(pa, pb), heads=[kv]),
-                             W.tensor_rows_np(w, "k_r", rows=np.arange(ra, rb), heads=[kv])])
-        vv = np.concatenate([W.tensor_rows_np(w, "v_p", rows=np.arange(pa, pb), heads=[kv]),
-                             W.tensor_rows_np(w, "v_r", rows=np.arange(ra, rb), heads=[kv])])
+        kk = np.concatenate([c["k_p"][pa:pb], c["k_r"][ra:rb]])
+        vv = np.concatenate([c["v_p"][pa:pb], c["v_r"][ra:rb]])
         q = W.tensor_rows_np(w, "q_" + kind, rows=[row], heads=heads)
         do = W.tensor_rows_np(w, "do_" + kind, rows=[row], heads=heads)
         o, lse, dq = A.rows_forward_backward(q, np.repeat(kk, len(heads), axis=1),
@@ -85,6 +87,7 @@ def test_full_size_sampled_rows_and_identities(cuda_device, name):
         assert np.max(np.abs(go - o[0])) <= fwd_tol, (kind, row)
         assert np.max(np.abs(gl - lse[:, 0])) <= fwd_tol, (kind, row)
         assert rel_frob(gq, dq[0]) <= grad_tol, (kind, row, rel_frob(gq, dq[0]))
+    del kv_cache
     # 2. gradient identities per (group, KV head), fp64 sums on the device
     po, bb, ro = offs
     d64 = {k: out[k] for k in ("dq_p", "dk_p", "dv_p", "dq_r", "dk_r", "dv_r")}

@@ -42,3 +42,11 @@ def test_tc_prompt_gradient_is_deterministic(cuda_device):
     b = run_cuda(w, kernel=at.KERNEL_TC, t=t, num_sms=4)
     for k in ("dk_p", "dv_p", "dk_r", "dv_r", "o_p", "o_r", "lse_p", "lse_r"):
         assert np.array_equal(a[k], b[k]), k
+
+
+def test_tc_long_item_pipelines(cuda_device):
+    """Items that walk hundreds of query tiles (no prompt-KV splitting): the producer,
+    MMA issuer, softmax and dQ warps run long pipelines over double buffers."""
+    w = W.custom(W.Tree([256], [[3000, 2000]]), hq=8, hkv=2, d=128, dtype="bf16", seed=41)
+    got = run_cuda(w, kernel=at.KERNEL_TC, num_sms=100000)
+    compare(got, run_oracle(w), "bf16")
