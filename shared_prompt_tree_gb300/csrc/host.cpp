@@ -223,7 +223,8 @@ BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
   w.dq_off = align256(stats_bytes(p, false));
   w.dkpart_off = w.dq_off + align256(R * hq * d * 4);
   w.dvpart_off = w.dkpart_off + align256((size_t)p->part_rows * hkv * d * 4);
-  w.total = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
+  w.slots_off = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
+  w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
   return w;
 }
 
@@ -232,8 +233,8 @@ BwdWorkspace prefill_bwd_ws(const augtree_plan* p) {
   const size_t hq = p->cfg.hq, d = p->cfg.head_dim, P = p->total_prompt;
   w.delta_off = 0;
   w.dq_off = align256(stats_bytes(p, true));
-  w.dkpart_off = w.dvpart_off = w.dq_off + align256(P * hq * d * 4);
-  w.total = w.dkpart_off;
+  w.dkpart_off = w.dvpart_off = w.slots_off = w.dq_off + align256(P * hq * d * 4);
+  w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
   return w;
 }
 
@@ -540,7 +541,7 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
   if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0) {
     if (tc)
       e = tc_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dq_acc, dkr, dvr, dk_part, dv_part,
-                 dkp_sum, dvp_sum, nullptr, nullptr, s);
+                 dkp_sum, dvp_sum, nullptr, nullptr, (float*)(base + w.slots_off), s);
     else
       e = simt_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
                    dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
@@ -576,7 +577,7 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
   if (e == cudaSuccess && p->n_items[AUGTREE_OP_PREFILL_BWD] > 0) {
     if (tc)
       e = tc_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dq_acc, dkp, dvp, nullptr,
-                 nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
+                 nullptr, nullptr, nullptr, dkp_acc, dvp_acc, (float*)(base + w.slots_off), s);
     else
       e = simt_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
                    nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);

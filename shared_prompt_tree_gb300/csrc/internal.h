@@ -7,7 +7,7 @@
 
 #include <vector>
 
-#include "../../include/augtree.h"
+#include "augtree.h"
 
 namespace augtree {
 
@@ -75,8 +75,11 @@ augtree_status build_queue(const std::vector<int32_t>& prompt_off, const std::ve
 
 // Workspace layout of the backward calls.
 struct BwdWorkspace {
-  size_t delta_off, dq_off, dkpart_off, dvpart_off, total;
+  size_t delta_off, dq_off, dkpart_off, dvpart_off, slots_off, total;
 };
+// fp32 flush slots of the tensor-core backward: one per SM id, 128 keys x 256 floats.
+constexpr int kFlushSlots = 256;
+constexpr size_t kFlushSlotBytes = (size_t)128 * 256 * 4;
 BwdWorkspace replay_bwd_ws(const augtree_plan* p);
 BwdWorkspace prefill_bwd_ws(const augtree_plan* p);
 
@@ -103,7 +106,7 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
 cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
                    const void* kr, const void* vr, const float* stats, const void* dO, float* dq_acc, void* dk_out, void* dv_out,
                    float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
-                   const float* dk_add, const float* dv_add, cudaStream_t st);
+                   const float* dk_add, const float* dv_add, float* slots, cudaStream_t st);
 
 // Memory-bound helpers.
 cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d,

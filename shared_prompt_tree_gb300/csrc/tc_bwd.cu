@@ -55,6 +55,14 @@ constexpr int BWD_SMEM = BAR_OFF + 256 + 1024;
 
 constexpr uint32_t T_ST = 0, T_DPT = 128, T_DQT = 192, T_DV = 256, T_DK = 384;
 
+// The tensor cores' fp32 accumulation into TMEM carries a small rounding bias per
+// accumulation (measured at about 1e-8 relative), which adds up over the tens of
+// thousands of accumulations of a long item.  Every kFlush query tiles the dK/dV
+// accumulators are therefore moved into an fp32 slot (round-to-nearest adds) and the
+// tensor-core accumulation restarts from zero.
+constexpr int kFlush = 512;
+constexpr int kSlotFloats = 128 * 256;  // per slot: 128 keys x {dK[128], dV[128]}
+
 struct BwdBars {
   uint64_t kv_full;
   uint64_t q_full[NQ];
@@ -71,6 +79,8 @@ struct BwdBars {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t acc_done;
+  uint64_t flush_ready;  // dK/dV accumulators complete up to a flush point
+  uint64_t flushed;      // softmax warps have moved them to the slot
   uint32_t tmem_base;
 };
 
@@ -108,7 +118,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     const float* __restrict__ stats, int ntiles,
     __nv_bfloat16* __restrict__ dk_out, __nv_bfloat16* __restrict__ dv_out, float* __restrict__ dk_part,
     float* __restrict__ dv_part, float* __restrict__ dk_sum, float* __restrict__ dv_sum,
-    const float* __restrict__ dk_add, const float* __restrict__ dv_add, uint32_t* __restrict__ err) {
+    const float* __restrict__ dk_add, const float* __restrict__ dv_add, float* __restrict__ slots, int n_slots,
+    uint32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + BAR_OFF);
@@ -128,7 +139,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
   const int64_t q_rows_total = prefill ? geo.total_prompt : geo.total_resp;
   const int nqt = it.b - it.a;
   const int n_iter = nqt * r;
-  // iteration i: query head kvh*r + i / nqt, query tile a + i % nqt
+  // One block per SM at a time (shared memory and TMEM), so the SM id names a private
+  // flush slot.
+  uint32_t smid;
+  asm("mov.u32 %0, %%smid;" : "=r"(smid));
+  const bool flush_on = n_iter > kFlush && (int)smid < n_slots;
+  if (n_iter > kFlush && (int)smid >= n_slots && threadIdx.x == 0) atomicOr(err, 2u);
+  // Iteration i: query head kvh*r + i / nqt, query tile b - 1 - i % nqt.  Tiles are
+  // walked from the last one down, so blocks that start together (largest first) and
+  // share a KV head meet the same query rows at about the same time: their Q/dO reads
+  // and dQ reductions then hit the same L2 lines.
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -149,6 +169,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->flush_ready, 1);
+    mbar_init(&bars->flushed, 128);
     fence_mbar_init();
   }
   if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
@@ -181,7 +203,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       const int stage = i % NQ, use = i / NQ;
       if (!(ok = mbar_wait(&bars->q_empty[stage], (use & 1) ^ 1, err))) break;
       const int h = kvh * r + i / nqt;
-      const int qt = it.a + i % nqt;
+      const int qt = it.b - 1 - i % nqt;
       const int64_t row0 = qbase + (int64_t)qt * bm;
       mbar_expect_tx(&bars->q_full[stage], 4 * Q_BLK + 2 * kStatRows * 4);
       for (int kb = 0; kb < 2; ++kb) {
@@ -249,13 +271,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         }
         const uint32_t q_addr = smem_u32(smem + Q_OFF + stage * 2 * Q_BLK);
         const uint32_t do_addr = smem_u32(smem + DO_OFF + stage * 2 * Q_BLK);
-        // dV += P^T dO
+        // dV += P^T dO (from zero at the start and after every flush)
+        const bool fresh = flush_on ? (i % kFlush == 0) : (i == 0);
+        if (flush_on && i > 0 && i % kFlush == 0 &&
+            !(ok = mbar_wait(&bars->flushed, (i / kFlush - 1) & 1, err)))
+          break;
         if (!(ok = mbar_wait(&bars->p_ready[i & 1], (i >> 1) & 1, err))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t b = smem_desc_sw128(do_addr + kk * 2048, Q_BLK, 1024);
-          mma_ts(tmem + T_DV, tmem + T_ST + (i & 1) * 64 + kk * 8, b, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + T_DV, tmem + T_ST + (i & 1) * 64 + kk * 8, b, id_acc, (!fresh || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->dv_done);
         // dP^T(i+1) as soon as dP^T(i) has been read out of TMEM
@@ -272,7 +298,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t a = smem_desc_sw128(ds_addr + kk * 32, 16, 1024);
           const uint64_t b = smem_desc_sw128(q_addr + kk * 2048, Q_BLK, 1024);
-          mma_ss(tmem + T_DK, a, b, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ss(tmem + T_DK, a, b, id_acc, (!fresh || kk > 0) ? 1u : 0u);
         }
         if (i >= 1 && !(ok = mbar_wait(&bars->dq_free, (i - 1) & 1, err))) break;
         tc_fence_after();
@@ -285,6 +311,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free[i & 1]);
         mma_commit(&bars->q_empty[stage]);
+        if (flush_on && i % kFlush == kFlush - 1 && more) mma_commit(&bars->flush_ready);
       }
       mma_commit(&bars->acc_done);
     }
@@ -307,7 +334,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
       const int stage = i % NQ;
-      const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
+      const int64_t row0 = qbase + (int64_t)(it.b - 1 - i % nqt) * bm;
       const float* rows = reinterpret_cast<const float*>(smem + ROWS_OFF) + stage * 128;
       // rows[] (lse, Delta) of this stage are published by the producer with q_full.
       if (!(ok = mbar_wait(&bars->q_full[stage], (i / NQ) & 1, err))) break;
@@ -359,6 +386,32 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->ds_ready[i & 1]);
+      if (flush_on && i % kFlush == kFlush - 1 && i + 1 < n_iter) {
+        // Move dK/dV to this block's slot (the first flush stores, later ones add).
+        if (!(ok = mbar_wait(&bars->flush_ready, (i / kFlush) & 1, err))) break;
+        tc_fence_after();
+        float* slot = slots + ((int64_t)smid * 128 + t) * 256;
+        const bool first = i == kFlush - 1;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + (c < 4 ? T_DK : T_DV) + (c & 3) * 32, v);
+          tmem_ld_wait();
+          float4* dst = reinterpret_cast<float4*>(slot + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 x = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+            if (!first) {
+              const float4 y = dst[e];
+              x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+            }
+            dst[e] = x;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->flushed);
+      }
     }
     // dV, dK rows of this key
     if (ok && mbar_wait(&bars->acc_done, 0, err) && n_iter > 0) {
@@ -384,6 +437,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         tmem_ld32(tmem + lane_off + T_DV + c * 32, vv);
         tmem_ld_wait();
         if (!key_ok) continue;
+        if (flush_on) {
+          const float* slot = slots + ((int64_t)smid * 128 + t) * 256;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            kv[i] = __float_as_uint(__uint_as_float(kv[i]) + slot[c * 32 + i]);
+            vv[i] = __float_as_uint(__uint_as_float(vv[i]) + slot[128 + c * 32 + i]);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) kv[i] = __float_as_uint(__uint_as_float(kv[i]) * geo.scale);
         if (fk) {
@@ -435,7 +496,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       if (!mbar_wait(&bars->dq_full, i & 1, err)) break;
       tc_fence_after();
       const int h = kvh * r + i / nqt;
-      const int64_t row0 = qbase + (int64_t)(it.a + i % nqt) * bm;
+      const int64_t row0 = qbase + (int64_t)(it.b - 1 - i % nqt) * bm;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t v[32];
@@ -475,7 +536,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
 cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
                    const void* vr, const float* stats, const void* dO, float* dq_acc,
                    void* dk_out, void* dv_out, float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
-                   const float* dk_add, const float* dv_add, cudaStream_t st) {
+                   const float* dk_add, const float* dv_add, float* slots, cudaStream_t st) {
   const bool prefill = op == AUGTREE_OP_PREFILL_BWD;
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
   CUtensorMap mq, mdo, mk, mv, mk2, mv2, mdq;
@@ -505,7 +566,7 @@ cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp,
   tc_bwd_kernel<<<(unsigned)p->n_items[op], BWD_THREADS, BWD_SMEM, st>>>(
       mq, mdo, mk, mv, mk2, mv2, mdq, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op], stats,
       prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, dk_part, dv_part, dk_sum, dv_sum, dk_add, dv_add,
-      p->err_d);
+      slots, kFlushSlots, p->err_d);
   return cudaGetLastError();
 }
 
