@@ -199,6 +199,26 @@ augtree_status augtree_prefill_bwd(const augtree_plan* plan, const void* qp, con
                                    void* dqp, void* dkp, void* dvp, void* ws, size_t ws_bytes,
                                    void* stream);
 
+/* Prefill backward that allocates nothing and takes no workspace.  The paper has no
+ * counterpart: this is a convenience for callers that cannot allocate device memory
+ * while they run (a caching-allocator or memory-pool callback, a real-time step that
+ * must not take the driver's allocation lock or meet an out-of-memory error, a host
+ * framework that only lends its own buffers).  Arguments and results are those of
+ * augtree_prefill_bwd; the plan must already exist (creating it allocates).
+ * Scratch: Delta and the fp32 dQ accumulator live in a 64 MiB array defined by the
+ * library, held on every device that loads it until the process exits.  A plan whose
+ * prefill-backward workspace (augtree_plan_workspace_bytes) exceeds 64 MiB is rejected
+ * with AUGTREE_ERR_WORKSPACE_TOO_SMALL before any work is queued.  The first call on a
+ * device looks up the array's device address; make that call before any stream
+ * capture.  Every call shares the array and re-initializes what it reads, so results do
+ * not depend on earlier calls, but calls that may overlap on the GPU (unordered
+ * streams) race on it. */
+augtree_status augtree_prefill_bwd_static(const augtree_plan* plan, const void* qp, const void* kp,
+                                          const void* vp, const void* op, const float* lse_p,
+                                          const void* dop, const float* dkp_acc,
+                                          const float* dvp_acc, void* dqp, void* dkp, void* dvp,
+                                          void* stream);
+
 /* State merge (+) of Sec. 3.3 in (O, lse) form, fp32:
  *   lse = log(exp(lse_a) + exp(lse_b)),  o = exp(lse_a - lse) oa + exp(lse_b - lse) ob.
  * oa/ob/o [rows, h, d], lse_a/lse_b/lse [h, rows].  (0, -inf) is the identity; two

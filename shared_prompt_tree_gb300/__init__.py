@@ -70,6 +70,7 @@ _SIGS = {
     "augtree_replay_fwd": [_P] * 8 + [_P, _SZ, _P],
     "augtree_replay_bwd": [_P] * 15 + [_SZ, _P],
     "augtree_prefill_bwd": [_P] * 13 + [_SZ, _P],
+    "augtree_prefill_bwd_static": [_P] * 13,
     "augtree_lse_merge": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 6 + [_P],
     "augtree_plan_check": [_P, _P],
     "augtree_status_string": [ctypes.c_int32],
@@ -232,6 +233,15 @@ def augtree_prefill_bwd(plan: Plan, qp, kp, vp, op, lse_p, dop, dkp_acc, dvp_acc
                                      _ptr(dkp_acc), _ptr(dvp_acc), _ptr(dqp), _ptr(dkp), _ptr(dvp), _ptr(ws),
                                      0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
            "augtree_prefill_bwd")
+
+
+def augtree_prefill_bwd_static(plan: Plan, qp, kp, vp, op, lse_p, dop, dkp_acc, dvp_acc, dqp, dkp, dvp,
+                               stream=None):
+    """augtree_prefill_bwd without a workspace: the library's fixed 64 MiB scratch array
+    is used instead, and the call allocates nothing."""
+    _check(lib().augtree_prefill_bwd_static(plan.handle, _ptr(qp), _ptr(kp), _ptr(vp), _ptr(op), _ptr(lse_p),
+                                            _ptr(dop), _ptr(dkp_acc), _ptr(dvp_acc), _ptr(dqp), _ptr(dkp), _ptr(dvp),
+                                            _stream(stream)), "augtree_prefill_bwd_static")
 
 
 def augtree_lse_merge(oa, lse_a, ob, lse_b, o, lse, stream=None):
