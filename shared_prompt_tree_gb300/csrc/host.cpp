@@ -105,6 +105,8 @@ void tiles_for(int family, int op, int* bm, int* bn) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+constexpr bool kUsePairForward = false;
+
 }  // namespace
 
 namespace augtree {
@@ -391,6 +393,7 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   // items of a (group, tile) next to each other, so pairs are checked, not assumed.
   for (int op = 0; op < 4; ++op) {
     p->paired[op] = 0;
+    p->quad[op] = 0;
     if (p->family != AUGTREE_KERNEL_TC || op > AUGTREE_OP_REPLAY_FWD) continue;
     const int r = cfg->hq / cfg->hkv;
     bool ok = (cfg->hq % 2 == 0) && (r % 2 == 0) && (p->n_items[op] % 2 == 0);
@@ -400,6 +403,20 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
       ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 2 == 0 && b[3] == a[3] + 1;
     }
     p->paired[op] = ok ? 1 : 0;
+    // Four-head units for the SM-pair kernel: heads 4k..4k+3 of one tile share a KV head
+    // when Hq/Hkv is a multiple of 4.
+    bool q4 = (cfg->hq % 4 == 0) && (r % 4 == 0) && (p->n_items[op] % 4 == 0);
+    for (size_t i = 0; q4 && i + 3 < p->n_items[op]; i += 4) {
+      const int32_t* a = &p->queue_h[op][i * AUGTREE_ITEM_WORDS];
+      for (int k = 1; k < 4 && q4; ++k) {
+        const int32_t* b = a + k * AUGTREE_ITEM_WORDS;
+        q4 = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 4 == 0 && b[3] == a[3] + k;
+      }
+    }
+    // The SM-pair kernel is correct but, with two softmax warpgroups per SM, slower than
+    // the single-CTA kernel on the measured configurations; it stays off until its
+    // softmax has more warps.
+    p->quad[op] = (q4 && kUsePairForward) ? 1 : 0;
   }
   // Split-K bookkeeping from the replay backward queue.
   p->splits_h.assign(std::max(1, p->n_groups), SplitInfo{0, 0, 0});

@@ -62,6 +62,7 @@ struct augtree_plan {
   augtree::SplitInfo* splits_d;
   int32_t* queue_d[4];
   int paired[4];      // forward tensor-core units take two items (two heads of one KV head)
+  int quad[4];        // forward units of four items (four heads of one KV head) for SM pairs
   int32_t ntiles_p, ntiles_r;  // 64-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
 };
@@ -92,6 +93,9 @@ bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads,
 bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads, int box_rows);
 
 // ---- launchers (return cudaGetLastError() of their launches) ---------------------
+// Forward on SM pairs (2-CTA clusters): used when the queue groups into four-head units.
+cudaError_t tc_fwd2(const augtree_plan* p, int op, const CUtensorMap& mq, const void* kp, const void* vp,
+                    const void* kr, const void* vr, void* o, float* lse, int64_t q_rows, cudaStream_t st);
 // SIMT family (any dtype).
 cudaError_t simt_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
                      const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);

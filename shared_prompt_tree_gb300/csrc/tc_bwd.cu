@@ -40,6 +40,7 @@ using namespace tc;
 
 constexpr int BWD_THREADS = 320;
 constexpr int NQ = 3;                                   // Q/dO ring stages
+constexpr int kPrefetch = 5;                            // L2 prefetch distance (iterations)
 constexpr int KV_BLK = 128 * 128;                       // 128 rows x 64 dims bf16 = 16 KB
 constexpr int Q_BLK = 64 * 128;                         // 64 rows x 64 dims bf16 = 8 KB
 constexpr int K_OFF = 0;                                // 2 blocks
@@ -102,12 +103,20 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
+__device__ __forceinline__ void named_bar(int id, int n) { named_bar_sync(id, n); }
 
 __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -215,6 +224,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
                 stats + ((int64_t)h * ntiles + tile_base + qt) * 2 * kStatRows, 2 * kStatRows * 4,
                 &bars->q_full[stage]);
       issued = i + 1;
+      // Warm L2 with the tiles a few iterations ahead, so that their copies into shared
+      // memory, issued once a stage frees up, do not wait on DRAM.
+      const int ip = i + kPrefetch;
+      if (ip < n_iter) {
+        const int hp = kvh * r + ip / nqt;
+        const int qp = it.b - 1 - ip % nqt;
+        const int rp = (int)(qbase + (int64_t)qp * bm);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_prefetch_3d(&tm_q, kb * 64, hp, rp);
+          tma_prefetch_3d(&tm_do, kb * 64, hp, rp);
+        }
+        bulk_prefetch(stats + ((int64_t)hp * ntiles + tile_base + qp) * 2 * kStatRows, 2 * kStatRows * 4);
+      }
     }
     if (lane == 0) {
       // Never leave a copy in flight.
@@ -227,28 +249,38 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);    // K Q^T, V dO^T
       constexpr uint32_t id_acc = idesc_bf16_f32(128, 128, false, true);  // P^T dO, dS^T Q (B MN-major)
       constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // K^T dS^T
-      const uint32_t k_addr = smem_u32(smem + K_OFF), v_addr = smem_u32(smem + V_OFF);
-      const uint32_t ds_addr0 = smem_u32(smem + DS_OFF);
+      // Descriptors are built once; each MMA step then only adds a compile-time offset
+      // (in 16-byte units) to the start-address field.  This keeps the single issuing
+      // thread's dependency chain per tcgen05.mma short.
+      const uint64_t dK = smem_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);      // K, K-major
+      const uint64_t dV = smem_desc_sw128(smem_u32(smem + V_OFF), 16, 1024);      // V, K-major
+      const uint64_t dKt = smem_desc_sw128(smem_u32(smem + K_OFF), KV_BLK, 1024);  // K^T, MN-major
+      // Stage st of the Q/dO ring sits 2 * Q_BLK bytes after stage st - 1.
+      const uint64_t dQk0 = smem_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+      const uint64_t dOk0 = smem_desc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
+      const uint64_t dQm0 = smem_desc_sw128(smem_u32(smem + Q_OFF), Q_BLK, 1024);
+      const uint64_t dOm0 = smem_desc_sw128(smem_u32(smem + DO_OFF), Q_BLK, 1024);
+      constexpr uint64_t kStageStep = (2 * Q_BLK) >> 4;
+      const uint64_t dSk0 = smem_desc_sw128(smem_u32(smem + DS_OFF), 16, 1024);       // dS^T, K-major
+      const uint64_t dSm0 = smem_desc_sw128(smem_u32(smem + DS_OFF), KV_BLK, 1024);   // dS^T, MN-major
+      constexpr uint64_t kDsStep = KV_BLK >> 4;  // second dS^T buffer
+      // K-major k-step kk: block kk/4, 32 bytes per step inside the 128-byte row.
+      auto koff_kv = [](int kk) { return (uint64_t)(((kk >> 2) * KV_BLK + (kk & 3) * 32) >> 4); };
+      auto koff_q = [](int kk) { return (uint64_t)(((kk >> 2) * Q_BLK + (kk & 3) * 32) >> 4); };
       bool ok = mbar_wait(&bars->kv_full, 0, err);
       tc_fence_after();
       auto issue_s = [&](int i) {  // S^T(i) -> ST[i % 2]
-        const uint32_t q_addr = smem_u32(smem + Q_OFF + (i % NQ) * 2 * Q_BLK);
+        const int st = i % NQ;
+        const uint32_t d = tmem + T_ST + (i & 1) * 64;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = smem_desc_sw128(k_addr + (kk >> 2) * KV_BLK + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(q_addr + (kk >> 2) * Q_BLK + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + T_ST + (i & 1) * 64, a, b, id_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk) mma_ss(d, dK + koff_kv(kk), dQk0 + st * kStageStep + koff_q(kk), id_s, kk > 0 ? 1u : 0u);
         mma_commit(&bars->s_full[i & 1]);
       };
       auto issue_dp = [&](int i) {  // dP^T(i) -> DPT
-        const uint32_t do_addr = smem_u32(smem + DO_OFF + (i % NQ) * 2 * Q_BLK);
+        const int st = i % NQ;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = smem_desc_sw128(v_addr + (kk >> 2) * KV_BLK + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(do_addr + (kk >> 2) * Q_BLK + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + T_DPT, a, b, id_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + T_DPT, dV + koff_kv(kk), dOk0 + st * kStageStep + koff_q(kk), id_s, kk > 0 ? 1u : 0u);
         mma_commit(&bars->dp_full);
       };
       if (ok && n_iter > 0) {
@@ -269,8 +301,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
           tc_fence_after();
           issue_s(i + 1);
         }
-        const uint32_t q_addr = smem_u32(smem + Q_OFF + stage * 2 * Q_BLK);
-        const uint32_t do_addr = smem_u32(smem + DO_OFF + stage * 2 * Q_BLK);
         // dV += P^T dO (from zero at the start and after every flush)
         const bool fresh = flush_on ? (i % kFlush == 0) : (i == 0);
         if (flush_on && i > 0 && i % kFlush == 0 &&
@@ -278,10 +308,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
           break;
         if (!(ok = mbar_wait(&bars->p_ready[i & 1], (i >> 1) & 1, err))) break;
         tc_fence_after();
+        {
+          const uint32_t pa = tmem + T_ST + (i & 1) * 64;
+          const uint64_t b0 = dOm0 + stage * kStageStep;
+          mma_ts(tmem + T_DV, pa, b0, id_acc, fresh ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t b = smem_desc_sw128(do_addr + kk * 2048, Q_BLK, 1024);
-          mma_ts(tmem + T_DV, tmem + T_ST + (i & 1) * 64 + kk * 8, b, id_acc, (!fresh || kk > 0) ? 1u : 0u);
+          for (int kk = 1; kk < 4; ++kk) mma_ts(tmem + T_DV, pa + kk * 8, b0 + kk * (2048 >> 4), id_acc, 1u);
         }
         mma_commit(&bars->dv_done);
         // dP^T(i+1) as soon as dP^T(i) has been read out of TMEM
@@ -293,24 +325,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
         // dK += dS^T Q ; dQ^T = K^T dS^T  (dS^T from shared-memory buffer i % 2)
         if (!(ok = mbar_wait(&bars->ds_ready[i & 1], (i >> 1) & 1, err))) break;
         tc_fence_after();
-        const uint32_t ds_addr = ds_addr0 + (i & 1) * KV_BLK;
+        {
+          const uint64_t a0 = dSk0 + (i & 1) * kDsStep, b0 = dQm0 + stage * kStageStep;
+          mma_ss(tmem + T_DK, a0, b0, id_acc, fresh ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc_sw128(ds_addr + kk * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(q_addr + kk * 2048, Q_BLK, 1024);
-          mma_ss(tmem + T_DK, a, b, id_acc, (!fresh || kk > 0) ? 1u : 0u);
+          for (int kk = 1; kk < 4; ++kk) mma_ss(tmem + T_DK, a0 + kk * (32 >> 4), b0 + kk * (2048 >> 4), id_acc, 1u);
         }
+        // dK(i) is the last reader of Q(i)/dO(i): release the stage to the producer.
+        mma_commit(&bars->q_empty[stage]);
         if (i >= 1 && !(ok = mbar_wait(&bars->dq_free, (i - 1) & 1, err))) break;
         tc_fence_after();
+        {
+          const uint64_t b0 = dSm0 + (i & 1) * kDsStep;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = smem_desc_sw128(k_addr + kk * 2048, KV_BLK, 1024);
-          const uint64_t b = smem_desc_sw128(ds_addr + kk * 2048, KV_BLK, 1024);
-          mma_ss(tmem + T_DQT, a, b, id_dq, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + T_DQT, dKt + kk * (2048 >> 4), b0 + kk * (2048 >> 4), id_dq, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free[i & 1]);
-        mma_commit(&bars->q_empty[stage]);
         if (flush_on && i % kFlush == kFlush - 1 && more) mma_commit(&bars->flush_ready);
       }
       mma_commit(&bars->acc_done);
@@ -348,12 +380,36 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       const int lo = lo64 < 0 ? 0 : (lo64 > 64 ? 64 : (int)lo64);
       const int hi = hi64 < 0 ? 0 : (hi64 > 64 ? 64 : (int)hi64);  // exclusive
       uint32_t pk[32];  // P^T as bf16 pairs: A operand of dV and the P factor of dS
+      const float4* l4 = reinterpret_cast<const float4*>(rows);
+      // One exponential in four runs on the FMA pipe (exp2_fma), three on the MUFU.
+      if (lo == 0 && hi == 64) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int c0 = 2 * c, c1 = 2 * c + 1;
-        const float e0 = fast_exp2(fmaf(__uint_as_float(sraw[c0 >> 5][c0 & 31]), sl2, -rows[c0]));
-        const float e1 = fast_exp2(fmaf(__uint_as_float(sraw[c1 >> 5][c1 & 31]), sl2, -rows[c1]));
-        pk[c] = pack_bf16x2((c0 >= lo && c0 < hi) ? e0 : 0.f, (c1 >= lo && c1 < hi) ? e1 : 0.f);
+        for (int g = 0; g < 16; ++g) {
+          const float4 l = l4[g];
+          const int c = 4 * g;
+          const float e0 = fast_exp2(fmaf(__uint_as_float(sraw[c >> 5][c & 31]), sl2, -l.x));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]), sl2, -l.y));
+          const float e2 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 2) >> 5][(c + 2) & 31]), sl2, -l.z));
+          const float e3 = exp2_fma(fmaf(__uint_as_float(sraw[(c + 3) >> 5][(c + 3) & 31]), sl2, -l.w));
+          pk[2 * g] = pack_bf16x2(e0, e1);
+          pk[2 * g + 1] = pack_bf16x2(e2, e3);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          const float4 l = l4[g];
+          const int c = 4 * g;
+          float e0 = fast_exp2(fmaf(__uint_as_float(sraw[c >> 5][c & 31]), sl2, -l.x));
+          float e1 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]), sl2, -l.y));
+          float e2 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 2) >> 5][(c + 2) & 31]), sl2, -l.z));
+          float e3 = exp2_fma(fmaf(__uint_as_float(sraw[(c + 3) >> 5][(c + 3) & 31]), sl2, -l.w));
+          e0 = (c >= lo && c < hi) ? e0 : 0.f;
+          e1 = (c + 1 >= lo && c + 1 < hi) ? e1 : 0.f;
+          e2 = (c + 2 >= lo && c + 2 < hi) ? e2 : 0.f;
+          e3 = (c + 3 >= lo && c + 3 < hi) ? e3 : 0.f;
+          pk[2 * g] = pack_bf16x2(e0, e1);
+          pk[2 * g + 1] = pack_bf16x2(e2, e3);
+        }
       }
       tmem_st32(tmem + lane_off + T_ST + (i & 1) * 64, pk);
       tmem_st_wait();
@@ -368,12 +424,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) tc_bwd_kernel(
       tc_fence_before();
       mbar_arrive(&bars->dp_free);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int c0 = 2 * c, c1 = 2 * c + 1;
-        const float p0 = __uint_as_float(pk[c] << 16), p1 = __uint_as_float(pk[c] & 0xFFFF0000u);
-        const float d0 = p0 * (__uint_as_float(sraw[c0 >> 5][c0 & 31]) - rows[64 + c0]);
-        const float d1 = p1 * (__uint_as_float(sraw[c1 >> 5][c1 & 31]) - rows[64 + c1]);
-        pk[c] = pack_bf16x2(d0, d1);
+      for (int g = 0; g < 16; ++g) {
+        const float4 dl = l4[16 + g];  // Delta of columns 4g .. 4g+3
+        const float dd[4] = {dl.x, dl.y, dl.z, dl.w};
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int c = 2 * g + h2, c0 = 2 * c, c1 = 2 * c + 1;
+          const float p0 = __uint_as_float(pk[c] << 16), p1 = __uint_as_float(pk[c] & 0xFFFF0000u);
+          const float d0 = p0 * (__uint_as_float(sraw[c0 >> 5][c0 & 31]) - dd[2 * h2]);
+          const float d1 = p1 * (__uint_as_float(sraw[c1 >> 5][c1 & 31]) - dd[2 * h2 + 1]);
+          pk[c] = pack_bf16x2(d0, d1);
+        }
       }
       // dS^T row into buffer i % 2, once dK(i-2) and dQ^T(i-2) have read that buffer
       if (i >= 2 && !(ok = mbar_wait(&bars->ds_free[i & 1], ((i >> 1) - 1) & 1, err))) break;

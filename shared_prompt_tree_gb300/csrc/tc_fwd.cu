@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "tc_common.cuh"
+#include "tc_fwd_softmax.cuh"
 
 namespace augtree {
 namespace {
@@ -134,47 +135,47 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // all 32 lanes: warp-uniform control flow; one elected lane issues
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
-      bool ok = mbar_wait(&bars->q_full, 0, err);
+      // Descriptors are built once; each MMA step adds a compile-time offset (16-byte
+      // units) to the start-address field, keeping the issuing thread's chain short.
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + V_OFF), TILE_BYTES, 1024);
+      constexpr uint64_t kSub = (2 * TILE_BYTES) >> 4;   // next query head's Q / next K,V stage
+      auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * TILE_BYTES + (kk & 3) * 32) >> 4); };
+      bool ok = mbar_wait_warp_all(&bars->q_full, 0, err);
       tc_fence_after();
-      const uint32_t q_addr = smem_u32(smem + Q_OFF);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int stage = j % NST, use = j / NST;
-        if (!(ok = mbar_wait(&bars->kv_full[stage], use & 1, err))) break;
+        if (!(ok = mbar_wait_warp_all(&bars->kv_full[stage], use & 1, err))) break;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + K_OFF + stage * 2 * TILE_BYTES);
-        const uint32_t v_addr = smem_u32(smem + V_OFF + stage * 2 * TILE_BYTES);
+        const uint64_t dk = dk0 + stage * kSub, dv = dv0 + stage * kSub;
         for (int s = 0; s < n_sub; ++s) {
           if (j > 0) {
             // S_s(j) overwrites P_s(j-1): wait until O_s += P_s(j-1) V has completed.
-            if (!(ok = mbar_wait(&bars->o_done[s], (j - 1) & 1, err))) break;
+            if (!(ok = mbar_wait_warp_all(&bars->o_done[s], (j - 1) & 1, err))) break;
             tc_fence_after();
           }
+          const uint64_t dq = dq0 + s * kSub;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
-            const uint64_t a = smem_desc_sw128(q_addr + s * 2 * TILE_BYTES + off, 16, 1024);
-            const uint64_t b = smem_desc_sw128(k_addr + off, 16, 1024);
-            mma_ss(tmem + s * 128, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->s_full[s]);
+          for (int kk = 0; kk < 8; ++kk) mma_ss_w(tmem + s * 128, dq + koff(kk), dk + koff(kk), idesc_qk, kk > 0 ? 1u : 0u);
+          mma_commit_w(&bars->s_full[s]);
         }
         if (!ok) break;
         for (int s = 0; s < n_sub; ++s) {
-          if (!(ok = mbar_wait(&bars->p_full[s], j & 1, err))) break;
+          if (!(ok = mbar_wait_warp_all(&bars->p_full[s], j & 1, err))) break;
           tc_fence_after();
+          // 16 keys per step: 16 swizzled 128-byte rows = 2048 bytes; the two 64-dim
+          // halves of V are 16 KB apart (leading byte offset).
+          const uint32_t pa = tmem + s * 128;
+          mma_ts_w(tmem + 256 + s * 128, pa, dv, idesc_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // 16 keys per step: 16 swizzled 128-byte rows = 2048 bytes; the two
-            // 64-dim halves of V are 16 KB apart (leading byte offset).
-            const uint64_t b = smem_desc_sw128(v_addr + kk * 2048, TILE_BYTES, 1024);
-            mma_ts(tmem + 256 + s * 128, tmem + s * 128 + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars->o_done[s]);
+          for (int kk = 1; kk < 8; ++kk) mma_ts_w(tmem + 256 + s * 128, pa + kk * 8, dv + kk * (2048 >> 4), idesc_pv, 1u);
+          mma_commit_w(&bars->o_done[s]);
         }
-        mma_commit(&bars->kv_empty[stage]);
+        mma_commit_w(&bars->kv_empty[stage]);
       }
     }
   } else {
@@ -184,116 +185,21 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
       const int q4 = warp & 3;
       const int r_local = q4 * 32 + lane;
       const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-      const uint32_t tS = tmem + s * 128 + lane_off;
-      const uint32_t tO = tmem + 256 + s * 128 + lane_off;
-      const int64_t row = row0 + r_local;
-      const bool row_ok = row < row_end;
-      const int64_t bs = (!prefill && row_ok) ? geo.row_bstart[row] : 0;
-      const float sl2 = geo.scale_log2;
-      float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n_tiles; ++j) {
-        if (!(ok = mbar_wait(&bars->s_full[s], j & 1, err))) break;
-        tc_fence_after();
-        uint32_t raw[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, raw[c]);
-        tmem_ld_wait();
-        float x[128];
-#pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(raw[c >> 5][c & 31]);
-        // valid key columns [lo, hi] of this row in tile j
-        const bool own = j >= n_a;
-        const int64_t key0 = own ? own0 + (int64_t)(j - n_a) * bn : G.p0 + (int64_t)j * bn;
-        int64_t lo, hi;
-        if (prefill) {
-          lo = 0;
-          hi = row - key0;
-        } else if (!own) {
-          lo = 0;
-          hi = (int64_t)G.p0 + G.lp - 1 - key0;
-        } else {
-          lo = bs - key0;
-          hi = row - key0;
-        }
-        if (!row_ok) {
-          lo = 1;
-          hi = 0;
-        }
-        if (lo > 0 || hi < 127) {
-          const int lo_i = lo < -1 ? -1 : (lo > 128 ? 128 : (int)lo);
-          const int hi_i = hi < -1 ? -1 : (hi > 128 ? 128 : (int)hi);
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < lo_i || c > hi_i) x[c] = -INFINITY;
-        }
-        float tmax = x[0];
-#pragma unroll
-        for (int c = 1; c < 128; ++c) tmax = fmaxf(tmax, x[c]);
-        const float mx = tmax * sl2;  // -inf stays -inf
-        const bool need = (m != -INFINITY) && (mx > m + 8.0f);
-        const float m_new = (m == -INFINITY) ? mx : (need ? mx : m);
-        const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-        m = m_new;
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        float psum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sl2, -mu));
-            const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sl2, -mu));
-            pk[i] = pack_bf16x2(p0, p1);
-            // The denominator sums the bf16 values the PV product uses, so numerator
-            // and denominator carry the same rounded weights.
-            psum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
-          }
-          tmem_st32(tS + c * 32, pk);
-        }
-        tmem_st_wait();
-        l = l * alpha + psum;
-        if (__any_sync(0xffffffffu, need)) {
-          // O_s += P_s(j-1) V must be complete before O is rescaled; PV(j) is issued
-          // only after p_full(j) below.
-          if (!(ok = mbar_wait(&bars->o_done[s], (j - 1) & 1, err))) break;
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[s]);
-      }
-      if (ok && mbar_wait(&bars->o_done[s], (n_tiles - 1) & 1, err)) {
-        tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int h = heads[s];
-        __nv_bfloat16* dst = out + (row * geo.hq + h) * 128;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-          if (row_ok) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-        if (row_ok) lse[(int64_t)h * lse_rows + row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      }
+      FwdRowGeom g;
+      g.row = row0 + r_local;
+      g.row_ok = g.row < row_end;
+      g.prefill = prefill;
+      g.bs = (!prefill && g.row_ok) ? geo.row_bstart[g.row] : 0;
+      g.p0 = G.p0;
+      g.p_end = (int64_t)G.p0 + G.lp;
+      g.own0 = own0;
+      g.n_a = n_a;
+      g.bn = bn;
+      const int h = heads[s];
+      uint64_t* p_full = &bars->p_full[s];
+      fwd_softmax_row(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles, geo.scale_log2,
+                      &bars->s_full[s], &bars->o_done[s], [p_full]() { mbar_arrive(p_full); },
+                      out + (g.row * geo.hq + h) * 128, lse + (int64_t)h * lse_rows + g.row, err);
     }
   }
   tc_fence_before();
@@ -354,6 +260,7 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
   CUtensorMap mq, mkp, mvp, mkr, mvr;
   if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, 128)) return cudaErrorInvalidValue;
+  if (p->quad[op]) return tc_fwd2(p, op, mq, kp, vp, kr, vr, o, lse, q_rows, st);
   const bool have_p = p->total_prompt > 0 && kp && vp;
   const bool have_r = !prefill && p->total_resp > 0 && kr && vr;
   if (have_p) {

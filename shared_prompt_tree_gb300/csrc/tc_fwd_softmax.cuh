@@ -1,0 +1,167 @@
+// The softmax warpgroup of the tensor-core forward kernels (one and two CTAs per MMA):
+// one thread per query row (TMEM lane), shared by tc_fwd.cu and tc_fwd2.cu.
+//
+// AugTree paper, Sec. 2.2 (online softmax over Q-KV tiles), Sec. 3.2 Eq. 1 (the row's
+// valid keys: the whole prompt of its group, then its own branch up to itself; causal
+// over the prompt for prefill rows) and Sec. 3.3 (the prompt-part and own-part states
+// merge associatively; here one running state crosses both parts).
+#pragma once
+
+#include <cmath>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace augtree {
+namespace tc {
+
+// Where the row's keys come from in KV tile j: prompt tiles first, then the own-branch
+// tiles, and the valid columns [lo, hi] of the row in that tile.
+struct FwdRowGeom {
+  int64_t row;      // global query row (prompt or response rows)
+  bool row_ok;      // row < end of its query tile's group
+  bool prefill;
+  int64_t bs;       // first response row of the row's branch (replay rows)
+  int64_t p0, p_end;  // the group's prompt keys
+  int64_t own0;     // first key of the own-branch tiles
+  int n_a;          // number of prompt tiles
+  int bn;           // keys per tile
+};
+
+__device__ __forceinline__ void fwd_valid_cols(const FwdRowGeom& g, int j, int& lo_i, int& hi_i) {
+  const bool own = j >= g.n_a;
+  const int64_t key0 = own ? g.own0 + (int64_t)(j - g.n_a) * g.bn : g.p0 + (int64_t)j * g.bn;
+  int64_t lo, hi;
+  if (g.prefill) {
+    lo = 0;
+    hi = g.row - key0;
+  } else if (!own) {
+    lo = 0;
+    hi = g.p_end - 1 - key0;
+  } else {
+    lo = g.bs - key0;
+    hi = g.row - key0;
+  }
+  if (!g.row_ok) {
+    lo = 1;
+    hi = 0;
+  }
+  lo_i = lo < -1 ? -1 : (lo > 128 ? 128 : (int)lo);
+  hi_i = hi < -1 ? -1 : (hi > 128 ? 128 : (int)hi);
+}
+
+// Runs the row's online softmax over n_tiles KV tiles of 128 keys.  For each tile:
+// waits s_full (S in TMEM), masks, keeps a running max with lazy rescaling of O
+// (only when the max grows by more than 2^8; exact, every term shares the offset),
+// writes P = exp2(s*log2e*S - m) as bf16 over S (one value in eight from the FMA-pipe
+// exponential), adds the bf16 values to the row sum, and calls signal_p() once its
+// warpgroup may hand P to the MMA issuer.  At the end writes O / l (bf16) and lse.
+template <typename SignalP>
+__device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const FwdRowGeom& g, int n_tiles, float sl2,
+                                                uint64_t* s_full, uint64_t* o_done, SignalP signal_p,
+                                                __nv_bfloat16* out_row, float* lse_ptr, uint32_t* err) {
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n_tiles; ++j) {
+    if (!(ok = mbar_wait(s_full, j & 1, err))) break;
+    tc_fence_after();
+    uint32_t raw[4][32];  // S row, reinterpreted as fp32 in place (no second copy)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, raw[c]);
+    tmem_ld_wait();
+#define AUGTREE_X(c) raw[(c) >> 5][(c) & 31]
+    int lo_i, hi_i;
+    fwd_valid_cols(g, j, lo_i, hi_i);
+    const bool masked = lo_i > 0 || hi_i < 127;
+    if (masked) {
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c < lo_i || c > hi_i) AUGTREE_X(c) = 0xFF800000u;  // -inf
+    }
+    // Row max with 8 independent partial maxima (a single 127-long dependent chain
+    // would dominate the latency of the warpgroup's turn).
+    float pm[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(AUGTREE_X(k));
+#pragma unroll
+    for (int c = 8; c < 128; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(AUGTREE_X(c)));
+    const float tmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+    const float mx = tmax * sl2;  // -inf stays -inf
+    const bool need = (m != -INFINITY) && (mx > m + 8.0f);
+    const float m_new = (m == -INFINITY) ? mx : (need ? mx : m);
+    const float alpha = need ? fast_exp2(m - m_new) : 1.f;
+    m = m_new;
+    const float mu = (m == -INFINITY) ? 0.f : m;
+    float ps[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial sums
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c0 = c * 64 + 2 * i;
+        const float a0 = fmaf(__uint_as_float(AUGTREE_X(c0)), sl2, -mu);
+        const float a1 = fmaf(__uint_as_float(AUGTREE_X(c0 + 1)), sl2, -mu);
+        float p0 = fast_exp2(a0), p1;
+        if (c == 1 && (i & 1)) {
+          // FMA-pipe exponential (second half of the row, where half of S has already
+          // been consumed and registers are free); a masked column (-inf) must stay
+          // exactly zero.
+          p1 = exp2_fma(a1);
+          if (masked && a1 == -INFINITY) p1 = 0.f;
+        } else {
+          p1 = fast_exp2(a1);
+        }
+        pk[i] = pack_bf16x2(p0, p1);
+        // The denominator sums the bf16 values the PV product uses, so numerator and
+        // denominator carry the same rounded weights.
+        ps[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+      }
+      tmem_st32(tS + c * 32, pk);
+    }
+#undef AUGTREE_X
+    tmem_st_wait();
+    const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    l = l * alpha + psum;
+    if (__any_sync(0xffffffffu, need)) {
+      // O += P(j-1) V must be complete before O is rescaled; PV(j) is issued only
+      // after this row's warpgroup signals P(j).
+      if (!(ok = mbar_wait(o_done, (j - 1) & 1, err))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tO + c * 32, o);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    signal_p();
+  }
+  if (ok && mbar_wait(o_done, (n_tiles - 1) & 1, err)) {
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + c * 32, o);
+      tmem_ld_wait();
+      if (g.row_ok) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        uint4* d4 = reinterpret_cast<uint4*>(out_row + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+    if (g.row_ok) *lse_ptr = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+}  // namespace tc
+}  // namespace augtree
