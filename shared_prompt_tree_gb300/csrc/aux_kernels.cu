@@ -37,8 +37,7 @@ __global__ void preprocess_kernel(const T* __restrict__ o, const T* __restrict__
 __global__ void preprocess_tiled_kernel(const GroupInfo* __restrict__ groups, int n_groups, bool prompt_side,
                                         int ntiles, const __nv_bfloat16* __restrict__ o,
                                         const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
-                                        int64_t rows_total, int hq, float* __restrict__ stats,
-                                        float* __restrict__ dq_acc) {
+                                        int64_t rows_total, int hq, float* __restrict__ stats) {
   const int tile = blockIdx.x;
   const int h = blockIdx.y;
   // group holding this tile: last group whose first tile is <= tile and that has tiles
@@ -71,7 +70,6 @@ __global__ void preprocess_tiled_kernel(const GroupInfo* __restrict__ groups, in
       }
       dl = warp_sum(acc);
       l2 = lse[(int64_t)h * rows_total + row] * 1.4426950408889634f;
-      *reinterpret_cast<float4*>(dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (lane == 0) {
       out[r] = l2;
@@ -178,14 +176,13 @@ cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t 
 }
 
 cudaError_t launch_preprocess_tiled(const augtree_plan* p, bool prompt_side, const void* o, const void* dO,
-                                    const float* lse, float* stats, float* dq_acc, cudaStream_t st) {
+                                    const float* lse, float* stats, cudaStream_t st) {
   const int ntiles = prompt_side ? p->ntiles_p : p->ntiles_r;
   if (ntiles == 0) return cudaSuccess;
   dim3 grid(ntiles, p->cfg.hq);
   preprocess_tiled_kernel<<<grid, 128, 0, st>>>(p->groups_d, p->n_groups, prompt_side, ntiles,
                                                 (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, lse,
-                                                prompt_side ? p->total_prompt : p->total_resp, p->cfg.hq, stats,
-                                                dq_acc);
+                                                prompt_side ? p->total_prompt : p->total_resp, p->cfg.hq, stats);
   return cudaGetLastError();
 }
 

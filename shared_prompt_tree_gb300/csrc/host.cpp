@@ -94,9 +94,9 @@ int resolve_family(const augtree_config* c) {
 
 void tiles_for(int family, int op, int* bm, int* bn) {
   if (family == AUGTREE_KERNEL_TC) {
-    // Forward: 128 query rows x 128 keys per tile; backward: 128 keys x 64 query rows.
+    // 128 query rows x 128 keys per tile, forward and backward.
     *bn = 128;
-    *bm = (op == AUGTREE_OP_PREFILL_FWD || op == AUGTREE_OP_REPLAY_FWD) ? 128 : 64;
+    *bm = 128;
   } else {
     *bm = 64;
     *bn = 64;
@@ -218,12 +218,17 @@ static size_t stats_bytes(const augtree_plan* p, bool prompt_side) {
   return hq * (size_t)(prompt_side ? p->total_prompt : p->total_resp) * 4;
 }
 
+// The tensor-core backward writes dQ once per query tile (no fp32 accumulator).
+static size_t dq_acc_bytes(const augtree_plan* p, size_t rows) {
+  return p->family == AUGTREE_KERNEL_TC ? 0 : align256(rows * p->cfg.hq * p->cfg.head_dim * 4);
+}
+
 BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
   BwdWorkspace w;
-  const size_t hq = p->cfg.hq, hkv = p->cfg.hkv, d = p->cfg.head_dim, R = p->total_resp;
+  const size_t hkv = p->cfg.hkv, d = p->cfg.head_dim, R = p->total_resp;
   w.delta_off = 0;
   w.dq_off = align256(stats_bytes(p, false));
-  w.dkpart_off = w.dq_off + align256(R * hq * d * 4);
+  w.dkpart_off = w.dq_off + dq_acc_bytes(p, R);
   w.dvpart_off = w.dkpart_off + align256((size_t)p->part_rows * hkv * d * 4);
   w.slots_off = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
   w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
@@ -232,10 +237,10 @@ BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
 
 BwdWorkspace prefill_bwd_ws(const augtree_plan* p) {
   BwdWorkspace w;
-  const size_t hq = p->cfg.hq, d = p->cfg.head_dim, P = p->total_prompt;
+  const size_t P = p->total_prompt;
   w.delta_off = 0;
   w.dq_off = align256(stats_bytes(p, true));
-  w.dkpart_off = w.dvpart_off = w.slots_off = w.dq_off + align256(P * hq * d * 4);
+  w.dkpart_off = w.dvpart_off = w.slots_off = w.dq_off + dq_acc_bytes(p, P);
   w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
   return w;
 }
@@ -552,17 +557,22 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
   const int dt = p->cfg.dtype;
   cudaError_t e = cudaSuccess;
   const bool tc = p->family == AUGTREE_KERNEL_TC;
-  if (p->total_resp > 0)
-    e = tc ? launch_preprocess_tiled(p, false, or_, dor, lse_r, delta, dq_acc, s)
-           : launch_preprocess(or_, dor, dt, p->total_resp, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
-  if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0) {
-    if (tc)
-      e = tc_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dq_acc, dkr, dvr, dk_part, dv_part,
-                 dkp_sum, dvp_sum, nullptr, nullptr, (float*)(base + w.slots_off), s);
-    else
-      e = simt_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
-                   dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
+  if (tc) {
+    // Key side (response dK/dV, prompt dK/dV summed over the branches), the split-K
+    // reduction of the prompt partials, then the query side (dQ).
+    if (p->total_resp > 0) e = launch_preprocess_tiled(p, false, or_, dor, lse_r, delta, s);
+    if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0)
+      e = tc_bwd_kv(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dkr, dvr, dk_part, dv_part, dkp_sum,
+                    dvp_sum, nullptr, nullptr, (float*)(base + w.slots_off), s);
+    if (e == cudaSuccess && p->total_prompt > 0) e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
+    if (e == cudaSuccess && p->total_resp > 0) e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dqr, s);
+    return from_cuda(e);
   }
+  if (p->total_resp > 0)
+    e = launch_preprocess(or_, dor, dt, p->total_resp, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
+  if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0)
+    e = simt_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
+                 dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
   if (e == cudaSuccess && p->total_prompt > 0) e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
   if (e == cudaSuccess && p->total_resp > 0)
     e = launch_dq_convert(dq_acc, dqr, dt, (int64_t)p->total_resp * p->cfg.hq * p->cfg.head_dim, s);
@@ -589,16 +599,18 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
   float* dq_acc = (float*)(base + w.dq_off);
   const int dt = p->cfg.dtype;
   const bool tc = p->family == AUGTREE_KERNEL_TC;
-  cudaError_t e = tc ? launch_preprocess_tiled(p, true, op, dop, lse_p, delta, dq_acc, s)
-                     : launch_preprocess(op, dop, dt, p->total_prompt, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
-  if (e == cudaSuccess && p->n_items[AUGTREE_OP_PREFILL_BWD] > 0) {
-    if (tc)
-      e = tc_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dq_acc, dkp, dvp, nullptr,
-                 nullptr, nullptr, nullptr, dkp_acc, dvp_acc, (float*)(base + w.slots_off), s);
-    else
-      e = simt_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
-                   nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
+  if (tc) {
+    cudaError_t e = launch_preprocess_tiled(p, true, op, dop, lse_p, delta, s);
+    if (e == cudaSuccess)
+      e = tc_bwd_kv(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dkp, dvp, nullptr, nullptr,
+                    nullptr, nullptr, dkp_acc, dvp_acc, (float*)(base + w.slots_off), s);
+    if (e == cudaSuccess) e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dqp, s);
+    return from_cuda(e);
   }
+  cudaError_t e = launch_preprocess(op, dop, dt, p->total_prompt, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
+  if (e == cudaSuccess && p->n_items[AUGTREE_OP_PREFILL_BWD] > 0)
+    e = simt_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
+                 nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
   if (e == cudaSuccess)
     e = launch_dq_convert(dq_acc, dqp, dt, (int64_t)p->total_prompt * p->cfg.hq * p->cfg.head_dim, s);
   return from_cuda(e);

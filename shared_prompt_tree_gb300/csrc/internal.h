@@ -15,14 +15,14 @@ enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3,
 constexpr int kMaxSplit = 64;
 
 // Per-group geometry on the device: first prompt row, prompt length, first response
-// row, total response length of the group's branches, and the group's first 64-row
+// row, total response length of the group's branches, and the group's first 128-row
 // query tile on the prompt side and on the response side in the tiled backward
 // row-statistics buffer (tensor-core family).
 struct GroupInfo {
   int32_t p0, lp, r0, lr;
   int32_t tp0, tr0;
 };
-constexpr int kStatRows = 64;  // rows per tile of the backward row-statistics buffer
+constexpr int kStatRows = 128;  // rows per tile of the backward row-statistics buffer
 
 // Per-group split-K bookkeeping of the replay backward (prompt dK/dV partials).
 struct SplitInfo {
@@ -63,7 +63,7 @@ struct augtree_plan {
   int32_t* queue_d[4];
   int paired[4];      // forward tensor-core units take two items (two heads of one KV head)
   int quad[4];        // forward units of four items (four heads of one KV head) for SM pairs
-  int32_t ntiles_p, ntiles_r;  // 64-row query tiles per side (row-statistics buffer)
+  int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
 };
 
@@ -107,18 +107,22 @@ cudaError_t simt_bwd(const augtree_plan* p, int op, const void* q, const void* k
 // Tensor-core family (bf16).
 cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
                    const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);
-cudaError_t tc_bwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
-                   const void* kr, const void* vr, const float* stats, const void* dO, float* dq_acc, void* dk_out, void* dv_out,
-                   float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
-                   const float* dk_add, const float* dv_add, float* slots, cudaStream_t st);
+// Backward, key side (dK, dV; prompt dK/dV summed over the branches, split-K partials
+// reduced afterwards) and query side (dQ, written once per query tile and head).
+cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
+                      const void* vr, const float* stats, const void* dO, void* dk_out, void* dv_out, float* dk_part,
+                      float* dv_part, float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add,
+                      float* slots, cudaStream_t st);
+cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
+                      const void* vr, const float* stats, const void* dO, void* dq, cudaStream_t st);
 
 // Memory-bound helpers.
 cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d,
                               float* delta, float* dq_acc, cudaStream_t st);
-// Tensor-core backward preprocess: per (64-row query tile, head) writes 512 bytes
-// {lse * log2(e) [64], Delta [64]} (zeros past the group's end) and zeroes dQ_acc.
+// Tensor-core backward preprocess: per (128-row query tile, head) writes 1 KB
+// {lse * log2(e) [128], Delta [128]} (zeros past the group's end).
 cudaError_t launch_preprocess_tiled(const augtree_plan* p, bool prompt_side, const void* o, const void* dO,
-                                    const float* lse, float* stats, float* dq_acc, cudaStream_t st);
+                                    const float* lse, float* stats, cudaStream_t st);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int dtype, int64_t n, cudaStream_t st);
 cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, const float* dv_part,
                                 float* dk_sum, float* dv_sum, cudaStream_t st);

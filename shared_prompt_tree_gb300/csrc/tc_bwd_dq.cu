@@ -1,0 +1,356 @@
+// Tensor-core backward of tree attention on sm_103a, query side: dQ.
+//
+// AugTree paper, "Splitting Prompt Prefill from Response Replay ...":
+//   Sec. 2.2  attention as Q-KV tile interactions;
+//   Sec. 3.2  prefill rows see the prompt causally; a replay row (Eq. 1) sees all prompt
+//             keys of its group and its own branch's keys up to itself;
+//   Sec. 3.3  the gradient of a response query sums over its prompt part and its own
+//             part: here one accumulator walks the prompt tiles, then the own tiles.
+//
+// One thread block per work item of the forward queue: one query tile of 128 rows for
+// one query head.  Q and dO stay in shared memory; K/V tiles stream through a 2-stage
+// ring.  Per KV tile j (thread = query row = TMEM lane; lse and Delta are per-thread
+// scalars):
+//   S    = Q K^T          (TMEM, fp32)  -> P  = exp2(s S log2e - lse)   (registers)
+//   dP   = dO V^T         (TMEM, fp32)  -> dS = P (dP - Delta)          (bf16 into TMEM
+//                                          over S, the A operand of the next product)
+//   dQ  += dS K           (A = dS from TMEM, B = K read MN-major from the same tile)
+// dQ accumulates in TMEM over every KV tile of the row and is written once (bf16, times
+// the softmax scale): no atomics, no fp32 accumulator in memory.
+// Warps: 0-7 two warpgroups, warpgroup w takes key columns [64w, 64w + 64) of every
+//        tile (lanes = rows, as TMEM access requires warp % 4 = lane quarter);
+//        8 TMA producer; 9 TMEM allocator + MMA issuer.
+// TMEM columns: S0/dS0 [0,128), S1/dS1 [128,256), dP [256,384), dQ [384,512).
+// MMA issue order S(j+1), dQ(j), dP(j+1): every TMEM reuse then waits on an MMA group
+// that already has another group queued behind it.
+#include <cuda.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+#include "tc_fwd_softmax.cuh"
+
+namespace augtree {
+namespace {
+
+using namespace tc;
+
+constexpr int DQ_THREADS = 320;
+constexpr int DQ_NST = 2;                          // K/V ring stages
+constexpr int BLK = 128 * 128;                     // 128 rows x 64 dims bf16 = 16 KB
+constexpr int DQ_Q_OFF = 0;                        // 2 blocks
+constexpr int DQ_DO_OFF = DQ_Q_OFF + 2 * BLK;      // 2 blocks
+constexpr int DQ_K_OFF = DQ_DO_OFF + 2 * BLK;      // [stage][2 blocks]
+constexpr int DQ_V_OFF = DQ_K_OFF + DQ_NST * 2 * BLK;
+constexpr int DQ_BAR_OFF = DQ_V_OFF + DQ_NST * 2 * BLK;
+constexpr int DQ_SMEM = DQ_BAR_OFF + 256 + 1024;
+
+constexpr uint32_t T_S = 0, T_DP = 256, T_DQ = 384;
+
+struct DqBars {
+  uint64_t q_full;
+  uint64_t kv_full[DQ_NST];
+  uint64_t kv_empty[DQ_NST];
+  uint64_t s_full[2];
+  uint64_t dp_full;
+  uint64_t dp_free;
+  uint64_t ds_ready[2];
+  uint64_t dq_done[2];
+  uint64_t acc_done;
+  uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+    const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
+    const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr, Geometry geo,
+    const int32_t* __restrict__ queue, int bm, int bn, const float* __restrict__ stats, int ntiles,
+    __nv_bfloat16* __restrict__ dq_out, uint32_t* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqBars* bars = reinterpret_cast<DqBars*>(smem + DQ_BAR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const WorkItem it = load_item(queue, blockIdx.x);
+  const int h = it.head;
+  const GroupInfo G = geo.groups[it.group];
+  const bool prefill = it.kind == K_PREFILL_Q;
+  const int64_t base = prefill ? G.p0 : G.r0;
+  const int64_t len = prefill ? G.lp : G.lr;
+  const int64_t row0 = base + (int64_t)it.tile * bm;
+  const int64_t row_end = min(row0 + (int64_t)bm, base + len);
+  const int n_a = it.a;
+  const int n_tiles = n_a + (prefill ? 0 : it.b);
+  const int64_t own0 = prefill ? 0 : geo.row_bstart[row0];
+  const int kvh = h / (geo.hq / geo.hkv);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < DQ_NST; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->ds_ready[b], 256);
+      mbar_init(&bars->dq_done[b], 1);
+    }
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 256);
+    mbar_init(&bars->acc_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_kp);
+    prefetch_tmap(&tm_vp);
+    prefetch_tmap(&tm_kr);
+    prefetch_tmap(&tm_vr);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(&bars->q_full, 4 * BLK);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_3d(smem + DQ_Q_OFF + kb * BLK, &tm_q, &bars->q_full, kb * 64, h, (int)row0);
+        tma_load_3d(smem + DQ_DO_OFF + kb * BLK, &tm_do, &bars->q_full, kb * 64, h, (int)row0);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int stage = j % DQ_NST, use = j / DQ_NST;
+        if (!mbar_wait(&bars->kv_empty[stage], (use & 1) ^ 1, err)) break;
+        mbar_expect_tx(&bars->kv_full[stage], 4 * BLK);
+        const bool own = j >= n_a;
+        const int krow = own ? (int)(own0 + (int64_t)(j - n_a) * bn) : (int)(G.p0 + (int64_t)j * bn);
+        const CUtensorMap* km = own ? &tm_kr : &tm_kp;
+        const CUtensorMap* vm = own ? &tm_vr : &tm_vp;
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_3d(smem + DQ_K_OFF + (stage * 2 + kb) * BLK, km, &bars->kv_full[stage], kb * 64, kvh, krow);
+          tma_load_3d(smem + DQ_V_OFF + (stage * 2 + kb) * BLK, vm, &bars->kv_full[stage], kb * 64, kvh, krow);
+        }
+        issued = j + 1;
+      }
+      // Never leave a copy in flight.
+      mbar_wait(&bars->q_full, 0, err);
+      for (int j = max(0, issued - DQ_NST); j < issued; ++j) mbar_wait(&bars->kv_full[j % DQ_NST], (j / DQ_NST) & 1, err);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // Q K^T, dO V^T
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, 128, false, true);   // dS K (B MN-major)
+      const uint64_t dQd = smem_desc_sw128(smem_u32(smem + DQ_Q_OFF), 16, 1024);
+      const uint64_t dOd = smem_desc_sw128(smem_u32(smem + DQ_DO_OFF), 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + DQ_K_OFF), 16, 1024);
+      const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + DQ_V_OFF), 16, 1024);
+      const uint64_t dKm0 = smem_desc_sw128(smem_u32(smem + DQ_K_OFF), BLK, 1024);  // K as [keys x dims], MN-major
+      constexpr uint64_t kStage = (2 * BLK) >> 4;
+      // K-major k-step kk (16 dims): dim block kk/4, 32 bytes per step in the 128-byte row.
+      auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * BLK + (kk & 3) * 32) >> 4); };
+      auto issue_s = [&](int j) {
+        const uint64_t dk = dK0 + (j % DQ_NST) * kStage;
+        const uint32_t d = tmem + T_S + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(d, dQd + koff(kk), dk + koff(kk), id_ss, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->s_full[j & 1]);
+      };
+      auto issue_dp = [&](int j) {
+        const uint64_t dv = dV0 + (j % DQ_NST) * kStage;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + T_DP, dOd + koff(kk), dv + koff(kk), id_ss, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dp_full);
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, err);
+      if (ok && n_tiles > 0) ok = mbar_wait(&bars->kv_full[0], 0, err);
+      tc_fence_after();
+      if (ok && n_tiles > 0) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const bool more = j + 1 < n_tiles;
+        if (more) {
+          // S(j+1) goes to the buffer that holds dS(j-1): dQ(j-1) must have read it.
+          if (!(ok = mbar_wait(&bars->kv_full[(j + 1) % DQ_NST], ((j + 1) / DQ_NST) & 1, err))) break;
+          if (j >= 1 && !(ok = mbar_wait(&bars->dq_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err))) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        // dQ += dS(j) K(j): 16 keys per step; keys [64w, 64w + 64) were packed by
+        // warpgroup w into columns [64w, 64w + 32) of the S buffer.
+        if (!(ok = mbar_wait(&bars->ds_ready[j & 1], (j >> 1) & 1, err))) break;
+        tc_fence_after();
+        {
+          const uint32_t a0 = tmem + T_S + (j & 1) * 128;
+          const uint64_t b0 = dKm0 + (j % DQ_NST) * kStage;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + T_DQ, a0 + (kk >> 2) * 64 + (kk & 3) * 8, b0 + kk * (2048 >> 4), id_dq,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars->dq_done[j & 1]);
+        mma_commit(&bars->kv_empty[j % DQ_NST]);
+        if (more) {
+          // dP(j+1) overwrites dP(j): the compute warps must have read it.
+          if (!(ok = mbar_wait(&bars->dp_free, j & 1, err))) break;
+          tc_fence_after();
+          issue_dp(j + 1);
+        }
+      }
+      mma_commit(&bars->acc_done);
+    }
+  } else {
+    // ------------------------------------------------------------ P, dS (thread = row)
+    const int w = warp >> 2;           // key columns [64w, 64w + 64)
+    const int q4 = warp & 3;           // TMEM lane quarter
+    const int r_local = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    FwdRowGeom g;
+    g.row = row0 + r_local;
+    g.row_ok = g.row < row_end;
+    g.prefill = prefill;
+    g.bs = (!prefill && g.row_ok) ? geo.row_bstart[g.row] : 0;
+    g.p0 = G.p0;
+    g.p_end = (int64_t)G.p0 + G.lp;
+    g.own0 = own0;
+    g.n_a = n_a;
+    g.bn = bn;
+    const int tile_base = prefill ? G.tp0 : G.tr0;
+    const float* st = stats + ((int64_t)h * ntiles + tile_base + it.tile) * 2 * kStatRows;
+    const float lse2 = st[r_local];
+    const float delta = st[kStatRows + r_local];
+    const float sl2 = geo.scale_log2;
+    const int c0 = 64 * w;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!(ok = mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, err))) break;
+      tc_fence_after();
+      const uint32_t ts = tmem + lane_off + T_S + (j & 1) * 128 + c0;
+      uint32_t sv[2][32];  // S, then P in place (fp32)
+      tmem_ld32(ts, sv[0]);
+      tmem_ld32(ts + 32, sv[1]);
+      tmem_ld_wait();
+      int lo, hi;
+      fwd_valid_cols(g, j, lo, hi);  // valid columns [lo, hi] of the tile, clamped
+      const int lo_r = lo - c0;
+      const uint32_t span = hi >= lo ? (uint32_t)(hi - lo) : 0xFFFFFFFFu;  // all-invalid if empty
+      if (lo_r <= 0 && hi - c0 >= 63 && hi >= lo) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          sv[c >> 5][c & 31] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]), sl2, -lse2)));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float e = fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]), sl2, -lse2));
+          const bool v = span != 0xFFFFFFFFu && (uint32_t)(c - lo_r) <= span;
+          sv[c >> 5][c & 31] = __float_as_uint(v ? e : 0.f);
+        }
+      }
+      if (!(ok = mbar_wait(&bars->dp_full, j & 1, err))) break;
+      tc_fence_after();
+      uint32_t pk[2][16];  // dS as bf16 pairs
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_off + T_DP + c0 + half * 32, dp);
+        tmem_ld_wait();
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->dp_free);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d0 = __uint_as_float(sv[half][2 * i]) * (__uint_as_float(dp[2 * i]) - delta);
+          const float d1 = __uint_as_float(sv[half][2 * i + 1]) * (__uint_as_float(dp[2 * i + 1]) - delta);
+          pk[half][i] = pack_bf16x2(d0, d1);
+        }
+      }
+      {
+        uint32_t all[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          all[i] = pk[0][i];
+          all[16 + i] = pk[1][i];
+        }
+        tmem_st32(ts, all);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_ready[j & 1]);
+    }
+    // dQ rows: warpgroup w writes dims [64w, 64w + 64) of its rows.
+    if (ok && mbar_wait(&bars->acc_done, 0, err)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + T_DQ + c0 + half * 32, v);
+        tmem_ld_wait();
+        if (g.row_ok) {
+          const bool any = n_tiles > 0;
+          uint32_t o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            o[i] = any ? pack_bf16x2(__uint_as_float(v[2 * i]) * geo.scale, __uint_as_float(v[2 * i + 1]) * geo.scale)
+                       : 0u;
+          uint4* d4 = reinterpret_cast<uint4*>(dq_out + (g.row * geo.hq + h) * 128 + c0 + half * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
+                      const void* vr, const float* stats, const void* dO, void* dq, cudaStream_t st) {
+  // The query-side items of the backward are those of the matching forward op.
+  const bool prefill = op == AUGTREE_OP_PREFILL_BWD;
+  const int fop = prefill ? AUGTREE_OP_PREFILL_FWD : AUGTREE_OP_REPLAY_FWD;
+  if (p->n_items[fop] == 0) return cudaSuccess;
+  const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
+  CUtensorMap mq, mdo, mkp, mvp, mkr, mvr;
+  if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, 128)) return cudaErrorInvalidValue;
+  if (!encode_rows_map(&mdo, dO, q_rows, p->cfg.hq, 128)) return cudaErrorInvalidValue;
+  const bool have_p = p->total_prompt > 0 && kp && vp;
+  const bool have_r = !prefill && p->total_resp > 0 && kr && vr;
+  if (have_p) {
+    if (!encode_rows_map(&mkp, kp, p->total_prompt, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+    if (!encode_rows_map(&mvp, vp, p->total_prompt, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+  }
+  if (have_r) {
+    if (!encode_rows_map(&mkr, kr, p->total_resp, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+    if (!encode_rows_map(&mvr, vr, p->total_resp, p->cfg.hkv, 128)) return cudaErrorInvalidValue;
+  }
+  if (!have_p) {
+    mkp = have_r ? mkr : mq;
+    mvp = have_r ? mvr : mq;
+  }
+  if (!have_r) {
+    mkr = mkp;
+    mvr = mvp;
+  }
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
+  if (e != cudaSuccess) return e;
+  tc_bwd_dq_kernel<<<(unsigned)p->n_items[fop], DQ_THREADS, DQ_SMEM, st>>>(
+      mq, mdo, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[fop], p->bm[fop], p->bn[fop], stats,
+      prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dq, p->err_d);
+  return cudaGetLastError();
+}
+
+}  // namespace augtree
