@@ -1,5 +1,6 @@
-// Memory-bound kernels of the path: the backward preprocess (Delta and the zeroed fp32
-// dQ accumulator), the dQ conversion, the fixed-order split-K reduction of the prompt
+// Memory-bound kernels of the path: the backward preprocess (Delta, the SIMT family's
+// zeroed fp32 dQ accumulator, the tensor-core family's tiled row statistics), the dQ
+// conversion, the fixed-order split-K reduction of the prompt
 // K/V gradient (Eq. 2), and the partial-state merge of Sec. 3.3.
 //
 // AugTree paper, Sec. 3.2 (Eq. 2: the prompt K/V gradient is the sum over branches,
@@ -30,14 +31,33 @@ __global__ void preprocess_kernel(const T* __restrict__ o, const T* __restrict__
   for (int c = lane; c < d; c += 32) dq_acc[base + c] = 0.f;
 }
 
-// One block (4 warps) per (64-row query tile, head); tiles of all groups are numbered
-// consecutively (GroupInfo::tp0 / tr0).  Writes stats[h][tile] = {lse*log2e [64],
-// Delta [64]} with zeros for rows past the group's end, and zeroes the valid rows'
-// dQ accumulator for head h.
+// Rounds to bf16 (nearest even) and returns the bits.
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+// x as hi + mid + lo, three bf16 values (the sum carries about 24 significant bits).
+__device__ __forceinline__ uint4 split3_row(float x) {
+  const uint16_t h = bf16_bits(x);
+  const float r1 = x - __bfloat162float(__ushort_as_bfloat16(h));
+  const uint16_t m = bf16_bits(r1);
+  const float r2 = r1 - __bfloat162float(__ushort_as_bfloat16(m));
+  const uint16_t l = bf16_bits(r2);
+  return make_uint4((uint32_t)h | ((uint32_t)m << 16), (uint32_t)l, 0u, 0u);
+}
+
+// One block (4 warps) per (128-row query tile, head); tiles of all groups are numbered
+// consecutively (GroupInfo::tp0 / tr0).  Writes
+//   stats[h][tile] = {lse*log2e [128], Delta [128]}  (fp32, for the query-side kernel)
+//   aug[h][tile]   = {L [128][8], D [128][8]}        (bf16, for the key-side kernel)
+// where row r of L holds -lse/s and row r of D holds -Delta, each split into three
+// bf16 values in columns 0-2 (columns 3-7 zero).  The key-side kernel multiplies these
+// rows by a constant ones operand in one extra K=16 MMA step, so its accumulators hold
+// S - lse/s and dP - Delta directly.  Rows past the group's end are zero.
 __global__ void preprocess_tiled_kernel(const GroupInfo* __restrict__ groups, int n_groups, bool prompt_side,
                                         int ntiles, const __nv_bfloat16* __restrict__ o,
                                         const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
-                                        int64_t rows_total, int hq, float* __restrict__ stats) {
+                                        int64_t rows_total, int hq, float inv_scale, float* __restrict__ stats,
+                                        uint4* __restrict__ aug) {
   const int tile = blockIdx.x;
   const int h = blockIdx.y;
   // group holding this tile: last group whose first tile is <= tile and that has tiles
@@ -51,12 +71,16 @@ __global__ void preprocess_tiled_kernel(const GroupInfo* __restrict__ groups, in
   const int64_t base = prompt_side ? G.p0 : G.r0;
   const int64_t len = prompt_side ? G.lp : G.lr;
   const int64_t row0 = base + (int64_t)(tile - (prompt_side ? G.tp0 : G.tr0)) * kStatRows;
-  float* out = stats + ((int64_t)h * ntiles + tile) * 2 * kStatRows;
+  const int64_t blk = (int64_t)h * ntiles + tile;
+  float* out = stats + blk * 2 * kStatRows;
+  uint4* aug_l = aug + blk * 2 * kStatRows;  // one 16-byte row per query row
+  uint4* aug_d = aug_l + kStatRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = warp; r < kStatRows; r += 4) {
     const int64_t row = row0 + r;
-    float dl = 0.f, l2 = 0.f;
-    if (row < base + len) {
+    float dl = 0.f, l2 = 0.f, ln = 0.f;
+    const bool valid = row < base + len;
+    if (valid) {
       const int64_t off = (row * hq + h) * 128 + lane * 4;
       const uint2 a = *reinterpret_cast<const uint2*>(o + off);
       const uint2 b = *reinterpret_cast<const uint2*>(dO + off);
@@ -69,14 +93,18 @@ __global__ void preprocess_tiled_kernel(const GroupInfo* __restrict__ groups, in
         acc += x.x * y.x + x.y * y.y;
       }
       dl = warp_sum(acc);
-      l2 = lse[(int64_t)h * rows_total + row] * 1.4426950408889634f;
+      ln = lse[(int64_t)h * rows_total + row];
+      l2 = ln * 1.4426950408889634f;
     }
     if (lane == 0) {
       out[r] = l2;
       out[kStatRows + r] = dl;
+      aug_l[r] = valid ? split3_row(-ln * inv_scale) : make_uint4(0u, 0u, 0u, 0u);
+      aug_d[r] = valid ? split3_row(-dl) : make_uint4(0u, 0u, 0u, 0u);
     }
   }
 }
+
 
 template <typename T>
 __global__ void convert_kernel(const float* __restrict__ src, T* __restrict__ dst, int64_t n) {
@@ -176,13 +204,14 @@ cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t 
 }
 
 cudaError_t launch_preprocess_tiled(const augtree_plan* p, bool prompt_side, const void* o, const void* dO,
-                                    const float* lse, float* stats, cudaStream_t st) {
+                                    const float* lse, float* stats, void* aug, cudaStream_t st) {
   const int ntiles = prompt_side ? p->ntiles_p : p->ntiles_r;
   if (ntiles == 0) return cudaSuccess;
   dim3 grid(ntiles, p->cfg.hq);
   preprocess_tiled_kernel<<<grid, 128, 0, st>>>(p->groups_d, p->n_groups, prompt_side, ntiles,
                                                 (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, lse,
-                                                prompt_side ? p->total_prompt : p->total_resp, p->cfg.hq, stats);
+                                                prompt_side ? p->total_prompt : p->total_resp, p->cfg.hq,
+                                                1.0f / geometry(p).scale, stats, (uint4*)aug);
   return cudaGetLastError();
 }
 

@@ -94,9 +94,10 @@ int resolve_family(const augtree_config* c) {
 
 void tiles_for(int family, int op, int* bm, int* bn) {
   if (family == AUGTREE_KERNEL_TC) {
-    // 128 query rows x 128 keys per tile, forward and backward.
+    // 128 keys per KV tile; 128 query rows per query tile (the backward's key-side
+    // queue walks tiles of kTcBwdKvRows rows).
     *bn = 128;
-    *bm = 128;
+    *bm = (op == AUGTREE_OP_PREFILL_FWD || op == AUGTREE_OP_REPLAY_FWD) ? 128 : kTcBwdKvRows;
   } else {
     *bm = 64;
     *bn = 64;
@@ -223,11 +224,18 @@ static size_t dq_acc_bytes(const augtree_plan* p, size_t rows) {
   return p->family == AUGTREE_KERNEL_TC ? 0 : align256(rows * p->cfg.hq * p->cfg.head_dim * 4);
 }
 
+// Tensor-core family: the key-side kernel's {-lse/s, -Delta} rows per query tile.
+static size_t aug_bytes(const augtree_plan* p, bool prompt_side) {
+  if (p->family != AUGTREE_KERNEL_TC) return 0;
+  return align256((size_t)p->cfg.hq * (prompt_side ? p->ntiles_p : p->ntiles_r) * kAugTileBytes);
+}
+
 BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
   BwdWorkspace w;
   const size_t hkv = p->cfg.hkv, d = p->cfg.head_dim, R = p->total_resp;
   w.delta_off = 0;
-  w.dq_off = align256(stats_bytes(p, false));
+  w.aug_off = align256(stats_bytes(p, false));
+  w.dq_off = w.aug_off + aug_bytes(p, false);
   w.dkpart_off = w.dq_off + dq_acc_bytes(p, R);
   w.dvpart_off = w.dkpart_off + align256((size_t)p->part_rows * hkv * d * 4);
   w.slots_off = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
@@ -239,7 +247,8 @@ BwdWorkspace prefill_bwd_ws(const augtree_plan* p) {
   BwdWorkspace w;
   const size_t P = p->total_prompt;
   w.delta_off = 0;
-  w.dq_off = align256(stats_bytes(p, true));
+  w.aug_off = align256(stats_bytes(p, true));
+  w.dq_off = w.aug_off + aug_bytes(p, true);
   w.dkpart_off = w.dvpart_off = w.slots_off = w.dq_off + dq_acc_bytes(p, P);
   w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
   return w;
@@ -560,9 +569,10 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
   if (tc) {
     // Key side (response dK/dV, prompt dK/dV summed over the branches), the split-K
     // reduction of the prompt partials, then the query side (dQ).
-    if (p->total_resp > 0) e = launch_preprocess_tiled(p, false, or_, dor, lse_r, delta, s);
+    void* aug = base + w.aug_off;
+    if (p->total_resp > 0) e = launch_preprocess_tiled(p, false, or_, dor, lse_r, delta, aug, s);
     if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0)
-      e = tc_bwd_kv(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dkr, dvr, dk_part, dv_part, dkp_sum,
+      e = tc_bwd_kv(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, aug, dor, dkr, dvr, dk_part, dv_part, dkp_sum,
                     dvp_sum, nullptr, nullptr, (float*)(base + w.slots_off), s);
     if (e == cudaSuccess && p->total_prompt > 0) e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
     if (e == cudaSuccess && p->total_resp > 0) e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dqr, s);
@@ -600,9 +610,10 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
   const int dt = p->cfg.dtype;
   const bool tc = p->family == AUGTREE_KERNEL_TC;
   if (tc) {
-    cudaError_t e = launch_preprocess_tiled(p, true, op, dop, lse_p, delta, s);
+    void* aug = base + w.aug_off;
+    cudaError_t e = launch_preprocess_tiled(p, true, op, dop, lse_p, delta, aug, s);
     if (e == cudaSuccess)
-      e = tc_bwd_kv(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dkp, dvp, nullptr, nullptr,
+      e = tc_bwd_kv(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, aug, dop, dkp, dvp, nullptr, nullptr,
                     nullptr, nullptr, dkp_acc, dvp_acc, (float*)(base + w.slots_off), s);
     if (e == cudaSuccess) e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dqp, s);
     return from_cuda(e);

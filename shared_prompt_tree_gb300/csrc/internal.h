@@ -23,6 +23,7 @@ struct GroupInfo {
   int32_t tp0, tr0;
 };
 constexpr int kStatRows = 128;  // rows per tile of the backward row-statistics buffer
+constexpr int kTcBwdKvRows = 128;  // query rows per tile of the tensor-core key-side backward (128 or 64)
 
 // Per-group split-K bookkeeping of the replay backward (prompt dK/dV partials).
 struct SplitInfo {
@@ -76,8 +77,9 @@ augtree_status build_queue(const std::vector<int32_t>& prompt_off, const std::ve
 
 // Workspace layout of the backward calls.
 struct BwdWorkspace {
-  size_t delta_off, dq_off, dkpart_off, dvpart_off, slots_off, total;
+  size_t delta_off, aug_off, dq_off, dkpart_off, dvpart_off, slots_off, total;
 };
+constexpr int kAugTileBytes = 2 * kStatRows * 16;  // {L, D} rows of one query tile
 // fp32 flush slots of the tensor-core backward: one per SM id, 128 keys x 256 floats.
 constexpr int kFlushSlots = 256;
 constexpr size_t kFlushSlotBytes = (size_t)128 * 256 * 4;
@@ -110,7 +112,7 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
 // Backward, key side (dK, dV; prompt dK/dV summed over the branches, split-K partials
 // reduced afterwards) and query side (dQ, written once per query tile and head).
 cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                      const void* vr, const float* stats, const void* dO, void* dk_out, void* dv_out, float* dk_part,
+                      const void* vr, const void* aug, const void* dO, void* dk_out, void* dv_out, float* dk_part,
                       float* dv_part, float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add,
                       float* slots, cudaStream_t st);
 cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
@@ -119,10 +121,11 @@ cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* 
 // Memory-bound helpers.
 cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d,
                               float* delta, float* dq_acc, cudaStream_t st);
-// Tensor-core backward preprocess: per (128-row query tile, head) writes 1 KB
-// {lse * log2(e) [128], Delta [128]} (zeros past the group's end).
+// Tensor-core backward preprocess: per (128-row query tile, head) writes 1 KB of fp32
+// {lse * log2(e) [128], Delta [128]} into stats and 4 KB of bf16 rows {-lse/s, -Delta}
+// split three ways into aug (zeros past the group's end).
 cudaError_t launch_preprocess_tiled(const augtree_plan* p, bool prompt_side, const void* o, const void* dO,
-                                    const float* lse, float* stats, cudaStream_t st);
+                                    const float* lse, float* stats, void* aug, cudaStream_t st);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int dtype, int64_t n, cudaStream_t st);
 cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, const float* dv_part,
                                 float* dk_sum, float* dv_sum, cudaStream_t st);

@@ -8,9 +8,9 @@
 //             part: here one accumulator walks the prompt tiles, then the own tiles.
 //
 // One thread block per work item of the forward queue: one query tile of 128 rows for
-// one query head.  Q and dO stay in shared memory; K/V tiles stream through a 2-stage
-// ring.  Per KV tile j (thread = query row = TMEM lane; lse and Delta are per-thread
-// scalars):
+// one query head.  Q and dO stay in shared memory; K tiles stream through a 3-stage
+// ring and V tiles through a 2-stage ring.  Per KV tile j (thread = query row = TMEM
+// lane; lse and Delta are per-thread scalars):
 //   S    = Q K^T          (TMEM, fp32)  -> P  = exp2(s S log2e - lse)   (registers)
 //   dP   = dO V^T         (TMEM, fp32)  -> dS = P (dP - Delta)          (bf16 into TMEM
 //                                          over S, the A operand of the next product)
@@ -37,21 +37,28 @@ namespace {
 using namespace tc;
 
 constexpr int DQ_THREADS = 320;
-constexpr int DQ_NST = 2;                          // K/V ring stages
+// K tiles are read by S(j) and dQ(j), V tiles only by dP(j), so the two rings are
+// separate: a V stage frees as soon as dP(j) is done, and the K ring has one stage more
+// so that K(j+2) can be in flight while dQ(j) still reads K(j).
+constexpr int KST = 3;                             // K ring stages
+constexpr int VST = 2;                             // V ring stages
+constexpr int kPrefetchTiles = 4;                  // L2 prefetch distance (KV tiles)
 constexpr int BLK = 128 * 128;                     // 128 rows x 64 dims bf16 = 16 KB
 constexpr int DQ_Q_OFF = 0;                        // 2 blocks
 constexpr int DQ_DO_OFF = DQ_Q_OFF + 2 * BLK;      // 2 blocks
-constexpr int DQ_K_OFF = DQ_DO_OFF + 2 * BLK;      // [stage][2 blocks]
-constexpr int DQ_V_OFF = DQ_K_OFF + DQ_NST * 2 * BLK;
-constexpr int DQ_BAR_OFF = DQ_V_OFF + DQ_NST * 2 * BLK;
+constexpr int DQ_K_OFF = DQ_DO_OFF + 2 * BLK;      // [KST][2 blocks]
+constexpr int DQ_V_OFF = DQ_K_OFF + KST * 2 * BLK; // [VST][2 blocks]
+constexpr int DQ_BAR_OFF = DQ_V_OFF + VST * 2 * BLK;
 constexpr int DQ_SMEM = DQ_BAR_OFF + 256 + 1024;
 
 constexpr uint32_t T_S = 0, T_DP = 256, T_DQ = 384;
 
 struct DqBars {
   uint64_t q_full;
-  uint64_t kv_full[DQ_NST];
-  uint64_t kv_empty[DQ_NST];
+  uint64_t k_full[KST];
+  uint64_t k_empty[KST];
+  uint64_t v_full[VST];
+  uint64_t v_empty[VST];
   uint64_t s_full[2];
   uint64_t dp_full;
   uint64_t dp_free;
@@ -60,6 +67,13 @@ struct DqBars {
   uint64_t acc_done;
   uint32_t tmem_base;
 };
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 
 __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -87,9 +101,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < DQ_NST; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+    for (int i = 0; i < KST; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < VST; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
@@ -122,24 +140,42 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         tma_load_3d(smem + DQ_Q_OFF + kb * BLK, &tm_q, &bars->q_full, kb * 64, h, (int)row0);
         tma_load_3d(smem + DQ_DO_OFF + kb * BLK, &tm_do, &bars->q_full, kb * 64, h, (int)row0);
       }
-      int issued = 0;
+      auto krow_of = [&](int j) {
+        return j >= n_a ? (int)(own0 + (int64_t)(j - n_a) * bn) : (int)(G.p0 + (int64_t)j * bn);
+      };
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
-        const int stage = j % DQ_NST, use = j / DQ_NST;
-        if (!mbar_wait(&bars->kv_empty[stage], (use & 1) ^ 1, err)) break;
-        mbar_expect_tx(&bars->kv_full[stage], 4 * BLK);
         const bool own = j >= n_a;
-        const int krow = own ? (int)(own0 + (int64_t)(j - n_a) * bn) : (int)(G.p0 + (int64_t)j * bn);
+        const int krow = krow_of(j);
         const CUtensorMap* km = own ? &tm_kr : &tm_kp;
         const CUtensorMap* vm = own ? &tm_vr : &tm_vp;
-        for (int kb = 0; kb < 2; ++kb) {
-          tma_load_3d(smem + DQ_K_OFF + (stage * 2 + kb) * BLK, km, &bars->kv_full[stage], kb * 64, kvh, krow);
-          tma_load_3d(smem + DQ_V_OFF + (stage * 2 + kb) * BLK, vm, &bars->kv_full[stage], kb * 64, kvh, krow);
+        const int ks = j % KST, vs = j % VST;
+        if (!mbar_wait(&bars->k_empty[ks], ((j / KST) & 1) ^ 1, err)) break;
+        mbar_expect_tx(&bars->k_full[ks], 2 * BLK);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_3d(smem + DQ_K_OFF + (ks * 2 + kb) * BLK, km, &bars->k_full[ks], kb * 64, kvh, krow);
+        k_issued = j + 1;
+        if (!mbar_wait(&bars->v_empty[vs], ((j / VST) & 1) ^ 1, err)) break;
+        mbar_expect_tx(&bars->v_full[vs], 2 * BLK);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_3d(smem + DQ_V_OFF + (vs * 2 + kb) * BLK, vm, &bars->v_full[vs], kb * 64, kvh, krow);
+        v_issued = j + 1;
+        // Warm L2 with the K/V tiles a few steps ahead.
+        const int jp = j + kPrefetchTiles;
+        if (jp < n_tiles) {
+          const CUtensorMap* kmp = jp >= n_a ? &tm_kr : &tm_kp;
+          const CUtensorMap* vmp = jp >= n_a ? &tm_vr : &tm_vp;
+          const int rp = krow_of(jp);
+          for (int kb = 0; kb < 2; ++kb) {
+            tma_prefetch_3d(kmp, kb * 64, kvh, rp);
+            tma_prefetch_3d(vmp, kb * 64, kvh, rp);
+          }
         }
-        issued = j + 1;
       }
       // Never leave a copy in flight.
       mbar_wait(&bars->q_full, 0, err);
-      for (int j = max(0, issued - DQ_NST); j < issued; ++j) mbar_wait(&bars->kv_full[j % DQ_NST], (j / DQ_NST) & 1, err);
+      for (int j = max(0, k_issued - KST); j < k_issued; ++j) mbar_wait(&bars->k_full[j % KST], (j / KST) & 1, err);
+      for (int j = max(0, v_issued - VST); j < v_issued; ++j) mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, err);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -155,20 +191,21 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       // K-major k-step kk (16 dims): dim block kk/4, 32 bytes per step in the 128-byte row.
       auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * BLK + (kk & 3) * 32) >> 4); };
       auto issue_s = [&](int j) {
-        const uint64_t dk = dK0 + (j % DQ_NST) * kStage;
+        const uint64_t dk = dK0 + (j % KST) * kStage;
         const uint32_t d = tmem + T_S + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ss(d, dQd + koff(kk), dk + koff(kk), id_ss, kk > 0 ? 1u : 0u);
         mma_commit(&bars->s_full[j & 1]);
       };
       auto issue_dp = [&](int j) {
-        const uint64_t dv = dV0 + (j % DQ_NST) * kStage;
+        const uint64_t dv = dV0 + (j % VST) * kStage;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + T_DP, dOd + koff(kk), dv + koff(kk), id_ss, kk > 0 ? 1u : 0u);
         mma_commit(&bars->dp_full);
+        mma_commit(&bars->v_empty[j % VST]);  // dP(j) is the only reader of V(j)
       };
       bool ok = mbar_wait(&bars->q_full, 0, err);
-      if (ok && n_tiles > 0) ok = mbar_wait(&bars->kv_full[0], 0, err);
+      if (ok && n_tiles > 0) ok = mbar_wait(&bars->k_full[0], 0, err) && mbar_wait(&bars->v_full[0], 0, err);
       tc_fence_after();
       if (ok && n_tiles > 0) {
         issue_s(0);
@@ -178,7 +215,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         const bool more = j + 1 < n_tiles;
         if (more) {
           // S(j+1) goes to the buffer that holds dS(j-1): dQ(j-1) must have read it.
-          if (!(ok = mbar_wait(&bars->kv_full[(j + 1) % DQ_NST], ((j + 1) / DQ_NST) & 1, err))) break;
+          if (!(ok = mbar_wait(&bars->k_full[(j + 1) % KST], ((j + 1) / KST) & 1, err))) break;
           if (j >= 1 && !(ok = mbar_wait(&bars->dq_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err))) break;
           tc_fence_after();
           issue_s(j + 1);
@@ -189,17 +226,18 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         tc_fence_after();
         {
           const uint32_t a0 = tmem + T_S + (j & 1) * 128;
-          const uint64_t b0 = dKm0 + (j % DQ_NST) * kStage;
+          const uint64_t b0 = dKm0 + (j % KST) * kStage;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tmem + T_DQ, a0 + (kk >> 2) * 64 + (kk & 3) * 8, b0 + kk * (2048 >> 4), id_dq,
                    (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->dq_done[j & 1]);
-        mma_commit(&bars->kv_empty[j % DQ_NST]);
+        mma_commit(&bars->k_empty[j % KST]);  // dQ(j) is the last reader of K(j)
         if (more) {
           // dP(j+1) overwrites dP(j): the compute warps must have read it.
           if (!(ok = mbar_wait(&bars->dp_free, j & 1, err))) break;
+          if (!(ok = mbar_wait(&bars->v_full[(j + 1) % VST], ((j + 1) / VST) & 1, err))) break;
           tc_fence_after();
           issue_dp(j + 1);
         }

@@ -11,21 +11,31 @@
 //                    few chunks when the prompt has few tiles; the chunks' partial sums
 //                    are reduced in a fixed order afterwards, no atomics).
 //
-// One thread block per work item: 128 keys of one KV head, query tiles [a, b) of 128
+// One thread block per work item: 128 keys of one KV head, query tiles [a, b) of BMQ
 // rows for each of the r query heads of that KV head.  Per query tile (keys are the
 // MMA M dimension, one key per TMEM lane):
-//   S^T  = K Q^T     (TMEM, fp32)  -> P^T  = exp2(s S^T log2e - lse), bf16 over S^T
-//   dP^T = V dO^T    (TMEM, fp32)  -> dS^T = P^T (dP^T - Delta),     bf16 over dP^T
-//   dV  += P^T dO    (A = P^T from TMEM, B = dO read MN-major)
-//   dK  += dS^T Q    (A = dS^T from TMEM, B = Q read MN-major)
+//   S^T  = K Q^T - lse/s   (TMEM, fp32)  -> P^T  = exp2(s log2e S^T),   bf16 over S^T
+//   dP^T = V dO^T - Delta  (TMEM, fp32)  -> dS^T = P^T dP^T,            bf16 over dP^T
+//   dV  += P^T dO          (A = P^T from TMEM, B = dO read MN-major)
+//   dK  += dS^T Q          (A = dS^T from TMEM, B = Q read MN-major)
+// The per-query terms -lse/s and -Delta enter through one extra K=16 MMA step each
+// (a ones column block times three-way bf16 splits of the values), so the compute
+// warps need no per-query values at all: no shared-memory broadcast loads, which would
+// otherwise take about as much shared-memory bandwidth as the MMA operands.
 // dQ is computed by the query-side kernel, so nothing here leaves the SM per query
-// tile.  Every operand read from shared memory is a 128-wide tile (N = 128).
-// Warps: 0-7 two warpgroups, warpgroup w takes query columns [64w, 64w + 64) of every
-//        tile (thread = key = TMEM lane); 8 TMA producer; 9 TMEM allocator + MMA issuer.
-// TMEM columns: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,384), dK [384,512).
-// MMA issue order S(i), dP(i), dV(i), dK(i), S(i+1), dP(i+1), ...: S(i+1) reuses the
-// columns dV(i) reads and dP(i+1) those dK(i) reads, and each waits for that reader's
-// completion with the next group already queued behind it.
+// tile.
+// MMA issue order per tile: dV(i), S(i+1), dK(i), dP(i+1).  S(i+1) overwrites the
+// columns dV reads and dP(i+1) those dK reads: with 128-row tiles each waits for the
+// completion of the group issued just before it (measured at about 280 cycles after
+// its last issue); with 64-row tiles S^T and dP^T are double-buffered (64 columns each)
+// and the waits target MMAs issued one tile earlier.  128-row tiles measured faster:
+// N=64 MMAs issue no faster than about 50 cycles each, and 64-row tiles take twice as
+// many round trips between the MMA issuer and the compute warps per unit of work.
+// Warps: 0 .. 4 NWG - 1 compute warpgroups, warpgroup w takes query columns
+//        [COLS w, COLS (w + 1)) of every tile (thread = key = TMEM lane); then the TMA
+//        producer warp and the TMEM allocator + MMA issuer warp.
+// TMEM columns: S^T/P^T [0,128), dP^T/dS^T [128,256) (each 2 x 64 when double-
+// buffered), dV [256,384), dK [384,512).
 #include <cuda.h>
 
 #include <cmath>
@@ -38,37 +48,58 @@ namespace {
 
 using namespace tc;
 
-constexpr int KV_THREADS = 320;
-constexpr int NQ = 2;                                   // Q/dO ring stages
-constexpr int kPrefetch = 4;                            // L2 prefetch distance (iterations)
-constexpr int BLK = 128 * 128;                          // 128 rows x 64 dims bf16 = 16 KB
+constexpr int BMQ = kTcBwdKvRows;                       // query rows per tile (128 or 64)
+// With 64-row tiles S^T and dP^T are double-buffered in TMEM (two 64-column halves);
+// with 128-row tiles they take 128 columns each and are reused every tile.
+constexpr bool DB = BMQ == 64;
+constexpr int NWG = 2;                                  // compute warpgroups
+constexpr int COLS = BMQ / NWG;                         // query columns per warpgroup
+constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1;
+constexpr int KV_THREADS = (4 * NWG + 2) * 32;
+constexpr int NQ = DB ? 4 : 2;                          // Q/dO ring stages
+constexpr int kPrefetch = DB ? 6 : 4;                   // L2 prefetch distance (iterations)
+constexpr int BLK = 128 * 128;                          // 128 keys x 64 dims bf16 = 16 KB
+constexpr int QBLK = BMQ * 128;                         // BMQ rows x 64 dims bf16
 constexpr int K_OFF = 0;                                // 2 blocks
 constexpr int V_OFF = K_OFF + 2 * BLK;                  // 2 blocks
 constexpr int Q_OFF = V_OFF + 2 * BLK;                  // [NQ][2 blocks]
-constexpr int DO_OFF = Q_OFF + NQ * 2 * BLK;            // [NQ][2 blocks]
-constexpr int ROWS_OFF = DO_OFF + NQ * 2 * BLK;         // [NQ] x {lse2[128], delta[128]}
-constexpr int BAR_OFF = ROWS_OFF + NQ * 2 * 128 * 4;
-constexpr int KV_SMEM = BAR_OFF + 256 + 1024;
+constexpr int DO_OFF = Q_OFF + NQ * 2 * QBLK;           // [NQ][2 blocks]
+// Operands of the extra K=16 step that adds -lse/s to S^T and -Delta to dP^T: a constant
+// A = [1 1 1 0 ... 0] per key and, per stage, B rows {hi, mid, lo, 0, ...} of -lse/s (L)
+// and -Delta (D) per query row.  Unswizzled K-major layout: core matrices of 8 rows x 16
+// bytes, 8-row groups 128 bytes apart; the second core matrix along K (columns 8-15) is
+// a zero block AUG_LBO bytes further.
+constexpr int AUG_ROWS = BMQ * 16;                      // bytes of one L or D block
+constexpr int AUG_LBO = 2 * AUG_ROWS;
+constexpr int AUGA_OFF = DO_OFF + NQ * 2 * QBLK;        // 2 KB ones rows + 2 KB zeros
+constexpr int AUG_OFF = AUGA_OFF + 4096;                // [NQ] x {L, D, zeros x 2}
+constexpr int AUG_STAGE = 4 * AUG_ROWS;
+constexpr int BAR_OFF = AUG_OFF + NQ * AUG_STAGE;
+constexpr int KV_SMEM = BAR_OFF + 512 + 1024;
 
-constexpr uint32_t T_ST = 0, T_DPT = 128, T_DV = 256, T_DK = 384;
+constexpr uint32_t T_ST = 0, T_DPT = 128, T_DV = 256, T_DK = 384;  // DB: S^T / dP^T buffer b at + 64 b
+// TMEM buffer, barrier index and barrier phase of tile i.
+__device__ __forceinline__ int kv_buf(int i) { return DB ? (i & 1) : 0; }
+__device__ __forceinline__ uint32_t kv_phase(int i) { return DB ? ((i >> 1) & 1) : (i & 1); }
 
 // The tensor cores' fp32 accumulation into TMEM carries a small rounding bias per
 // accumulation (measured at about 1e-8 relative), which adds up over the tens of
 // thousands of accumulations of a long item.  Every kFlush query tiles the dK/dV
 // accumulators are therefore moved into an fp32 slot (round-to-nearest adds) and the
 // tensor-core accumulation restarts from zero.
-constexpr int kFlush = 256;
+constexpr int kFlush = 32768 / BMQ;  // 2048 accumulation steps (16 query rows each) of dK/dV
 
 struct KvBars {
   uint64_t kv_full;
   uint64_t q_full[NQ];
   uint64_t q_empty[NQ];
-  uint64_t s_full;
-  uint64_t dp_full;
-  uint64_t p_ready;
-  uint64_t ds_ready;
-  uint64_t dv_done;
-  uint64_t dk_done;
+  // per TMEM buffer b = tile % 2
+  uint64_t s_full[2];
+  uint64_t dp_full[2];
+  uint64_t p_ready[2];
+  uint64_t ds_ready[2];
+  uint64_t dv_done[2];
+  uint64_t dk_done[2];
   uint64_t acc_done;
   uint64_t flush_ready;  // dK/dV accumulators complete up to a flush point
   uint64_t flushed;      // compute warps have moved them to the slot
@@ -97,7 +128,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2, Geometry geo,
     const int32_t* __restrict__ queue, const int32_t* __restrict__ row_bend, int bm, int bn,
-    const float* __restrict__ stats, int ntiles, __nv_bfloat16* __restrict__ dk_out,
+    const uint8_t* __restrict__ aug, int ntiles, __nv_bfloat16* __restrict__ dk_out,
     __nv_bfloat16* __restrict__ dv_out, float* __restrict__ dk_part, float* __restrict__ dv_part,
     float* __restrict__ dk_sum, float* __restrict__ dv_sum, const float* __restrict__ dk_add,
     const float* __restrict__ dv_add, float* __restrict__ slots, int n_slots, uint32_t* __restrict__ err) {
@@ -136,19 +167,31 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, 256);
-    mbar_init(&bars->ds_ready, 256);
-    mbar_init(&bars->dv_done, 1);
-    mbar_init(&bars->dk_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->dp_full[b], 1);
+      mbar_init(&bars->p_ready[b], 128 * NWG);
+      mbar_init(&bars->ds_ready[b], 128 * NWG);
+      mbar_init(&bars->dv_done[b], 1);
+      mbar_init(&bars->dk_done[b], 1);
+    }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->flush_ready, 1);
-    mbar_init(&bars->flushed, 256);
+    mbar_init(&bars->flushed, 128 * NWG);
     fence_mbar_init();
   }
-  if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
-  if (warp == 8 && lane == 0) {
+  {
+    uint4* a = reinterpret_cast<uint4*>(smem + AUGA_OFF);
+    for (int r = threadIdx.x; r < 128; r += blockDim.x) a[r] = make_uint4(0x3F803F80u, 0x3F80u, 0u, 0u);  // bf16 1,1,1
+    for (int r = threadIdx.x; r < 128; r += blockDim.x) a[128 + r] = make_uint4(0u, 0u, 0u, 0u);
+    for (int st = 0; st < NQ; ++st) {
+      uint4* z = reinterpret_cast<uint4*>(smem + AUG_OFF + st * AUG_STAGE + 2 * AUG_ROWS);
+      for (int r = threadIdx.x; r < 2 * AUG_ROWS / 16; r += blockDim.x) z[r] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == MMA_WARP) tmem_alloc(&bars->tmem_base, 512);
+  if (warp == PRODUCER_WARP && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_do);
     prefetch_tmap(resp_keys ? &tm_k2 : &tm_k);
@@ -158,7 +201,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 8) {
+  if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const CUtensorMap* km = resp_keys ? &tm_k2 : &tm_k;
@@ -169,6 +212,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         tma_load_3d(smem + V_OFF + kb * BLK, vm, &bars->kv_full, kb * 64, kvh, (int)key0);
       }
       const int tile_base = prefill ? G.tp0 : G.tr0;
+      // The {-lse/s, -Delta} rows of query tile qt are those of 128-row statistics tile
+      // qt * BMQ / 128 (one half of them for 64-row tiles).
+      auto aug_src = [&](int h, int qt) {
+        constexpr int per = kStatRows / BMQ;
+        return aug + ((int64_t)h * ntiles + tile_base + qt / per) * kAugTileBytes + (qt % per) * AUG_ROWS;
+      };
       int issued = 0;
       for (int i = 0; i < n_iter; ++i) {
         const int stage = i % NQ, use = i / NQ;
@@ -176,15 +225,14 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         const int h = kvh * r + i / nqt;
         const int qt = it.b - 1 - i % nqt;
         const int64_t row0 = qbase + (int64_t)qt * bm;
-        mbar_expect_tx(&bars->q_full[stage], 4 * BLK + 2 * kStatRows * 4);
+        mbar_expect_tx(&bars->q_full[stage], 4 * QBLK + 2 * AUG_ROWS);
         for (int kb = 0; kb < 2; ++kb) {
-          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * BLK, &tm_q, &bars->q_full[stage], kb * 64, h, (int)row0);
-          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * BLK, &tm_do, &bars->q_full[stage], kb * 64, h, (int)row0);
+          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * QBLK, &tm_q, &bars->q_full[stage], kb * 64, h, (int)row0);
+          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * QBLK, &tm_do, &bars->q_full[stage], kb * 64, h, (int)row0);
         }
-        // {lse * log2(e), Delta} of the tile's 128 rows: one 1 KB bulk copy.
-        bulk_load(smem + ROWS_OFF + stage * 2 * kStatRows * 4,
-                  stats + ((int64_t)h * ntiles + tile_base + qt) * 2 * kStatRows, 2 * kStatRows * 4,
-                  &bars->q_full[stage]);
+        const uint8_t* src = aug_src(h, qt);
+        bulk_load(smem + AUG_OFF + stage * AUG_STAGE, src, AUG_ROWS, &bars->q_full[stage]);
+        bulk_load(smem + AUG_OFF + stage * AUG_STAGE + AUG_ROWS, src + kStatRows * 16, AUG_ROWS, &bars->q_full[stage]);
         issued = i + 1;
         // Warm L2 with the tiles a few iterations ahead.
         const int ip = i + kPrefetch;
@@ -196,40 +244,48 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
             tma_prefetch_3d(&tm_q, kb * 64, hp, rp);
             tma_prefetch_3d(&tm_do, kb * 64, hp, rp);
           }
-          bulk_prefetch(stats + ((int64_t)hp * ntiles + tile_base + qp) * 2 * kStatRows, 2 * kStatRows * 4);
         }
       }
       // Never leave a copy in flight.
       mbar_wait(&bars->kv_full, 0, err);
       for (int i = max(0, issued - NQ); i < issued; ++i) mbar_wait(&bars->q_full[i % NQ], (i / NQ) & 1, err);
     }
-  } else if (warp == 9) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // K Q^T, V dO^T
+      constexpr uint32_t id_ss = idesc_bf16_f32(128, BMQ, false, false);  // K Q^T, V dO^T
       constexpr uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);   // P^T dO, dS^T Q (B MN-major)
       const uint64_t dK = smem_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
       const uint64_t dV = smem_desc_sw128(smem_u32(smem + V_OFF), 16, 1024);
       const uint64_t dQk0 = smem_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
       const uint64_t dOk0 = smem_desc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
-      const uint64_t dQm0 = smem_desc_sw128(smem_u32(smem + Q_OFF), BLK, 1024);
-      const uint64_t dOm0 = smem_desc_sw128(smem_u32(smem + DO_OFF), BLK, 1024);
-      constexpr uint64_t kStage = (2 * BLK) >> 4;
-      auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * BLK + (kk & 3) * 32) >> 4); };
+      const uint64_t dQm0 = smem_desc_sw128(smem_u32(smem + Q_OFF), QBLK, 1024);
+      const uint64_t dOm0 = smem_desc_sw128(smem_u32(smem + DO_OFF), QBLK, 1024);
+      constexpr uint64_t kStage = (2 * QBLK) >> 4;
+      const uint64_t dAa = smem_desc_noswz(smem_u32(smem + AUGA_OFF), 2048, 128);
+      const uint64_t dL0 = smem_desc_noswz(smem_u32(smem + AUG_OFF), AUG_LBO, 128);
+      const uint64_t dD0 = smem_desc_noswz(smem_u32(smem + AUG_OFF + AUG_ROWS), AUG_LBO, 128);
+      constexpr uint64_t kAugStage = AUG_STAGE >> 4;
+      auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * BLK + (kk & 3) * 32) >> 4); };   // K, V
+      auto qoff = [](int kk) { return (uint64_t)(((kk >> 2) * QBLK + (kk & 3) * 32) >> 4); };  // Q, dO
       // TMEM column of the bf16 A operand for query step kk (16 rows): warpgroup w packed
-      // rows [64w, 64w + 64) into columns [64w, 64w + 32) of its region.
-      auto acol = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
+      // rows [COLS w, COLS (w + 1)) into columns [COLS w, COLS w + COLS / 2) of the buffer.
+      auto acol = [](int kk) { return (uint32_t)((kk / (COLS / 16)) * COLS + (kk % (COLS / 16)) * 8); };
       auto issue_s = [&](int i) {
         const uint64_t b = dQk0 + (i % NQ) * kStage;
+        const uint32_t d = tmem + T_ST + kv_buf(i) * 64;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + T_ST, dK + koff(kk), b + koff(kk), id_ss, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->s_full);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(d, dK + koff(kk), b + qoff(kk), id_ss, kk > 0 ? 1u : 0u);
+        mma_ss(d, dAa, dL0 + (i % NQ) * kAugStage, id_ss, 1u);  // - lse/s
+        mma_commit(&bars->s_full[kv_buf(i)]);
       };
       auto issue_dp = [&](int i) {
         const uint64_t b = dOk0 + (i % NQ) * kStage;
+        const uint32_t d = tmem + T_DPT + kv_buf(i) * 64;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + T_DPT, dV + koff(kk), b + koff(kk), id_ss, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->dp_full);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(d, dV + koff(kk), b + qoff(kk), id_ss, kk > 0 ? 1u : 0u);
+        mma_ss(d, dAa, dD0 + (i % NQ) * kAugStage, id_ss, 1u);  // - Delta
+        mma_commit(&bars->dp_full[kv_buf(i)]);
       };
       bool ok = mbar_wait(&bars->kv_full, 0, err);
       if (ok && n_iter > 0) ok = mbar_wait(&bars->q_full[0], 0, err);
@@ -240,41 +296,49 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       }
       for (int i = 0; ok && i < n_iter; ++i) {
         const int stage = i % NQ;
+        const int b = kv_buf(i);
+        // The tile whose MMAs last read the buffers that tile i + 1 overwrites: i - 1 with
+        // double buffering, i itself otherwise.
+        const int prev = DB ? i - 1 : i;
         const bool more = i + 1 < n_iter;
         const bool fresh = flush_on ? (i % kFlush == 0) : (i == 0);
         // dV += P^T dO (from zero at the start and after every flush)
         if (flush_on && i > 0 && i % kFlush == 0 && !(ok = mbar_wait(&bars->flushed, (i / kFlush - 1) & 1, err)))
           break;
-        if (!(ok = mbar_wait(&bars->p_ready, i & 1, err))) break;
+        if (!(ok = mbar_wait(&bars->p_ready[b], kv_phase(i), err))) break;
         tc_fence_after();
         {
           const uint64_t b0 = dOm0 + stage * kStage;
+          const uint32_t a0 = tmem + T_ST + b * 64;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + T_DV, tmem + T_ST + acol(kk), b0 + kk * (2048 >> 4), id_ts, (fresh && kk == 0) ? 0u : 1u);
+          for (int kk = 0; kk < BMQ / 16; ++kk)
+            mma_ts(tmem + T_DV, a0 + acol(kk), b0 + kk * (2048 >> 4), id_ts, (fresh && kk == 0) ? 0u : 1u);
         }
-        mma_commit(&bars->dv_done);
+        mma_commit(&bars->dv_done[b]);
+        if (more) {
+          // S(i+1) overwrites P^T(prev): dV(prev) must have read it.
+          if (!(ok = mbar_wait(&bars->q_full[(i + 1) % NQ], ((i + 1) / NQ) & 1, err))) break;
+          if (prev >= 0 && !(ok = mbar_wait(&bars->dv_done[kv_buf(prev)], kv_phase(prev), err))) break;
+          tc_fence_after();
+          issue_s(i + 1);
+        }
         // dK += dS^T Q
-        if (!(ok = mbar_wait(&bars->ds_ready, i & 1, err))) break;
+        if (!(ok = mbar_wait(&bars->ds_ready[b], kv_phase(i), err))) break;
         tc_fence_after();
         {
           const uint64_t b0 = dQm0 + stage * kStage;
+          const uint32_t a0 = tmem + T_DPT + b * 64;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + T_DK, tmem + T_DPT + acol(kk), b0 + kk * (2048 >> 4), id_ts, (fresh && kk == 0) ? 0u : 1u);
+          for (int kk = 0; kk < BMQ / 16; ++kk)
+            mma_ts(tmem + T_DK, a0 + acol(kk), b0 + kk * (2048 >> 4), id_ts, (fresh && kk == 0) ? 0u : 1u);
         }
-        mma_commit(&bars->dk_done);
-        // dK(i) is the last reader of Q(i)/dO(i) and of the stage's row statistics.
+        mma_commit(&bars->dk_done[b]);
+        // dK(i) is the last reader of Q(i)/dO(i) and of the stage's extra-step rows.
         mma_commit(&bars->q_empty[stage]);
         if (flush_on && i % kFlush == kFlush - 1 && more) mma_commit(&bars->flush_ready);
         if (more) {
-          // S(i+1) overwrites P^T(i): dV(i) must have read it (dK(i) is queued behind it).
-          if (!(ok = mbar_wait(&bars->q_full[(i + 1) % NQ], ((i + 1) / NQ) & 1, err))) break;
-          if (!(ok = mbar_wait(&bars->dv_done, i & 1, err))) break;
-          tc_fence_after();
-          issue_s(i + 1);
-          // dP(i+1) overwrites dS^T(i): dK(i) must have read it (S(i+1) is queued).
-          if (!(ok = mbar_wait(&bars->dk_done, i & 1, err))) break;
+          // dP(i+1) overwrites dS^T(prev): dK(prev) must have read it.
+          if (prev >= 0 && !(ok = mbar_wait(&bars->dk_done[kv_buf(prev)], kv_phase(prev), err))) break;
           tc_fence_after();
           issue_dp(i + 1);
         }
@@ -283,11 +347,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     }
   } else {
     // ------------------------------------------------------------ P^T and dS^T
-    const int w = warp >> 2;                 // query columns [64w, 64w + 64)
+    const int w = warp >> 2;                 // query columns [COLS w, COLS (w + 1))
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int t = q4 * 32 + lane;            // key row / TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int c0 = 64 * w;
+    const int c0 = COLS * w;
     const int64_t key = key0 + t;
     const bool key_ok = key < key_end;
     // valid query rows for this key: [q_lo, q_hi)
@@ -300,94 +364,81 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     }
     if (!key_ok) q_hi = q_lo;
     const float sl2 = geo.scale_log2;
+    // This warpgroup's share of the key's {dK, dV} row (256 floats): [po, po + 256 / NWG).
+    constexpr int SHARE = 256 / NWG;
+    const int po = w * SHARE;
+    const uint32_t acc_col = (po < 128 ? T_DK : T_DV) + (po & 127);
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
       const int stage = i % NQ;
       const int64_t row0 = qbase + (int64_t)(it.b - 1 - i % nqt) * bm;
-      const float* rows = reinterpret_cast<const float*>(smem + ROWS_OFF) + stage * 2 * kStatRows;
-      // rows[] (lse, Delta) of this stage are published by the producer with q_full.
-      if (!(ok = mbar_wait(&bars->q_full[stage], (i / NQ) & 1, err))) break;
-      if (!(ok = mbar_wait(&bars->s_full, i & 1, err))) break;
+      const int b = kv_buf(i);
+      const uint32_t ts = tmem + lane_off + T_ST + b * 64 + c0, tdp = tmem + lane_off + T_DPT + b * 64 + c0;
+      if (!(ok = mbar_wait(&bars->s_full[b], kv_phase(i), err))) break;
       tc_fence_after();
-      uint32_t sraw[2][32];
-      tmem_ld32(tmem + lane_off + T_ST + c0, sraw[0]);
-      tmem_ld32(tmem + lane_off + T_ST + c0 + 32, sraw[1]);
+      uint32_t sraw[COLS / 32][32];
+#pragma unroll
+      for (int k = 0; k < COLS / 32; ++k) tmem_ld32(ts + 32 * k, sraw[k]);
       tmem_ld_wait();
       // this warpgroup's valid columns: [lo, hi) relative to c0
       const int64_t lo64 = q_lo - row0 - c0, hi64 = q_hi - row0 - c0;
-      const int lo = lo64 < 0 ? 0 : (lo64 > 64 ? 64 : (int)lo64);
-      const int hi = hi64 < 0 ? 0 : (hi64 > 64 ? 64 : (int)hi64);
-      uint32_t pk[32];  // P^T as bf16 pairs: A operand of dV and the P factor of dS
-      const float4* l4 = reinterpret_cast<const float4*>(rows + c0);
-      if (lo == 0 && hi == 64) {
+      const int lo = lo64 < 0 ? 0 : (lo64 > COLS ? COLS : (int)lo64);
+      const int hi = hi64 < 0 ? 0 : (hi64 > COLS ? COLS : (int)hi64);
+      // P^T as bf16 pairs (A operand of dV and the P factor of dS): the accumulator
+      // already holds S^T - lse/s, so P = exp2(s log2e (S^T - lse/s)).
+      uint32_t pk[COLS / 2];
+      if (lo == 0 && hi == COLS) {
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const float4 l = l4[g];
-          const int c = 4 * g;
-          const float e0 = fast_exp2(fmaf(__uint_as_float(sraw[c >> 5][c & 31]), sl2, -l.x));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]), sl2, -l.y));
-          const float e2 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 2) >> 5][(c + 2) & 31]), sl2, -l.z));
-          const float e3 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 3) >> 5][(c + 3) & 31]), sl2, -l.w));
-          pk[2 * g] = pack_bf16x2(e0, e1);
-          pk[2 * g + 1] = pack_bf16x2(e2, e3);
+        for (int c = 0; c < COLS; c += 2) {
+          const float e0 = fast_exp2(__uint_as_float(sraw[c >> 5][c & 31]) * sl2);
+          const float e1 = fast_exp2(__uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]) * sl2);
+          pk[c >> 1] = pack_bf16x2(e0, e1);
         }
       } else {
         const uint32_t span = (uint32_t)(hi - lo);  // valid iff (c - lo) < span (unsigned)
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const float4 l = l4[g];
-          const int c = 4 * g;
-          float e0 = fast_exp2(fmaf(__uint_as_float(sraw[c >> 5][c & 31]), sl2, -l.x));
-          float e1 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]), sl2, -l.y));
-          float e2 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 2) >> 5][(c + 2) & 31]), sl2, -l.z));
-          float e3 = fast_exp2(fmaf(__uint_as_float(sraw[(c + 3) >> 5][(c + 3) & 31]), sl2, -l.w));
+        for (int c = 0; c < COLS; c += 2) {
+          float e0 = fast_exp2(__uint_as_float(sraw[c >> 5][c & 31]) * sl2);
+          float e1 = fast_exp2(__uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]) * sl2);
           e0 = (uint32_t)(c - lo) < span ? e0 : 0.f;
           e1 = (uint32_t)(c + 1 - lo) < span ? e1 : 0.f;
-          e2 = (uint32_t)(c + 2 - lo) < span ? e2 : 0.f;
-          e3 = (uint32_t)(c + 3 - lo) < span ? e3 : 0.f;
-          pk[2 * g] = pack_bf16x2(e0, e1);
-          pk[2 * g + 1] = pack_bf16x2(e2, e3);
+          pk[c >> 1] = pack_bf16x2(e0, e1);
         }
       }
-      tmem_st32(tmem + lane_off + T_ST + c0, pk);
+      tmem_st_words<COLS / 2>(ts, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_ready);
+      mbar_arrive(&bars->p_ready[b]);
       // dS^T = P^T (dP^T - Delta), with the same bf16 P the dV product uses
-      if (!(ok = mbar_wait(&bars->dp_full, i & 1, err))) break;
+      if (!(ok = mbar_wait(&bars->dp_full[b], kv_phase(i), err))) break;
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + T_DPT + c0, sraw[0]);
-      tmem_ld32(tmem + lane_off + T_DPT + c0 + 32, sraw[1]);
+#pragma unroll
+      for (int k = 0; k < COLS / 32; ++k) tmem_ld32(tdp + 32 * k, sraw[k]);
       tmem_ld_wait();
-      const float4* d4 = reinterpret_cast<const float4*>(rows + kStatRows + c0);
+      // the accumulator holds dP^T - Delta
 #pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        const float4 dl = d4[g];  // Delta of columns 4g .. 4g+3
-        const float dd[4] = {dl.x, dl.y, dl.z, dl.w};
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int c = 2 * g + h2, e0 = 2 * c, e1 = 2 * c + 1;
-          const float p0 = __uint_as_float(pk[c] << 16), p1 = __uint_as_float(pk[c] & 0xFFFF0000u);
-          const float d0 = p0 * (__uint_as_float(sraw[e0 >> 5][e0 & 31]) - dd[2 * h2]);
-          const float d1 = p1 * (__uint_as_float(sraw[e1 >> 5][e1 & 31]) - dd[2 * h2 + 1]);
-          pk[c] = pack_bf16x2(d0, d1);
-        }
+      for (int c = 0; c < COLS / 2; ++c) {
+        const int e0 = 2 * c, e1 = 2 * c + 1;
+        const float p0 = __uint_as_float(pk[c] << 16), p1 = __uint_as_float(pk[c] & 0xFFFF0000u);
+        const float d0 = p0 * __uint_as_float(sraw[e0 >> 5][e0 & 31]);
+        const float d1 = p1 * __uint_as_float(sraw[e1 >> 5][e1 & 31]);
+        pk[c] = pack_bf16x2(d0, d1);
       }
-      tmem_st32(tmem + lane_off + T_DPT + c0, pk);
+      tmem_st_words<COLS / 2>(tdp, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_ready);
+      mbar_arrive(&bars->ds_ready[b]);
       if (flush_on && i % kFlush == kFlush - 1 && i + 1 < n_iter) {
-        // Move dK (warpgroup 0) or dV (warpgroup 1) to this block's slot (the first
-        // flush stores, later ones add).
+        // Move this warpgroup's share of dK/dV to this block's slot (the first flush
+        // stores, later ones add).
         if (!(ok = mbar_wait(&bars->flush_ready, (i / kFlush) & 1, err))) break;
         tc_fence_after();
-        float* slot = slots + ((int64_t)smid * 128 + t) * 256 + w * 128;
+        float* slot = slots + ((int64_t)smid * 128 + t) * 256 + po;
         const bool first = i == kFlush - 1;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < SHARE / 32; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + (w == 0 ? T_DK : T_DV) + c * 32, v);
+          tmem_ld32(tmem + lane_off + acc_col + c * 32, v);
           tmem_ld_wait();
           float4* dst = reinterpret_cast<float4*>(slot + c * 32);
 #pragma unroll
@@ -405,28 +456,30 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         mbar_arrive(&bars->flushed);
       }
     }
-    // dK (warpgroup 0) or dV (warpgroup 1) row of this key
+    // This warpgroup's share of the key's dK (scaled by s) / dV row
     if (ok && mbar_wait(&bars->acc_done, 0, err) && n_iter > 0) {
       tc_fence_after();
-      const int64_t off = (key * geo.hkv + kvh) * 128;
+      const bool is_dk = po < 128;
+      const int col0 = po & 127;
+      const int64_t off = (key * geo.hkv + kvh) * 128 + col0;
       float* fdst = nullptr;
       int64_t foff = off;
       if (it.kind == K_PROMPT_KV) {
         const SplitInfo s = geo.splits[it.group];
-        fdst = w == 0 ? dk_sum : dv_sum;
+        fdst = is_dk ? dk_sum : dv_sum;
         if (s.nsplit > 1) {
-          fdst = w == 0 ? dk_part : dv_part;
-          foff = ((s.part_row0 + (int64_t)it.split * G.lp + (key - G.p0)) * geo.hkv + kvh) * 128;
+          fdst = is_dk ? dk_part : dv_part;
+          foff = ((s.part_row0 + (int64_t)it.split * G.lp + (key - G.p0)) * geo.hkv + kvh) * 128 + col0;
         }
       }
-      const float mul = w == 0 ? geo.scale : 1.f;
-      const float* slot = slots + ((int64_t)smid * 128 + t) * 256 + w * 128;
-      __nv_bfloat16* bdst = w == 0 ? dk_out : dv_out;
-      const float* add = w == 0 ? dk_add : dv_add;
+      const float mul = is_dk ? geo.scale : 1.f;
+      const float* slot = slots + ((int64_t)smid * 128 + t) * 256 + po;
+      __nv_bfloat16* bdst = is_dk ? dk_out : dv_out;
+      const float* add = is_dk ? dk_add : dv_add;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < SHARE / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + (w == 0 ? T_DK : T_DV) + c * 32, v);
+        tmem_ld32(tmem + lane_off + acc_col + c * 32, v);
         tmem_ld_wait();
         if (!key_ok) continue;
         float a[32];
@@ -462,7 +515,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -471,15 +524,16 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
 }  // namespace
 
 cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                      const void* vr, const float* stats, const void* dO, void* dk_out, void* dv_out, float* dk_part,
+                      const void* vr, const void* aug, const void* dO, void* dk_out, void* dv_out, float* dk_part,
                       float* dv_part, float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add,
                       float* slots, cudaStream_t st) {
   const bool prefill = op == AUGTREE_OP_PREFILL_BWD;
   if (p->n_items[op] == 0) return cudaSuccess;
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
   CUtensorMap mq, mdo, mk, mv, mk2, mv2;
-  if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, 128)) return cudaErrorInvalidValue;
-  if (!encode_rows_map(&mdo, dO, q_rows, p->cfg.hq, 128)) return cudaErrorInvalidValue;
+  if (p->bm[op] != BMQ || p->bn[op] != 128) return cudaErrorInvalidValue;
+  if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
+  if (!encode_rows_map(&mdo, dO, q_rows, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
   const bool have_p = p->total_prompt > 0 && kp && vp;
   const bool have_r = !prefill && p->total_resp > 0 && kr && vr;
   if (have_p) {
@@ -501,7 +555,7 @@ cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* 
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
   if (e != cudaSuccess) return e;
   tc_bwd_kv_kernel<<<(unsigned)p->n_items[op], KV_THREADS, KV_SMEM, st>>>(
-      mq, mdo, mk, mv, mk2, mv2, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op], stats,
+      mq, mdo, mk, mv, mk2, mv2, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op], (const uint8_t*)aug,
       prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, dk_part, dv_part, dk_sum,
       dv_sum, dk_add, dv_add, slots, kFlushSlots, p->err_d);
   return cudaGetLastError();

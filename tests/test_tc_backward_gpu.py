@@ -47,8 +47,8 @@ def test_tc_prompt_gradient_is_deterministic(cuda_device):
 def test_tc_long_item_pipelines(cuda_device):
     """Items that walk hundreds of query tiles (no prompt-KV splitting): the producer,
     MMA issuer and compute warps run long pipelines over their buffers, and the prompt
-    KV items (40 query tiles x 8 heads = 320 tiles) pass the periodic move of dK/dV
-    from TMEM to the fp32 slots (every 256 tiles)."""
+    KV items (5000 response rows x 8 heads: 5000 x 8 / 16 = 2500 accumulation steps of
+    16 rows) pass the periodic move of dK/dV from TMEM to the fp32 slots (every 2048)."""
     w = W.custom(W.Tree([256], [[3000, 2000]]), hq=16, hkv=2, d=128, dtype="bf16", seed=41)
     got = run_cuda(w, kernel=at.KERNEL_TC, num_sms=100000)
     compare(got, run_oracle(w), "bf16")
