@@ -35,6 +35,13 @@ DEFAULT_WORKLOAD = "prompt_heavy"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
+# DRAM bytes (read + write) per launch of a kernel on a full-size workload, from a
+# one-pass ncu capture of dram__bytes_read.sum + dram__bytes_write.sum averaged over
+# the kernel's launches in one step (the summary under profiles/ gives the command).
+# Valid for the kernel versions it was taken on; absent entries report null.
+TRAFFIC_PER_LAUNCH = {("prompt_heavy", "bwd_key_side"): 19.86e9}
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -234,6 +241,8 @@ def run_ours(args):
     time.sleep(0.3)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # per-kernel CUDA events inside the library's calls, on the calls' stream
+    plan.set_timing(args.steps <= at.TIMING_RING)
     barrier()
     start.record(stream)
     for k in range(args.steps):
@@ -242,6 +251,15 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     plan.check()  # raises if any kernel of the step gave up on a bounded wait
+    kernel_ms = {}  # kind -> [ms per step summed over the step's launches, launches per step]
+    if args.steps <= at.TIMING_RING:
+        for op in range(4):
+            for back in range(args.steps):
+                for kind, t_ms in plan.kernel_times(op, back):
+                    e = kernel_ms.setdefault((op, kind), [0.0, 0])
+                    e[0] += t_ms / args.steps
+                    e[1] += 1
+        plan.set_timing(False)
     ms = max_over_ranks(start.elapsed_time(end), dev)
     per_call = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(n_ev - 1)]
                          for k in range(args.steps)]).mean(0)
@@ -277,8 +295,28 @@ def run_ours(args):
     n_pairs = w.tree.pair_count()
     per_flops = [4 * w.d * w.hq * n_pairs_prompt, 4 * w.d * w.hq * (n_pairs - n_pairs_prompt),
                  10 * w.d * w.hq * (n_pairs - n_pairs_prompt), 10 * w.d * w.hq * n_pairs_prompt]
-    dom = int(np.argmax(per_call))
-    ach = per_flops[dom] / (per_call[dom] * 1e-3) / 1e12
+    # The dominant kernel: per-launch algorithmic FLOPs (the GEMMs the kernel itself
+    # performs on valid pairs: forward 2, key side S, dP, dV, dK = 4, query side S, dP,
+    # dQ = 3, each 2 d Hq per pair) over its launches' measured durations.
+    pairs = {0: n_pairs_prompt, 1: n_pairs - n_pairs_prompt, 2: n_pairs - n_pairs_prompt, 3: n_pairs_prompt}
+    gemms = {"fwd_tc": 2, "fwd_simt": 2, "bwd_key_side": 4, "bwd_query_side": 3, "bwd_simt": 5}
+    kinds = {}
+    for (op, kind), (t_ms, launches) in kernel_ms.items():
+        e = kinds.setdefault(kind, [0.0, 0, 0.0])
+        e[0] += t_ms
+        e[1] += launches / args.steps
+        e[2] += 2.0 * w.d * w.hq * pairs[op] * gemms.get(kind, 0)
+    if kinds:
+        dom_kind = max(kinds, key=lambda k: kinds[k][0])
+        ms_k, launches_k, flops_k = kinds[dom_kind]
+        ach = flops_k / (ms_k * 1e-3) / 1e12
+        dom_name = {"bwd_key_side": "tc_bwd_kv_kernel (backward, key side)",
+                    "bwd_query_side": "tc_bwd_dq_kernel (backward, query side)",
+                    "fwd_tc": "tc_fwd_kernel (forward)"}.get(dom_kind, dom_kind)
+    else:
+        dom = int(np.argmax(per_call))
+        ach = per_flops[dom] / (per_call[dom] * 1e-3) / 1e12
+        dom_kind, dom_name, launches_k = names[dom], names[dom] + " call", 1
     peak_s = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     launches_per_step = count_launches(plan, at)
 
@@ -305,9 +343,14 @@ def run_ours(args):
         "pct_of_bf16_peak": round(100.0 * tflops / world / pk["bf16_tflops"], 2),
         "per_call_ms": {n: round(float(x), 4) for n, x in zip(names, per_call)},
         "per_call_tflops": {n: round(f / (x * 1e-3) / 1e12, 2) for n, f, x in zip(names, per_flops, per_call)},
-        "roofline": {"bound": "tensor", "kernel": names[dom], "achieved": round(ach, 2), "peak": peak_s,
-                     "unit": "TFLOP/s", "frac": round(ach / peak_s, 4), "traffic": None,
+        "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": round(ach, 2), "peak": peak_s,
+                     "unit": "TFLOP/s", "frac": round(ach / peak_s, 4),
+                     "traffic": TRAFFIC_PER_LAUNCH.get((w.name, dom_kind)),
+                     "launches_per_step": launches_k,
                      "peak_kind": f"bf16 dense sustained ({pk_kind})"},
+        "kernels": {k: {"ms_per_step": round(v[0], 4), "launches_per_step": v[1],
+                        "tflops": round(v[2] / (v[0] * 1e-3) / 1e12, 2) if v[2] > 0 else None}
+                    for k, v in sorted(kinds.items(), key=lambda kv: -kv[1][0])},
         "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,

@@ -234,6 +234,35 @@ augtree_status augtree_lse_merge(int64_t rows, int32_t h, int32_t d, const float
  * AUGTREE_ERR_DEVICE_CHECK for any other recorded device-side failure, else OK. */
 augtree_status augtree_plan_check(const augtree_plan* plan, void* stream);
 
+/* ---- Per-kernel timing (tracing aid; not part of the paper's method) -------------------
+ * Off by default.  When enabled, every compute call of the plan records CUDA events on
+ * its stream before each kernel it launches and after the last one, in a ring that
+ * keeps the last AUGTREE_TIMING_RING calls of each op.  The cost is a few event
+ * records per call; nothing else changes.  Kernel kinds (augtree_plan_kernel_times): */
+typedef enum {
+  AUGTREE_KID_FWD_TC = 1,        /* tensor-core forward (prefill or replay)             */
+  AUGTREE_KID_FWD_SIMT = 2,      /* SIMT forward                                        */
+  AUGTREE_KID_PREPROCESS = 3,    /* backward preprocess (Delta, row statistics)         */
+  AUGTREE_KID_BWD_KEY_SIDE = 4,  /* tensor-core backward, key side (dK, dV)             */
+  AUGTREE_KID_SPLIT_REDUCE = 5,  /* fixed-order reduction of prompt dK/dV partials      */
+  AUGTREE_KID_BWD_QUERY_SIDE = 6,/* tensor-core backward, query side (dQ)               */
+  AUGTREE_KID_DQ_CONVERT = 7,    /* fp32 dQ accumulator to the output dtype (SIMT)      */
+  AUGTREE_KID_BWD_SIMT = 8       /* SIMT backward                                       */
+} augtree_kernel_id;
+#define AUGTREE_TIMING_RING 64
+
+/* Turns per-kernel timing on (enable != 0) or off.  Turning it on creates the events
+ * (on the plan's device); turning it off keeps them until the plan is destroyed. */
+augtree_status augtree_plan_set_timing(augtree_plan* plan, int32_t enable);
+
+/* Durations of the kernels of the `back`-th most recent timed call of `op` (back = 0:
+ * the last one), in launch order: kind[i] (augtree_kernel_id) and ms[i] for
+ * i < *n <= cap.  Waits for that call's events.  AUGTREE_ERR_INVALID_ARG if timing is
+ * off, op is not an AUGTREE_OP_*, back >= AUGTREE_TIMING_RING or fewer than back + 1
+ * timed calls of op were made. */
+augtree_status augtree_plan_kernel_times(const augtree_plan* plan, int32_t op, int32_t back, int32_t* kind,
+                                         float* ms, int32_t cap, int32_t* n);
+
 const char* augtree_status_string(augtree_status s);
 
 /* Library version, major*10000 + minor*100 + patch. */

@@ -29,6 +29,10 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEV
 FP32, BF16 = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC = 0, 1, 2
 OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD = 0, 1, 2, 3
+# augtree_kernel_id: kinds reported by augtree_plan_kernel_times
+KERNEL_IDS = {1: "fwd_tc", 2: "fwd_simt", 3: "preprocess", 4: "bwd_key_side", 5: "split_reduce",
+              6: "bwd_query_side", 7: "dq_convert", 8: "bwd_simt"}
+TIMING_RING = 64
 ITEM_WORDS = 8
 
 
@@ -73,6 +77,9 @@ _SIGS = {
     "augtree_prefill_bwd_static": [_P] * 13,
     "augtree_lse_merge": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 6 + [_P],
     "augtree_plan_check": [_P, _P],
+    "augtree_plan_set_timing": [_P, ctypes.c_int32],
+    "augtree_plan_kernel_times": [_P, ctypes.c_int32, ctypes.c_int32, _P, _P, ctypes.c_int32,
+                                  ctypes.POINTER(ctypes.c_int32)],
     "augtree_status_string": [ctypes.c_int32],
     "augtree_version": [],
 }
@@ -177,6 +184,19 @@ class Plan:
         _check(lib().augtree_schedule_export(self.handle, op, out.ctypes.data, n.value, ctypes.byref(n)),
                "augtree_schedule_export")
         return out[:n.value]
+
+    def set_timing(self, enable: bool):
+        """Per-kernel timing of this plan's calls (CUDA events around each launch)."""
+        _check(lib().augtree_plan_set_timing(self.handle, 1 if enable else 0), "augtree_plan_set_timing")
+
+    def kernel_times(self, op: int, back: int = 0):
+        """[(kind, ms)] of the kernels of the back-th most recent timed call of op."""
+        kind = (ctypes.c_int32 * 8)()
+        ms = (ctypes.c_float * 8)()
+        n = ctypes.c_int32()
+        _check(lib().augtree_plan_kernel_times(self.handle, op, back, ctypes.cast(kind, _P), ctypes.cast(ms, _P), 8,
+                                               ctypes.byref(n)), "augtree_plan_kernel_times")
+        return [(KERNEL_IDS.get(kind[i], str(kind[i])), float(ms[i])) for i in range(n.value)]
 
     def check(self, stream=None):
         """Synchronize and raise if a kernel of this plan recorded a device-side error."""

@@ -269,6 +269,24 @@ Geometry geometry(const augtree_plan* p) {
   return g;
 }
 
+CallTimer::CallTimer(const augtree_plan* p, int op, cudaStream_t s) : p_(p), op_(op), slot_(0), n_(0), s_(s) {
+  if (p_->timing.on) slot_ = (int)(p_->timing.calls[op_] % AUGTREE_TIMING_RING);
+}
+void CallTimer::mark(int kind) {
+  auto& T = p_->timing;
+  if (!T.on || n_ >= augtree_plan::kTimingMarks - 1) return;
+  cudaEventRecord(T.ev[op_][slot_][n_], s_);
+  T.kind[op_][slot_][n_] = kind;
+  ++n_;
+}
+void CallTimer::finish() {
+  auto& T = p_->timing;
+  if (!T.on || n_ == 0) return;
+  cudaEventRecord(T.ev[op_][slot_][n_], s_);
+  T.n_marks[op_][slot_] = n_ + 1;
+  T.calls[op_] += 1;
+}
+
 }  // namespace augtree
 
 // =====================================================================================
@@ -336,6 +354,10 @@ augtree_status augtree_plan_destroy(augtree_plan* p) {
   cudaFree(p->splits_d);
   cudaFree(p->err_d);
   for (int i = 0; i < 4; ++i) cudaFree(p->queue_d[i]);
+  if (p->timing.created)
+    for (int op = 0; op < 4; ++op)
+      for (int c = 0; c < AUGTREE_TIMING_RING; ++c)
+        for (int k = 0; k < augtree_plan::kTimingMarks; ++k) cudaEventDestroy(p->timing.ev[op][c][k]);
   if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
   delete p;
   return AUGTREE_OK;
@@ -521,9 +543,17 @@ augtree_status augtree_prefill_fwd(const augtree_plan* p, const void* qp, const 
   if (st != AUGTREE_OK) return st;
   if (p->n_items[AUGTREE_OP_PREFILL_FWD] == 0) return AUGTREE_OK;
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->family == AUGTREE_KERNEL_TC)
-    return from_cuda(tc_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s));
-  return from_cuda(simt_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s));
+  CallTimer tm(p, AUGTREE_OP_PREFILL_FWD, s);
+  cudaError_t e;
+  if (p->family == AUGTREE_KERNEL_TC) {
+    tm.mark(AUGTREE_KID_FWD_TC);
+    e = tc_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s);
+  } else {
+    tm.mark(AUGTREE_KID_FWD_SIMT);
+    e = simt_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s);
+  }
+  tm.finish();
+  return from_cuda(e);
 }
 
 augtree_status augtree_replay_fwd(const augtree_plan* p, const void* qr, const void* kp, const void* vp,
@@ -538,9 +568,17 @@ augtree_status augtree_replay_fwd(const augtree_plan* p, const void* qr, const v
   if (st != AUGTREE_OK) return st;
   if (p->n_items[AUGTREE_OP_REPLAY_FWD] == 0) return AUGTREE_OK;
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->family == AUGTREE_KERNEL_TC)
-    return from_cuda(tc_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s));
-  return from_cuda(simt_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s));
+  CallTimer tm(p, AUGTREE_OP_REPLAY_FWD, s);
+  cudaError_t e;
+  if (p->family == AUGTREE_KERNEL_TC) {
+    tm.mark(AUGTREE_KID_FWD_TC);
+    e = tc_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s);
+  } else {
+    tm.mark(AUGTREE_KID_FWD_SIMT);
+    e = simt_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s);
+  }
+  tm.finish();
+  return from_cuda(e);
 }
 
 augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const void* kp, const void* vp,
@@ -566,26 +604,49 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
   const int dt = p->cfg.dtype;
   cudaError_t e = cudaSuccess;
   const bool tc = p->family == AUGTREE_KERNEL_TC;
+  CallTimer tm(p, AUGTREE_OP_REPLAY_BWD, s);
   if (tc) {
     // Key side (response dK/dV, prompt dK/dV summed over the branches), the split-K
     // reduction of the prompt partials, then the query side (dQ).
     void* aug = base + w.aug_off;
-    if (p->total_resp > 0) e = launch_preprocess_tiled(p, false, or_, dor, lse_r, delta, aug, s);
-    if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0)
+    if (p->total_resp > 0) {
+      tm.mark(AUGTREE_KID_PREPROCESS);
+      e = launch_preprocess_tiled(p, false, or_, dor, lse_r, delta, aug, s);
+    }
+    if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0) {
+      tm.mark(AUGTREE_KID_BWD_KEY_SIDE);
       e = tc_bwd_kv(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, aug, dor, dkr, dvr, dk_part, dv_part, dkp_sum,
                     dvp_sum, nullptr, nullptr, (float*)(base + w.slots_off), s);
-    if (e == cudaSuccess && p->total_prompt > 0) e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
-    if (e == cudaSuccess && p->total_resp > 0) e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dqr, s);
+    }
+    if (e == cudaSuccess && p->total_prompt > 0) {
+      tm.mark(AUGTREE_KID_SPLIT_REDUCE);
+      e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
+    }
+    if (e == cudaSuccess && p->total_resp > 0) {
+      tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
+      e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dqr, s);
+    }
+    tm.finish();
     return from_cuda(e);
   }
-  if (p->total_resp > 0)
+  if (p->total_resp > 0) {
+    tm.mark(AUGTREE_KID_PREPROCESS);
     e = launch_preprocess(or_, dor, dt, p->total_resp, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
-  if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0)
+  }
+  if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0) {
+    tm.mark(AUGTREE_KID_BWD_SIMT);
     e = simt_bwd(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, lse_r, dor, delta, dq_acc, dkr, dvr, dk_part,
                  dv_part, dkp_sum, dvp_sum, nullptr, nullptr, s);
-  if (e == cudaSuccess && p->total_prompt > 0) e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
-  if (e == cudaSuccess && p->total_resp > 0)
+  }
+  if (e == cudaSuccess && p->total_prompt > 0) {
+    tm.mark(AUGTREE_KID_SPLIT_REDUCE);
+    e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
+  }
+  if (e == cudaSuccess && p->total_resp > 0) {
+    tm.mark(AUGTREE_KID_DQ_CONVERT);
     e = launch_dq_convert(dq_acc, dqr, dt, (int64_t)p->total_resp * p->cfg.hq * p->cfg.head_dim, s);
+  }
+  tm.finish();
   return from_cuda(e);
 }
 
@@ -609,22 +670,74 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
   float* dq_acc = (float*)(base + w.dq_off);
   const int dt = p->cfg.dtype;
   const bool tc = p->family == AUGTREE_KERNEL_TC;
+  CallTimer tm(p, AUGTREE_OP_PREFILL_BWD, s);
   if (tc) {
     void* aug = base + w.aug_off;
+    tm.mark(AUGTREE_KID_PREPROCESS);
     cudaError_t e = launch_preprocess_tiled(p, true, op, dop, lse_p, delta, aug, s);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess) {
+      tm.mark(AUGTREE_KID_BWD_KEY_SIDE);
       e = tc_bwd_kv(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, aug, dop, dkp, dvp, nullptr, nullptr,
                     nullptr, nullptr, dkp_acc, dvp_acc, (float*)(base + w.slots_off), s);
-    if (e == cudaSuccess) e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dqp, s);
+    }
+    if (e == cudaSuccess) {
+      tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
+      e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dqp, s);
+    }
+    tm.finish();
     return from_cuda(e);
   }
+  tm.mark(AUGTREE_KID_PREPROCESS);
   cudaError_t e = launch_preprocess(op, dop, dt, p->total_prompt, p->cfg.hq, p->cfg.head_dim, delta, dq_acc, s);
-  if (e == cudaSuccess && p->n_items[AUGTREE_OP_PREFILL_BWD] > 0)
+  if (e == cudaSuccess && p->n_items[AUGTREE_OP_PREFILL_BWD] > 0) {
+    tm.mark(AUGTREE_KID_BWD_SIMT);
     e = simt_bwd(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, lse_p, dop, delta, dq_acc, dkp, dvp,
                  nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc, s);
-  if (e == cudaSuccess)
+  }
+  if (e == cudaSuccess) {
+    tm.mark(AUGTREE_KID_DQ_CONVERT);
     e = launch_dq_convert(dq_acc, dqp, dt, (int64_t)p->total_prompt * p->cfg.hq * p->cfg.head_dim, s);
+  }
+  tm.finish();
   return from_cuda(e);
+}
+
+augtree_status augtree_plan_set_timing(augtree_plan* p, int32_t enable) {
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  if (enable && !p->timing.created) {
+    for (int op = 0; op < 4; ++op)
+      for (int c = 0; c < AUGTREE_TIMING_RING; ++c)
+        for (int k = 0; k < augtree_plan::kTimingMarks; ++k)
+          if (cudaEventCreate(&p->timing.ev[op][c][k]) != cudaSuccess) return AUGTREE_ERR_CUDA;
+    p->timing.created = true;
+  }
+  p->timing.on = enable != 0;
+  return AUGTREE_OK;
+}
+
+augtree_status augtree_plan_kernel_times(const augtree_plan* p, int32_t op, int32_t back, int32_t* kind, float* ms,
+                                         int32_t cap, int32_t* n) {
+  if (!p || !n || op < 0 || op > 3 || back < 0 || back >= AUGTREE_TIMING_RING || cap < 0) return AUGTREE_ERR_INVALID_ARG;
+  const auto& T = p->timing;
+  if (!T.on || T.calls[op] <= (uint32_t)back) return AUGTREE_ERR_INVALID_ARG;
+  if (cap > 0 && (!kind || !ms)) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  const int slot = (int)((T.calls[op] - 1 - (uint32_t)back) % AUGTREE_TIMING_RING);
+  const int kernels = T.n_marks[op][slot] - 1;
+  if (cudaEventSynchronize(T.ev[op][slot][kernels]) != cudaSuccess) return AUGTREE_ERR_CUDA;
+  int written = 0;
+  for (int k = 0; k < kernels && written < cap; ++k) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, T.ev[op][slot][k], T.ev[op][slot][k + 1]) != cudaSuccess) return AUGTREE_ERR_CUDA;
+    kind[written] = T.kind[op][slot][k];
+    ms[written] = t;
+    ++written;
+  }
+  *n = written;
+  return AUGTREE_OK;
 }
 
 augtree_status augtree_plan_check(const augtree_plan* p, void* stream) {

@@ -66,6 +66,19 @@ struct augtree_plan {
   int quad[4];        // forward units of four items (four heads of one KV head) for SM pairs
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
+  // Opt-in per-kernel timing: a ring of AUGTREE_TIMING_RING calls per op, each with up
+  // to kTimingMarks events (before each kernel, after the last).  Written by the compute
+  // calls, which take the plan as const.
+  static constexpr int kTimingMarks = 6;
+  struct Timing {
+    bool on = false;
+    bool created = false;
+    cudaEvent_t ev[4][AUGTREE_TIMING_RING][kTimingMarks];
+    int32_t kind[4][AUGTREE_TIMING_RING][kTimingMarks];
+    int32_t n_marks[4][AUGTREE_TIMING_RING] = {};
+    uint32_t calls[4] = {0, 0, 0, 0};
+  };
+  mutable Timing timing;
 };
 
 namespace augtree {
@@ -87,6 +100,20 @@ BwdWorkspace replay_bwd_ws(const augtree_plan* p);
 BwdWorkspace prefill_bwd_ws(const augtree_plan* p);
 
 Geometry geometry(const augtree_plan* p);
+
+// Records the timing marks of one compute call (no-op unless the plan's timing is on):
+// mark(kind) before each kernel launch, then finish() after the last one.
+class CallTimer {
+ public:
+  CallTimer(const augtree_plan* p, int op, cudaStream_t s);
+  void mark(int kind);
+  void finish();
+
+ private:
+  const augtree_plan* p_;
+  int op_, slot_, n_;
+  cudaStream_t s_;
+};
 
 // 3-D TMA map over a [rows, heads, 128] bf16 tensor (box 64 x 1 x box_rows, 128-byte
 // swizzle, zero fill outside the tensor).
