@@ -13,16 +13,19 @@
 // lane; lse and Delta are per-thread scalars):
 //   S    = Q K^T          (TMEM, fp32)  -> P  = exp2(s S log2e - lse)   (registers)
 //   dP   = dO V^T         (TMEM, fp32)  -> dS = P (dP - Delta)          (bf16 into TMEM
-//                                          over S, the A operand of the next product)
+//                                          over dP, the A operand of the next product)
 //   dQ  += dS K           (A = dS from TMEM, B = K read MN-major from the same tile)
 // dQ accumulates in TMEM over every KV tile of the row and is written once (bf16, times
 // the softmax scale): no atomics, no fp32 accumulator in memory.
 // Warps: 0-7 two warpgroups, warpgroup w takes key columns [64w, 64w + 64) of every
 //        tile (lanes = rows, as TMEM access requires warp % 4 = lane quarter);
-//        8 TMA producer; 9 TMEM allocator + MMA issuer.
-// TMEM columns: S0/dS0 [0,128), S1/dS1 [128,256), dP [256,384), dQ [384,512).
-// MMA issue order S(j+1), dQ(j), dP(j+1): every TMEM reuse then waits on an MMA group
-// that already has another group queued behind it.
+//        8 TMA producer; 9 TMEM allocator + issuer of S and dP; 10 issuer of dQ.
+// TMEM columns: S [0,128); dP(j), then dS(j) over it, in region j % 2 ([128,256) or
+// [256,384)); dQ [384,512).
+// MMA issue order S(j+1), dP(j+1), dQ(j).  S(j+1) waits only for the compute warps to
+// have loaded S(j) into registers; dP(j+1) reuses the region dQ(j-1), issued a tile
+// earlier, read; dQ(j) waits for dS(j).  No MMA waits on the group issued just before
+// it (a tcgen05 group's completion is seen about 280 cycles after its last issue).
 #include <cuda.h>
 
 #include <cmath>
@@ -36,7 +39,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int DQ_THREADS = 320;
+constexpr int DQ_THREADS = 352;  // 8 compute warps, producer, two MMA issuers
 // K tiles are read by S(j) and dQ(j), V tiles only by dP(j), so the two rings are
 // separate: a V stage frees as soon as dP(j) is done, and the K ring has one stage more
 // so that K(j+2) can be in flight while dQ(j) still reads K(j).
@@ -51,7 +54,9 @@ constexpr int DQ_V_OFF = DQ_K_OFF + KST * 2 * BLK; // [VST][2 blocks]
 constexpr int DQ_BAR_OFF = DQ_V_OFF + VST * 2 * BLK;
 constexpr int DQ_SMEM = DQ_BAR_OFF + 256 + 1024;
 
-constexpr uint32_t T_S = 0, T_DP = 256, T_DQ = 384;
+// S [0,128) is reused every tile (free once the compute warps have loaded it); dP and
+// then dS of tile j live in region j % 2 at [128,256) / [256,384); dQ [384,512).
+constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 384;
 
 struct DqBars {
   uint64_t q_full;
@@ -59,9 +64,9 @@ struct DqBars {
   uint64_t k_empty[KST];
   uint64_t v_full[VST];
   uint64_t v_empty[VST];
-  uint64_t s_full[2];
-  uint64_t dp_full;
-  uint64_t dp_free;
+  uint64_t s_full;       // S(j) in TMEM
+  uint64_t s_free;       // the compute warps have loaded S(j)
+  uint64_t dp_full[2];   // per dP/dS region
   uint64_t ds_ready[2];
   uint64_t dq_done[2];
   uint64_t acc_done;
@@ -109,13 +114,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 256);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->dp_full[b], 1);
       mbar_init(&bars->ds_ready[b], 256);
       mbar_init(&bars->dq_done[b], 1);
     }
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 256);
     mbar_init(&bars->acc_done, 1);
     fence_mbar_init();
   }
@@ -178,30 +183,28 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       for (int j = max(0, v_issued - VST); j < v_issued; ++j) mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, err);
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer: S, dP
     if (lane == 0) {
       constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // Q K^T, dO V^T
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, 128, false, true);   // dS K (B MN-major)
       const uint64_t dQd = smem_desc_sw128(smem_u32(smem + DQ_Q_OFF), 16, 1024);
       const uint64_t dOd = smem_desc_sw128(smem_u32(smem + DQ_DO_OFF), 16, 1024);
       const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + DQ_K_OFF), 16, 1024);
       const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + DQ_V_OFF), 16, 1024);
-      const uint64_t dKm0 = smem_desc_sw128(smem_u32(smem + DQ_K_OFF), BLK, 1024);  // K as [keys x dims], MN-major
       constexpr uint64_t kStage = (2 * BLK) >> 4;
       // K-major k-step kk (16 dims): dim block kk/4, 32 bytes per step in the 128-byte row.
       auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * BLK + (kk & 3) * 32) >> 4); };
       auto issue_s = [&](int j) {
         const uint64_t dk = dK0 + (j % KST) * kStage;
-        const uint32_t d = tmem + T_S + (j & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(d, dQd + koff(kk), dk + koff(kk), id_ss, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->s_full[j & 1]);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + T_S, dQd + koff(kk), dk + koff(kk), id_ss, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->s_full);
       };
       auto issue_dp = [&](int j) {
         const uint64_t dv = dV0 + (j % VST) * kStage;
+        const uint32_t d = tmem + T_DP + (j & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + T_DP, dOd + koff(kk), dv + koff(kk), id_ss, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->dp_full);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(d, dOd + koff(kk), dv + koff(kk), id_ss, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dp_full[j & 1]);
         mma_commit(&bars->v_empty[j % VST]);  // dP(j) is the only reader of V(j)
       };
       bool ok = mbar_wait(&bars->q_full, 0, err);
@@ -211,37 +214,47 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         issue_s(0);
         issue_dp(0);
       }
+      for (int j = 0; ok && j + 1 < n_tiles; ++j) {
+        // S(j+1) overwrites S(j): the compute warps must have loaded it.
+        if (!(ok = mbar_wait(&bars->k_full[(j + 1) % KST], ((j + 1) / KST) & 1, err))) break;
+        if (!(ok = mbar_wait(&bars->s_free, j & 1, err))) break;
+        tc_fence_after();
+        issue_s(j + 1);
+        // dP(j+1) goes to the region that held dS(j-1): dQ(j-1), issued a tile earlier by
+        // the other issuer, must have read it.
+        if (!(ok = mbar_wait(&bars->v_full[(j + 1) % VST], ((j + 1) / VST) & 1, err))) break;
+        if (j >= 1 && !(ok = mbar_wait(&bars->dq_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err))) break;
+        tc_fence_after();
+        issue_dp(j + 1);
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ MMA issuer: dQ
+    // A second issuing thread: while one issuer waits on a completion, the other keeps
+    // the tensor pipe fed (two issuers measured 72 cycles per N=128 MMA with a wait per
+    // group, one issuer 92; 64 is the full rate).
+    if (lane == 0) {
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, 128, false, true);  // dS K (B MN-major)
+      const uint64_t dKm0 = smem_desc_sw128(smem_u32(smem + DQ_K_OFF), BLK, 1024);  // K as [keys x dims], MN-major
+      constexpr uint64_t kStage = (2 * BLK) >> 4;
+      bool ok = true;
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const bool more = j + 1 < n_tiles;
-        if (more) {
-          // S(j+1) goes to the buffer that holds dS(j-1): dQ(j-1) must have read it.
-          if (!(ok = mbar_wait(&bars->k_full[(j + 1) % KST], ((j + 1) / KST) & 1, err))) break;
-          if (j >= 1 && !(ok = mbar_wait(&bars->dq_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err))) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
         // dQ += dS(j) K(j): 16 keys per step; keys [64w, 64w + 64) were packed by
-        // warpgroup w into columns [64w, 64w + 32) of the S buffer.
+        // warpgroup w into columns [64w, 64w + 32) of region j % 2.
         if (!(ok = mbar_wait(&bars->ds_ready[j & 1], (j >> 1) & 1, err))) break;
         tc_fence_after();
-        {
-          const uint32_t a0 = tmem + T_S + (j & 1) * 128;
-          const uint64_t b0 = dKm0 + (j % KST) * kStage;
+        const uint32_t a0 = tmem + T_DP + (j & 1) * 128;
+        const uint64_t b0 = dKm0 + (j % KST) * kStage;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + T_DQ, a0 + (kk >> 2) * 64 + (kk & 3) * 8, b0 + kk * (2048 >> 4), id_dq,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + T_DQ, a0 + (kk >> 2) * 64 + (kk & 3) * 8, b0 + kk * (2048 >> 4), id_dq,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->dq_done[j & 1]);
-        mma_commit(&bars->k_empty[j % KST]);  // dQ(j) is the last reader of K(j)
-        if (more) {
-          // dP(j+1) overwrites dP(j): the compute warps must have read it.
-          if (!(ok = mbar_wait(&bars->dp_free, j & 1, err))) break;
-          if (!(ok = mbar_wait(&bars->v_full[(j + 1) % VST], ((j + 1) / VST) & 1, err))) break;
-          tc_fence_after();
-          issue_dp(j + 1);
-        }
+        // dQ(j) is the last reader of K(j) (S(j) completed before dS(j) existed).
+        mma_commit(&bars->k_empty[j % KST]);
       }
+      // Every MMA of the item is complete once the last dQ is: the other issuer's S and
+      // dP of the last tile completed before its dS was written.
       mma_commit(&bars->acc_done);
     }
   } else {
@@ -268,13 +281,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     const int c0 = 64 * w;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!(ok = mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, err))) break;
+      if (!(ok = mbar_wait(&bars->s_full, j & 1, err))) break;
       tc_fence_after();
-      const uint32_t ts = tmem + lane_off + T_S + (j & 1) * 128 + c0;
+      const uint32_t ts = tmem + lane_off + T_S + c0;
+      const uint32_t tdp = tmem + lane_off + T_DP + (j & 1) * 128 + c0;
       uint32_t sv[2][32];  // S, then P in place (fp32)
       tmem_ld32(ts, sv[0]);
       tmem_ld32(ts + 32, sv[1]);
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);
       int lo, hi;
       fwd_valid_cols(g, j, lo, hi);  // valid columns [lo, hi] of the tile, clamped
       const int lo_r = lo - c0;
@@ -291,18 +307,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
           sv[c >> 5][c & 31] = __float_as_uint(v ? e : 0.f);
         }
       }
-      if (!(ok = mbar_wait(&bars->dp_full, j & 1, err))) break;
+      if (!(ok = mbar_wait(&bars->dp_full[j & 1], (j >> 1) & 1, err))) break;
       tc_fence_after();
       uint32_t pk[2][16];  // dS as bf16 pairs
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + T_DP + c0 + half * 32, dp);
+        tmem_ld32(tdp + half * 32, dp);
         tmem_ld_wait();
-        if (half == 1) {
-          tc_fence_before();
-          mbar_arrive(&bars->dp_free);
-        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float d0 = __uint_as_float(sv[half][2 * i]) * (__uint_as_float(dp[2 * i]) - delta);
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
           all[i] = pk[0][i];
           all[16 + i] = pk[1][i];
         }
-        tmem_st32(ts, all);
+        tmem_st32(tdp, all);
       }
       tmem_st_wait();
       tc_fence_before();

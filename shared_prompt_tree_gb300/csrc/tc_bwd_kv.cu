@@ -33,7 +33,8 @@
 // many round trips between the MMA issuer and the compute warps per unit of work.
 // Warps: 0 .. 4 NWG - 1 compute warpgroups, warpgroup w takes query columns
 //        [COLS w, COLS (w + 1)) of every tile (thread = key = TMEM lane); then the TMA
-//        producer warp and the TMEM allocator + MMA issuer warp.
+//        producer warp, the TMEM allocator + issuer of S^T and dP^T, and the issuer of
+//        dV and dK.
 // TMEM columns: S^T/P^T [0,128), dP^T/dS^T [128,256) (each 2 x 64 when double-
 // buffered), dV [256,384), dK [384,512).
 #include <cuda.h>
@@ -54,8 +55,8 @@ constexpr int BMQ = kTcBwdKvRows;                       // query rows per tile (
 constexpr bool DB = BMQ == 64;
 constexpr int NWG = 2;                                  // compute warpgroups
 constexpr int COLS = BMQ / NWG;                         // query columns per warpgroup
-constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1;
-constexpr int KV_THREADS = (4 * NWG + 2) * 32;
+constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1, MMA2_WARP = 4 * NWG + 2;
+constexpr int KV_THREADS = (4 * NWG + 3) * 32;
 constexpr int NQ = DB ? 4 : 2;                          // Q/dO ring stages
 constexpr int kPrefetch = DB ? 6 : 4;                   // L2 prefetch distance (iterations)
 constexpr int BLK = 128 * 128;                          // 128 keys x 64 dims bf16 = 16 KB
@@ -244,6 +245,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
             tma_prefetch_3d(&tm_q, kb * 64, hp, rp);
             tma_prefetch_3d(&tm_do, kb * 64, hp, rp);
           }
+          const uint8_t* ap = aug_src(hp, qp);
+          bulk_prefetch(ap, AUG_ROWS);
+          bulk_prefetch(ap + kStatRows * 16, AUG_ROWS);
         }
       }
       // Never leave a copy in flight.
@@ -251,16 +255,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       for (int i = max(0, issued - NQ); i < issued; ++i) mbar_wait(&bars->q_full[i % NQ], (i / NQ) & 1, err);
     }
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer: S^T, dP^T
     if (lane == 0) {
       constexpr uint32_t id_ss = idesc_bf16_f32(128, BMQ, false, false);  // K Q^T, V dO^T
-      constexpr uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);   // P^T dO, dS^T Q (B MN-major)
       const uint64_t dK = smem_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
       const uint64_t dV = smem_desc_sw128(smem_u32(smem + V_OFF), 16, 1024);
       const uint64_t dQk0 = smem_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
       const uint64_t dOk0 = smem_desc_sw128(smem_u32(smem + DO_OFF), 16, 1024);
-      const uint64_t dQm0 = smem_desc_sw128(smem_u32(smem + Q_OFF), QBLK, 1024);
-      const uint64_t dOm0 = smem_desc_sw128(smem_u32(smem + DO_OFF), QBLK, 1024);
       constexpr uint64_t kStage = (2 * QBLK) >> 4;
       const uint64_t dAa = smem_desc_noswz(smem_u32(smem + AUGA_OFF), 2048, 128);
       const uint64_t dL0 = smem_desc_noswz(smem_u32(smem + AUG_OFF), AUG_LBO, 128);
@@ -268,9 +269,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       constexpr uint64_t kAugStage = AUG_STAGE >> 4;
       auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * BLK + (kk & 3) * 32) >> 4); };   // K, V
       auto qoff = [](int kk) { return (uint64_t)(((kk >> 2) * QBLK + (kk & 3) * 32) >> 4); };  // Q, dO
-      // TMEM column of the bf16 A operand for query step kk (16 rows): warpgroup w packed
-      // rows [COLS w, COLS (w + 1)) into columns [COLS w, COLS w + COLS / 2) of the buffer.
-      auto acol = [](int kk) { return (uint32_t)((kk / (COLS / 16)) * COLS + (kk % (COLS / 16)) * 8); };
       auto issue_s = [&](int i) {
         const uint64_t b = dQk0 + (i % NQ) * kStage;
         const uint32_t d = tmem + T_ST + kv_buf(i) * 64;
@@ -294,12 +292,38 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         issue_s(0);
         issue_dp(0);
       }
+      for (int i = 0; ok && i + 1 < n_iter; ++i) {
+        // The tile whose dV/dK last read the buffers that tile i + 1 overwrites: i - 1
+        // with double buffering, i itself otherwise (issued by the other issuer).
+        const int prev = DB ? i - 1 : i;
+        // S(i+1) overwrites P^T(prev): dV(prev) must have read it.
+        if (!(ok = mbar_wait(&bars->q_full[(i + 1) % NQ], ((i + 1) / NQ) & 1, err))) break;
+        if (prev >= 0 && !(ok = mbar_wait(&bars->dv_done[kv_buf(prev)], kv_phase(prev), err))) break;
+        tc_fence_after();
+        issue_s(i + 1);
+        // dP(i+1) overwrites dS^T(prev): dK(prev) must have read it.
+        if (prev >= 0 && !(ok = mbar_wait(&bars->dk_done[kv_buf(prev)], kv_phase(prev), err))) break;
+        tc_fence_after();
+        issue_dp(i + 1);
+      }
+    }
+  } else if (warp == MMA2_WARP) {
+    // ------------------------------------------------------------ MMA issuer: dV, dK
+    // A second issuing thread: while one issuer waits on a completion, the other keeps
+    // the tensor pipe fed (two issuers measured 72 cycles per N=128 MMA with a wait per
+    // group, one issuer 92; 64 is the full rate).
+    if (lane == 0) {
+      constexpr uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);  // P^T dO, dS^T Q (B MN-major)
+      const uint64_t dQm0 = smem_desc_sw128(smem_u32(smem + Q_OFF), QBLK, 1024);
+      const uint64_t dOm0 = smem_desc_sw128(smem_u32(smem + DO_OFF), QBLK, 1024);
+      constexpr uint64_t kStage = (2 * QBLK) >> 4;
+      // TMEM column of the bf16 A operand for query step kk (16 rows): warpgroup w packed
+      // rows [COLS w, COLS (w + 1)) into columns [COLS w, COLS w + COLS / 2) of the buffer.
+      auto acol = [](int kk) { return (uint32_t)((kk / (COLS / 16)) * COLS + (kk % (COLS / 16)) * 8); };
+      bool ok = true;
       for (int i = 0; ok && i < n_iter; ++i) {
         const int stage = i % NQ;
         const int b = kv_buf(i);
-        // The tile whose MMAs last read the buffers that tile i + 1 overwrites: i - 1 with
-        // double buffering, i itself otherwise.
-        const int prev = DB ? i - 1 : i;
         const bool more = i + 1 < n_iter;
         const bool fresh = flush_on ? (i % kFlush == 0) : (i == 0);
         // dV += P^T dO (from zero at the start and after every flush)
@@ -315,13 +339,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
             mma_ts(tmem + T_DV, a0 + acol(kk), b0 + kk * (2048 >> 4), id_ts, (fresh && kk == 0) ? 0u : 1u);
         }
         mma_commit(&bars->dv_done[b]);
-        if (more) {
-          // S(i+1) overwrites P^T(prev): dV(prev) must have read it.
-          if (!(ok = mbar_wait(&bars->q_full[(i + 1) % NQ], ((i + 1) / NQ) & 1, err))) break;
-          if (prev >= 0 && !(ok = mbar_wait(&bars->dv_done[kv_buf(prev)], kv_phase(prev), err))) break;
-          tc_fence_after();
-          issue_s(i + 1);
-        }
         // dK += dS^T Q
         if (!(ok = mbar_wait(&bars->ds_ready[b], kv_phase(i), err))) break;
         tc_fence_after();
@@ -333,16 +350,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
             mma_ts(tmem + T_DK, a0 + acol(kk), b0 + kk * (2048 >> 4), id_ts, (fresh && kk == 0) ? 0u : 1u);
         }
         mma_commit(&bars->dk_done[b]);
-        // dK(i) is the last reader of Q(i)/dO(i) and of the stage's extra-step rows.
+        // dK(i) is the last reader of Q(i)/dO(i) and of the stage's extra-step rows (S(i)
+        // and dP(i) completed before P^T(i) and dS^T(i) existed).
         mma_commit(&bars->q_empty[stage]);
         if (flush_on && i % kFlush == kFlush - 1 && more) mma_commit(&bars->flush_ready);
-        if (more) {
-          // dP(i+1) overwrites dS^T(prev): dK(prev) must have read it.
-          if (prev >= 0 && !(ok = mbar_wait(&bars->dk_done[kv_buf(prev)], kv_phase(prev), err))) break;
-          tc_fence_after();
-          issue_dp(i + 1);
-        }
       }
+      // All MMAs of the item are complete once the last dK is.
       mma_commit(&bars->acc_done);
     }
   } else {
@@ -370,7 +383,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     const uint32_t acc_col = (po < 128 ? T_DK : T_DV) + (po & 127);
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
-      const int stage = i % NQ;
       const int64_t row0 = qbase + (int64_t)(it.b - 1 - i % nqt) * bm;
       const int b = kv_buf(i);
       const uint32_t ts = tmem + lane_off + T_ST + b * 64 + c0, tdp = tmem + lane_off + T_DPT + b * 64 + c0;

@@ -14,8 +14,9 @@
 // heads of the same KV head (both heads share every K/V tile, loaded once).
 //   warp 8      TMA producer: Q tiles, then a 2-stage ring of K/V tiles (128-byte
 //               swizzle, 128 keys x 128 dims each)
-//   warp 9      TMEM allocator and MMA issuer: S = Q K^T (bf16 x bf16 -> fp32 TMEM),
-//               O += P V with P read from TMEM as the A operand
+//   warps 9-10  MMA issuers, one per query head (warp 9 also allocates TMEM):
+//               S = Q K^T (bf16 x bf16 -> fp32 TMEM), O += P V with P read from TMEM as
+//               the A operand
 //   warps 0-7   two softmax warpgroups, one per query head; thread i owns row i
 //               (TMEM lane i): masks, running max with lazy rescaling of O (only
 //               when the max grows by more than 2^8), P = exp2(...) as bf16 back
@@ -37,7 +38,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int FWD_THREADS = 320;
+constexpr int FWD_THREADS = 352;  // 8 softmax warps, producer, one MMA issuer per head
 constexpr int NST = 2;                  // K/V ring stages
 constexpr int TILE_BYTES = 128 * 128;   // one 128-row x 64-column bf16 block = 16 KB
 constexpr int Q_OFF = 0;                                  // [2 heads][2 blocks]
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < NST; ++i) {
       mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->kv_empty[i], n_sub);  // one commit per head's issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -133,48 +134,44 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
       mbar_wait(&bars->q_full, 0, err);
       for (int j = max(0, issued - NST); j < issued; ++j) mbar_wait(&bars->kv_full[j % NST], (j / NST) & 1, err);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    {  // all 32 lanes: warp-uniform control flow; one elected lane issues
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 9 + s issues head s's products, so that while one head's issuer waits for its
+    // softmax, the other keeps the tensor pipe fed.
+    const int s = warp - 9;
+    if (s < n_sub) {  // all 32 lanes: warp-uniform control flow; one elected lane issues
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
       // Descriptors are built once; each MMA step adds a compile-time offset (16-byte
       // units) to the start-address field, keeping the issuing thread's chain short.
-      const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+      const uint64_t dq = smem_desc_sw128(smem_u32(smem + Q_OFF + s * 2 * TILE_BYTES), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + V_OFF), TILE_BYTES, 1024);
-      constexpr uint64_t kSub = (2 * TILE_BYTES) >> 4;   // next query head's Q / next K,V stage
+      constexpr uint64_t kSub = (2 * TILE_BYTES) >> 4;   // next K,V stage
       auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * TILE_BYTES + (kk & 3) * 32) >> 4); };
+      const uint32_t ts = tmem + s * 128, to = tmem + 256 + s * 128;
       bool ok = mbar_wait_warp_all(&bars->q_full, 0, err);
       tc_fence_after();
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int stage = j % NST, use = j / NST;
         if (!(ok = mbar_wait_warp_all(&bars->kv_full[stage], use & 1, err))) break;
+        if (j > 0) {
+          // S(j) overwrites P(j-1): wait until O += P(j-1) V has completed.
+          if (!(ok = mbar_wait_warp_all(&bars->o_done[s], (j - 1) & 1, err))) break;
+        }
         tc_fence_after();
         const uint64_t dk = dk0 + stage * kSub, dv = dv0 + stage * kSub;
-        for (int s = 0; s < n_sub; ++s) {
-          if (j > 0) {
-            // S_s(j) overwrites P_s(j-1): wait until O_s += P_s(j-1) V has completed.
-            if (!(ok = mbar_wait_warp_all(&bars->o_done[s], (j - 1) & 1, err))) break;
-            tc_fence_after();
-          }
-          const uint64_t dq = dq0 + s * kSub;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_w(tmem + s * 128, dq + koff(kk), dk + koff(kk), idesc_qk, kk > 0 ? 1u : 0u);
-          mma_commit_w(&bars->s_full[s]);
-        }
-        if (!ok) break;
-        for (int s = 0; s < n_sub; ++s) {
-          if (!(ok = mbar_wait_warp_all(&bars->p_full[s], j & 1, err))) break;
-          tc_fence_after();
-          // 16 keys per step: 16 swizzled 128-byte rows = 2048 bytes; the two 64-dim
-          // halves of V are 16 KB apart (leading byte offset).
-          const uint32_t pa = tmem + s * 128;
-          mma_ts_w(tmem + 256 + s * 128, pa, dv, idesc_pv, j > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) mma_ss_w(ts, dq + koff(kk), dk + koff(kk), idesc_qk, kk > 0 ? 1u : 0u);
+        mma_commit_w(&bars->s_full[s]);
+        if (!(ok = mbar_wait_warp_all(&bars->p_full[s], j & 1, err))) break;
+        tc_fence_after();
+        // 16 keys per step: 16 swizzled 128-byte rows = 2048 bytes; the two 64-dim
+        // halves of V are 16 KB apart (leading byte offset).
+        mma_ts_w(to, ts, dv, idesc_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 1; kk < 8; ++kk) mma_ts_w(tmem + 256 + s * 128, pa + kk * 8, dv + kk * (2048 >> 4), idesc_pv, 1u);
-          mma_commit_w(&bars->o_done[s]);
-        }
+        for (int kk = 1; kk < 8; ++kk) mma_ts_w(to, ts + kk * 8, dv + kk * (2048 >> 4), idesc_pv, 1u);
+        mma_commit_w(&bars->o_done[s]);
         mma_commit_w(&bars->kv_empty[stage]);
       }
     }
