@@ -356,6 +356,14 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if args.flattened:
+        # The same trees with no prompt reuse (every pair on its own): the speedup of the
+        # shared-prompt tree over flattening, measured with the same kernels.
+        wf = flattened(w)
+        ms_f = time_device_steps(wf, at, dev, max(1, min(args.steps, 3)), 1)
+        result["flattened_per_pair"] = {
+            "ms_per_step": round(ms_f, 3), "pairs": wf.tree.pair_count(),
+            "tree_pairs": w.tree.pair_count(), "speedup_of_tree": round(ms_f / ms_step, 3)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, desc, per = time_oracle(w, min_seconds=args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads_used(),
@@ -365,6 +373,67 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def flattened(w):
+    """The workload with every prompt-response pair as its own group: each branch carries
+    its own copy of its group's prompt, so the prompt is prefilled and attended once per
+    branch (the no-reuse baseline the pages compare against, on this GPU)."""
+    import workloads as W
+    prompts, branches = [], []
+    for lp, bl in zip(w.tree.prompt_lens, w.tree.branch_lens):
+        if not bl:
+            prompts.append(lp)
+            branches.append([])
+        for li in bl:
+            prompts.append(lp)
+            branches.append([li])
+    return W.custom(W.Tree(prompts, branches), w.hq, w.hkv, w.d, w.dtype, w.seed, w.scale, name=f"{w.name}/flattened")
+
+
+def time_device_steps(w, at, dev, steps, warmup):
+    """ms per fwd+bwd step of workload w through the C ABI, inputs resident on the
+    device (the same four calls as the timed region of run_ours)."""
+    import torch
+    import workloads as W
+    dt = at.BF16 if w.dtype == "bf16" else at.FP32
+    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt)
+    t = {n: W.tensor_torch(w, n, dev) for n in W.TENSORS}
+    stream = torch.cuda.current_stream()
+    f32 = torch.float32
+    o_p, o_r = torch.empty_like(t["q_p"]), torch.empty_like(t["q_r"])
+    lse_p = torch.empty(w.hq, w.tree.total_prompt, dtype=f32, device=dev)
+    lse_r = torch.empty(w.hq, w.tree.total_resp, dtype=f32, device=dev)
+    dq_p, dk_p, dv_p = (torch.empty_like(t[n]) for n in ("q_p", "k_p", "v_p"))
+    dq_r, dk_r, dv_r = (torch.empty_like(t[n]) for n in ("q_r", "k_r", "v_r"))
+    dkp_sum = torch.empty(t["k_p"].shape, dtype=f32, device=dev)
+    dvp_sum = torch.empty(t["v_p"].shape, dtype=f32, device=dev)
+    ws_r = torch.empty(max(1, plan.workspace_bytes(at.OP_REPLAY_BWD)), dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(max(1, plan.workspace_bytes(at.OP_PREFILL_BWD)), dtype=torch.uint8, device=dev)
+
+    def step():
+        at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, stream=stream)
+        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, stream=stream)
+        at.augtree_replay_bwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, t["do_r"],
+                              dq_r, dk_r, dv_r, dkp_sum, dvp_sum, ws_r, stream=stream)
+        at.augtree_prefill_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], dkp_sum, dvp_sum,
+                               dq_p, dk_p, dv_p, ws_p, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    plan.check()
+    ms = e0.elapsed_time(e1) / steps
+    del t, o_p, o_r, lse_p, lse_r, dq_p, dk_p, dv_p, dq_r, dk_r, dv_r, dkp_sum, dvp_sum, ws_r, ws_p
+    plan.close()
+    torch.cuda.empty_cache()
+    return ms
 
 
 def scaled_down(w, k):
@@ -427,6 +496,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale-down", type=int, default=1, help="divide every length by this (profiling only)")
+    ap.add_argument("--flattened", action="store_true",
+                    help="also time the flattened-per-pair structure (no prompt reuse) with the same kernels")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -228,6 +228,20 @@ augtree_status augtree_lse_merge(int64_t rows, int32_t h, int32_t d, const float
                                  const float* lse_a, const float* ob, const float* lse_b,
                                  float* o, float* lse, void* stream);
 
+/* Backward of augtree_lse_merge (same layouts), fp32.  Given the upstream gradient
+ * dout [rows, h, d] of the merged o and, optionally, dlse [h, rows] of the merged lse
+ * (NULL: zero), writes the gradients with respect to the inputs:
+ *   w_a = exp(lse_a - lse), w_b = exp(lse_b - lse)  (lse recomputed from lse_a, lse_b),
+ *   doa = w_a dout,  dob = w_b dout,
+ *   dlse_a = w_a w_b <dout, oa - ob> + w_a dlse,  dlse_b = w_a w_b <dout, ob - oa> + w_b dlse.
+ * An input with lse = -inf has weight 0 and receives zero gradients.  Outputs must not
+ * alias inputs.  It makes the merge of Sec. 3.3 usable as a differentiable operator
+ * (the pages' MoveQ reduction is a custom autograd operator). */
+augtree_status augtree_lse_merge_bwd(int64_t rows, int32_t h, int32_t d, const float* oa,
+                                     const float* lse_a, const float* ob, const float* lse_b,
+                                     const float* dout, const float* dlse, float* doa, float* dlse_a,
+                                     float* dob, float* dlse_b, void* stream);
+
 /* Synchronizes `stream`, then reads and clears the plan's device error word.  Returns
  * AUGTREE_ERR_TIMEOUT if a kernel launched with this plan gave up on a bounded
  * device-side wait (it then skipped the rest of its work item and exited cleanly),

@@ -17,7 +17,8 @@ Context-Parallel Long-Context LLM Post-Training".
   * Sec. 3.2, Eq. 2: grad KV_P = sum_{i=1..G} grad_{KV_P} L_i (prompt gradients summed
     over all branches, then propagated through the prefill graph).
   * Sec. 3.3: partial online-softmax states S = (m, l, O_acc) merge associatively;
-    here they are carried as (O, lse) with lse = m + log l and O = O_acc / l.
+    here they are carried as (O, lse) with lse = m + log l and O = O_acc / l.  The
+    merge's backward (lse_merge_backward) is its chain rule, written out.
 
 Layout (token-major, "THD"): q [L, Hq, D], k/v [L, Hkv, D]; query head h uses KV head
 floor(h / r), r = Hq / Hkv.  lse is [Hq, L] in natural log.
@@ -338,6 +339,35 @@ def lse_merge(o_a, lse_a, o_b, lse_b):
     wb = np.where(fin & np.isfinite(lse_b), np.exp(np.where(np.isfinite(lse_b), lse_b, 0.0) - lse_safe), 0.0)
     o = wa[..., None] * o_a + wb[..., None] * o_b
     return o, lse
+
+
+def lse_merge_backward(o_a, lse_a, o_b, lse_b, d_o, d_lse=None):
+    """Gradients of the state merge (+) (Sec. 3.3) with respect to its two inputs, given
+    the upstream gradient d_o of the merged O and, optionally, d_lse of the merged lse.
+
+    With w_a = e^(lse_a - lse), w_b = e^(lse_b - lse) (so w_a + w_b = 1):
+        O = w_a O_a + w_b O_b,   lse = log(e^lse_a + e^lse_b),
+        dw_a/dlse_a = w_a w_b,   dw_b/dlse_a = -w_a w_b,   dlse/dlse_a = w_a,
+    hence
+        dO_a = w_a d_o,   dO_b = w_b d_o,
+        dlse_a = w_a w_b <d_o, O_a - O_b> + w_a d_lse,
+        dlse_b = w_a w_b <d_o, O_b - O_a> + w_b d_lse.
+    An empty input (lse = -inf) has weight 0 and receives zero gradients; the other
+    input then passes d_o and d_lse through unchanged."""
+    if d_lse is None:
+        d_lse = np.zeros(np.shape(lse_a))
+    lse = np.logaddexp(lse_a, lse_b)
+    fin = np.isfinite(lse)
+    lse_safe = np.where(fin, lse, 0.0)
+    wa = np.where(fin & np.isfinite(lse_a), np.exp(np.where(np.isfinite(lse_a), lse_a, 0.0) - lse_safe), 0.0)
+    wb = np.where(fin & np.isfinite(lse_b), np.exp(np.where(np.isfinite(lse_b), lse_b, 0.0) - lse_safe), 0.0)
+    sa = np.sum(d_o * o_a, axis=-1)
+    sb = np.sum(d_o * o_b, axis=-1)
+    do_a = wa[..., None] * d_o
+    do_b = wb[..., None] * d_o
+    dl_a = wa * wb * (sa - sb) + wa * d_lse
+    dl_b = wa * wb * (sb - sa) + wb * d_lse
+    return do_a, dl_a, do_b, dl_b
 
 
 def to_float64(t: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:

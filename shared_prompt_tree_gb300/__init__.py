@@ -76,6 +76,7 @@ _SIGS = {
     "augtree_prefill_bwd": [_P] * 13 + [_SZ, _P],
     "augtree_prefill_bwd_static": [_P] * 13,
     "augtree_lse_merge": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 6 + [_P],
+    "augtree_lse_merge_bwd": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 10 + [_P],
     "augtree_plan_check": [_P, _P],
     "augtree_plan_set_timing": [_P, ctypes.c_int32],
     "augtree_plan_kernel_times": [_P, ctypes.c_int32, ctypes.c_int32, _P, _P, ctypes.c_int32,
@@ -271,6 +272,14 @@ def augtree_lse_merge(oa, lse_a, ob, lse_b, o, lse, stream=None):
                                    _stream(stream)), "augtree_lse_merge")
 
 
+def augtree_lse_merge_bwd(oa, lse_a, ob, lse_b, dout, dlse, doa, dlse_a, dob, dlse_b, stream=None):
+    """Gradients of the (O, lse) merge with respect to its inputs (dlse may be None)."""
+    rows, h, d = oa.shape
+    _check(lib().augtree_lse_merge_bwd(rows, h, d, _ptr(oa), _ptr(lse_a), _ptr(ob), _ptr(lse_b), _ptr(dout),
+                                       _ptr(dlse), _ptr(doa), _ptr(dlse_a), _ptr(dob), _ptr(dlse_b),
+                                       _stream(stream)), "augtree_lse_merge_bwd")
+
+
 # ------------------------------------------------------------------------------------
 # Autograd
 # ------------------------------------------------------------------------------------
@@ -342,6 +351,44 @@ def _autograd_fn():
 
 
 _FN = None
+
+
+_MERGE_FN = None
+
+
+def _merge_fn():
+    import torch
+
+    class LseMergeFn(torch.autograd.Function):
+        """(O, lse) merge of two partial attention states as a differentiable operator."""
+
+        @staticmethod
+        def forward(ctx, oa, lse_a, ob, lse_b):
+            oa, lse_a, ob, lse_b = (x.contiguous() for x in (oa, lse_a, ob, lse_b))
+            o, lse = torch.empty_like(oa), torch.empty_like(lse_a)
+            augtree_lse_merge(oa, lse_a, ob, lse_b, o, lse)
+            ctx.save_for_backward(oa, lse_a, ob, lse_b)
+            return o, lse
+
+        @staticmethod
+        def backward(ctx, do, dlse):
+            oa, lse_a, ob, lse_b = ctx.saved_tensors
+            do = torch.zeros_like(oa) if do is None else do.contiguous()
+            dlse = None if dlse is None else dlse.contiguous()
+            doa, dob = torch.empty_like(oa), torch.empty_like(ob)
+            dla, dlb = torch.empty_like(lse_a), torch.empty_like(lse_b)
+            augtree_lse_merge_bwd(oa, lse_a, ob, lse_b, do, dlse, doa, dla, dob, dlb)
+            return doa, dla, dob, dlb
+
+    return LseMergeFn
+
+
+def lse_merge(oa, lse_a, ob, lse_b):
+    """Differentiable (O, lse) merge of fp32 CUDA tensors oa/ob [rows, h, d], lse [h, rows]."""
+    global _MERGE_FN
+    if _MERGE_FN is None:
+        _MERGE_FN = _merge_fn()
+    return _MERGE_FN.apply(oa, lse_a, ob, lse_b)
 
 
 def tree_attention(plan: Plan, q_p, k_p, v_p, q_r, k_r, v_r):

@@ -1,6 +1,6 @@
 // Memory-bound kernels of the path: the backward preprocess (Delta, the SIMT family's
 // zeroed fp32 dQ accumulator, the tensor-core family's tiled row statistics), the dQ
-// conversion, the fixed-order split-K reduction of the prompt
+// conversion, the merge's backward, the fixed-order split-K reduction of the prompt
 // K/V gradient (Eq. 2), and the partial-state merge of Sec. 3.3.
 //
 // AugTree paper, Sec. 3.2 (Eq. 2: the prompt K/V gradient is the sum over branches,
@@ -186,6 +186,49 @@ __global__ void lse_merge_kernel(int64_t rows, int h, int d, const float* __rest
   if (lane == 0) l[li] = lse;
 }
 
+// Backward of the state merge: one warp per (row, head).  With w_a = e^(lse_a - lse),
+// w_b = e^(lse_b - lse): doa = w_a do, dob = w_b do,
+// dlse_a = w_a w_b <do, oa - ob> + w_a dlse, dlse_b = w_a w_b <do, ob - oa> + w_b dlse.
+__global__ void lse_merge_bwd_kernel(int64_t rows, int h, int d, const float* __restrict__ oa,
+                                     const float* __restrict__ la, const float* __restrict__ ob,
+                                     const float* __restrict__ lb, const float* __restrict__ dout,
+                                     const float* __restrict__ dl, float* __restrict__ doa,
+                                     float* __restrict__ dla, float* __restrict__ dob, float* __restrict__ dlb) {
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows * h) return;
+  const int64_t row = warp / h;
+  const int head = (int)(warp % h);
+  const int64_t li = (int64_t)head * rows + row;
+  const float a = la[li], b = lb[li];
+  const float m = fmaxf(a, b);
+  float wa = 0.f, wb = 0.f;
+  if (m != -INFINITY) {
+    const float ea = (a == -INFINITY) ? 0.f : expf(a - m);
+    const float eb = (b == -INFINITY) ? 0.f : expf(b - m);
+    const float s = ea + eb;
+    wa = ea / s;
+    wb = eb / s;
+  }
+  const int64_t base = warp * d;
+  float sa = 0.f, sb = 0.f;
+  for (int c = lane; c < d; c += 32) {
+    const float g = dout[base + c];
+    sa = fmaf(g, oa[base + c], sa);
+    sb = fmaf(g, ob[base + c], sb);
+    doa[base + c] = wa * g;
+    dob[base + c] = wb * g;
+  }
+  sa = warp_sum(sa);
+  sb = warp_sum(sb);
+  if (lane == 0) {
+    const float g = dl ? dl[li] : 0.f;
+    const float ww = wa * wb;
+    dla[li] = ww * (sa - sb) + wa * g;
+    dlb[li] = ww * (sb - sa) + wb * g;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d, float* delta,
@@ -244,4 +287,16 @@ cudaError_t launch_lse_merge(int64_t rows, int h, int d, const float* oa, const 
   return cudaGetLastError();
 }
 
+}  // namespace augtree
+
+namespace augtree {
+cudaError_t launch_lse_merge_bwd(int64_t rows, int h, int d, const float* oa, const float* la, const float* ob,
+                                 const float* lb, const float* dout, const float* dl, float* doa, float* dla,
+                                 float* dob, float* dlb, cudaStream_t st) {
+  const int64_t warps = rows * h;
+  if (warps == 0) return cudaSuccess;
+  const int64_t blocks = (warps + 7) / 8;
+  lse_merge_bwd_kernel<<<(unsigned)blocks, 256, 0, st>>>(rows, h, d, oa, la, ob, lb, dout, dl, doa, dla, dob, dlb);
+  return cudaGetLastError();
+}
 }  // namespace augtree

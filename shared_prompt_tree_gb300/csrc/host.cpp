@@ -763,4 +763,14 @@ augtree_status augtree_lse_merge(int64_t rows, int32_t h, int32_t d, const float
   return from_cuda(launch_lse_merge(rows, h, d, oa, lse_a, ob, lse_b, o, lse, (cudaStream_t)stream));
 }
 
+augtree_status augtree_lse_merge_bwd(int64_t rows, int32_t h, int32_t d, const float* oa, const float* lse_a,
+                                     const float* ob, const float* lse_b, const float* dout, const float* dlse,
+                                     float* doa, float* dlse_a, float* dob, float* dlse_b, void* stream) {
+  if (rows < 0 || h <= 0 || d <= 0) return AUGTREE_ERR_INVALID_ARG;
+  if (rows == 0) return AUGTREE_OK;
+  if (!oa || !lse_a || !ob || !lse_b || !dout || !doa || !dlse_a || !dob || !dlse_b) return AUGTREE_ERR_INVALID_ARG;
+  return from_cuda(launch_lse_merge_bwd(rows, h, d, oa, lse_a, ob, lse_b, dout, dlse, doa, dlse_a, dob, dlse_b,
+                                        (cudaStream_t)stream));
+}
+
 }  // extern "C"

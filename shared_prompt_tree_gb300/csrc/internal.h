@@ -158,5 +158,8 @@ cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, con
                                 float* dk_sum, float* dv_sum, cudaStream_t st);
 cudaError_t launch_lse_merge(int64_t rows, int h, int d, const float* oa, const float* la,
                              const float* ob, const float* lb, float* o, float* l, cudaStream_t st);
+cudaError_t launch_lse_merge_bwd(int64_t rows, int h, int d, const float* oa, const float* la, const float* ob,
+                                 const float* lb, const float* dout, const float* dl, float* doa, float* dla,
+                                 float* dob, float* dlb, cudaStream_t st);
 
 }  // namespace augtree

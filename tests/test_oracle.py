@@ -445,3 +445,49 @@ def test_gqa_equals_mha_with_repeated_kv():
     for k in ("dk_p", "dv_p", "dk_r", "dv_r"):
         summed = mha[k].reshape(mha[k].shape[0], hkv, hq // hkv, d).sum(2)
         np.testing.assert_allclose(gqa[k], summed, atol=1e-13, rtol=0)
+
+
+def test_lse_merge_backward_matches_finite_differences():
+    """The merge's backward against central differences of the merge itself (fp64), for
+    a loss L = <g, O> + <h, lse> with random g, h."""
+    rng = np.random.default_rng(31)
+    n, d = 6, 5
+    oa, ob = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    la, lb = rng.standard_normal(n) * 2, rng.standard_normal(n) * 2
+    g, h = rng.standard_normal((n, d)), rng.standard_normal(n)
+
+    def loss(oa_, la_, ob_, lb_):
+        o, l = A.lse_merge(oa_, la_, ob_, lb_)
+        return float(np.sum(g * o) + np.sum(h * l))
+
+    got = A.lse_merge_backward(oa, la, ob, lb, g, h)
+    eps = 1e-6
+    for idx, base in enumerate((oa, la, ob, lb)):
+        num = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            args_p = [x.copy() for x in (oa, la, ob, lb)]
+            args_m = [x.copy() for x in (oa, la, ob, lb)]
+            args_p[idx][i] += eps
+            args_m[idx][i] -= eps
+            num[i] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(got[idx], num, rtol=1e-6, atol=1e-8)
+
+
+def test_lse_merge_backward_special_cases():
+    """An empty partner passes the gradient through; two empty inputs get zeros; equal
+    inputs split d_o in halves."""
+    rng = np.random.default_rng(32)
+    o, do = rng.standard_normal((3, 4)), rng.standard_normal((3, 4))
+    l, dl = rng.standard_normal(3), rng.standard_normal(3)
+    ninf, z = np.full(3, -np.inf), np.zeros((3, 4))
+    doa, dla, dob, dlb = A.lse_merge_backward(o, l, z, ninf, do, dl)
+    np.testing.assert_allclose(doa, do, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(dla, dl, rtol=0, atol=1e-15)
+    assert np.all(dob == 0) and np.all(dlb == 0)
+    r = A.lse_merge_backward(z, ninf, z, ninf, do, dl)
+    assert all(np.all(x == 0) for x in r)
+    doa, dla, dob, dlb = A.lse_merge_backward(o, l, o, l, do, dl)
+    np.testing.assert_allclose(doa, do / 2, rtol=1e-15)
+    np.testing.assert_allclose(dla, dl / 2, rtol=1e-15)  # <do, oa - ob> = 0

@@ -89,6 +89,42 @@ def test_lse_merge_matches_oracle(cuda_device):
     np.testing.assert_allclose(oa_t.cpu().numpy(), o.cpu().numpy(), atol=0, rtol=0)
 
 
+def test_lse_merge_backward_matches_oracle(cuda_device):
+    """The merge's backward (C ABI and the differentiable merge) against the fp64 oracle,
+    with empty states on either side and on both."""
+    rng = np.random.default_rng(5)
+    rows, h, d = 41, 3, 64
+    oa, ob = rng.standard_normal((rows, h, d)), rng.standard_normal((rows, h, d))
+    la, lb = rng.standard_normal((h, rows)) * 3, rng.standard_normal((h, rows)) * 3
+    la[0, :5] = -np.inf
+    lb[0, 3:8] = -np.inf
+    g, gl = rng.standard_normal((rows, h, d)), rng.standard_normal((h, rows))
+    dev = cuda_device
+    f32 = lambda x: x.astype(np.float32).astype(np.float64)
+    T = lambda x: torch.tensor(x, dtype=torch.float32, device=dev)
+    want = A.lse_merge_backward(f32(oa).transpose(1, 0, 2), f32(la), f32(ob).transpose(1, 0, 2), f32(lb),
+                                f32(g).transpose(1, 0, 2), f32(gl))
+    outs = [torch.empty(rows, h, d, device=dev), torch.empty(h, rows, device=dev),
+            torch.empty(rows, h, d, device=dev), torch.empty(h, rows, device=dev)]
+    at.augtree_lse_merge_bwd(T(oa), T(la), T(ob), T(lb), T(g), T(gl), *outs)
+    got = [x.cpu().numpy().astype(np.float64) for x in outs]
+    got[0], got[2] = got[0].transpose(1, 0, 2), got[2].transpose(1, 0, 2)
+    for name, a, b in zip(("doa", "dlse_a", "dob", "dlse_b"), got, want):
+        np.testing.assert_allclose(a, b, atol=1e-4, rtol=1e-5, err_msg=name)
+    # through autograd
+    ta, tla, tb, tlb = (T(x).requires_grad_() for x in (oa, la, ob, lb))
+    o, l = at.lse_merge(ta, tla, tb, tlb)
+    (o * T(g)).sum().add((torch.where(torch.isfinite(l), l, torch.zeros_like(l)) * T(gl)).sum()).backward()
+    fin = np.isfinite(np.logaddexp(la, lb))
+    gl_eff = np.where(fin, gl, 0.0)
+    want2 = A.lse_merge_backward(f32(oa).transpose(1, 0, 2), f32(la), f32(ob).transpose(1, 0, 2), f32(lb),
+                                 f32(g).transpose(1, 0, 2), gl_eff)
+    for name, t, b, tr in (("oa", ta, want2[0], True), ("la", tla, want2[1], False), ("ob", tb, want2[2], True),
+                           ("lb", tlb, want2[3], False)):
+        a = t.grad.cpu().numpy().astype(np.float64)
+        np.testing.assert_allclose(a.transpose(1, 0, 2) if tr else a, b, atol=1e-4, rtol=1e-5, err_msg=name)
+
+
 def test_schedule_export_matches_host_build(cuda_device):
     w = W.custom(RAGGED[2], hq=8, hkv=2, d=128, dtype="bf16", seed=1)
     for kernel in (at.KERNEL_SIMT, at.KERNEL_TC):
