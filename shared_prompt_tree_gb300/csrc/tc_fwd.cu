@@ -38,6 +38,10 @@ namespace {
 
 using namespace tc;
 
+#ifndef AUGTREE_FWD_PINGPONG
+#define AUGTREE_FWD_PINGPONG 1
+#endif
+constexpr bool kFwdPingPong = AUGTREE_FWD_PINGPONG != 0;
 constexpr int FWD_THREADS = 352;  // 8 softmax warps, producer, one MMA issuer per head
 constexpr int NST = 2;                  // K/V ring stages
 constexpr int TILE_BYTES = 128 * 128;   // one 128-row x 64-column bf16 block = 16 KB
@@ -54,6 +58,7 @@ struct FwdBars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
+  uint64_t turn[2];  // softmax hand-off: turn[s] completes when head s may run its exponentials
   uint32_t tmem_base;
 };
 
@@ -93,6 +98,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 128);
       mbar_init(&bars->o_done[i], 1);
+      mbar_init(&bars->turn[i], 4);
     }
     fence_mbar_init();
   }
@@ -194,9 +200,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
       g.bn = bn;
       const int h = heads[s];
       uint64_t* p_full = &bars->p_full[s];
-      fwd_softmax_row(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles, geo.scale_log2,
-                      &bars->s_full[s], &bars->o_done[s], [p_full]() { mbar_arrive(p_full); },
-                      out + (g.row * geo.hq + h) * 128, lse + (int64_t)h * lse_rows + g.row, err);
+      auto signal = [p_full]() { mbar_arrive(p_full); };
+      __nv_bfloat16* orow = out + (g.row * geo.hq + h) * 128;
+      float* lrow = lse + (int64_t)h * lse_rows + g.row;
+      if (kFwdPingPong && n_sub == 2) {
+        const PingPong turn{&bars->turn[s], &bars->turn[s ^ 1], s == 0 ? 1 : 0};
+        fwd_softmax_row(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles, geo.scale_log2,
+                        &bars->s_full[s], &bars->o_done[s], signal, orow, lrow, err, turn);
+      } else {
+        fwd_softmax_row(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles, geo.scale_log2,
+                        &bars->s_full[s], &bars->o_done[s], signal, orow, lrow, err);
+      }
     }
   }
   tc_fence_before();

@@ -50,16 +50,42 @@ __device__ __forceinline__ void fwd_valid_cols(const FwdRowGeom& g, int j, int& 
   hi_i = hi < -1 ? -1 : (hi > 128 ? 128 : (int)hi);
 }
 
+// Exponential-phase hand-off between a block's two softmax warpgroups.  The two heads
+// of a block otherwise run their softmax in step, share the MUFU (about twice as slow
+// each) and leave the tensor pipe idle meanwhile; alternating them lets one head's
+// exponentials overlap the other head's MMAs.  NoTurn: no hand-off.
+struct NoTurn {
+  __device__ __forceinline__ bool wait(int, uint32_t*) const { return true; }
+  __device__ __forceinline__ void pass() const {}
+};
+// mine / other: mbarriers with an arrival count of 4 (one per warp of the warpgroup
+// that passes the turn).  first = 1 for the warpgroup that starts: its tile j waits for
+// the other's tile j-1; the other warpgroup's tile j waits for this one's tile j.
+struct PingPong {
+  uint64_t* mine;
+  uint64_t* other;
+  int first;
+  __device__ __forceinline__ bool wait(int j, uint32_t* err) const {
+    const int n = j - first;
+    return n < 0 || mbar_wait(mine, n & 1, err);
+  }
+  __device__ __forceinline__ void pass() const {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(other);
+  }
+};
+
 // Runs the row's online softmax over n_tiles KV tiles of 128 keys.  For each tile:
 // waits s_full (S in TMEM), masks, keeps a running max with lazy rescaling of O
 // (only when the max grows by more than 2^8; exact, every term shares the offset),
 // writes P = exp2(s*log2e*S - m) as bf16 over S (one value in eight from the FMA-pipe
 // exponential), adds the bf16 values to the row sum, and calls signal_p() once its
 // warpgroup may hand P to the MMA issuer.  At the end writes O / l (bf16) and lse.
-template <typename SignalP>
+template <typename SignalP, typename Turn = NoTurn>
 __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const FwdRowGeom& g, int n_tiles, float sl2,
                                                 uint64_t* s_full, uint64_t* o_done, SignalP signal_p,
-                                                __nv_bfloat16* out_row, float* lse_ptr, uint32_t* err) {
+                                                __nv_bfloat16* out_row, float* lse_ptr, uint32_t* err,
+                                                Turn turn = Turn()) {
   float m = -INFINITY, l = 0.f;
   bool ok = true;
   for (int j = 0; j < n_tiles; ++j) {
@@ -92,6 +118,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     const float alpha = need ? fast_exp2(m - m_new) : 1.f;
     m = m_new;
     const float mu = (m == -INFINITY) ? 0.f : m;
+    if (!(ok = turn.wait(j, err))) break;
     float ps[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial sums
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -119,6 +146,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
       tmem_st32(tS + c * 32, pk);
     }
 #undef AUGTREE_X
+    turn.pass();
     tmem_st_wait();
     const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
     l = l * alpha + psum;
