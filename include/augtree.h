@@ -148,6 +148,23 @@ augtree_status augtree_schedule_build(const augtree_desc* desc, const augtree_co
                                       int32_t op, int32_t* out, size_t cap_items,
                                       size_t* n_items);
 
+/* AssignGrid (Sec. 3.4, Eq. 6), host only, no GPU needed: places n_units replay units
+ * with work estimates w[n_units] (>= 0) on a grid of `rounds` x `lanes` cells, at most
+ * one unit per cell (a lane runs its rounds one after another), minimising the
+ * largest lane total max_j sum_{k on lane j} w[k].  With n_units <= u_max the
+ * placement is exact (subset dynamic program over lanes; u_max <= 16, cost about
+ * lanes * 3^n_units / 2 steps); otherwise it is the largest-first greedy: units in
+ * order of weight descending (index ascending on ties), each to the lane with the
+ * smallest total among those with a free round (lowest lane on ties).  u_max = 0
+ * always takes the greedy.  Within a lane, rounds follow the same largest-first order.
+ * Out: round_out[k] in [0, rounds), lane_out[k] in [0, lanes), *makespan_out = the
+ * largest lane total, *exact_out (nullable) = 1 if the dynamic program ran.  Errors:
+ * AUGTREE_ERR_INVALID_ARG for null pointers, a negative weight, rounds or lanes < 1,
+ * u_max outside [0, 16] or n_units > rounds * lanes. */
+augtree_status augtree_assign_grid(const int64_t* w, int32_t n_units, int32_t rounds, int32_t lanes,
+                                   int32_t u_max, int32_t* round_out, int32_t* lane_out,
+                                   int64_t* makespan_out, int32_t* exact_out);
+
 /* ---- Plans ------------------------------------------------------------------------ */
 
 /* Validates the descriptors and config, builds all four work queues on the host and

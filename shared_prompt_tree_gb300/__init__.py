@@ -66,6 +66,8 @@ _SIGS = {
                            ctypes.POINTER(ctypes.c_int32)],
     "augtree_schedule_build": [ctypes.POINTER(Desc), ctypes.POINTER(Config), ctypes.c_int32, _P, _SZ,
                                ctypes.POINTER(_SZ)],
+    "augtree_assign_grid": [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                            ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)],
     "augtree_plan_create": [ctypes.POINTER(Desc), ctypes.POINTER(Config), ctypes.POINTER(_P)],
     "augtree_plan_destroy": [_P],
     "augtree_plan_workspace_bytes": [_P, ctypes.c_int32, ctypes.POINTER(_SZ)],
@@ -148,6 +150,25 @@ def schedule_build(offsets, cfg: Config, op: int) -> np.ndarray:
     _check(lib().augtree_schedule_build(ctypes.byref(d), ctypes.byref(cfg), op, out.ctypes.data, n.value,
                                         ctypes.byref(n)), "augtree_schedule_build")
     return out[:n.value]
+
+
+ASSIGN_GRID_MAX_EXACT = 16
+
+
+def assign_grid(w, rounds: int, lanes: int, u_max: int = 12):
+    """AssignGrid (host only): places replay units with work estimates `w` on a grid of
+    `rounds` x `lanes` cells, one unit per cell, minimising the largest lane total;
+    exact for len(w) <= u_max, largest-first greedy otherwise (u_max=0: always greedy).
+    Returns (round int32 [U], lane int32 [U], makespan, exact)."""
+    wa = np.ascontiguousarray(np.asarray(w, dtype=np.int64))
+    n = int(wa.size)
+    rnd = np.zeros(max(1, n), dtype=np.int32)
+    lane = np.zeros(max(1, n), dtype=np.int32)
+    mk, ex = ctypes.c_int64(), ctypes.c_int32()
+    _check(lib().augtree_assign_grid(wa.ctypes.data if n else None, n, int(rounds), int(lanes), int(u_max),
+                                     rnd.ctypes.data, lane.ctypes.data, ctypes.byref(mk), ctypes.byref(ex)),
+           "augtree_assign_grid")
+    return rnd[:n], lane[:n], int(mk.value), bool(ex.value)
 
 
 class Plan:
