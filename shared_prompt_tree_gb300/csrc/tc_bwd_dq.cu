@@ -39,6 +39,12 @@ namespace {
 
 using namespace tc;
 
+// All exponentials on the MUFU: moving one in eight to the FMA pipe measured 5 % slower
+// here (unlike the key side, this kernel's compute phase is issue-bound).
+#ifndef AUGTREE_DQ_EXP_FMA
+#define AUGTREE_DQ_EXP_FMA 0
+#endif
+constexpr int kDqExpFma = AUGTREE_DQ_EXP_FMA;  // 0, or N: one exponential in N via exp2_fma
 constexpr int DQ_THREADS = 352;  // 8 compute warps, producer, two MMA issuers
 // K tiles are read by S(j) and dQ(j), V tiles only by dP(j), so the two rings are
 // separate: a V stage frees as soon as dP(j) is done, and the K ring has one stage more
@@ -297,8 +303,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       const uint32_t span = hi >= lo ? (uint32_t)(hi - lo) : 0xFFFFFFFFu;  // all-invalid if empty
       if (lo_r <= 0 && hi - c0 >= 63 && hi >= lo) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          sv[c >> 5][c & 31] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]), sl2, -lse2)));
+        for (int c = 0; c < 64; ++c) {
+          const float x = fmaf(__uint_as_float(sv[c >> 5][c & 31]), sl2, -lse2);
+          // One exponential in kDqExpFma on the FMA pipe.
+          const bool on_fma = kDqExpFma > 0 && c % kDqExpFma == kDqExpFma - 1;
+          sv[c >> 5][c & 31] = __float_as_uint(on_fma ? exp2_fma(x) : fast_exp2(x));
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < 64; ++c) {

@@ -53,6 +53,15 @@ constexpr int BMQ = kTcBwdKvRows;                       // query rows per tile (
 // With 64-row tiles S^T and dP^T are double-buffered in TMEM (two 64-column halves);
 // with 128-row tiles they take 128 columns each and are reused every tile.
 constexpr bool DB = BMQ == 64;
+// One exponential in kKvExpFma of the P^T phase runs on the FMA pipe (exp2_fma): the
+// phase is MUFU-bound (16 exponentials per clock per SM), on the critical chain
+// S(i) -> P(i) -> dV(i) -> S(i+1).  Measured: one in eight +2.7 % on this kernel
+// (prompt-heavy), one in four -1.5 %.
+#ifndef AUGTREE_KV_EXP_FMA
+#define AUGTREE_KV_EXP_FMA 8
+#endif
+constexpr int kKvExpFma = AUGTREE_KV_EXP_FMA;           // 0, or N: one exponential in N via exp2_fma
+static_assert(kKvExpFma == 0 || (kKvExpFma >= 2 && kKvExpFma % 2 == 0), "exp2_fma fraction");
 constexpr int NWG = 2;                                  // compute warpgroups
 constexpr int COLS = BMQ / NWG;                         // query columns per warpgroup
 constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1, MMA2_WARP = 4 * NWG + 2;
@@ -403,7 +412,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
 #pragma unroll
         for (int c = 0; c < COLS; c += 2) {
           const float e0 = fast_exp2(__uint_as_float(sraw[c >> 5][c & 31]) * sl2);
-          const float e1 = fast_exp2(__uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]) * sl2);
+          const float x1 = __uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]) * sl2;
+          // One exponential in kKvExpFma on the FMA pipe: the MUFU sets this phase's pace.
+          const float e1 = (kKvExpFma > 0 && (c / 2) % (kKvExpFma / 2) == kKvExpFma / 2 - 1) ? exp2_fma(x1)
+                                                                                            : fast_exp2(x1);
           pk[c >> 1] = pack_bf16x2(e0, e1);
         }
       } else {
