@@ -55,10 +55,10 @@ constexpr int BMQ = kTcBwdKvRows;                       // query rows per tile (
 constexpr bool DB = BMQ == 64;
 // One exponential in kKvExpFma of the P^T phase runs on the FMA pipe (exp2_fma): the
 // phase is MUFU-bound (16 exponentials per clock per SM), on the critical chain
-// S(i) -> P(i) -> dV(i) -> S(i+1).  Measured: one in eight +2.7 % on this kernel
-// (prompt-heavy), one in four -1.5 %.
+// S(i) -> P(i) -> dV(i) -> S(i+1).  Measured on this kernel (prompt-heavy, TFLOP/s):
+// none 1,357; one in 4: 1,335; in 6: 1,410; in 8: 1,393; in 12: 1,406; in 16: 1,400.
 #ifndef AUGTREE_KV_EXP_FMA
-#define AUGTREE_KV_EXP_FMA 8
+#define AUGTREE_KV_EXP_FMA 12
 #endif
 constexpr int kKvExpFma = AUGTREE_KV_EXP_FMA;           // 0, or N: one exponential in N via exp2_fma
 static_assert(kKvExpFma == 0 || (kKvExpFma >= 2 && kKvExpFma % 2 == 0), "exp2_fma fraction");

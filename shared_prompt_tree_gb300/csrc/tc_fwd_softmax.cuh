@@ -15,6 +15,15 @@
 namespace augtree {
 namespace tc {
 
+// In the row's second half, every kFwdFmaStride-th pair's second exponential runs on
+// the FMA pipe (exp2_fma): 16 -> one exponential in 64 overall; 0 -> none.  Measured
+// with the two heads' exponential phases alternating (prompt-heavy forward, TFLOP/s):
+// one in 4: 1,094; in 8: 1,155; in 16: 1,267; in 32: 1,245; in 64: 1,326; none: 1,174.
+#ifndef AUGTREE_FWD_FMA_STRIDE
+#define AUGTREE_FWD_FMA_STRIDE 16
+#endif
+constexpr int kFwdFmaStride = AUGTREE_FWD_FMA_STRIDE;
+
 // Where the row's keys come from in KV tile j: prompt tiles first, then the own-branch
 // tiles, and the valid columns [lo, hi] of the row in that tile.
 struct FwdRowGeom {
@@ -78,7 +87,7 @@ struct PingPong {
 // Runs the row's online softmax over n_tiles KV tiles of 128 keys.  For each tile:
 // waits s_full (S in TMEM), masks, keeps a running max with lazy rescaling of O
 // (only when the max grows by more than 2^8; exact, every term shares the offset),
-// writes P = exp2(s*log2e*S - m) as bf16 over S (one value in eight from the FMA-pipe
+// writes P = exp2(s*log2e*S - m) as bf16 over S (one value in 64 from the FMA-pipe
 // exponential), adds the bf16 values to the row sum, and calls signal_p() once its
 // warpgroup may hand P to the MMA issuer.  At the end writes O / l (bf16) and lse.
 template <typename SignalP, typename Turn = NoTurn>
@@ -129,7 +138,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
         const float a0 = fmaf(__uint_as_float(AUGTREE_X(c0)), sl2, -mu);
         const float a1 = fmaf(__uint_as_float(AUGTREE_X(c0 + 1)), sl2, -mu);
         float p0 = fast_exp2(a0), p1;
-        if (c == 1 && (i & 1)) {
+        if (kFwdFmaStride > 0 && c == 1 && i % kFwdFmaStride == kFwdFmaStride - 1) {
           // FMA-pipe exponential (second half of the row, where half of S has already
           // been consumed and registers are free); a masked column (-inf) must stay
           // exactly zero.
