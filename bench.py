@@ -209,10 +209,14 @@ def run_ours(args):
     dq_r, dk_r, dv_r = (torch.empty_like(t[n]) for n in ("q_r", "k_r", "v_r"))
     dkp_sum = torch.empty(t["k_p"].shape, dtype=f32, device=dev)
     dvp_sum = torch.empty(t["v_p"].shape, dtype=f32, device=dev)
-    ws_r = torch.empty(max(1, plan.workspace_bytes(at.OP_REPLAY_BWD)), dtype=torch.uint8, device=dev)
-    ws_p = torch.empty(max(1, plan.workspace_bytes(at.OP_PREFILL_BWD)), dtype=torch.uint8, device=dev)
+    fused = args.bwd == "fused"
+    if fused:
+        ws_t = torch.empty(max(1, plan.workspace_bytes(at.OP_TREE_BWD)), dtype=torch.uint8, device=dev)
+    else:
+        ws_r = torch.empty(max(1, plan.workspace_bytes(at.OP_REPLAY_BWD)), dtype=torch.uint8, device=dev)
+        ws_p = torch.empty(max(1, plan.workspace_bytes(at.OP_PREFILL_BWD)), dtype=torch.uint8, device=dev)
 
-    n_ev = 5
+    n_ev = 4 if fused else 5
     def step(evs=None):
         rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
         rec(0)
@@ -220,6 +224,12 @@ def run_ours(args):
         rec(1)
         at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, stream=stream)
         rec(2)
+        if fused:
+            at.augtree_tree_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], t["q_r"], t["k_r"],
+                                t["v_r"], o_r, lse_r, t["do_r"], dq_p, dk_p, dv_p, dq_r, dk_r, dv_r, ws_t,
+                                stream=stream)
+            rec(3)
+            return
         at.augtree_replay_bwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, t["do_r"],
                               dq_r, dk_r, dv_r, dkp_sum, dvp_sum, ws_r, stream=stream)
         rec(3)
@@ -253,9 +263,13 @@ def run_ours(args):
     plan.check()  # raises if any kernel of the step gave up on a bounded wait
     kernel_ms = {}  # kind -> [ms per step summed over the step's launches, launches per step]
     if args.steps <= at.TIMING_RING:
-        for op in range(4):
+        for op in range(5):
             for back in range(args.steps):
-                for kind, t_ms in plan.kernel_times(op, back):
+                try:
+                    kt = plan.kernel_times(op, back)
+                except at.AugtreeError:  # the step makes no timed call of this op
+                    break
+                for kind, t_ms in kt:
                     e = kernel_ms.setdefault((op, kind), [0.0, 0])
                     e[0] += t_ms / args.steps
                     e[1] += 1
@@ -290,15 +304,21 @@ def run_ours(args):
     tokens = w.tokens
     tflops = flops * world / (ms_step * 1e-3) / 1e12
     pk, pk_kind = peaks()
-    names = ["prefill_fwd", "replay_fwd", "replay_bwd", "prefill_bwd"]
     n_pairs_prompt = sum(lp * (lp + 1) // 2 for lp in w.tree.prompt_lens)
     n_pairs = w.tree.pair_count()
-    per_flops = [4 * w.d * w.hq * n_pairs_prompt, 4 * w.d * w.hq * (n_pairs - n_pairs_prompt),
-                 10 * w.d * w.hq * (n_pairs - n_pairs_prompt), 10 * w.d * w.hq * n_pairs_prompt]
+    if fused:
+        names = ["prefill_fwd", "replay_fwd", "tree_bwd"]
+        per_flops = [4 * w.d * w.hq * n_pairs_prompt, 4 * w.d * w.hq * (n_pairs - n_pairs_prompt),
+                     10 * w.d * w.hq * n_pairs]
+    else:
+        names = ["prefill_fwd", "replay_fwd", "replay_bwd", "prefill_bwd"]
+        per_flops = [4 * w.d * w.hq * n_pairs_prompt, 4 * w.d * w.hq * (n_pairs - n_pairs_prompt),
+                     10 * w.d * w.hq * (n_pairs - n_pairs_prompt), 10 * w.d * w.hq * n_pairs_prompt]
     # The dominant kernel: per-launch algorithmic FLOPs (the GEMMs the kernel itself
     # performs on valid pairs: forward 2, key side S, dP, dV, dK = 4, query side S, dP,
     # dQ = 3, each 2 d Hq per pair) over its launches' measured durations.
-    pairs = {0: n_pairs_prompt, 1: n_pairs - n_pairs_prompt, 2: n_pairs - n_pairs_prompt, 3: n_pairs_prompt}
+    pairs = {0: n_pairs_prompt, 1: n_pairs - n_pairs_prompt, 2: n_pairs - n_pairs_prompt, 3: n_pairs_prompt,
+             4: n_pairs}
     gemms = {"fwd_tc": 2, "fwd_simt": 2, "bwd_key_side": 4, "bwd_query_side": 3, "bwd_simt": 5}
     kinds = {}
     for (op, kind), (t_ms, launches) in kernel_ms.items():
@@ -318,7 +338,7 @@ def run_ours(args):
         ach = per_flops[dom] / (per_call[dom] * 1e-3) / 1e12
         dom_kind, dom_name, launches_k = names[dom], names[dom] + " call", 1
     peak_s = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    launches_per_step = count_launches(plan, at)
+    launches_per_step = count_launches(plan, at, fused)
 
     result = {
         "metric": "tree-attn fwd+bwd useful TFLOP/s & tokens/s; % of GB300 BF16 tensor peak",
@@ -337,6 +357,7 @@ def run_ours(args):
                    "branches": w.tree.n_branches, "total_prompt": w.tree.total_prompt,
                    "total_resp": w.tree.total_resp, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
                    "parallelism": f"replicas x{world}", "kernel_family": args.kernel,
+                   "backward": "one augtree_tree_bwd call" if fused else "augtree_replay_bwd + augtree_prefill_bwd",
                    "l2": "inputs larger than L2 (no flush)"},
         "tokens_per_s": round(tokens * world / (ms_step * 1e-3), 1),
         "flattened_tokens_per_s": round(w.tree.flattened_tokens() * world / (ms_step * 1e-3), 1),
@@ -443,12 +464,20 @@ def scaled_down(w, k):
     return W.custom(tree, w.hq, w.hkv, w.d, w.dtype, w.seed, w.scale, name=f"{w.name}/{k}")
 
 
-def count_launches(plan, at):
-    """Kernels one step launches: prefill fwd 1, replay fwd 1, replay bwd 4
-    (preprocess, main, split reduce, dQ convert), prefill bwd 3."""
+def count_launches(plan, at, fused=False):
+    """Kernels one step launches: prefill fwd 1, replay fwd 1; then either the fused
+    backward (preprocess per side, key side, split reduce when a group is split, query
+    side per side) or replay bwd 4 (preprocess, key side, split reduce, query side) and
+    prefill bwd 3."""
     n = 0
     n += 1 if plan.schedule(at.OP_PREFILL_FWD).shape[0] else 0
     n += 1 if plan.schedule(at.OP_REPLAY_FWD).shape[0] else 0
+    if fused:
+        q = plan.schedule(at.OP_TREE_BWD)
+        split = bool(q.shape[0]) and bool((q[:, 4] > 0).any())
+        n += 2 * (1 if plan.total_resp else 0) + 2 * (1 if plan.total_prompt else 0)
+        n += (1 if q.shape[0] else 0) + (1 if split else 0)
+        return n
     n += (1 if plan.total_resp else 0) + (1 if plan.schedule(at.OP_REPLAY_BWD).shape[0] else 0) \
         + (1 if plan.total_prompt else 0) + (1 if plan.total_resp else 0)
     n += 3 if plan.total_prompt else 0
@@ -493,6 +522,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--bwd", choices=["fused", "two-call"], default="fused",
+                    help="backward as one augtree_tree_bwd call, or replay_bwd then prefill_bwd")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale-down", type=int, default=1, help="divide every length by this (profiling only)")

@@ -68,7 +68,8 @@ typedef enum {
   AUGTREE_OP_PREFILL_FWD = 0,
   AUGTREE_OP_REPLAY_FWD = 1,
   AUGTREE_OP_REPLAY_BWD = 2,
-  AUGTREE_OP_PREFILL_BWD = 3
+  AUGTREE_OP_PREFILL_BWD = 3,
+  AUGTREE_OP_TREE_BWD = 4   /* the whole backward in one call (augtree_tree_bwd) */
 } augtree_op;
 
 /* Ragged group / branch descriptors (host memory, read during plan creation only).
@@ -124,6 +125,14 @@ typedef struct augtree_plan augtree_plan;
  *    covers the end of the branch holding the tile's last key.  cost = (b - a) * r.
  *  kind 4 PREFILL_KV (prefill_bwd): prompt KV tile `tile`, KV head `head`: prompt
  *    query tiles [a, b) = [floor(tile*BN/BM), ceil(L_P/BM)).  cost = (b - a) * r.
+ *  kind 5 TREE_PROMPT_KV (tree_bwd): prompt KV tile `tile`, KV head `head`, split
+ *    `split`: response query tiles [a, b) of the group as in PROMPT_KV and, for split
+ *    0 only, also the prompt query tiles [floor(tile*BN/BM), ceil(L_P/BM)) as in
+ *    PREFILL_KV.  cost = (b - a + (split == 0 ? ceil(L_P/BM) - floor(tile*BN/BM) : 0)) * r.
+ *    The tree_bwd queue holds: for every prompt KV tile and KV head of a group with
+ *    L_P > 0, one kind-5 item per split of the replay_bwd split rule below (one item,
+ *    a = b = 0, when the group has no response rows); and the RESP_KV items of
+ *    replay_bwd.
  *
  * Split rule (replay_bwd, atomic-free split-K of the prompt dK/dV, Eq. 2): let
  * U = sum of the costs of all replay_bwd items before splitting, T = max(r,
@@ -215,6 +224,24 @@ augtree_status augtree_prefill_bwd(const augtree_plan* plan, const void* qp, con
                                    const void* dop, const float* dkp_acc, const float* dvp_acc,
                                    void* dqp, void* dkp, void* dvp, void* ws, size_t ws_bytes,
                                    void* stream);
+
+/* The whole backward in one call (Sec. 3.2, Eq. 2: the prompt K/V gradient is the sum
+ * over branches of the replay gradients plus the prompt's own causal gradient).  The
+ * results equal augtree_replay_bwd followed by augtree_prefill_bwd with the replay sums
+ * (up to fp32 summation order), without the fp32 sums in memory: with the tensor-core
+ * kernels each prompt KV tile accumulates the prompt's own causal query tiles and all
+ * branches' query tiles in one pass (work queue AUGTREE_OP_TREE_BWD; split-K partials,
+ * reduced in a fixed order, only for groups split by the replay_bwd split rule); the
+ * SIMT family runs the two calls.
+ * In: the prefill inputs qp, kp, vp, op, lse_p, dop and the replay inputs qr, kr, vr,
+ * or_, lse_r, dor (layouts as above).  Out: dqp, dkp, dvp, dqr, dkr, dvr (plan dtype).
+ * Workspace: augtree_plan_workspace_bytes(AUGTREE_OP_TREE_BWD). */
+augtree_status augtree_tree_bwd(const augtree_plan* plan, const void* qp, const void* kp,
+                                const void* vp, const void* op, const float* lse_p,
+                                const void* dop, const void* qr, const void* kr, const void* vr,
+                                const void* or_, const float* lse_r, const void* dor, void* dqp,
+                                void* dkp, void* dvp, void* dqr, void* dkr, void* dvr, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* Prefill backward that allocates nothing and takes no workspace.  The paper has no
  * counterpart: this is a convenience for callers that cannot allocate device memory

@@ -19,8 +19,8 @@ from typing import List, Tuple
 
 import numpy as np
 
-PREFILL_Q, REPLAY_Q, PROMPT_KV, RESP_KV, PREFILL_KV = 0, 1, 2, 3, 4
-OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD = 0, 1, 2, 3
+PREFILL_Q, REPLAY_Q, PROMPT_KV, RESP_KV, PREFILL_KV, TREE_PROMPT_KV = 0, 1, 2, 3, 4, 5
+OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD, OP_TREE_BWD = 0, 1, 2, 3, 4
 MAX_SPLIT = 64
 
 
@@ -73,8 +73,11 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
                 b = _cdiv(row_end - bstart, bn)
                 for h in range(hq):
                     items.append((REPLAY_Q, g, t, h, 0, a + b, a, b))
-    elif op == OP_REPLAY_BWD:
-        # Unsplit costs first, to fix the split target.
+    elif op in (OP_REPLAY_BWD, OP_TREE_BWD):
+        # Unsplit costs first, to fix the split target.  The fused backward (all of the
+        # backward in one call) uses the replay backward's split rule; split 0 of a
+        # prompt KV tile also walks the prompt's own causal query tiles of that tile.
+        tree = op == OP_TREE_BWD
         total = 0
         resp_items = []
         for g, grp in enumerate(groups):
@@ -92,7 +95,13 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
         target = max(r, _cdiv(total, 2 * num_sms))
         for g, grp in enumerate(groups):
             nq = _cdiv(grp["lr"], bm)
-            if grp["lp"] == 0 or nq == 0:
+            nqp = _cdiv(grp["lp"], bm)
+            if grp["lp"] == 0 or (nq == 0 and not tree):
+                continue
+            if nq == 0:
+                for j in range(_cdiv(grp["lp"], bn)):
+                    for h in range(hkv):
+                        items.append((TREE_PROMPT_KV, g, j, h, 0, (nqp - (j * bn) // bm) * r, 0, 0))
                 continue
             s = min(MAX_SPLIT, max(1, _cdiv(nq * r, target)))
             c = _cdiv(nq, s)
@@ -100,8 +109,9 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
             for j in range(_cdiv(grp["lp"], bn)):
                 for k in range(s):
                     qa, qb = k * c, min((k + 1) * c, nq)
+                    own = nqp - (j * bn) // bm if (tree and k == 0) else 0
                     for h in range(hkv):
-                        items.append((PROMPT_KV, g, j, h, k, (qb - qa) * r, qa, qb))
+                        items.append((TREE_PROMPT_KV if tree else PROMPT_KV, g, j, h, k, (qb - qa + own) * r, qa, qb))
         for (g, j, qa, qb) in resp_items:
             for h in range(hkv):
                 items.append((RESP_KV, g, j, h, 0, (qb - qa) * r, qa, qb))

@@ -28,7 +28,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEV
     ERR_CAPACITY = range(8)
 FP32, BF16 = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC = 0, 1, 2
-OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD = 0, 1, 2, 3
+OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD, OP_TREE_BWD = 0, 1, 2, 3, 4
 # augtree_kernel_id: kinds reported by augtree_plan_kernel_times
 KERNEL_IDS = {1: "fwd_tc", 2: "fwd_simt", 3: "preprocess", 4: "bwd_key_side", 5: "split_reduce",
               6: "bwd_query_side", 7: "dq_convert", 8: "bwd_simt"}
@@ -77,6 +77,7 @@ _SIGS = {
     "augtree_replay_bwd": [_P] * 15 + [_SZ, _P],
     "augtree_prefill_bwd": [_P] * 13 + [_SZ, _P],
     "augtree_prefill_bwd_static": [_P] * 13,
+    "augtree_tree_bwd": [_P] * 20 + [_SZ, _P],
     "augtree_lse_merge": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 6 + [_P],
     "augtree_lse_merge_bwd": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 10 + [_P],
     "augtree_plan_check": [_P, _P],
@@ -277,6 +278,14 @@ def augtree_prefill_bwd(plan: Plan, qp, kp, vp, op, lse_p, dop, dkp_acc, dvp_acc
            "augtree_prefill_bwd")
 
 
+def augtree_tree_bwd(plan: Plan, qp, kp, vp, op, lse_p, dop, qr, kr, vr, or_, lse_r, dor, dqp, dkp, dvp, dqr, dkr, dvr,
+                     ws, stream=None):
+    _check(lib().augtree_tree_bwd(plan.handle, *(_ptr(t) for t in (qp, kp, vp, op, lse_p, dop, qr, kr, vr, or_, lse_r,
+                                                                  dor, dqp, dkp, dvp, dqr, dkr, dvr, ws)),
+                                  0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "augtree_tree_bwd")
+
+
 def augtree_prefill_bwd_static(plan: Plan, qp, kp, vp, op, lse_p, dop, dkp_acc, dvp_acc, dqp, dkp, dvp,
                                stream=None):
     """augtree_prefill_bwd without a workspace: the library's fixed 64 MiB scratch array
@@ -327,11 +336,20 @@ def forward(plan: Plan, q_p, k_p, v_p, q_r, k_r, v_r):
     return o_p, lse_p, o_r, lse_r
 
 
-def backward(plan: Plan, q_p, k_p, v_p, q_r, k_r, v_r, o_p, lse_p, o_r, lse_r, do_p, do_r):
-    """Replay backward (prompt K/V gradient summed over branches, Eq. 2), then the
-    prefill backward that adds that sum.  Returns dq_p, dk_p, dv_p, dq_r, dk_r, dv_r."""
+def backward(plan: Plan, q_p, k_p, v_p, q_r, k_r, v_r, o_p, lse_p, o_r, lse_r, do_p, do_r, fused: bool = True):
+    """The tree backward (the prompt K/V gradient sums every branch's replay gradient and
+    the prompt's own causal part, Eq. 2).  fused: one augtree_tree_bwd call; otherwise
+    the replay backward, then the prefill backward that adds its sums.
+    Returns dq_p, dk_p, dv_p, dq_r, dk_r, dv_r."""
     import torch
     dev = (q_p if q_p.numel() else q_r).device
+    if fused:
+        dq_p, dk_p, dv_p = _empty(q_p.shape, plan, dev), _empty(k_p.shape, plan, dev), _empty(v_p.shape, plan, dev)
+        dq_r, dk_r, dv_r = _empty(q_r.shape, plan, dev), _empty(k_r.shape, plan, dev), _empty(v_r.shape, plan, dev)
+        ws = torch.empty(max(1, plan.workspace_bytes(OP_TREE_BWD)), dtype=torch.uint8, device=dev)
+        augtree_tree_bwd(plan, q_p, k_p, v_p, o_p, lse_p, do_p, q_r, k_r, v_r, o_r, lse_r, do_r, dq_p, dk_p, dv_p,
+                         dq_r, dk_r, dv_r, ws)
+        return dq_p, dk_p, dv_p, dq_r, dk_r, dv_r
     f32 = torch.float32
     dq_r, dk_r, dv_r = _empty(q_r.shape, plan, dev), _empty(k_r.shape, plan, dev), _empty(v_r.shape, plan, dev)
     dkp_sum = _empty(k_p.shape, plan, dev, f32)

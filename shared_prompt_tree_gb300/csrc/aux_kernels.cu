@@ -7,6 +7,7 @@
 // "exact many-to-one gradient aggregation") and Sec. 3.3 (partial online-softmax
 // states S = (m, l, O_acc) merge associatively; here in (O, lse) form).
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -115,10 +116,15 @@ __global__ void convert_kernel(const float* __restrict__ src, T* __restrict__ ds
 // Per prompt row (one block per row, Hkv*D columns): groups with several splits sum
 // their partials in ascending split order; groups without prompt-KV items (no
 // responses) get zeros; single-split groups were written in place by the backward.
+// Out = float: the replay sums (an unsplit group was written by the key side, a group
+// with no prompt-KV items gets zeros).  Out = bf16: the fused backward's final prompt
+// gradient, for split groups only (the key side wrote the others).
+template <typename Out>
 __global__ void split_reduce_kernel(const GroupInfo* __restrict__ groups, const SplitInfo* __restrict__ splits,
                                     int n_groups, int cols, const float* __restrict__ dk_part,
-                                    const float* __restrict__ dv_part, float* __restrict__ dk_sum,
-                                    float* __restrict__ dv_sum, int total_prompt) {
+                                    const float* __restrict__ dv_part, Out* __restrict__ dk_sum,
+                                    Out* __restrict__ dv_sum, int total_prompt) {
+  constexpr bool kFinal = !std::is_same<Out, float>::value;
   const int row = blockIdx.x;
   if (row >= total_prompt) return;
   // group of this row: binary search over p0
@@ -134,11 +140,11 @@ __global__ void split_reduce_kernel(const GroupInfo* __restrict__ groups, const 
   if (g >= n_groups) return;
   const SplitInfo s = splits[g];
   const int64_t out = (int64_t)row * cols;
-  if (s.nsplit == 1) return;
+  if (s.nsplit == 1 || (kFinal && s.nsplit == 0)) return;
   if (s.nsplit == 0) {
     for (int c = threadIdx.x; c < cols; c += blockDim.x) {
-      dk_sum[out + c] = 0.f;
-      dv_sum[out + c] = 0.f;
+      dk_sum[out + c] = Out(0.f);
+      dv_sum[out + c] = Out(0.f);
     }
     return;
   }
@@ -151,8 +157,13 @@ __global__ void split_reduce_kernel(const GroupInfo* __restrict__ groups, const 
       ak += dk_part[pr];
       av += dv_part[pr];
     }
-    dk_sum[out + c] = ak;
-    dv_sum[out + c] = av;
+    if constexpr (kFinal) {
+      dk_sum[out + c] = __float2bfloat16_rn(ak);
+      dv_sum[out + c] = __float2bfloat16_rn(av);
+    } else {
+      dk_sum[out + c] = ak;
+      dv_sum[out + c] = av;
+    }
   }
 }
 
@@ -274,8 +285,18 @@ cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, con
                                 float* dv_sum, cudaStream_t st) {
   if (p->total_prompt == 0 || p->n_groups == 0) return cudaSuccess;
   const int cols = p->cfg.hkv * p->cfg.head_dim;
-  split_reduce_kernel<<<p->total_prompt, 256, 0, st>>>(p->groups_d, p->splits_d, p->n_groups, cols, dk_part, dv_part,
-                                                       dk_sum, dv_sum, p->total_prompt);
+  split_reduce_kernel<float><<<p->total_prompt, 256, 0, st>>>(p->groups_d, p->splits_d, p->n_groups, cols, dk_part,
+                                                              dv_part, dk_sum, dv_sum, p->total_prompt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_reduce_final(const augtree_plan* p, const float* dk_part, const float* dv_part, void* dkp,
+                                      void* dvp, cudaStream_t st) {
+  if (p->total_prompt == 0 || p->n_groups == 0 || p->part_rows == 0) return cudaSuccess;
+  const int cols = p->cfg.hkv * p->cfg.head_dim;
+  split_reduce_kernel<__nv_bfloat16><<<p->total_prompt, 256, 0, st>>>(
+      p->groups_d, p->splits_d, p->n_groups, cols, dk_part, dv_part, (__nv_bfloat16*)dkp, (__nv_bfloat16*)dvp,
+      p->total_prompt);
   return cudaGetLastError();
 }
 

@@ -147,8 +147,9 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
         for (int h = 0; h < hq; ++h) push(K_REPLAY_Q, g, t, h, 0, a + b, a, b);
       }
     }
-  } else if (op == AUGTREE_OP_REPLAY_BWD) {
-    // Costs before splitting fix the split target.
+  } else if (op == AUGTREE_OP_REPLAY_BWD || op == AUGTREE_OP_TREE_BWD) {
+    // Costs before splitting fix the split target (replay items only, in both queues).
+    const bool tree = op == AUGTREE_OP_TREE_BWD;
     int64_t total = 0;
     struct RI { int g; int64_t j, qa, qb; };
     std::vector<RI> resp;
@@ -171,14 +172,25 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
     for (int g = 0; g < ng; ++g) {
       const Grp& G = groups[g];
       int64_t nq = cdiv(G.lr, bm);
-      if (G.lp == 0 || nq == 0) continue;
+      const int64_t nqp = cdiv(G.lp, bm);
+      if (G.lp == 0 || (nq == 0 && !tree)) continue;
+      if (nq == 0) {
+        // Fused backward, no response rows: the prompt's own causal part only.
+        for (int64_t j = 0; j < cdiv(G.lp, bn); ++j)
+          for (int h = 0; h < hkv; ++h) push(K_TREE_PROMPT_KV, g, j, h, 0, (nqp - (j * bn) / bm) * r, 0, 0);
+        continue;
+      }
       int64_t s = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, cdiv(nq * r, target)));
       int64_t c = cdiv(nq, s);
       s = cdiv(nq, c);
       for (int64_t j = 0; j < cdiv(G.lp, bn); ++j)
         for (int64_t k = 0; k < s; ++k) {
           int64_t qa = k * c, qb = std::min((k + 1) * c, nq);
-          for (int h = 0; h < hkv; ++h) push(K_PROMPT_KV, g, j, h, (int)k, (qb - qa) * r, qa, qb);
+          // In the fused backward, split 0 also walks the prompt's own causal query
+          // tiles of this KV tile.
+          const int64_t own = (tree && k == 0) ? nqp - (j * bn) / bm : 0;
+          for (int h = 0; h < hkv; ++h)
+            push(tree ? K_TREE_PROMPT_KV : K_PROMPT_KV, g, j, h, (int)k, (qb - qa + own) * r, qa, qb);
         }
     }
     for (const RI& x : resp)
@@ -241,6 +253,21 @@ BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
   w.slots_off = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
   w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
   return w;
+}
+
+TreeWorkspace tree_bwd_ws(const augtree_plan* p) {
+  TreeWorkspace t;
+  t.r = replay_bwd_ws(p);
+  t.p = prefill_bwd_ws(p);
+  // The replay part keeps its flush slots; the prefill part needs none of its own (the
+  // kernels run one after the other).
+  t.p_off = align256(t.r.total);
+  t.sum_off = align256(t.p_off + t.p.slots_off);
+  const size_t sum_bytes =
+      p->family == AUGTREE_KERNEL_TC ? 0 : align256((size_t)p->total_prompt * p->cfg.hkv * p->cfg.head_dim * 4);
+  t.total = t.sum_off + 2 * sum_bytes;
+  t.sum_bytes = sum_bytes;
+  return t;
 }
 
 BwdWorkspace prefill_bwd_ws(const augtree_plan* p) {
@@ -313,7 +340,7 @@ int32_t augtree_version(void) { return 100; }
 augtree_status augtree_tile_sizes(const augtree_config* cfg, int32_t op, int32_t* bm, int32_t* bn) {
   augtree_status st = validate_cfg(cfg, false);
   if (st != AUGTREE_OK) return st;
-  if (!bm || !bn || op < 0 || op > 3) return AUGTREE_ERR_INVALID_ARG;
+  if (!bm || !bn || op < 0 || op >= kNumOps) return AUGTREE_ERR_INVALID_ARG;
   int m, n;
   tiles_for(resolve_family(cfg), op, &m, &n);
   *bm = m;
@@ -327,7 +354,7 @@ augtree_status augtree_schedule_build(const augtree_desc* desc, const augtree_co
   augtree_status st = validate_desc(desc, po, bb, ro);
   if (st != AUGTREE_OK) return st;
   if ((st = validate_cfg(cfg, true)) != AUGTREE_OK) return st;
-  if (!n_items || op < 0 || op > 3 || (cap_items > 0 && !out)) return AUGTREE_ERR_INVALID_ARG;
+  if (!n_items || op < 0 || op >= kNumOps || (cap_items > 0 && !out)) return AUGTREE_ERR_INVALID_ARG;
   int bm, bn;
   tiles_for(resolve_family(cfg), op, &bm, &bn);
   std::vector<int32_t> q;
@@ -353,9 +380,9 @@ augtree_status augtree_plan_destroy(augtree_plan* p) {
   cudaFree(p->row_bend_d);
   cudaFree(p->splits_d);
   cudaFree(p->err_d);
-  for (int i = 0; i < 4; ++i) cudaFree(p->queue_d[i]);
+  for (int i = 0; i < kNumOps; ++i) cudaFree(p->queue_d[i]);
   if (p->timing.created)
-    for (int op = 0; op < 4; ++op)
+    for (int op = 0; op < kNumOps; ++op)
       for (int c = 0; c < AUGTREE_TIMING_RING; ++c)
         for (int k = 0; k < augtree_plan::kTimingMarks; ++k) cudaEventDestroy(p->timing.ev[op][c][k]);
   if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
@@ -378,7 +405,7 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   p->row_bstart_d = nullptr;
   p->row_bend_d = nullptr;
   p->splits_d = nullptr;
-  for (int i = 0; i < 4; ++i) p->queue_d[i] = nullptr;
+  for (int i = 0; i < kNumOps; ++i) p->queue_d[i] = nullptr;
   if (cudaGetDevice(&p->device) != cudaSuccess) {
     delete p;
     return AUGTREE_ERR_CUDA;
@@ -415,7 +442,7 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
       bstart[row] = ro[b];
       bend[row] = ro[b + 1];
     }
-  for (int op = 0; op < 4; ++op) {
+  for (int op = 0; op < kNumOps; ++op) {
     tiles_for(p->family, op, &p->bm[op], &p->bn[op]);
     st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, p->bm[op], p->bn[op], p->cfg.num_sms, p->queue_h[op]);
     if (st != AUGTREE_OK) {
@@ -427,7 +454,7 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   // Forward tensor-core units pair consecutive items: heads h, h+1 (h even) of one
   // query tile share their KV head when Hq/Hkv is even.  The sort order puts the Hq
   // items of a (group, tile) next to each other, so pairs are checked, not assumed.
-  for (int op = 0; op < 4; ++op) {
+  for (int op = 0; op < kNumOps; ++op) {
     p->paired[op] = 0;
     p->quad[op] = 0;
     if (p->family != AUGTREE_KERNEL_TC || op > AUGTREE_OP_REPLAY_FWD) continue;
@@ -480,7 +507,7 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   ok = ok && up((void**)&p->row_bend_d, bend.data(), bend.size() * sizeof(int32_t));
   ok = ok && up((void**)&p->err_d, pad.data(), sizeof(uint32_t));
   ok = ok && up((void**)&p->splits_d, p->splits_h.data(), p->splits_h.size() * sizeof(SplitInfo));
-  for (int op = 0; op < 4 && ok; ++op)
+  for (int op = 0; op < kNumOps && ok; ++op)
     ok = up((void**)&p->queue_d[op], p->queue_h[op].empty() ? (const void*)pad.data() : p->queue_h[op].data(),
             p->queue_h[op].size() * sizeof(int32_t));
   if (!ok) {
@@ -499,13 +526,14 @@ augtree_status augtree_plan_workspace_bytes(const augtree_plan* p, int32_t op, s
     case AUGTREE_OP_REPLAY_FWD: *bytes = 0; return AUGTREE_OK;
     case AUGTREE_OP_REPLAY_BWD: *bytes = replay_bwd_ws(p).total; return AUGTREE_OK;
     case AUGTREE_OP_PREFILL_BWD: *bytes = prefill_bwd_ws(p).total; return AUGTREE_OK;
+    case AUGTREE_OP_TREE_BWD: *bytes = tree_bwd_ws(p).total; return AUGTREE_OK;
   }
   return AUGTREE_ERR_INVALID_ARG;
 }
 
 augtree_status augtree_schedule_export(const augtree_plan* p, int32_t op, int32_t* host_out, size_t cap_items,
                                        size_t* n_items) {
-  if (!p || !n_items || op < 0 || op > 3) return AUGTREE_ERR_INVALID_ARG;
+  if (!p || !n_items || op < 0 || op >= kNumOps) return AUGTREE_ERR_INVALID_ARG;
   *n_items = p->n_items[op];
   if (p->n_items[op] > cap_items) return AUGTREE_ERR_CAPACITY;
   if (p->n_items[op] == 0) return AUGTREE_OK;
@@ -615,8 +643,9 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
     }
     if (e == cudaSuccess && p->n_items[AUGTREE_OP_REPLAY_BWD] > 0) {
       tm.mark(AUGTREE_KID_BWD_KEY_SIDE);
-      e = tc_bwd_kv(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, aug, dor, dkr, dvr, dk_part, dv_part, dkp_sum,
-                    dvp_sum, nullptr, nullptr, (float*)(base + w.slots_off), s);
+      e = tc_bwd_kv(p, AUGTREE_OP_REPLAY_BWD, qr, dor, aug, nullptr, nullptr, nullptr, kp, vp, kr, vr, dkr, dvr,
+                    nullptr, nullptr, dk_part, dv_part, dkp_sum, dvp_sum, nullptr, nullptr,
+                    (float*)(base + w.slots_off), s);
     }
     if (e == cudaSuccess && p->total_prompt > 0) {
       tm.mark(AUGTREE_KID_SPLIT_REDUCE);
@@ -677,8 +706,9 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
     cudaError_t e = launch_preprocess_tiled(p, true, op, dop, lse_p, delta, aug, s);
     if (e == cudaSuccess) {
       tm.mark(AUGTREE_KID_BWD_KEY_SIDE);
-      e = tc_bwd_kv(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, aug, dop, dkp, dvp, nullptr, nullptr,
-                    nullptr, nullptr, dkp_acc, dvp_acc, (float*)(base + w.slots_off), s);
+      e = tc_bwd_kv(p, AUGTREE_OP_PREFILL_BWD, qp, dop, aug, nullptr, nullptr, nullptr, kp, vp, nullptr, nullptr, dkp,
+                    dvp, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dkp_acc, dvp_acc,
+                    (float*)(base + w.slots_off), s);
     }
     if (e == cudaSuccess) {
       tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
@@ -702,12 +732,79 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
   return from_cuda(e);
 }
 
+augtree_status augtree_tree_bwd(const augtree_plan* p, const void* qp, const void* kp, const void* vp, const void* op,
+                                const float* lse_p, const void* dop, const void* qr, const void* kr, const void* vr,
+                                const void* or_, const float* lse_r, const void* dor, void* dqp, void* dkp, void* dvp,
+                                void* dqr, void* dkr, void* dvr, void* ws, size_t ws_bytes, void* stream) {
+  if (!p) return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_prompt > 0 && (!qp || !kp || !vp || !op || !lse_p || !dop || !dqp || !dkp || !dvp))
+    return AUGTREE_ERR_INVALID_ARG;
+  if (p->total_resp > 0 && (!qr || !kr || !vr || !or_ || !lse_r || !dor || !dqr || !dkr || !dvr))
+    return AUGTREE_ERR_INVALID_ARG;
+  const TreeWorkspace w = tree_bwd_ws(p);
+  if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
+  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  char* base = (char*)ws;
+  if (p->family != AUGTREE_KERNEL_TC) {
+    // SIMT family: the two calls, with the replay sums in the workspace.
+    float* dks = (float*)(base + w.sum_off);
+    float* dvs = (float*)(base + w.sum_off + w.sum_bytes);
+    st = augtree_replay_bwd(p, qr, kp, vp, kr, vr, or_, lse_r, dor, dqr, dkr, dvr, p->total_prompt ? dks : nullptr,
+                            p->total_prompt ? dvs : nullptr, base, w.r.total, stream);
+    if (st != AUGTREE_OK) return st;
+    return augtree_prefill_bwd(p, qp, kp, vp, op, lse_p, dop, p->total_prompt ? dks : nullptr,
+                               p->total_prompt ? dvs : nullptr, dqp, dkp, dvp, base + w.p_off, w.p.slots_off, stream);
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  float* delta_r = (float*)(base + w.r.delta_off);
+  void* aug_r = base + w.r.aug_off;
+  float* delta_p = (float*)(base + w.p_off + w.p.delta_off);
+  void* aug_p = base + w.p_off + w.p.aug_off;
+  float* dk_part = (float*)(base + w.r.dkpart_off);
+  float* dv_part = (float*)(base + w.r.dvpart_off);
+  cudaError_t e = cudaSuccess;
+  CallTimer tm(p, AUGTREE_OP_TREE_BWD, s);
+  // Row statistics of both sides, then one key-side pass: every prompt KV tile walks its
+  // prompt's own causal query tiles and all branches' query tiles in one accumulator
+  // (split-K partials only where the prompt has few tiles), every response KV tile its
+  // branch's tiles; then the query side of both.
+  if (p->total_resp > 0) {
+    tm.mark(AUGTREE_KID_PREPROCESS);
+    e = launch_preprocess_tiled(p, false, or_, dor, lse_r, delta_r, aug_r, s);
+  }
+  if (e == cudaSuccess && p->total_prompt > 0) {
+    tm.mark(AUGTREE_KID_PREPROCESS);
+    e = launch_preprocess_tiled(p, true, op, dop, lse_p, delta_p, aug_p, s);
+  }
+  if (e == cudaSuccess && p->n_items[AUGTREE_OP_TREE_BWD] > 0) {
+    tm.mark(AUGTREE_KID_BWD_KEY_SIDE);
+    e = tc_bwd_kv(p, AUGTREE_OP_TREE_BWD, qr, dor, aug_r, qp, dop, aug_p, kp, vp, kr, vr, dkr, dvr, dkp, dvp,
+                  dk_part, dv_part, nullptr, nullptr, nullptr, nullptr, (float*)(base + w.r.slots_off), s);
+  }
+  if (e == cudaSuccess && p->part_rows > 0) {
+    tm.mark(AUGTREE_KID_SPLIT_REDUCE);
+    e = launch_split_reduce_final(p, dk_part, dv_part, dkp, dvp, s);
+  }
+  if (e == cudaSuccess && p->total_prompt > 0) {
+    tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
+    e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta_p, dop, dqp, s);
+  }
+  if (e == cudaSuccess && p->total_resp > 0) {
+    tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
+    e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta_r, dor, dqr, s);
+  }
+  tm.finish();
+  return from_cuda(e);
+}
+
 augtree_status augtree_plan_set_timing(augtree_plan* p, int32_t enable) {
   if (!p) return AUGTREE_ERR_INVALID_ARG;
   augtree_status st = check_device(p);
   if (st != AUGTREE_OK) return st;
   if (enable && !p->timing.created) {
-    for (int op = 0; op < 4; ++op)
+    for (int op = 0; op < kNumOps; ++op)
       for (int c = 0; c < AUGTREE_TIMING_RING; ++c)
         for (int k = 0; k < augtree_plan::kTimingMarks; ++k)
           if (cudaEventCreate(&p->timing.ev[op][c][k]) != cudaSuccess) return AUGTREE_ERR_CUDA;
@@ -719,7 +816,7 @@ augtree_status augtree_plan_set_timing(augtree_plan* p, int32_t enable) {
 
 augtree_status augtree_plan_kernel_times(const augtree_plan* p, int32_t op, int32_t back, int32_t* kind, float* ms,
                                          int32_t cap, int32_t* n) {
-  if (!p || !n || op < 0 || op > 3 || back < 0 || back >= AUGTREE_TIMING_RING || cap < 0) return AUGTREE_ERR_INVALID_ARG;
+  if (!p || !n || op < 0 || op >= kNumOps || back < 0 || back >= AUGTREE_TIMING_RING || cap < 0) return AUGTREE_ERR_INVALID_ARG;
   const auto& T = p->timing;
   if (!T.on || T.calls[op] <= (uint32_t)back) return AUGTREE_ERR_INVALID_ARG;
   if (cap > 0 && (!kind || !ms)) return AUGTREE_ERR_INVALID_ARG;

@@ -11,7 +11,8 @@
 
 namespace augtree {
 
-enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3, K_PREFILL_KV = 4 };
+enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3, K_PREFILL_KV = 4, K_TREE_PROMPT_KV = 5 };
+constexpr int kNumOps = 5;  // queues per plan: the four calls' ops and the fused backward
 constexpr int kMaxSplit = 64;
 
 // Per-group geometry on the device: first prompt row, prompt length, first response
@@ -50,33 +51,33 @@ struct augtree_plan {
   int device;
   int family;  // AUGTREE_KERNEL_SIMT or AUGTREE_KERNEL_TC
   int32_t n_groups, n_branches, total_prompt, total_resp;
-  int32_t bm[4], bn[4];
+  int32_t bm[augtree::kNumOps], bn[augtree::kNumOps];
   std::vector<augtree::GroupInfo> groups_h;
   std::vector<augtree::SplitInfo> splits_h;
   int64_t part_rows;  // rows of split partials (per dK and per dV), over all groups
-  std::vector<int32_t> queue_h[4];
-  size_t n_items[4];
+  std::vector<int32_t> queue_h[augtree::kNumOps];
+  size_t n_items[augtree::kNumOps];
   // device copies
   augtree::GroupInfo* groups_d;
   int32_t* row_bstart_d;
   int32_t* row_bend_d;  // [total_resp] one past the last response row of each row's branch
   augtree::SplitInfo* splits_d;
-  int32_t* queue_d[4];
-  int paired[4];      // forward tensor-core units take two items (two heads of one KV head)
-  int quad[4];        // forward units of four items (four heads of one KV head) for SM pairs
+  int32_t* queue_d[augtree::kNumOps];
+  int paired[augtree::kNumOps];      // forward tensor-core units take two items (two heads of one KV head)
+  int quad[augtree::kNumOps];        // forward units of four items (four heads of one KV head) for SM pairs
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
   // Opt-in per-kernel timing: a ring of AUGTREE_TIMING_RING calls per op, each with up
   // to kTimingMarks events (before each kernel, after the last).  Written by the compute
   // calls, which take the plan as const.
-  static constexpr int kTimingMarks = 6;
+  static constexpr int kTimingMarks = 8;
   struct Timing {
     bool on = false;
     bool created = false;
-    cudaEvent_t ev[4][AUGTREE_TIMING_RING][kTimingMarks];
-    int32_t kind[4][AUGTREE_TIMING_RING][kTimingMarks];
-    int32_t n_marks[4][AUGTREE_TIMING_RING] = {};
-    uint32_t calls[4] = {0, 0, 0, 0};
+    cudaEvent_t ev[augtree::kNumOps][AUGTREE_TIMING_RING][kTimingMarks];
+    int32_t kind[augtree::kNumOps][AUGTREE_TIMING_RING][kTimingMarks];
+    int32_t n_marks[augtree::kNumOps][AUGTREE_TIMING_RING] = {};
+    uint32_t calls[augtree::kNumOps] = {};
   };
   mutable Timing timing;
 };
@@ -98,6 +99,13 @@ constexpr int kFlushSlots = 256;
 constexpr size_t kFlushSlotBytes = (size_t)128 * 256 * 4;
 BwdWorkspace replay_bwd_ws(const augtree_plan* p);
 BwdWorkspace prefill_bwd_ws(const augtree_plan* p);
+// Fused backward: the replay layout (with the flush slots), then the prefill layout up
+// to its slots, then (SIMT family only) the fp32 prompt-gradient sums.
+struct TreeWorkspace {
+  BwdWorkspace r, p;
+  size_t p_off, sum_off, sum_bytes, total;
+};
+TreeWorkspace tree_bwd_ws(const augtree_plan* p);
 
 Geometry geometry(const augtree_plan* p);
 
@@ -138,10 +146,15 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
                    const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);
 // Backward, key side (dK, dV; prompt dK/dV summed over the branches, split-K partials
 // reduced afterwards) and query side (dQ, written once per query tile and head).
-cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                      const void* vr, const void* aug, const void* dO, void* dk_out, void* dv_out, float* dk_part,
-                      float* dv_part, float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add,
-                      float* slots, cudaStream_t st);
+// Key side of the tensor-core backward.  Primary query rows q / dO / aug: the prompt for
+// prefill_bwd, the responses otherwise; secondary rows q2 / dO2 / aug2: the prompt rows
+// of the fused backward (nullable elsewhere).  dk2_out / dv2_out: the fused backward's
+// bf16 prompt gradient of unsplit groups.
+cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* dO, const void* aug, const void* q2,
+                      const void* dO2, const void* aug2, const void* kp, const void* vp, const void* kr, const void* vr,
+                      void* dk_out, void* dv_out, void* dk2_out, void* dv2_out, float* dk_part, float* dv_part,
+                      float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add, float* slots,
+                      cudaStream_t st);
 cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
                       const void* vr, const float* stats, const void* dO, void* dq, cudaStream_t st);
 
@@ -156,6 +169,9 @@ cudaError_t launch_preprocess_tiled(const augtree_plan* p, bool prompt_side, con
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int dtype, int64_t n, cudaStream_t st);
 cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, const float* dv_part,
                                 float* dk_sum, float* dv_sum, cudaStream_t st);
+// Fused backward: bf16 prompt dK/dV of the split groups from their partials, in split order.
+cudaError_t launch_split_reduce_final(const augtree_plan* p, const float* dk_part, const float* dv_part, void* dkp,
+                                      void* dvp, cudaStream_t st);
 cudaError_t launch_lse_merge(int64_t rows, int h, int d, const float* oa, const float* la,
                              const float* ob, const float* lb, float* o, float* l, cudaStream_t st);
 cudaError_t launch_lse_merge_bwd(int64_t rows, int h, int d, const float* oa, const float* la, const float* ob,

@@ -136,10 +136,12 @@ __device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
 __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2, Geometry geo,
+    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2,
+    const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_do2, Geometry geo,
     const int32_t* __restrict__ queue, const int32_t* __restrict__ row_bend, int bm, int bn,
-    const uint8_t* __restrict__ aug, int ntiles, __nv_bfloat16* __restrict__ dk_out,
-    __nv_bfloat16* __restrict__ dv_out, float* __restrict__ dk_part, float* __restrict__ dv_part,
+    const uint8_t* __restrict__ aug, int ntiles, const uint8_t* __restrict__ aug2, int ntiles2,
+    __nv_bfloat16* __restrict__ dk_out, __nv_bfloat16* __restrict__ dv_out, __nv_bfloat16* __restrict__ dk2_out,
+    __nv_bfloat16* __restrict__ dv2_out, float* __restrict__ dk_part, float* __restrict__ dv_part,
     float* __restrict__ dk_sum, float* __restrict__ dv_sum, const float* __restrict__ dk_add,
     const float* __restrict__ dv_add, float* __restrict__ slots, int n_slots, uint32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
@@ -153,23 +155,43 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   const int kvh = it.head;
   const bool resp_keys = it.kind == K_RESP_KV;
   const bool prefill = it.kind == K_PREFILL_KV;
+  const bool tree_p = it.kind == K_TREE_PROMPT_KV;
   const int64_t kbase = resp_keys ? G.r0 : G.p0;
   const int64_t key0 = kbase + (int64_t)it.tile * bn;
   const int64_t key_end = min(key0 + (int64_t)bn, kbase + (int64_t)(resp_keys ? G.lr : G.lp));
+  // Primary query tiles [a, b): prompt rows for PREFILL_KV, response rows otherwise.
   const int64_t qbase = prefill ? G.p0 : G.r0;
   const int64_t q_end = qbase + (prefill ? G.lp : G.lr);
   const int nqt = it.b - it.a;
-  const int n_iter = nqt * r;
+  // Secondary query tiles (fused backward, split 0 only): the prompt's own causal query
+  // tiles [qa2, qb2) of this prompt KV tile, read through tm_q2 / tm_do2 / aug2.
+  const int qb2 = (int)((G.lp + bm - 1) / bm);
+  const int qa2 = (int)(((int64_t)it.tile * bn) / bm);
+  const int nqt2 = (tree_p && it.split == 0) ? qb2 - qa2 : 0;
+  const int nph = nqt + nqt2;  // query tiles per query head
+  const int n_iter = nph * r;
   // One block per SM at a time (shared memory and TMEM), so the SM id names a private
   // flush slot.
   uint32_t smid;
   asm("mov.u32 %0, %%smid;" : "=r"(smid));
   const bool flush_on = n_iter > kFlush && (int)smid < n_slots;
   if (n_iter > kFlush && (int)smid >= n_slots && threadIdx.x == 0) atomicOr(err, 2u);
-  // Iteration i: query head kvh*r + i / nqt, query tile b - 1 - i % nqt.  Tiles are
-  // walked from the last one down, so blocks that start together (largest first) and
-  // share a KV head meet the same query rows at about the same time: their Q/dO reads
-  // then hit the same L2 lines.
+  // Iteration i: query head kvh*r + i / nph; within a head the primary tiles b - 1 down
+  // to a, then the secondary tiles qb2 - 1 down to qa2.  Tiles are walked from the last
+  // one down, so blocks that start together (largest first) and share a KV head meet the
+  // same query rows at about the same time: their Q/dO reads then hit the same L2 lines.
+  struct QTile {
+    int h, qt;
+    bool sec;
+  };
+  auto qtile = [&](int i) {
+    QTile t;
+    const int l = i % nph;
+    t.h = kvh * r + i / nph;
+    t.sec = l >= nqt;
+    t.qt = t.sec ? qb2 - 1 - (l - nqt) : it.b - 1 - l;
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -204,6 +226,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   if (warp == PRODUCER_WARP && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_do);
+    if (nqt2 > 0) {
+      prefetch_tmap(&tm_q2);
+      prefetch_tmap(&tm_do2);
+    }
     prefetch_tmap(resp_keys ? &tm_k2 : &tm_k);
     prefetch_tmap(resp_keys ? &tm_v2 : &tm_v);
   }
@@ -223,38 +249,41 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       }
       const int tile_base = prefill ? G.tp0 : G.tr0;
       // The {-lse/s, -Delta} rows of query tile qt are those of 128-row statistics tile
-      // qt * BMQ / 128 (one half of them for 64-row tiles).
-      auto aug_src = [&](int h, int qt) {
+      // qt * BMQ / 128 (one half of them for 64-row tiles); secondary tiles are prompt rows.
+      auto aug_src = [&](const QTile& t) {
         constexpr int per = kStatRows / BMQ;
-        return aug + ((int64_t)h * ntiles + tile_base + qt / per) * kAugTileBytes + (qt % per) * AUG_ROWS;
+        const uint8_t* a = t.sec ? aug2 : aug;
+        const int64_t nt = t.sec ? ntiles2 : ntiles, tb = t.sec ? G.tp0 : tile_base;
+        return a + ((int64_t)t.h * nt + tb + t.qt / per) * kAugTileBytes + (t.qt % per) * AUG_ROWS;
       };
+      auto row_of = [&](const QTile& t) { return (t.sec ? (int64_t)G.p0 : qbase) + (int64_t)t.qt * bm; };
       int issued = 0;
       for (int i = 0; i < n_iter; ++i) {
         const int stage = i % NQ, use = i / NQ;
         if (!mbar_wait(&bars->q_empty[stage], (use & 1) ^ 1, err)) break;
-        const int h = kvh * r + i / nqt;
-        const int qt = it.b - 1 - i % nqt;
-        const int64_t row0 = qbase + (int64_t)qt * bm;
+        const QTile t = qtile(i);
+        const int64_t row0 = row_of(t);
+        const CUtensorMap* qm = t.sec ? &tm_q2 : &tm_q;
+        const CUtensorMap* om = t.sec ? &tm_do2 : &tm_do;
         mbar_expect_tx(&bars->q_full[stage], 4 * QBLK + 2 * AUG_ROWS);
         for (int kb = 0; kb < 2; ++kb) {
-          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * QBLK, &tm_q, &bars->q_full[stage], kb * 64, h, (int)row0);
-          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * QBLK, &tm_do, &bars->q_full[stage], kb * 64, h, (int)row0);
+          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * QBLK, qm, &bars->q_full[stage], kb * 64, t.h, (int)row0);
+          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * QBLK, om, &bars->q_full[stage], kb * 64, t.h, (int)row0);
         }
-        const uint8_t* src = aug_src(h, qt);
+        const uint8_t* src = aug_src(t);
         bulk_load(smem + AUG_OFF + stage * AUG_STAGE, src, AUG_ROWS, &bars->q_full[stage]);
         bulk_load(smem + AUG_OFF + stage * AUG_STAGE + AUG_ROWS, src + kStatRows * 16, AUG_ROWS, &bars->q_full[stage]);
         issued = i + 1;
         // Warm L2 with the tiles a few iterations ahead.
         const int ip = i + kPrefetch;
         if (ip < n_iter) {
-          const int hp = kvh * r + ip / nqt;
-          const int qp = it.b - 1 - ip % nqt;
-          const int rp = (int)(qbase + (int64_t)qp * bm);
+          const QTile tp = qtile(ip);
+          const int rp = (int)row_of(tp);
           for (int kb = 0; kb < 2; ++kb) {
-            tma_prefetch_3d(&tm_q, kb * 64, hp, rp);
-            tma_prefetch_3d(&tm_do, kb * 64, hp, rp);
+            tma_prefetch_3d(tp.sec ? &tm_q2 : &tm_q, kb * 64, tp.h, rp);
+            tma_prefetch_3d(tp.sec ? &tm_do2 : &tm_do, kb * 64, tp.h, rp);
           }
-          const uint8_t* ap = aug_src(hp, qp);
+          const uint8_t* ap = aug_src(tp);
           bulk_prefetch(ap, AUG_ROWS);
           bulk_prefetch(ap + kStatRows * 16, AUG_ROWS);
         }
@@ -385,6 +414,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       q_hi = be < q_end ? be : q_end;
     }
     if (!key_ok) q_hi = q_lo;
+    // Secondary (prompt) query tiles of a fused item: causal over the prompt.
+    const int64_t q_lo2 = key, q_hi2 = key_ok ? (int64_t)G.p0 + G.lp : key;
     const float sl2 = geo.scale_log2;
     // This warpgroup's share of the key's {dK, dV} row (256 floats): [po, po + 256 / NWG).
     constexpr int SHARE = 256 / NWG;
@@ -392,7 +423,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     const uint32_t acc_col = (po < 128 ? T_DK : T_DV) + (po & 127);
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
-      const int64_t row0 = qbase + (int64_t)(it.b - 1 - i % nqt) * bm;
+      const int l = i % nph;
+      const bool sec = l >= nqt;
+      const int64_t row0 = sec ? (int64_t)G.p0 + (int64_t)(qb2 - 1 - (l - nqt)) * bm : qbase + (int64_t)(it.b - 1 - l) * bm;
+      const int64_t v_lo = sec ? q_lo2 : q_lo, v_hi = sec ? q_hi2 : q_hi;
       const int b = kv_buf(i);
       const uint32_t ts = tmem + lane_off + T_ST + b * 64 + c0, tdp = tmem + lane_off + T_DPT + b * 64 + c0;
       if (!(ok = mbar_wait(&bars->s_full[b], kv_phase(i), err))) break;
@@ -402,7 +436,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       for (int k = 0; k < COLS / 32; ++k) tmem_ld32(ts + 32 * k, sraw[k]);
       tmem_ld_wait();
       // this warpgroup's valid columns: [lo, hi) relative to c0
-      const int64_t lo64 = q_lo - row0 - c0, hi64 = q_hi - row0 - c0;
+      const int64_t lo64 = v_lo - row0 - c0, hi64 = v_hi - row0 - c0;
       const int lo = lo64 < 0 ? 0 : (lo64 > COLS ? COLS : (int)lo64);
       const int hi = hi64 < 0 ? 0 : (hi64 > COLS ? COLS : (int)hi64);
       // P^T as bf16 pairs (A operand of dV and the P factor of dS): the accumulator
@@ -488,18 +522,25 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       const int64_t off = (key * geo.hkv + kvh) * 128 + col0;
       float* fdst = nullptr;
       int64_t foff = off;
-      if (it.kind == K_PROMPT_KV) {
+      __nv_bfloat16* bdst = is_dk ? dk_out : dv_out;
+      const float* add = is_dk ? dk_add : dv_add;
+      if (it.kind == K_PROMPT_KV || tree_p) {
+        // Split groups write fp32 partials (reduced in split order afterwards); an unsplit
+        // group writes the replay sum (PROMPT_KV) or, in the fused backward, the final
+        // prompt gradient.
         const SplitInfo s = geo.splits[it.group];
-        fdst = is_dk ? dk_sum : dv_sum;
         if (s.nsplit > 1) {
           fdst = is_dk ? dk_part : dv_part;
           foff = ((s.part_row0 + (int64_t)it.split * G.lp + (key - G.p0)) * geo.hkv + kvh) * 128 + col0;
+        } else if (!tree_p) {
+          fdst = is_dk ? dk_sum : dv_sum;
+        } else {
+          bdst = is_dk ? dk2_out : dv2_out;
+          add = nullptr;
         }
       }
       const float mul = is_dk ? geo.scale : 1.f;
       const float* slot = slots + ((int64_t)smid * 128 + t) * 256 + po;
-      __nv_bfloat16* bdst = is_dk ? dk_out : dv_out;
-      const float* add = is_dk ? dk_add : dv_add;
 #pragma unroll 1
       for (int c = 0; c < SHARE / 32; ++c) {
         uint32_t v[32];
@@ -547,17 +588,39 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
 
 }  // namespace
 
-cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                      const void* vr, const void* aug, const void* dO, void* dk_out, void* dv_out, float* dk_part,
-                      float* dv_part, float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add,
-                      float* slots, cudaStream_t st) {
+cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* dO, const void* aug, const void* q2,
+                      const void* dO2, const void* aug2, const void* kp, const void* vp, const void* kr, const void* vr,
+                      void* dk_out, void* dv_out, void* dk2_out, void* dv2_out, float* dk_part, float* dv_part,
+                      float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add, float* slots,
+                      cudaStream_t st) {
+  // Primary query rows: the prompt for prefill_bwd, the responses otherwise; secondary
+  // query rows (the fused backward's prompt rows) come through q2 / dO2 / aug2.
   const bool prefill = op == AUGTREE_OP_PREFILL_BWD;
+  const bool tree = op == AUGTREE_OP_TREE_BWD;
   if (p->n_items[op] == 0) return cudaSuccess;
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
-  CUtensorMap mq, mdo, mk, mv, mk2, mv2;
+  CUtensorMap mq, mdo, mq2, mdo2, mk, mv, mk2, mv2;
   if (p->bm[op] != BMQ || p->bn[op] != 128) return cudaErrorInvalidValue;
-  if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
-  if (!encode_rows_map(&mdo, dO, q_rows, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
+  const bool have_q = q_rows > 0 && q && dO;
+  const bool have_q2 = tree && p->total_prompt > 0 && q2 && dO2;
+  if (have_q) {
+    if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
+    if (!encode_rows_map(&mdo, dO, q_rows, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
+  }
+  if (have_q2) {
+    if (!encode_rows_map(&mq2, q2, p->total_prompt, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
+    if (!encode_rows_map(&mdo2, dO2, p->total_prompt, p->cfg.hq, BMQ)) return cudaErrorInvalidValue;
+  }
+  if (!have_q && !have_q2) return cudaErrorInvalidValue;
+  // Maps that the queue never reads alias a used one.
+  if (!have_q) {
+    mq = mq2;
+    mdo = mdo2;
+  }
+  if (!have_q2) {
+    mq2 = mq;
+    mdo2 = mdo;
+  }
   const bool have_p = p->total_prompt > 0 && kp && vp;
   const bool have_r = !prefill && p->total_resp > 0 && kr && vr;
   if (have_p) {
@@ -579,9 +642,10 @@ cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* 
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
   if (e != cudaSuccess) return e;
   tc_bwd_kv_kernel<<<(unsigned)p->n_items[op], KV_THREADS, KV_SMEM, st>>>(
-      mq, mdo, mk, mv, mk2, mv2, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op], (const uint8_t*)aug,
-      prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, dk_part, dv_part, dk_sum,
-      dv_sum, dk_add, dv_add, slots, kFlushSlots, p->err_d);
+      mq, mdo, mk, mv, mk2, mv2, mq2, mdo2, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op],
+      (const uint8_t*)aug, prefill ? p->ntiles_p : p->ntiles_r, (const uint8_t*)(aug2 ? aug2 : aug), p->ntiles_p,
+      (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, (__nv_bfloat16*)dk2_out, (__nv_bfloat16*)dv2_out, dk_part,
+      dv_part, dk_sum, dv_sum, dk_add, dv_add, slots, kFlushSlots, p->err_d);
   return cudaGetLastError();
 }
 

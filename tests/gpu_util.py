@@ -22,9 +22,10 @@ def host_inputs(w):
     return {n: W.tensor_rows_np(w, n) for n in W.TENSORS}
 
 
-def run_cuda(w, kernel=at.KERNEL_AUTO, device="cuda", num_sms=0, t=None, plan=None):
-    """Forward + backward of workload w through the C ABI.  Returns numpy float64
-    arrays keyed like the oracle's output."""
+def run_cuda(w, kernel=at.KERNEL_AUTO, device="cuda", num_sms=0, t=None, plan=None, fused=True):
+    """Forward + backward of workload w through the C ABI (fused: one augtree_tree_bwd
+    call; otherwise replay_bwd then prefill_bwd).  Returns numpy float64 arrays keyed
+    like the oracle's output."""
     dt = at.BF16 if w.dtype == "bf16" else at.FP32
     if plan is None:
         plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt, kernel=kernel, num_sms=num_sms)
@@ -32,8 +33,9 @@ def run_cuda(w, kernel=at.KERNEL_AUTO, device="cuda", num_sms=0, t=None, plan=No
         t = device_inputs(w, device)
     o_p, lse_p, o_r, lse_r = at.forward(plan, t["q_p"], t["k_p"], t["v_p"], t["q_r"], t["k_r"], t["v_r"])
     g = at.backward(plan, t["q_p"], t["k_p"], t["v_p"], t["q_r"], t["k_r"], t["v_r"], o_p, lse_p, o_r, lse_r,
-                    t["do_p"], t["do_r"])
+                    t["do_p"], t["do_r"], fused=fused)
     torch.cuda.synchronize()
+    plan.check()
     out = {"o_p": o_p, "lse_p": lse_p, "o_r": o_r, "lse_r": lse_r}
     out.update(dict(zip(GRADS, g)))
     return {k: v.double().cpu().numpy() for k, v in out.items()}

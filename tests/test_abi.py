@@ -45,7 +45,7 @@ TREES = [
 def test_schedule_bit_exact_with_reference_builder(augtree_lib, ti, kernel, dtype, hq, hkv, sms):
     tree = TREES[ti]
     cfg = at.make_config(hq, hkv, 128, dtype, 0.0, sms, kernel)
-    for op in range(4):
+    for op in range(5):
         bm, bn = at.tile_sizes(cfg, op)
         got = at.schedule_build(tree.offsets(), cfg, op)
         want = S.build(tree.offsets(), hq, hkv, op, bm, bn, sms)
@@ -56,7 +56,7 @@ def test_schedule_bit_exact_on_the_benchmark_shapes(augtree_lib):
     for name in ("response_heavy", "mixed", "prompt_heavy"):
         w = W.workload(name)
         cfg = at.make_config(w.hq, w.hkv, w.d, at.BF16, 0.0, 152, at.KERNEL_TC)
-        for op in range(4):
+        for op in range(5):
             bm, bn = at.tile_sizes(cfg, op)
             got = at.schedule_build(w.tree.offsets(), cfg, op)
             want = S.build(w.tree.offsets(), w.hq, w.hkv, op, bm, bn, 152)
@@ -91,7 +91,8 @@ def test_host_validation_errors(augtree_lib):
     assert _status(good, at.make_config(4, 2, 128, at.BF16, -1.0, 8))[0] == at.ERR_INVALID_ARG
     assert _status(good, at.make_config(4, 2, 128, at.BF16, 0.0, 0))[0] == at.ERR_INVALID_ARG  # host build needs SMs
     assert _status(good, at.make_config(4, 2, 128, at.BF16, 0.0, 8, 9))[0] == at.ERR_INVALID_ARG
-    assert _status(good, cfg, op=4)[0] == at.ERR_INVALID_ARG
+    assert _status(good, cfg, op=at.OP_TREE_BWD)[0] == at.OK
+    assert _status(good, cfg, op=5)[0] == at.ERR_INVALID_ARG
     # capacity
     st, n = _status(good, cfg, cap=1)
     assert st == at.ERR_CAPACITY and n > 1
@@ -106,7 +107,7 @@ def test_host_validation_errors(augtree_lib):
 def test_empty_structures_build_empty_queues(augtree_lib):
     cfg = at.make_config(2, 1, 64, at.FP32, 0.0, 4)
     for tree in (W.Tree([0], [[0]]), W.Tree([], []), W.Tree([3], [[]])):
-        for op in range(4):
+        for op in range(5):
             q = at.schedule_build(tree.offsets(), cfg, op)
             want = S.build(tree.offsets(), 2, 1, op, 64, 64, 4)
             assert np.array_equal(q, want)

@@ -159,13 +159,72 @@ def test_backward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv, sms):
             assert lst[-1][2] == -(-groups[g]["lr"] // bm)
 
 
+@pytest.mark.parametrize("ti", range(len(TREES)))
+@pytest.mark.parametrize("bm,bn", TILES)
+@pytest.mark.parametrize("hq,hkv,sms", [(4, 2, 1), (4, 2, 64), (2, 2, 2), (8, 1, 1)])
+def test_fused_backward_queue_covers_every_pair_once(ti, bm, bn, hq, hkv, sms):
+    """The fused backward's queue (all of the backward in one call) covers the pairs of
+    both backward queues: prompt->prompt, response->prompt and response->response, each
+    exactly once per query head; a prompt KV tile's split 0 carries its prompt rows."""
+    tree = TREES[ti]
+    groups = valid_pairs(tree)
+    offs = tree.offsets()
+    r = hq // hkv
+    q = S.build(offs, hq, hkv, S.OP_TREE_BWD, bm, bn, num_sms=sms)
+    check_order(q)
+    rb = S.build(offs, hq, hkv, S.OP_REPLAY_BWD, bm, bn, num_sms=sms)
+    nsplit = {}
+    for it in rb:
+        if it[0] == S.PROMPT_KV:
+            nsplit[int(it[1])] = max(nsplit.get(int(it[1]), 0), int(it[4]) + 1)
+    covered = set()
+    for it in q:
+        kind, g, tile, hk, split, cost, a, b = map(int, it)
+        grp = groups[g]
+        assert kind in (S.TREE_PROMPT_KV, S.RESP_KV)
+        ranges = []
+        if kind == S.TREE_PROMPT_KV:
+            k0, klen = grp["p0"], grp["lp"]
+            assert split < max(1, nsplit.get(g, 1))  # the replay backward's split rule
+            ranges.append((grp["r0"], grp["r0"] + grp["lr"], a, b, grp["rp"], "rp"))
+            own = 0
+            if split == 0:
+                qa2, qb2 = (tile * bn) // bm, -(-grp["lp"] // bm)
+                own = qb2 - qa2
+                ranges.append((grp["p0"], grp["p0"] + grp["lp"], qa2, qb2, grp["pp"], "pp"))
+            assert cost == (b - a + own) * r and cost > 0
+        else:
+            assert split == 0 and cost == (b - a) * r
+            k0, klen = grp["r0"], grp["lr"]
+            ranges.append((grp["r0"], grp["r0"] + grp["lr"], a, b, grp["rr"], "rr"))
+        keys = range(k0 + tile * bn, min(k0 + (tile + 1) * bn, k0 + klen))
+        assert len(keys) > 0
+        for rows0, rows1, qa, qb, pairs, side in ranges:
+            for qt in range(qa, qb):
+                rows = range(rows0 + qt * bm, min(rows0 + (qt + 1) * bm, rows1))
+                hit = 0
+                for row in rows:
+                    for key in keys:
+                        if (row, key) in pairs:
+                            for h in range(hk * r, (hk + 1) * r):
+                                assert (side, row, key, h) not in covered
+                                covered.add((side, row, key, h))
+                            hit += 1
+                assert hit > 0, "empty query tile in an item"
+    for grp in groups:
+        for side in ("pp", "rp", "rr"):
+            for (row, key) in grp[side]:
+                for h in range(hq):
+                    assert (side, row, key, h) in covered
+
+
 def test_lpt_order_meets_the_list_scheduling_bound():
     """Items are taken largest first (Sec. 3.4).  Any list schedule on m lanes has
     makespan <= total/m + largest item; LPT order must also be non-increasing."""
     import heapq
     tree = W.Tree([300, 20], [[37, 200, 5, 90], [400, 3]])
     offs = tree.offsets()
-    for op in (S.OP_PREFILL_FWD, S.OP_REPLAY_FWD, S.OP_REPLAY_BWD, S.OP_PREFILL_BWD):
+    for op in (S.OP_PREFILL_FWD, S.OP_REPLAY_FWD, S.OP_REPLAY_BWD, S.OP_PREFILL_BWD, S.OP_TREE_BWD):
         q = S.build(offs, 4, 2, op, 16, 16, num_sms=4)
         costs = [int(c) for c in q[:, 5]]
         assert costs == sorted(costs, reverse=True)
