@@ -23,6 +23,12 @@ namespace tc {
 #define AUGTREE_FWD_FMA_STRIDE 16
 #endif
 constexpr int kFwdFmaStride = AUGTREE_FWD_FMA_STRIDE;
+#ifndef AUGTREE_FWD_FMA_OFFSET
+#define AUGTREE_FWD_FMA_OFFSET (AUGTREE_FWD_FMA_STRIDE - 1)
+#endif
+// Which pair of each stride: measured (stride 16) offset 15: 1,293-1,300 TFLOP/s,
+// offsets 7 and 0: 1,277; stride 32 offset 31: 1,293 (prompt-heavy forward, one box).
+constexpr int kFwdFmaOffset = AUGTREE_FWD_FMA_OFFSET;
 
 // Where the row's keys come from in KV tile j: prompt tiles first, then the own-branch
 // tiles, and the valid columns [lo, hi] of the row in that tile.
@@ -138,7 +144,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
         const float a0 = fmaf(__uint_as_float(AUGTREE_X(c0)), sl2, -mu);
         const float a1 = fmaf(__uint_as_float(AUGTREE_X(c0 + 1)), sl2, -mu);
         float p0 = fast_exp2(a0), p1;
-        if (kFwdFmaStride > 0 && c == 1 && i % kFwdFmaStride == kFwdFmaStride - 1) {
+        if (kFwdFmaStride > 0 && c == 1 && i % kFwdFmaStride == kFwdFmaOffset) {
           // FMA-pipe exponential (second half of the row, where half of S has already
           // been consumed and registers are free); a masked column (-inf) must stay
           // exactly zero.
