@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # one-pass ncu capture of dram__bytes_read.sum + dram__bytes_write.sum averaged over
 # the kernel's launches in one step (the summary under profiles/ gives the command).
 # Valid for the kernel versions it was taken on; absent entries report null.
-TRAFFIC_PER_LAUNCH = {("prompt_heavy", "bwd_key_side"): 14.05e9}
+TRAFFIC_PER_LAUNCH = {("prompt_heavy", "bwd_key_side"): 32.71e9}
 
 
 def peaks():

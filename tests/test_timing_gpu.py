@@ -24,7 +24,7 @@ def test_kernel_times_cover_each_call(cuda_device):
     o_p, lse_p, o_r, lse_r = at.forward(plan, t["q_p"], t["k_p"], t["v_p"], t["q_r"], t["k_r"], t["v_r"])
     ev[1].record(stream)
     at.backward(plan, t["q_p"], t["k_p"], t["v_p"], t["q_r"], t["k_r"], t["v_r"], o_p, lse_p, o_r, lse_r,
-                t["do_p"], t["do_r"])
+                t["do_p"], t["do_r"], fused=False)
     ev[2].record(stream)
     torch.cuda.synchronize()
     plan.check()
@@ -40,4 +40,30 @@ def test_kernel_times_cover_each_call(cuda_device):
         assert 0.0 < part <= whole * 1.02 + 0.02, (part, whole)
     with pytest.raises(at.AugtreeError):
         plan.kernel_times(at.OP_REPLAY_BWD, back=1)  # only one timed call so far
+    plan.set_timing(False)
+
+
+def test_kernel_times_of_the_fused_backward(cuda_device):
+    w = W.custom(W.Tree([700, 300], [[200, 90, 40], [513]]), hq=8, hkv=2, d=128, dtype="bf16", seed=29)
+    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=at.BF16)
+    t = device_inputs(w, cuda_device)
+    o_p, lse_p, o_r, lse_r = at.forward(plan, t["q_p"], t["k_p"], t["v_p"], t["q_r"], t["k_r"], t["v_r"])
+    plan.set_timing(True)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    at.backward(plan, t["q_p"], t["k_p"], t["v_p"], t["q_r"], t["k_r"], t["v_r"], o_p, lse_p, o_r, lse_r,
+                t["do_p"], t["do_r"], fused=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    plan.check()
+    tb = plan.kernel_times(at.OP_TREE_BWD)
+    split = bool((plan.schedule(at.OP_TREE_BWD)[:, 4] > 0).any())
+    want = ["preprocess", "preprocess", "bwd_key_side"] + (["split_reduce"] if split else []) + \
+        ["bwd_query_side", "bwd_query_side"]
+    assert [k for k, _ in tb] == want
+    part = sum(m for _, m in tb)
+    assert 0.0 < part <= e0.elapsed_time(e1) * 1.02 + 0.02
+    with pytest.raises(at.AugtreeError):
+        plan.kernel_times(at.OP_REPLAY_BWD)  # the fused call makes no replay_bwd call
     plan.set_timing(False)
