@@ -167,6 +167,33 @@ def time_oracle(w, min_seconds=10.0, max_reps=50):
     return rate, desc, el / reps
 
 
+def cpu_model():
+    """The host CPU's model string (x86 'model name', else the Arm implementer/part)."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+        for key in ("model name", "Model"):
+            for line in info:
+                if line.startswith(key) and ":" in line:
+                    return line.split(":", 1)[1].strip()
+        impl = next((l.split(":", 1)[1].strip() for l in info if l.startswith("CPU implementer")), None)
+        part = next((l.split(":", 1)[1].strip() for l in info if l.startswith("CPU part")), None)
+        if impl or part:
+            return f"{platform.machine()} implementer {impl} part {part}"
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def oracle_fields(rate, desc, w):
+    """cpu_baseline object: the oracle's rate on its sample, the host, and the full
+    workload's step time at that rate (an extrapolation, labelled so)."""
+    return {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads_used(), "kind": "oracle",
+            "sample": desc, "cpu_model": cpu_model(),
+            "full_step_s_extrapolated": round(useful_flops(w) / (rate * 1e12), 1) if rate > 0 else None}
+
+
 def threads_used():
     try:
         from threadpoolctl import threadpool_info
@@ -278,6 +305,8 @@ def run_ours(args):
     per_call = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(n_ev - 1)]
                          for k in range(args.steps)]).mean(0)
     ms_step = ms / args.steps
+    # Median over the timed steps of one step's duration (first to last call event).
+    ms_median = float(np.median([evs[k][0].elapsed_time(evs[k][n_ev - 1]) for k in range(args.steps)]))
 
     # e2e through the public API with host buffers: H2D of the step's inputs from
     # pinned memory, the step, D2H of its results (outputs and all gradients).
@@ -348,6 +377,7 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
+        "median_ms_per_step": round(ms_median, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -387,8 +417,7 @@ def run_ours(args):
             "tree_pairs": w.tree.pair_count(), "speedup_of_tree": round(ms_f / ms_step, 3)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, desc, per = time_oracle(w, min_seconds=args.cpu_seconds)
-        result["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads_used(),
-                                  "kind": "oracle", "sample": desc}
+        result["cpu_baseline"] = oracle_fields(rate, desc, w)
     if rank == 0:
         print(json.dumps(result))
     if world > 1:
@@ -508,8 +537,7 @@ def run_reference(args):
            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
            "config": {"workload": w.name, "sample": desc},
-           "cpu_baseline": {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads_used(), "kind": "oracle",
-                            "sample": desc},
+           "cpu_baseline": oracle_fields(rate, desc, w),
            "e2e": {"value": round(rate, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res))
 
