@@ -40,7 +40,8 @@ namespace {
 using namespace tc;
 
 // All exponentials on the MUFU: moving one in eight to the FMA pipe measured 5 % slower
-// here (unlike the key side, this kernel's compute phase is issue-bound).
+// here, one in 32 or 64 about 1 % slower (unlike the key side, this kernel's compute
+// phase is issue-bound).
 #ifndef AUGTREE_DQ_EXP_FMA
 #define AUGTREE_DQ_EXP_FMA 0
 #endif
