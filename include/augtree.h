@@ -296,7 +296,10 @@ augtree_status augtree_plan_check(const augtree_plan* plan, void* stream);
  * Off by default.  When enabled, every compute call of the plan records CUDA events on
  * its stream before each kernel it launches and after the last one, in a ring that
  * keeps the last AUGTREE_TIMING_RING calls of each op.  The cost is a few event
- * records per call; nothing else changes.  Kernel kinds (augtree_plan_kernel_times): */
+ * records per call; nothing else changes.  A call launches at most seven kernels
+ * (augtree_tree_bwd); with the SIMT family, augtree_tree_bwd records its two internal
+ * calls under AUGTREE_OP_REPLAY_BWD and AUGTREE_OP_PREFILL_BWD.  Kernel kinds
+ * (augtree_plan_kernel_times): */
 typedef enum {
   AUGTREE_KID_FWD_TC = 1,        /* tensor-core forward (prefill or replay)             */
   AUGTREE_KID_FWD_SIMT = 2,      /* SIMT forward                                        */

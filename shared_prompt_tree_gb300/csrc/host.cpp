@@ -335,7 +335,7 @@ const char* augtree_status_string(augtree_status s) {
   return "unknown status";
 }
 
-int32_t augtree_version(void) { return 100; }
+int32_t augtree_version(void) { return 200; }  // 0.2.0: augtree_tree_bwd, augtree_assign_grid
 
 augtree_status augtree_tile_sizes(const augtree_config* cfg, int32_t op, int32_t* bm, int32_t* bn) {
   augtree_status st = validate_cfg(cfg, false);
