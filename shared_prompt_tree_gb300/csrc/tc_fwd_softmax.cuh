@@ -29,6 +29,13 @@ constexpr int kFwdFmaStride = AUGTREE_FWD_FMA_STRIDE;
 // Which pair of each stride: measured (stride 16) offset 15: 1,293-1,300 TFLOP/s,
 // offsets 7 and 0: 1,277; stride 32 offset 31: 1,293 (prompt-heavy forward, one box).
 constexpr int kFwdFmaOffset = AUGTREE_FWD_FMA_OFFSET;
+// Where the two heads' softmax hand off: 0 = around the exponential loop, 1 = the turn
+// passes after the first half of the loop, 2 = the wait also covers the row max.
+// Measured (prompt-heavy forward, one box): 1,327 / 1,317 / 1,288 TFLOP/s.
+#ifndef AUGTREE_FWD_TURN_POS
+#define AUGTREE_FWD_TURN_POS 0
+#endif
+constexpr int kFwdTurnPos = AUGTREE_FWD_TURN_POS;
 
 // Where the row's keys come from in KV tile j: prompt tiles first, then the own-branch
 // tiles, and the valid columns [lo, hi] of the row in that tile.
@@ -111,6 +118,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, raw[c]);
     tmem_ld_wait();
 #define AUGTREE_X(c) raw[(c) >> 5][(c) & 31]
+    if (kFwdTurnPos == 2 && !(ok = turn.wait(j, err))) break;
     int lo_i, hi_i;
     fwd_valid_cols(g, j, lo_i, hi_i);
     const bool masked = lo_i > 0 || hi_i < 127;
@@ -133,7 +141,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     const float alpha = need ? fast_exp2(m - m_new) : 1.f;
     m = m_new;
     const float mu = (m == -INFINITY) ? 0.f : m;
-    if (!(ok = turn.wait(j, err))) break;
+    if (kFwdTurnPos != 2 && !(ok = turn.wait(j, err))) break;
     float ps[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial sums
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -159,9 +167,10 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
         ps[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
       }
       tmem_st32(tS + c * 32, pk);
+      if (kFwdTurnPos == 1 && c == 0) turn.pass();
     }
 #undef AUGTREE_X
-    turn.pass();
+    if (kFwdTurnPos != 1) turn.pass();
     tmem_st_wait();
     const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
     l = l * alpha + psum;
