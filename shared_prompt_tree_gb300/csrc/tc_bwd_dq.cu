@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         for (int c = 0; c < 64; ++c) {
           const float x = fmaf(__uint_as_float(sv[c >> 5][c & 31]), sl2, -lse2);
           // One exponential in kDqExpFma on the FMA pipe.
-          const bool on_fma = kDqExpFma > 0 && c % kDqExpFma == kDqExpFma - 1;
+          const bool on_fma = kDqExpFma > 0 && c % (kDqExpFma > 0 ? kDqExpFma : 1) == kDqExpFma - 1;
           sv[c >> 5][c & 31] = __float_as_uint(on_fma ? exp2_fma(x) : fast_exp2(x));
         }
       } else {

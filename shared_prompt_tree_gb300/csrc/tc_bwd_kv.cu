@@ -448,8 +448,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
           const float e0 = fast_exp2(__uint_as_float(sraw[c >> 5][c & 31]) * sl2);
           const float x1 = __uint_as_float(sraw[(c + 1) >> 5][(c + 1) & 31]) * sl2;
           // One exponential in kKvExpFma on the FMA pipe: the MUFU sets this phase's pace.
-          const float e1 = (kKvExpFma > 0 && (c / 2) % (kKvExpFma / 2) == kKvExpFma / 2 - 1) ? exp2_fma(x1)
-                                                                                            : fast_exp2(x1);
+          constexpr int kPairs = kKvExpFma > 0 ? kKvExpFma / 2 : 1;  // FMA exponential every kPairs pairs
+          const float e1 = (kKvExpFma > 0 && (c / 2) % kPairs == kPairs - 1) ? exp2_fma(x1) : fast_exp2(x1);
           pk[c >> 1] = pack_bf16x2(e0, e1);
         }
       } else {

@@ -152,7 +152,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
         const float a0 = fmaf(__uint_as_float(AUGTREE_X(c0)), sl2, -mu);
         const float a1 = fmaf(__uint_as_float(AUGTREE_X(c0 + 1)), sl2, -mu);
         float p0 = fast_exp2(a0), p1;
-        if (kFwdFmaStride > 0 && c == 1 && i % kFwdFmaStride == kFwdFmaOffset) {
+        if (kFwdFmaStride > 0 && c == 1 && i % (kFwdFmaStride > 0 ? kFwdFmaStride : 1) == kFwdFmaOffset) {
           // FMA-pipe exponential (second half of the row, where half of S has already
           // been consumed and registers are free); a masked column (-inf) must stay
           // exactly zero.
