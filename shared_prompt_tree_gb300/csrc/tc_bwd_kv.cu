@@ -12,8 +12,10 @@
 //                    are reduced in a fixed order afterwards, no atomics).
 //
 // One thread block per work item: 128 keys of one KV head, query tiles [a, b) of BMQ
-// rows for each of the r query heads of that KV head.  Per query tile (keys are the
-// MMA M dimension, one key per TMEM lane):
+// rows for each of the r query heads of that KV head (in the fused backward, split 0
+// of a prompt KV tile also walks the prompt's own causal query tiles, so one
+// accumulator holds the prompt gradient's replay and prefill parts).  Per query tile
+// (keys are the MMA M dimension, one key per TMEM lane):
 //   S^T  = K Q^T - lse/s   (TMEM, fp32)  -> P^T  = exp2(s log2e S^T),   bf16 over S^T
 //   dP^T = V dO^T - Delta  (TMEM, fp32)  -> dS^T = P^T dP^T,            bf16 over dP^T
 //   dV  += P^T dO          (A = P^T from TMEM, B = dO read MN-major)

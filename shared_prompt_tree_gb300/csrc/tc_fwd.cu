@@ -21,7 +21,9 @@
 //               (TMEM lane i): masks, running max with lazy rescaling of O (only
 //               when the max grows by more than 2^8), P = exp2(...) as bf16 back
 //               into TMEM over S, the row sum l of those bf16 values, and the final
-//               O / l and lse.
+//               O / l and lse.  The two warpgroups' exponential loops alternate (an
+//               mbarrier hand-off), so one head's exponentials overlap the other
+//               head's MMAs.
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,384), O1 [384,512).
 #include <cuda.h>
 #include <cudaTypedefs.h>
