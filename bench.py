@@ -136,7 +136,7 @@ def replica_throughput(units_per_rank: float, ms_local: float, world: int, devic
 # ---------------------------------------------------------------------------------
 def oracle_sample(w):
     """A down-scaled sample with the same structure: the first group, prompt and
-    branch lengths scaled by 1/8, one KV head and its query heads... bounded to a few
+    branch lengths scaled by 1/16, one KV head and its query heads, bounded to a few
     seconds of fp64 work.  Returns (workload, description)."""
     import workloads as W
     lp = max(1, w.tree.prompt_lens[0] // 16)
