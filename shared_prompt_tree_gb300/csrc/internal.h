@@ -131,6 +131,10 @@ bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int he
 
 // ---- launchers (return cudaGetLastError() of their launches) ---------------------
 // Forward on SM pairs (2-CTA clusters): used when the queue groups into four-head units.
+// One query head per block, double-buffered S (tc_fwd1.cu).
+cudaError_t tc_fwd1(const augtree_plan* p, int op, const CUtensorMap& mq, const CUtensorMap& mkp,
+                    const CUtensorMap& mvp, const CUtensorMap& mkr, const CUtensorMap& mvr, void* o, float* lse,
+                    int64_t q_rows, cudaStream_t st);
 cudaError_t tc_fwd2(const augtree_plan* p, int op, const CUtensorMap& mq, const void* kp, const void* vp,
                     const void* kr, const void* vr, void* o, float* lse, int64_t q_rows, cudaStream_t st);
 // SIMT family (any dtype).

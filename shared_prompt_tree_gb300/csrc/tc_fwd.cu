@@ -44,6 +44,12 @@ using namespace tc;
 #define AUGTREE_FWD_PINGPONG 1
 #endif
 constexpr bool kFwdPingPong = AUGTREE_FWD_PINGPONG != 0;
+// One query head per block with a double-buffered S (tc_fwd1.cu) instead of two heads
+// per block.
+#ifndef AUGTREE_FWD_ONE_HEAD
+#define AUGTREE_FWD_ONE_HEAD 0
+#endif
+constexpr bool kOneHeadForward = AUGTREE_FWD_ONE_HEAD != 0;
 constexpr int FWD_THREADS = 352;  // 8 softmax warps, producer, one MMA issuer per head
 constexpr int NST = 2;                  // K/V ring stages
 constexpr int TILE_BYTES = 128 * 128;   // one 128-row x 64-column bf16 block = 16 KB
@@ -293,6 +299,7 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
     mkr = mkp;
     mvr = mvp;
   }
+  if (kOneHeadForward) return tc_fwd1(p, op, mq, mkp, mvp, mkr, mvr, o, lse, q_rows, st);
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;
   const int paired = p->paired[op];
