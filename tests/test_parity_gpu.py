@@ -162,3 +162,19 @@ def test_autograd_binding_matches_oracle(cuda_device):
     got.update({"d" + k: leaves[k].grad for k in leaves})
     got = {k: v.detach().double().cpu().numpy() for k, v in got.items()}
     compare(got, run_oracle(w), "fp32")
+
+
+def test_autograd_binding_tensor_cores_matches_oracle(cuda_device):
+    # The differentiable operator on the bf16 tensor-core kernels (its backward is one
+    # augtree_tree_bwd call).
+    w = W.custom(RAGGED[3], hq=8, hkv=2, d=128, dtype="bf16", seed=22)
+    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=at.BF16, kernel=at.KERNEL_TC)
+    t = device_inputs(w, cuda_device)
+    leaves = {k: t[k].clone().requires_grad_(True) for k in ("q_p", "k_p", "v_p", "q_r", "k_r", "v_r")}
+    o_p, o_r, lse_p, lse_r = at.tree_attention(plan, *(leaves[k] for k in ("q_p", "k_p", "v_p", "q_r", "k_r", "v_r")))
+    ((o_p.float() * t["do_p"].float()).sum() + (o_r.float() * t["do_r"].float()).sum()).backward()
+    plan.check()
+    got = {"o_p": o_p, "o_r": o_r, "lse_p": lse_p, "lse_r": lse_r}
+    got.update({"d" + k: leaves[k].grad for k in leaves})
+    got = {k: v.detach().double().cpu().numpy() for k, v in got.items()}
+    compare(got, run_oracle(w), "bf16")
