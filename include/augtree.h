@@ -245,18 +245,24 @@ augtree_status augtree_tree_bwd(const augtree_plan* plan, const void* qp, const 
 
 /* Prefill backward that allocates nothing and takes no workspace.  The paper has no
  * counterpart: this is a convenience for callers that cannot allocate device memory
- * while they run (a caching-allocator or memory-pool callback, a real-time step that
- * must not take the driver's allocation lock or meet an out-of-memory error, a host
- * framework that only lends its own buffers).  Arguments and results are those of
- * augtree_prefill_bwd; the plan must already exist (creating it allocates).
- * Scratch: Delta and the fp32 dQ accumulator live in a 64 MiB array defined by the
- * library, held on every device that loads it until the process exits.  A plan whose
- * prefill-backward workspace (augtree_plan_workspace_bytes) exceeds 64 MiB is rejected
- * with AUGTREE_ERR_WORKSPACE_TOO_SMALL before any work is queued.  The first call on a
- * device looks up the array's device address; make that call before any stream
- * capture.  Every call shares the array and re-initializes what it reads, so results do
- * not depend on earlier calls, but calls that may overlap on the GPU (unordered
- * streams) race on it. */
+ * while they run (a caching-allocator or memory-pool callback, where allocating would
+ * recurse; a real-time step that must not take the driver's allocation lock or meet an
+ * out-of-memory error; a host framework that only lends its own buffers).  Arguments
+ * and results are those of augtree_prefill_bwd; the plan must already exist (creating
+ * it allocates).
+ * Scratch: a 64 MiB array defined by the library.  augtree_plan_create looks up its
+ * device address on the plan's device (loading the library module that holds it, which
+ * reserves the 64 MiB on that device until the process exits), so this call does no
+ * lookup and no allocation.  Per prompt row and query head the array holds 40 bytes
+ * with the tensor-core kernels (row statistics and extra-MMA rows) plus 32 MiB of dK/dV
+ * flush slots overall, so prompt rows x query heads up to about 838,000; with the SIMT
+ * kernels 4 + 4 * head_dim bytes (Delta and the fp32 dQ accumulator), up to about
+ * 130,000 at head_dim 128.  A plan whose prefill-backward workspace
+ * (augtree_plan_workspace_bytes) exceeds 64 MiB is rejected with
+ * AUGTREE_ERR_WORKSPACE_TOO_SMALL before any work is queued; AUGTREE_ERR_CUDA if the
+ * lookup at plan creation failed.  Every call shares the array and re-initializes what
+ * it reads, so results do not depend on earlier calls, but calls that may overlap on
+ * the GPU (unordered streams) race on it. */
 augtree_status augtree_prefill_bwd_static(const augtree_plan* plan, const void* qp, const void* kp,
                                           const void* vp, const void* op, const float* lse_p,
                                           const void* dop, const float* dkp_acc,

@@ -405,6 +405,7 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   p->row_bstart_d = nullptr;
   p->row_bend_d = nullptr;
   p->splits_d = nullptr;
+  p->static_scratch = nullptr;
   for (int i = 0; i < kNumOps; ++i) p->queue_d[i] = nullptr;
   if (cudaGetDevice(&p->device) != cudaSuccess) {
     delete p;
@@ -514,6 +515,13 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
     cudaGetLastError();
     augtree_plan_destroy(p);
     return AUGTREE_ERR_CUDA;
+  }
+  // The allocation-free prefill backward's scratch array: its device address on this
+  // device, looked up here so that the call itself never loads a module or allocates.
+  // A failed lookup only disables that entry point (it then returns AUGTREE_ERR_CUDA).
+  if (static_scratch_address(&p->static_scratch) != cudaSuccess) {
+    cudaGetLastError();
+    p->static_scratch = nullptr;
   }
   *out = p;
   return AUGTREE_OK;

@@ -67,6 +67,9 @@ struct augtree_plan {
   int quad[augtree::kNumOps];        // forward units of four items (four heads of one KV head) for SM pairs
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
+  // Device address of the library's fixed scratch array (augtree_prefill_bwd_static),
+  // looked up at plan creation on the plan's device; null if that lookup failed.
+  void* static_scratch;
   // Opt-in per-kernel timing: a ring of AUGTREE_TIMING_RING calls per op, each with up
   // to kTimingMarks events (before each kernel, after the last).  Written by the compute
   // calls, which take the plan as const.
@@ -161,6 +164,11 @@ cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* 
                       cudaStream_t st);
 cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
                       const void* vr, const float* stats, const void* dO, void* dq, cudaStream_t st);
+
+// Fixed scratch array of augtree_prefill_bwd_static (static_scratch.cu): its size, and
+// the lookup of its device address on the current device.
+constexpr size_t kStaticScratchBytes = 64ull << 20;
+cudaError_t static_scratch_address(void** out);
 
 // Memory-bound helpers.
 cudaError_t launch_preprocess(const void* o, const void* dO, int dtype, int64_t rows, int hq, int d,

@@ -10,47 +10,45 @@
 // and output; the plan must have been created beforehand (augtree_plan_create does
 // allocate), and only the call itself allocates nothing.
 //
-// The scratch (the backward's row statistics, the fp32 dQ accumulator [P, Hq, D] and,
-// for the tensor-core kernels, 32 MiB of per-SM fp32 dK/dV flush slots) is the
-// file-scope device array below, 64 MiB: enough for P * Hq up to about 60,000 at
-// D = 128 with the tensor-core kernels (about 520 bytes per prompt row and query head).
-// The first call on a device looks up the array's device address (cudaGetSymbolAddress,
-// which may load this module); make that first call before any stream capture.  Every
-// GPU that loads this library reserves the array until the process exits.  All calls share it and it keeps the last call's contents; the call
-// re-initializes everything it reads (Delta is overwritten, the dQ accumulator is
-// zeroed by the first kernel of the call), so nothing carries over between calls.
-// Calls that can overlap on the GPU (different streams without ordering between them)
-// race on the array.
-#include <mutex>
-
+// The scratch is the file-scope device array below, 64 MiB.  What it holds per prompt
+// row and query head (the prefill backward's workspace layout):
+//   tensor-core kernels: 8 bytes of row statistics {lse*log2(e), Delta} and 32 bytes of
+//     the key side's extra-MMA rows, 40 bytes in all, plus 32 MiB of per-SM fp32 dK/dV
+//     flush slots: prompt rows x query heads up to about 838,000;
+//   SIMT kernels: Delta (4 bytes) and the fp32 dQ accumulator (4 * head_dim bytes), 516
+//     bytes at head_dim 128 and 260 at 64: up to about 130,000 (resp. 258,000).
+//
+// Address lookup: in host code the array's name is a host-side stand-in, not a device
+// address.  augtree_plan_create calls static_scratch_address() with the plan's device
+// current and keeps the result in the plan, so the lookup (which loads this file's
+// module and with it reserves the array on that device, under lazy module loading)
+// happens at plan creation, and the entry point itself neither looks anything up nor
+// allocates.  A plan is tied to its device and its context, so the address can never
+// outlive the context it was taken in.
+//
+// Every GPU that loads this library's module reserves the array until the process
+// exits.  All calls share it and it keeps the last call's contents; the call
+// re-initializes everything it reads (row statistics are overwritten, the SIMT dQ
+// accumulator is zeroed by the call's first kernel, and the flush slots are stored
+// before they are added to), so nothing carries over between calls.  Calls that can
+// overlap on the GPU (different streams without ordering between them) race on the
+// array.
 #include "internal.h"
 
-#define AUGTREE_STATIC_SCRATCH_BYTES (64ull << 20)
+static __device__ __align__(256) unsigned char g_prefill_bwd_scratch[augtree::kStaticScratchBytes];
 
-static __device__ __align__(256) unsigned char g_prefill_bwd_scratch[AUGTREE_STATIC_SCRATCH_BYTES];
+namespace augtree {
 
-namespace {
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
-
-// Device address of the array on device `dev` (which must be current).  In host code
-// the array's name is only a host-side stand-in, so the address comes from the runtime.
-cudaError_t scratch_address(int dev, void** out) {
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_prefill_bwd_scratch);
-    if (e != cudaSuccess) return e;
-    g_addr[dev] = p;
-  }
-  *out = g_addr[dev];
+// Device address of the array on the current device.
+cudaError_t static_scratch_address(void** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_prefill_bwd_scratch);
+  if (e != cudaSuccess) return e;
+  *out = p;
   return cudaSuccess;
 }
 
-}  // namespace
+}  // namespace augtree
 
 extern "C" augtree_status augtree_prefill_bwd_static(const augtree_plan* plan, const void* qp, const void* kp,
                                                      const void* vp, const void* op, const float* lse_p,
@@ -60,14 +58,9 @@ extern "C" augtree_status augtree_prefill_bwd_static(const augtree_plan* plan, c
   size_t need = 0;
   augtree_status st = augtree_plan_workspace_bytes(plan, AUGTREE_OP_PREFILL_BWD, &need);
   if (st != AUGTREE_OK) return st;
-  if (need > (size_t)AUGTREE_STATIC_SCRATCH_BYTES) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return AUGTREE_ERR_CUDA;
-  void* scratch = nullptr;
-  if (scratch_address(dev, &scratch) != cudaSuccess) {
-    cudaGetLastError();
-    return AUGTREE_ERR_CUDA;
-  }
-  return augtree_prefill_bwd(plan, qp, kp, vp, op, lse_p, dop, dkp_acc, dvp_acc, dqp, dkp, dvp, scratch,
-                             (size_t)AUGTREE_STATIC_SCRATCH_BYTES, stream);
+  if (need > augtree::kStaticScratchBytes) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
+  // Null when the lookup at plan creation failed (the device could not reserve it).
+  if (!plan->static_scratch) return AUGTREE_ERR_CUDA;
+  return augtree_prefill_bwd(plan, qp, kp, vp, op, lse_p, dop, dkp_acc, dvp_acc, dqp, dkp, dvp, plan->static_scratch,
+                             augtree::kStaticScratchBytes, stream);
 }
