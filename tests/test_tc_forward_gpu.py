@@ -29,8 +29,12 @@ def test_tc_forward_matches_oracle(cuda_device, ti, hq, hkv):
 
 def test_tc_forward_large_scores(cuda_device):
     """Q and K scaled by 4 (exact in bf16): scores spread 16x wider, so the running max
-    grows past the lazy-rescale threshold and O is rescaled in TMEM.  V keeps unit
-    variance, so the stated 1e-2 bound applies to O unchanged."""
+    grows past the lazy-rescale threshold and O is rescaled in TMEM.  Single keys then
+    dominate their rows and |O| reaches about 4.3, where storing O in bf16 (8 significant
+    bits) moves it by up to 2^-8 |O|.  The bound is the stated 1e-2 on the arithmetic
+    plus that output rounding; tests/test_bf16_output_bound.py derives it on this very
+    input (an ideal bf16-P forward exceeds a plain 1e-2 and stays within this bound).
+    lse is fp32 and keeps the plain 1e-2."""
     import torch
     from oracle import attention as A
     w = W.custom(TREES[4], hq=4, hkv=2, d=128, dtype="bf16", seed=77)
@@ -41,12 +45,8 @@ def test_tc_forward_large_scores(cuda_device):
         h[n] = h[n] * 4
     got = run_cuda_fwd(w, kernel=at.KERNEL_TC, t=t)
     ref = A.tree_attention_direct(h, w.tree.offsets(), A.default_scale(w.d), grad=False)
-    # With scores this peaked a few keys carry each row, and the bf16 rounding of P
-    # (relative 2^-9 per weight) moves O by up to about 2^-8 * max|v - O| on top of the
-    # bf16 rounding of O itself.  A CPU emulation of exactly that arithmetic (bf16 P
-    # with the exact row max, fp32 sums) reaches 1.35e-2 on this input, so the bound
-    # here is 2e-2; the N(0,1) configurations keep the stated 1e-2.
     for k in ("o_p", "o_r"):
-        assert np.max(np.abs(got[k] - ref[k])) <= 2e-2, k
+        err = np.abs(got[k] - ref[k])
+        assert np.all(err <= 1e-2 + 2.0 ** -8 * np.abs(ref[k])), (k, float(err.max()))
     for k in ("lse_p", "lse_r"):
-        assert np.max(np.abs(got[k] - ref[k]) / np.maximum(1.0, np.abs(ref[k]))) <= 1e-2, k
+        assert np.max(np.abs(got[k] - ref[k])) <= 1e-2, k
