@@ -35,11 +35,11 @@ DEFAULT_WORKLOAD = "prompt_heavy"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
-# DRAM bytes (read + write) per launch of a kernel on a full-size workload, from a
-# one-pass ncu capture of dram__bytes_read.sum + dram__bytes_write.sum averaged over
-# the kernel's launches in one step (the summary under profiles/ gives the command).
-# Valid for the kernel versions it was taken on; absent entries report null.
-TRAFFIC_PER_LAUNCH = {("prompt_heavy", "bwd_key_side"): 32.71e9}
+# DRAM bytes (read + write) per launch of a kernel on a full-size workload, from an ncu
+# capture of dram__bytes_read.sum + dram__bytes_write.sum (the summary named in
+# "profile" gives the command).  Each entry records a digest of the kernel's sources
+# at capture time; once they change, the figure is reported as null.
+TRAFFIC = {}
 
 
 def peaks():
@@ -191,7 +191,9 @@ def oracle_fields(rate, desc, w):
     workload's step time at that rate (an extrapolation, labelled so)."""
     return {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads_used(), "kind": "oracle",
             "sample": desc, "cpu_model": cpu_model(),
-            "full_step_s_extrapolated": round(useful_flops(w) / (rate * 1e12), 1) if rate > 0 else None}
+            "full_step_s_extrapolated": round(useful_flops(w) / (rate * 1e12), 1) if rate > 0 else None,
+            "extrapolation": ("rate-scaled estimate: the sample's rate applied to the full step's useful FLOPs; "
+                              "the /16 sample's prompt/response mix differs from the full step's")}
 
 
 def threads_used():
@@ -208,6 +210,187 @@ def threads_used():
 # ---------------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------------
+def kernel_source_digest(files):
+    """First 16 hex digits of the SHA-256 of a kernel's source files (identifies the
+    kernel version a DRAM-traffic capture was taken on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "shared_prompt_tree_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_entry(workload: str, kind: str):
+    """(bytes per launch, note) of TRAFFIC for a kernel, or (None, why not)."""
+    e = TRAFFIC.get((workload, kind))
+    if e is None:
+        return None, "no capture for this kernel and workload"
+    if kernel_source_digest(e["sources"]) != e["digest"]:
+        return None, "stale: the kernel's source changed since the capture"
+    return e["bytes_per_launch"], e["profile"]
+
+
+class Run:
+    """Device buffers and plan of one workload, and its fwd+bwd step through the C ABI
+    (prefill fwd, replay fwd, then one augtree_tree_bwd call, or replay_bwd +
+    prefill_bwd)."""
+
+    def __init__(self, w, at, dev, kernel, fused=True):
+        import torch
+        import workloads as W
+        self.w, self.at, self.dev, self.fused = w, at, dev, fused
+        dt = at.BF16 if w.dtype == "bf16" else at.FP32
+        self.plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt, kernel=kernel)
+        self.t = {n: W.tensor_torch(w, n, dev) for n in W.TENSORS}
+        t = self.t
+        f32 = torch.float32
+        self.o_p, self.o_r = torch.empty_like(t["q_p"]), torch.empty_like(t["q_r"])
+        self.lse_p = torch.empty(w.hq, w.tree.total_prompt, dtype=f32, device=dev)
+        self.lse_r = torch.empty(w.hq, w.tree.total_resp, dtype=f32, device=dev)
+        self.dq_p, self.dk_p, self.dv_p = (torch.empty_like(t[n]) for n in ("q_p", "k_p", "v_p"))
+        self.dq_r, self.dk_r, self.dv_r = (torch.empty_like(t[n]) for n in ("q_r", "k_r", "v_r"))
+        plan = self.plan
+        if fused:
+            self.ws_t = torch.empty(max(1, plan.workspace_bytes(at.OP_TREE_BWD)), dtype=torch.uint8, device=dev)
+        else:
+            self.dkp_sum = torch.empty(t["k_p"].shape, dtype=f32, device=dev)
+            self.dvp_sum = torch.empty(t["v_p"].shape, dtype=f32, device=dev)
+            self.ws_r = torch.empty(max(1, plan.workspace_bytes(at.OP_REPLAY_BWD)), dtype=torch.uint8, device=dev)
+            self.ws_p = torch.empty(max(1, plan.workspace_bytes(at.OP_PREFILL_BWD)), dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream()
+        self.n_ev = 4 if fused else 5
+
+    def outputs(self):
+        return [self.o_p, self.o_r, self.lse_p, self.lse_r, self.dq_p, self.dk_p, self.dv_p, self.dq_r, self.dk_r,
+                self.dv_r]
+
+    def step(self, evs=None):
+        at, t, s, plan = self.at, self.t, self.stream, self.plan
+        rec = (lambda i: evs[i].record(s)) if evs else (lambda i: None)
+        rec(0)
+        at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], self.o_p, self.lse_p, stream=s)
+        rec(1)
+        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], self.o_r, self.lse_r, stream=s)
+        rec(2)
+        if self.fused:
+            at.augtree_tree_bwd(plan, t["q_p"], t["k_p"], t["v_p"], self.o_p, self.lse_p, t["do_p"], t["q_r"],
+                                t["k_r"], t["v_r"], self.o_r, self.lse_r, t["do_r"], self.dq_p, self.dk_p, self.dv_p,
+                                self.dq_r, self.dk_r, self.dv_r, self.ws_t, stream=s)
+            rec(3)
+            return
+        at.augtree_replay_bwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], self.o_r, self.lse_r,
+                              t["do_r"], self.dq_r, self.dk_r, self.dv_r, self.dkp_sum, self.dvp_sum, self.ws_r,
+                              stream=s)
+        rec(3)
+        at.augtree_prefill_bwd(plan, t["q_p"], t["k_p"], t["v_p"], self.o_p, self.lse_p, t["do_p"], self.dkp_sum,
+                               self.dvp_sum, self.dq_p, self.dk_p, self.dv_p, self.ws_p, stream=s)
+        rec(4)
+
+    def close(self):
+        import torch
+        self.plan.close()
+        for k in list(vars(self)):
+            if k not in ("w", "at", "dev", "fused", "n_ev"):
+                delattr(self, k)
+        torch.cuda.empty_cache()
+
+
+def barrier(world):
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def measure(run, steps, warmup, world, local, sample_clocks=True):
+    """Times `steps` fwd+bwd steps after `warmup` untimed ones (CUDA events on the calls'
+    stream, barrier + synchronize on both sides) with per-kernel CUDA events recorded by
+    the library.  Returns a dict of the step time (max over ranks), the per-call and
+    per-kernel times and the sampled clocks."""
+    import torch
+    at, plan = run.at, run.plan
+    for _ in range(warmup):
+        run.step()
+    barrier(world)
+    clocks = ClockSampler(local) if sample_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(run.n_ev)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    plan.set_timing(steps <= at.TIMING_RING)
+    barrier(world)
+    start.record(run.stream)
+    for k in range(steps):
+        run.step(evs[k])
+    end.record(run.stream)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    plan.check()  # raises if any kernel of the step gave up on a bounded wait
+    kernel_ms = {}  # (op, kind) -> [ms per step summed over the step's launches, launches]
+    if steps <= at.TIMING_RING:
+        for op in range(5):
+            for back in range(steps):
+                try:
+                    kt = plan.kernel_times(op, back)
+                except at.AugtreeError:  # the step makes no timed call of this op
+                    break
+                for kind, t_ms in kt:
+                    e = kernel_ms.setdefault((op, kind), [0.0, 0])
+                    e[0] += t_ms / steps
+                    e[1] += 1
+        plan.set_timing(False)
+    ms = max_over_ranks(start.elapsed_time(end), run.dev) / steps
+    per_call = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(run.n_ev - 1)]
+                         for k in range(steps)]).mean(0)
+    ms_median = float(np.median([evs[k][0].elapsed_time(evs[k][run.n_ev - 1]) for k in range(steps)]))
+    return {"ms": ms, "ms_median": ms_median, "per_call": per_call, "kernel_ms": kernel_ms, "clocks": clk}
+
+
+# GEMMs a kernel performs per valid pair (2 D Hq FLOPs each): forward S and PV; key side
+# S^T, dP^T, dV, dK; query side S, dP, dQ; SIMT backward all five.
+GEMMS = {"fwd_tc": 2, "fwd_simt": 2, "bwd_key_side": 4, "bwd_query_side": 3, "bwd_simt": 5}
+KERNEL_NAMES = {"bwd_key_side": "tc_bwd_kv_kernel (backward, key side)",
+                "bwd_query_side": "tc_bwd_dq_kernel (backward, query side)",
+                "fwd_tc": "tc_fwd_kernel (forward)"}
+
+
+def kernel_table(w, m):
+    """Per kernel kind: [ms per step, launches per step, GEMM FLOPs per step]."""
+    n_pairs_prompt = sum(lp * (lp + 1) // 2 for lp in w.tree.prompt_lens)
+    n_pairs = w.tree.pair_count()
+    pairs = {0: n_pairs_prompt, 1: n_pairs - n_pairs_prompt, 2: n_pairs - n_pairs_prompt, 3: n_pairs_prompt,
+             4: n_pairs}
+    steps = None
+    kinds = {}
+    for (op, kind), (t_ms, launches) in m["kernel_ms"].items():
+        e = kinds.setdefault(kind, [0.0, 0, 0.0])
+        e[0] += t_ms
+        e[1] += launches
+        e[2] += 2.0 * w.d * w.hq * pairs[op] * GEMMS.get(kind, 0)
+    return kinds
+
+
+def roofline(w, m, steps, peak_s, pk_kind):
+    """The dominant kernel's live roofline: its GEMM FLOPs per step over its measured
+    time per step (the library's CUDA events around each launch)."""
+    kinds = kernel_table(w, m)
+    if not kinds:
+        return None, {}
+    dom = max(kinds, key=lambda k: kinds[k][0])
+    ms_k, launches, flops_k = kinds[dom]
+    ach = flops_k / (ms_k * 1e-3) / 1e12
+    traffic, note = traffic_entry(w.name, dom)
+    return ({"bound": "tensor", "kernel": KERNEL_NAMES.get(dom, dom), "achieved": round(ach, 2), "peak": peak_s,
+             "unit": "TFLOP/s", "frac": round(ach / peak_s, 4), "traffic": traffic, "traffic_source": note,
+             "launches_per_step": launches / steps, "peak_kind": f"bf16 dense sustained ({pk_kind})"},
+            {k: {"ms_per_step": round(v[0], 4), "launches_per_step": v[1] / steps,
+                 "tflops": round(v[2] / (v[0] * 1e-3) / 1e12, 2) if v[2] > 0 else None}
+             for k, v in sorted(kinds.items(), key=lambda kv: -kv[1][0])})
+
+
 def run_ours(args):
     import torch
     import shared_prompt_tree_gb300 as at
@@ -223,116 +406,39 @@ def run_ours(args):
     if args.scale_down > 1:
         w = scaled_down(w, args.scale_down)
     kernel = {"auto": at.KERNEL_AUTO, "simt": at.KERNEL_SIMT, "tc": at.KERNEL_TC}[args.kernel]
-    dt = at.BF16 if w.dtype == "bf16" else at.FP32
-    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt, kernel=kernel)
-    t = {n: W.tensor_torch(w, n, dev) for n in W.TENSORS}
-    stream = torch.cuda.current_stream()
-    tdt = torch.bfloat16 if dt == at.BF16 else torch.float32
-    f32 = torch.float32
-    o_p, o_r = torch.empty_like(t["q_p"]), torch.empty_like(t["q_r"])
-    lse_p = torch.empty(w.hq, w.tree.total_prompt, dtype=f32, device=dev)
-    lse_r = torch.empty(w.hq, w.tree.total_resp, dtype=f32, device=dev)
-    dq_p, dk_p, dv_p = (torch.empty_like(t[n]) for n in ("q_p", "k_p", "v_p"))
-    dq_r, dk_r, dv_r = (torch.empty_like(t[n]) for n in ("q_r", "k_r", "v_r"))
-    dkp_sum = torch.empty(t["k_p"].shape, dtype=f32, device=dev)
-    dvp_sum = torch.empty(t["v_p"].shape, dtype=f32, device=dev)
     fused = args.bwd == "fused"
-    if fused:
-        ws_t = torch.empty(max(1, plan.workspace_bytes(at.OP_TREE_BWD)), dtype=torch.uint8, device=dev)
-    else:
-        ws_r = torch.empty(max(1, plan.workspace_bytes(at.OP_REPLAY_BWD)), dtype=torch.uint8, device=dev)
-        ws_p = torch.empty(max(1, plan.workspace_bytes(at.OP_PREFILL_BWD)), dtype=torch.uint8, device=dev)
-
-    n_ev = 4 if fused else 5
-    def step(evs=None):
-        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
-        rec(0)
-        at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, stream=stream)
-        rec(1)
-        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, stream=stream)
-        rec(2)
-        if fused:
-            at.augtree_tree_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], t["q_r"], t["k_r"],
-                                t["v_r"], o_r, lse_r, t["do_r"], dq_p, dk_p, dv_p, dq_r, dk_r, dv_r, ws_t,
-                                stream=stream)
-            rec(3)
-            return
-        at.augtree_replay_bwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, t["do_r"],
-                              dq_r, dk_r, dv_r, dkp_sum, dvp_sum, ws_r, stream=stream)
-        rec(3)
-        at.augtree_prefill_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], dkp_sum, dvp_sum,
-                               dq_p, dk_p, dv_p, ws_p, stream=stream)
-        rec(4)
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    for _ in range(args.warmup):
-        step()
-    barrier()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # per-kernel CUDA events inside the library's calls, on the calls' stream
-    plan.set_timing(args.steps <= at.TIMING_RING)
-    barrier()
-    start.record(stream)
-    for k in range(args.steps):
-        step(evs[k])
-    end.record(stream)
-    barrier()
-    clk = clocks.stop()
-    plan.check()  # raises if any kernel of the step gave up on a bounded wait
-    kernel_ms = {}  # kind -> [ms per step summed over the step's launches, launches per step]
-    if args.steps <= at.TIMING_RING:
-        for op in range(5):
-            for back in range(args.steps):
-                try:
-                    kt = plan.kernel_times(op, back)
-                except at.AugtreeError:  # the step makes no timed call of this op
-                    break
-                for kind, t_ms in kt:
-                    e = kernel_ms.setdefault((op, kind), [0.0, 0])
-                    e[0] += t_ms / args.steps
-                    e[1] += 1
-        plan.set_timing(False)
-    ms = max_over_ranks(start.elapsed_time(end), dev)
-    per_call = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(n_ev - 1)]
-                         for k in range(args.steps)]).mean(0)
-    ms_step = ms / args.steps
-    # Median over the timed steps of one step's duration (first to last call event).
-    ms_median = float(np.median([evs[k][0].elapsed_time(evs[k][n_ev - 1]) for k in range(args.steps)]))
+    run = Run(w, at, dev, kernel, fused)
+    m = measure(run, args.steps, args.warmup, world, local)
+    ms_step = m["ms"]
 
     # e2e through the public API with host buffers: H2D of the step's inputs from
     # pinned memory, the step, D2H of its results (outputs and all gradients).
-    host_in = {n: t[n].cpu().pin_memory() for n in W.TENSORS}
-    outs = [o_p, o_r, lse_p, lse_r, dq_p, dk_p, dv_p, dq_r, dk_r, dv_r]
+    host_in = {n: run.t[n].cpu().pin_memory() for n in W.TENSORS}
+    outs = run.outputs()
     host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in outs)
     e_steps = max(1, min(args.steps, 5))
-    barrier()
+    barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(run.stream)
     for _ in range(e_steps):
         for n in W.TENSORS:
-            t[n].copy_(host_in[n], non_blocking=True)
-        step()
+            run.t[n].copy_(host_in[n], non_blocking=True)
+        run.step()
         for x, hx in zip(outs, host_out):
             hx.copy_(x, non_blocking=True)
-    e1.record(stream)
-    barrier()
+    e1.record(run.stream)
+    barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
+    launches_per_step = count_launches(run.plan, at, fused)
+    del host_in, host_out, outs
+    run.close()
 
     flops = useful_flops(w)
-    tokens = w.tokens
     tflops = flops * world / (ms_step * 1e-3) / 1e12
     pk, pk_kind = peaks()
+    peak_s = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     n_pairs_prompt = sum(lp * (lp + 1) // 2 for lp in w.tree.prompt_lens)
     n_pairs = w.tree.pair_count()
     if fused:
@@ -343,31 +449,7 @@ def run_ours(args):
         names = ["prefill_fwd", "replay_fwd", "replay_bwd", "prefill_bwd"]
         per_flops = [4 * w.d * w.hq * n_pairs_prompt, 4 * w.d * w.hq * (n_pairs - n_pairs_prompt),
                      10 * w.d * w.hq * (n_pairs - n_pairs_prompt), 10 * w.d * w.hq * n_pairs_prompt]
-    # The dominant kernel: per-launch algorithmic FLOPs (the GEMMs the kernel itself
-    # performs on valid pairs: forward 2, key side S, dP, dV, dK = 4, query side S, dP,
-    # dQ = 3, each 2 d Hq per pair) over its launches' measured durations.
-    pairs = {0: n_pairs_prompt, 1: n_pairs - n_pairs_prompt, 2: n_pairs - n_pairs_prompt, 3: n_pairs_prompt,
-             4: n_pairs}
-    gemms = {"fwd_tc": 2, "fwd_simt": 2, "bwd_key_side": 4, "bwd_query_side": 3, "bwd_simt": 5}
-    kinds = {}
-    for (op, kind), (t_ms, launches) in kernel_ms.items():
-        e = kinds.setdefault(kind, [0.0, 0, 0.0])
-        e[0] += t_ms
-        e[1] += launches / args.steps
-        e[2] += 2.0 * w.d * w.hq * pairs[op] * gemms.get(kind, 0)
-    if kinds:
-        dom_kind = max(kinds, key=lambda k: kinds[k][0])
-        ms_k, launches_k, flops_k = kinds[dom_kind]
-        ach = flops_k / (ms_k * 1e-3) / 1e12
-        dom_name = {"bwd_key_side": "tc_bwd_kv_kernel (backward, key side)",
-                    "bwd_query_side": "tc_bwd_dq_kernel (backward, query side)",
-                    "fwd_tc": "tc_fwd_kernel (forward)"}.get(dom_kind, dom_kind)
-    else:
-        dom = int(np.argmax(per_call))
-        ach = per_flops[dom] / (per_call[dom] * 1e-3) / 1e12
-        dom_kind, dom_name, launches_k = names[dom], names[dom] + " call", 1
-    peak_s = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    launches_per_step = count_launches(plan, at, fused)
+    roof, ktab = roofline(w, m, args.steps, peak_s, pk_kind)
 
     result = {
         "metric": "tree-attn fwd+bwd useful TFLOP/s & tokens/s; % of GB300 BF16 tensor peak",
@@ -377,11 +459,11 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
-        "median_ms_per_step": round(ms_median, 4),
+        "median_ms_per_step": round(m["ms_median"], 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if dt == at.BF16 else "fp32",
+        "dtype": "bf16" if w.dtype == "bf16" else "fp32",
         "data": "synthetic (seeded counter-hash N(0,1) values, bf16-rounded)",
         "config": {"workload": w.name, "groups": w.tree.n_groups, "prompt_lens": w.tree.prompt_lens[:4],
                    "branches": w.tree.n_branches, "total_prompt": w.tree.total_prompt,
@@ -389,34 +471,49 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}", "kernel_family": args.kernel,
                    "backward": "one augtree_tree_bwd call" if fused else "augtree_replay_bwd + augtree_prefill_bwd",
                    "l2": "inputs larger than L2 (no flush)"},
-        "tokens_per_s": round(tokens * world / (ms_step * 1e-3), 1),
+        "tokens_per_s": round(w.tokens * world / (ms_step * 1e-3), 1),
         "flattened_tokens_per_s": round(w.tree.flattened_tokens() * world / (ms_step * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * tflops / world / pk["bf16_tflops"], 2),
-        "per_call_ms": {n: round(float(x), 4) for n, x in zip(names, per_call)},
-        "per_call_tflops": {n: round(f / (x * 1e-3) / 1e12, 2) for n, f, x in zip(names, per_flops, per_call)},
-        "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": round(ach, 2), "peak": peak_s,
-                     "unit": "TFLOP/s", "frac": round(ach / peak_s, 4),
-                     "traffic": TRAFFIC_PER_LAUNCH.get((w.name, dom_kind)),
-                     "launches_per_step": launches_k,
-                     "peak_kind": f"bf16 dense sustained ({pk_kind})"},
-        "kernels": {k: {"ms_per_step": round(v[0], 4), "launches_per_step": v[1],
-                        "tflops": round(v[2] / (v[0] * 1e-3) / 1e12, 2) if v[2] > 0 else None}
-                    for k, v in sorted(kinds.items(), key=lambda kv: -kv[1][0])},
+        "per_call_ms": {n: round(float(x), 4) for n, x in zip(names, m["per_call"])},
+        "per_call_tflops": {n: round(f / (x * 1e-3) / 1e12, 2) for n, f, x in zip(names, per_flops, m["per_call"])},
+        "roofline": roof,
+        "kernels": ktab,
         "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+        "clocks": m["clocks"],
     }
-    if args.flattened:
+    if not args.no_flattened:
         # The same trees with no prompt reuse (every pair on its own): the speedup of the
-        # shared-prompt tree over flattening, measured with the same kernels.
+        # shared-prompt tree over flattening, measured with the same kernels and the same
+        # fused backward.
         wf = flattened(w)
-        ms_f = time_device_steps(wf, at, dev, max(1, min(args.steps, 3)), 1)
+        rf = Run(wf, at, dev, kernel, fused)
+        mf = measure(rf, max(1, min(args.steps, 3)), 1, world, local, sample_clocks=False)
+        rf.close()
         result["flattened_per_pair"] = {
-            "ms_per_step": round(ms_f, 3), "pairs": wf.tree.pair_count(),
-            "tree_pairs": w.tree.pair_count(), "speedup_of_tree": round(ms_f / ms_step, 3)}
+            "ms_per_step": round(mf["ms"], 3), "pairs": wf.tree.pair_count(), "tree_pairs": w.tree.pair_count(),
+            "speedup_of_tree": round(mf["ms"] / ms_step, 3), "steps": max(1, min(args.steps, 3)),
+            "backward": result["config"]["backward"]}
+    if not args.no_per_workload and args.scale_down == 1:
+        # The other bf16 configurations, each timed the same way (fewer steps for the
+        # long one, whose step takes seconds).
+        per = {}
+        for name in [n for n in ("prompt_heavy", "response_heavy", "mixed", "long") if n != w.name]:
+            wo = W.workload(name)
+            st, wu = (2, 1) if name == "long" else (args.steps, args.warmup)
+            ro = Run(wo, at, dev, kernel, fused)
+            mo = measure(ro, st, wu, world, local)
+            ro.close()
+            tf = useful_flops(wo) * world / (mo["ms"] * 1e-3) / 1e12
+            roof_o, ktab_o = roofline(wo, mo, st, peak_s, pk_kind)
+            per[name] = {"ms_per_step": round(mo["ms"], 4), "steps": st, "warmup": wu,
+                         "useful_tflops": round(tf, 3), "pct_of_bf16_peak": round(100.0 * tf / world / pk["bf16_tflops"], 2),
+                         "tokens_per_s": round(wo.tokens * world / (mo["ms"] * 1e-3), 1),
+                         "roofline": roof_o, "kernels": ktab_o, "clocks": mo["clocks"]}
+        result["per_workload"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, per = time_oracle(w, min_seconds=args.cpu_seconds)
+        rate, desc, per_rep = time_oracle(w, min_seconds=args.cpu_seconds)
         result["cpu_baseline"] = oracle_fields(rate, desc, w)
     if rank == 0:
         print(json.dumps(result))
@@ -439,51 +536,6 @@ def flattened(w):
             prompts.append(lp)
             branches.append([li])
     return W.custom(W.Tree(prompts, branches), w.hq, w.hkv, w.d, w.dtype, w.seed, w.scale, name=f"{w.name}/flattened")
-
-
-def time_device_steps(w, at, dev, steps, warmup):
-    """ms per fwd+bwd step of workload w through the C ABI, inputs resident on the
-    device (the same four calls as the timed region of run_ours)."""
-    import torch
-    import workloads as W
-    dt = at.BF16 if w.dtype == "bf16" else at.FP32
-    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt)
-    t = {n: W.tensor_torch(w, n, dev) for n in W.TENSORS}
-    stream = torch.cuda.current_stream()
-    f32 = torch.float32
-    o_p, o_r = torch.empty_like(t["q_p"]), torch.empty_like(t["q_r"])
-    lse_p = torch.empty(w.hq, w.tree.total_prompt, dtype=f32, device=dev)
-    lse_r = torch.empty(w.hq, w.tree.total_resp, dtype=f32, device=dev)
-    dq_p, dk_p, dv_p = (torch.empty_like(t[n]) for n in ("q_p", "k_p", "v_p"))
-    dq_r, dk_r, dv_r = (torch.empty_like(t[n]) for n in ("q_r", "k_r", "v_r"))
-    dkp_sum = torch.empty(t["k_p"].shape, dtype=f32, device=dev)
-    dvp_sum = torch.empty(t["v_p"].shape, dtype=f32, device=dev)
-    ws_r = torch.empty(max(1, plan.workspace_bytes(at.OP_REPLAY_BWD)), dtype=torch.uint8, device=dev)
-    ws_p = torch.empty(max(1, plan.workspace_bytes(at.OP_PREFILL_BWD)), dtype=torch.uint8, device=dev)
-
-    def step():
-        at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, stream=stream)
-        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, stream=stream)
-        at.augtree_replay_bwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, t["do_r"],
-                              dq_r, dk_r, dv_r, dkp_sum, dvp_sum, ws_r, stream=stream)
-        at.augtree_prefill_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], dkp_sum, dvp_sum,
-                               dq_p, dk_p, dv_p, ws_p, stream=stream)
-
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    plan.check()
-    ms = e0.elapsed_time(e1) / steps
-    del t, o_p, o_r, lse_p, lse_r, dq_p, dk_p, dv_p, dq_r, dk_r, dv_r, dkp_sum, dvp_sum, ws_r, ws_p
-    plan.close()
-    torch.cuda.empty_cache()
-    return ms
 
 
 def scaled_down(w, k):
@@ -542,6 +594,19 @@ def run_reference(args):
     print(json.dumps(res))
 
 
+def spawn_replicas(n: int) -> int:
+    """`--gpus N` without a launcher: re-runs this script under torch.distributed.run
+    with N ranks on this node (one GPU each), passing the same arguments.  Returns the
+    launcher's exit code."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.run(cmd).returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -555,9 +620,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale-down", type=int, default=1, help="divide every length by this (profiling only)")
-    ap.add_argument("--flattened", action="store_true",
-                    help="also time the flattened-per-pair structure (no prompt reuse) with the same kernels")
+    ap.add_argument("--no-flattened", action="store_true",
+                    help="skip timing the flattened-per-pair structure (no prompt reuse)")
+    ap.add_argument("--no-per-workload", action="store_true", help="skip timing the other configurations")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_replicas(args.gpus))
     if args.impl == "reference":
         run_reference(args)
     else:

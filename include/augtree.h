@@ -140,9 +140,16 @@ typedef struct augtree_plan augtree_plan;
  * gets s = min(64, max(1, ceil(nq*r / T))) splits of C = ceil(nq / s) query tiles
  * (then s = ceil(nq / C)); split k covers query tiles [k*C, min((k+1)*C, nq)).
  *
- * Order: items are sorted by cost descending, then by (group, tile, kind, split,
- * head) ascending - the largest-first greedy balancing of replay units (Sec. 3.4);
- * thread blocks take items in this order.
+ * Order: thread blocks take items in queue order.  Forward queues (prefill_fwd,
+ * replay_fwd): cost descending, then (group, tile, kind, split, head) ascending - the
+ * largest-first greedy balancing of replay units (Sec. 3.4).  Key-side queues
+ * (replay_bwd, prefill_bwd, tree_bwd): each item walks the query tiles of one stream -
+ * the group's, for its KV head (kinds 2, 4, 5), or the branch holding the tile's first
+ * key (kind 3).  The items of a stream are contiguous; streams come by total cost
+ * descending, then (group, KV head, branch) ascending with -1 for the group-wide
+ * stream; within a stream items come by cost descending, then (tile, kind, split)
+ * ascending.  Blocks that run side by side then walk the same Q/dO tiles, which L2
+ * holds once for all of them.
  */
 #define AUGTREE_ITEM_WORDS 8
 
@@ -291,6 +298,19 @@ augtree_status augtree_lse_merge_bwd(int64_t rows, int32_t h, int32_t d, const f
                                      const float* lse_a, const float* ob, const float* lse_b,
                                      const float* dout, const float* dlse, float* doa, float* dlse_a,
                                      float* dob, float* dlse_b, void* stream);
+
+/* Sets how long a device-side wait of this plan's kernels on another warp's work (a
+ * tile landing, a product finishing, a softmax handing over P) may last before the
+ * kernel gives up: ns nanoseconds, 2 s by default, 1 ns to 60 s.  A kernel that gives
+ * up records AUGTREE_ERR_TIMEOUT for augtree_plan_check, skips the rest of its work
+ * item (its outputs are then unspecified), waits for its own bulk copies and MMAs to
+ * finish (those waits keep a fixed 2 s limit, since they always end on their own),
+ * frees its tensor memory and exits; the device stays usable.  No limit is part of the
+ * paper's method: this bounds a wait that a fault elsewhere would make endless.  The
+ * value lives in device memory and is written synchronously (cudaMemcpy); it applies to
+ * kernels launched after the call.  Errors: AUGTREE_ERR_INVALID_ARG outside the range
+ * or on another device's plan. */
+augtree_status augtree_plan_set_wait_limit(augtree_plan* plan, uint64_t ns);
 
 /* Synchronizes `stream`, then reads and clears the plan's device error word.  Returns
  * AUGTREE_ERR_TIMEOUT if a kernel launched with this plan gave up on a bounded

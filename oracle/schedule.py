@@ -12,6 +12,16 @@ tile interactions, and blocks take items in order of decreasing weight.
 
 The item encoding, split rule and tie-break order are the library contract written
 out below in plain Python loops; the comparison with the library is bit for bit.
+
+Order.  Forward queues: largest first, ties by (group, tile, kind, split, head).
+Key-side backward queues: every item walks the Q/dO tiles of one stream - the group's
+query tiles for its KV head (prompt-key items) or its own branch's (response-key
+items).  The items of a stream form a chunk; chunks go largest first by their total
+cost (ties by group, KV head, branch, with -1 for the group-wide stream), and items
+within a chunk largest first (ties by tile, kind, split).  This keeps largest-first
+balancing within a chunk and makes the blocks that run side by side share one stream
+(cache locality of the on-chip scheduling; the pages' balancing is across lanes of a
+multi-node cluster and says nothing about it).
 """
 from __future__ import annotations
 
@@ -56,6 +66,7 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
     r = hq // hkv
     groups = _groups(offsets)
     items: List[Tuple[int, ...]] = []
+    branch_of_item = {}  # response-key items: index of the branch whose tiles they walk
     if op == OP_PREFILL_FWD:
         for g, grp in enumerate(groups):
             for t in range(_cdiv(grp["lp"], bm)):
@@ -90,7 +101,7 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
                 e = grp["ends"][_branch_of(grp, k_hi - 1)]
                 qa = (k_lo - grp["r0"]) // bm
                 qb = _cdiv(e - grp["r0"], bm)
-                resp_items.append((g, j, qa, qb))
+                resp_items.append((g, j, qa, qb, _branch_of(grp, k_lo)))
                 total += (qb - qa) * r * hkv
         target = max(r, _cdiv(total, 2 * num_sms))
         for g, grp in enumerate(groups):
@@ -112,9 +123,10 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
                     own = nqp - (j * bn) // bm if (tree and k == 0) else 0
                     for h in range(hkv):
                         items.append((TREE_PROMPT_KV if tree else PROMPT_KV, g, j, h, k, (qb - qa + own) * r, qa, qb))
-        for (g, j, qa, qb) in resp_items:
+        for (g, j, qa, qb, br) in resp_items:
             for h in range(hkv):
                 items.append((RESP_KV, g, j, h, 0, (qb - qa) * r, qa, qb))
+                branch_of_item[len(items) - 1] = br
     elif op == OP_PREFILL_BWD:
         for g, grp in enumerate(groups):
             nq = _cdiv(grp["lp"], bm)
@@ -124,9 +136,18 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
                     items.append((PREFILL_KV, g, j, h, 0, (nq - qa) * r, qa, nq))
     else:
         raise ValueError(op)
-    # Largest first; ties by (group, tile, kind, split, head).
-    items.sort(key=lambda it: (-it[5], it[1], it[2], it[0], it[4], it[3]))
-    return np.array(items, dtype=np.int32).reshape(-1, 8)
+    if op in (OP_PREFILL_FWD, OP_REPLAY_FWD):
+        # Largest first; ties by (group, tile, kind, split, head).
+        items.sort(key=lambda it: (-it[5], it[1], it[2], it[0], it[4], it[3]))
+        return np.array(items, dtype=np.int32).reshape(-1, 8)
+    # Key side: chunks of one stream (group, KV head, branch or -1), largest chunk first.
+    chunk = [(it[1], it[3], branch_of_item.get(i, -1)) for i, it in enumerate(items)]
+    total = {}
+    for c, it in zip(chunk, items):
+        total[c] = total.get(c, 0) + it[5]
+    order = sorted(range(len(items)), key=lambda i: (-total[chunk[i]], chunk[i], -items[i][5], items[i][2],
+                                                     items[i][0], items[i][4]))
+    return np.array([items[i] for i in order], dtype=np.int32).reshape(-1, 8)
 
 
 def splits_per_group(queue: np.ndarray, n_groups: int) -> List[int]:

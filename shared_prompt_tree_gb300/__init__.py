@@ -81,6 +81,7 @@ _SIGS = {
     "augtree_lse_merge": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 6 + [_P],
     "augtree_lse_merge_bwd": [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [_P] * 10 + [_P],
     "augtree_plan_check": [_P, _P],
+    "augtree_plan_set_wait_limit": [_P, ctypes.c_uint64],
     "augtree_plan_set_timing": [_P, ctypes.c_int32],
     "augtree_plan_kernel_times": [_P, ctypes.c_int32, ctypes.c_int32, _P, _P, ctypes.c_int32,
                                   ctypes.POINTER(ctypes.c_int32)],
@@ -220,6 +221,11 @@ class Plan:
         _check(lib().augtree_plan_kernel_times(self.handle, op, back, ctypes.cast(kind, _P), ctypes.cast(ms, _P), 8,
                                                ctypes.byref(n)), "augtree_plan_kernel_times")
         return [(KERNEL_IDS.get(kind[i], str(kind[i])), float(ms[i])) for i in range(n.value)]
+
+    def set_wait_limit(self, ns: int):
+        """Limit in nanoseconds of a device-side wait on another warp's work (2 s by
+        default); a kernel that runs past it gives up and check() raises ERR_TIMEOUT."""
+        _check(lib().augtree_plan_set_wait_limit(self.handle, int(ns)), "augtree_plan_set_wait_limit")
 
     def check(self, stream=None):
         """Synchronize and raise if a kernel of this plan recorded a device-side error."""

@@ -12,6 +12,8 @@
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <tuple>
+#include <utility>
 
 #include "internal.h"
 
@@ -106,8 +108,6 @@ void tiles_for(int family, int op, int* bm, int* bn) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-constexpr bool kUsePairForward = false;
-
 }  // namespace
 
 namespace augtree {
@@ -119,11 +119,16 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   read_groups(po, bb, ro, groups);
   const int r = hq / hkv;
   std::vector<Item> items;
-  auto push = [&](int kind, int g, int64_t tile, int head, int split, int64_t cost, int64_t a, int64_t b) {
+  // Key-side queues: the branch (index within the group) whose query tiles a response-key
+  // item walks, -1 for prompt-key items (they walk the group's query tiles).
+  std::vector<int32_t> walk_branch;
+  auto push = [&](int kind, int g, int64_t tile, int head, int split, int64_t cost, int64_t a, int64_t b,
+                  int branch = -1) {
     Item it;
     it.w[0] = kind; it.w[1] = g; it.w[2] = (int32_t)tile; it.w[3] = head;
     it.w[4] = split; it.w[5] = (int32_t)cost; it.w[6] = (int32_t)a; it.w[7] = (int32_t)b;
     items.push_back(it);
+    walk_branch.push_back(branch);
   };
   const int ng = (int)groups.size();
   if (op == AUGTREE_OP_PREFILL_FWD) {
@@ -151,7 +156,7 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
     // Costs before splitting fix the split target (replay items only, in both queues).
     const bool tree = op == AUGTREE_OP_TREE_BWD;
     int64_t total = 0;
-    struct RI { int g; int64_t j, qa, qb; };
+    struct RI { int g; int64_t j, qa, qb; int br; };
     std::vector<RI> resp;
     for (int g = 0; g < ng; ++g) {
       const Grp& G = groups[g];
@@ -164,7 +169,7 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
         int64_t e = G.ends[branch_of(G, k_hi - 1)];
         int64_t qa = (k_lo - G.r0) / bm;
         int64_t qb = cdiv(e - G.r0, bm);
-        resp.push_back({g, j, qa, qb});
+        resp.push_back({g, j, qa, qb, branch_of(G, k_lo)});
         total += (qb - qa) * r * hkv;
       }
     }
@@ -194,7 +199,7 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
         }
     }
     for (const RI& x : resp)
-      for (int h = 0; h < hkv; ++h) push(K_RESP_KV, x.g, x.j, h, 0, (x.qb - x.qa) * r, x.qa, x.qb);
+      for (int h = 0; h < hkv; ++h) push(K_RESP_KV, x.g, x.j, h, 0, (x.qb - x.qa) * r, x.qa, x.qb, x.br);
   } else if (op == AUGTREE_OP_PREFILL_BWD) {
     for (int g = 0; g < ng; ++g) {
       const Grp& G = groups[g];
@@ -207,16 +212,68 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   } else {
     return AUGTREE_ERR_INVALID_ARG;
   }
-  // Largest first; ties by (group, tile, kind, split, head).  The key is unique per
-  // item, so the order is fully determined.
-  std::sort(items.begin(), items.end(), [](const Item& x, const Item& y) {
-    if (x.w[5] != y.w[5]) return x.w[5] > y.w[5];
-    if (x.w[1] != y.w[1]) return x.w[1] < y.w[1];
-    if (x.w[2] != y.w[2]) return x.w[2] < y.w[2];
-    if (x.w[0] != y.w[0]) return x.w[0] < y.w[0];
-    if (x.w[4] != y.w[4]) return x.w[4] < y.w[4];
-    return x.w[3] < y.w[3];
-  });
+  if (op == AUGTREE_OP_PREFILL_FWD || op == AUGTREE_OP_REPLAY_FWD) {
+    // Largest first; ties by (group, tile, kind, split, head).  The key is unique per
+    // item, so the order is fully determined.
+    std::sort(items.begin(), items.end(), [](const Item& x, const Item& y) {
+      if (x.w[5] != y.w[5]) return x.w[5] > y.w[5];
+      if (x.w[1] != y.w[1]) return x.w[1] < y.w[1];
+      if (x.w[2] != y.w[2]) return x.w[2] < y.w[2];
+      if (x.w[0] != y.w[0]) return x.w[0] < y.w[0];
+      if (x.w[4] != y.w[4]) return x.w[4] < y.w[4];
+      return x.w[3] < y.w[3];
+    });
+  } else {
+    // Key side: items walk the Q/dO tiles of a stream - the group's query tiles for a
+    // KV head (prompt keys), or one branch's (response keys).  Items of one stream form
+    // a chunk; chunks run largest first (by total cost; ties by group, KV head, branch)
+    // and within a chunk items run largest first (ties by tile, kind, split).  Blocks
+    // that run side by side then mostly share one stream, which L2 holds once for all.
+    struct Key {
+      int64_t chunk_cost;
+      int32_t g, h, br;
+      size_t idx;
+    };
+    std::vector<Key> keys(items.size());
+    std::vector<std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>> totals;
+    {
+      std::vector<std::tuple<int32_t, int32_t, int32_t, int64_t>> cs(items.size());
+      for (size_t i = 0; i < items.size(); ++i)
+        cs[i] = std::make_tuple(items[i].w[1], items[i].w[3], walk_branch[i], (int64_t)items[i].w[5]);
+      std::sort(cs.begin(), cs.end());
+      for (size_t i = 0; i < cs.size();) {
+        size_t k = i;
+        int64_t tot = 0;
+        while (k < cs.size() && std::get<0>(cs[k]) == std::get<0>(cs[i]) && std::get<1>(cs[k]) == std::get<1>(cs[i]) &&
+               std::get<2>(cs[k]) == std::get<2>(cs[i]))
+          tot += std::get<3>(cs[k++]);
+        totals.push_back({std::make_tuple(std::get<0>(cs[i]), std::get<1>(cs[i]), std::get<2>(cs[i])), tot});
+        i = k;
+      }
+    }
+    for (size_t i = 0; i < items.size(); ++i) {
+      const auto c = std::make_tuple(items[i].w[1], items[i].w[3], walk_branch[i]);
+      auto pos = std::lower_bound(totals.begin(), totals.end(), c,
+                                  [](const std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>& e,
+                                     const std::tuple<int32_t, int32_t, int32_t>& v) { return e.first < v; });
+      keys[i] = Key{pos->second, items[i].w[1], items[i].w[3], walk_branch[i], i};
+    }
+    std::sort(keys.begin(), keys.end(), [&](const Key& x, const Key& y) {
+      if (x.chunk_cost != y.chunk_cost) return x.chunk_cost > y.chunk_cost;
+      if (x.g != y.g) return x.g < y.g;
+      if (x.h != y.h) return x.h < y.h;
+      if (x.br != y.br) return x.br < y.br;
+      const Item& a = items[x.idx];
+      const Item& b = items[y.idx];
+      if (a.w[5] != b.w[5]) return a.w[5] > b.w[5];
+      if (a.w[2] != b.w[2]) return a.w[2] < b.w[2];
+      if (a.w[0] != b.w[0]) return a.w[0] < b.w[0];
+      return a.w[4] < b.w[4];
+    });
+    std::vector<Item> sorted(items.size());
+    for (size_t i = 0; i < keys.size(); ++i) sorted[i] = items[keys[i].idx];
+    items.swap(sorted);
+  }
   out.resize(items.size() * AUGTREE_ITEM_WORDS);
   if (!items.empty()) std::memcpy(out.data(), items.data(), items.size() * sizeof(Item));
   return AUGTREE_OK;
@@ -457,7 +514,6 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   // items of a (group, tile) next to each other, so pairs are checked, not assumed.
   for (int op = 0; op < kNumOps; ++op) {
     p->paired[op] = 0;
-    p->quad[op] = 0;
     if (p->family != AUGTREE_KERNEL_TC || op > AUGTREE_OP_REPLAY_FWD) continue;
     const int r = cfg->hq / cfg->hkv;
     bool ok = (cfg->hq % 2 == 0) && (r % 2 == 0) && (p->n_items[op] % 2 == 0);
@@ -467,20 +523,6 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
       ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 2 == 0 && b[3] == a[3] + 1;
     }
     p->paired[op] = ok ? 1 : 0;
-    // Four-head units for the SM-pair kernel: heads 4k..4k+3 of one tile share a KV head
-    // when Hq/Hkv is a multiple of 4.
-    bool q4 = (cfg->hq % 4 == 0) && (r % 4 == 0) && (p->n_items[op] % 4 == 0);
-    for (size_t i = 0; q4 && i + 3 < p->n_items[op]; i += 4) {
-      const int32_t* a = &p->queue_h[op][i * AUGTREE_ITEM_WORDS];
-      for (int k = 1; k < 4 && q4; ++k) {
-        const int32_t* b = a + k * AUGTREE_ITEM_WORDS;
-        q4 = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 4 == 0 && b[3] == a[3] + k;
-      }
-    }
-    // The SM-pair kernel is correct but, with two softmax warpgroups per SM, slower than
-    // the single-CTA kernel on the measured configurations; it stays off until its
-    // softmax has more warps.
-    p->quad[op] = (q4 && kUsePairForward) ? 1 : 0;
   }
   // Split-K bookkeeping from the replay backward queue.
   p->splits_h.assign(std::max(1, p->n_groups), SplitInfo{0, 0, 0});
@@ -506,7 +548,10 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
                 p->groups_h.size() * sizeof(GroupInfo));
   ok = ok && up((void**)&p->row_bstart_d, bstart.data(), bstart.size() * sizeof(int32_t));
   ok = ok && up((void**)&p->row_bend_d, bend.data(), bend.size() * sizeof(int32_t));
-  ok = ok && up((void**)&p->err_d, pad.data(), sizeof(uint32_t));
+  // Error block: word 0 error bits, word 1 reserved, words 2-3 the wait limit (ns).
+  const uint64_t lim = kDefaultWaitLimitNs;
+  const uint32_t err_init[4] = {0u, 0u, (uint32_t)lim, (uint32_t)(lim >> 32)};
+  ok = ok && up((void**)&p->err_d, err_init, sizeof(err_init));
   ok = ok && up((void**)&p->splits_d, p->splits_h.data(), p->splits_h.size() * sizeof(SplitInfo));
   for (int op = 0; op < kNumOps && ok; ++op)
     ok = up((void**)&p->queue_d[op], p->queue_h[op].empty() ? (const void*)pad.data() : p->queue_h[op].data(),
@@ -842,6 +887,14 @@ augtree_status augtree_plan_kernel_times(const augtree_plan* p, int32_t op, int3
     ++written;
   }
   *n = written;
+  return AUGTREE_OK;
+}
+
+augtree_status augtree_plan_set_wait_limit(augtree_plan* p, uint64_t ns) {
+  if (!p || ns == 0 || ns > kMaxWaitLimitNs) return AUGTREE_ERR_INVALID_ARG;
+  augtree_status st = check_device(p);
+  if (st != AUGTREE_OK) return st;
+  if (cudaMemcpy(p->err_d + 2, &ns, sizeof(ns), cudaMemcpyHostToDevice) != cudaSuccess) return AUGTREE_ERR_CUDA;
   return AUGTREE_OK;
 }
 

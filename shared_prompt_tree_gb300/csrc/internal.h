@@ -14,6 +14,9 @@ namespace augtree {
 enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3, K_PREFILL_KV = 4, K_TREE_PROMPT_KV = 5 };
 constexpr int kNumOps = 5;  // queues per plan: the four calls' ops and the fused backward
 constexpr int kMaxSplit = 64;
+// Limit of a device-side wait on another warp's work: default and largest settable.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+constexpr uint64_t kMaxWaitLimitNs = 60000000000ull;
 
 // Per-group geometry on the device: first prompt row, prompt length, first response
 // row, total response length of the group's branches, and the group's first 128-row
@@ -64,9 +67,8 @@ struct augtree_plan {
   augtree::SplitInfo* splits_d;
   int32_t* queue_d[augtree::kNumOps];
   int paired[augtree::kNumOps];      // forward tensor-core units take two items (two heads of one KV head)
-  int quad[augtree::kNumOps];        // forward units of four items (four heads of one KV head) for SM pairs
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
-  uint32_t* err_d;    // error word written by kernels that gave up on a bounded wait
+  uint32_t* err_d;    // error block: word 0 error bits written by kernels, words 2-3 the wait limit (ns)
   // Device address of the library's fixed scratch array (augtree_prefill_bwd_static),
   // looked up at plan creation on the plan's device; null if that lookup failed.
   void* static_scratch;
@@ -133,13 +135,9 @@ bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads,
 bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads, int box_rows);
 
 // ---- launchers (return cudaGetLastError() of their launches) ---------------------
-// Forward on SM pairs (2-CTA clusters): used when the queue groups into four-head units.
-// One query head per block, double-buffered S (tc_fwd1.cu).
-cudaError_t tc_fwd1(const augtree_plan* p, int op, const CUtensorMap& mq, const CUtensorMap& mkp,
-                    const CUtensorMap& mvp, const CUtensorMap& mkr, const CUtensorMap& mvr, void* o, float* lse,
-                    int64_t q_rows, cudaStream_t st);
-cudaError_t tc_fwd2(const augtree_plan* p, int op, const CUtensorMap& mq, const void* kp, const void* vp,
-                    const void* kr, const void* vr, void* o, float* lse, int64_t q_rows, cudaStream_t st);
+// Forward on SM pairs (2-CTA clusters, one query head per CTA) for paired queues.
+cudaError_t tc_fwdp(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
+                    const void* vr, void* o, float* lse, cudaStream_t st);
 // SIMT family (any dtype).
 cudaError_t simt_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
                      const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);

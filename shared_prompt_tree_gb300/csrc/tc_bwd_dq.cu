@@ -77,8 +77,11 @@ struct DqBars {
   uint64_t ds_ready[2];
   uint64_t dq_done[2];
   uint64_t acc_done;
+  uint64_t drain;        // every S / dP MMA of the first issuer has completed
   uint32_t tmem_base;
 };
+
+static_assert(sizeof(DqBars) <= 256, "barrier area");
 
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       mbar_init(&bars->dq_done[b], 1);
     }
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->drain, 1);
     fence_mbar_init();
   }
   if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
@@ -184,10 +188,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
           }
         }
       }
-      // Never leave a copy in flight.
-      mbar_wait(&bars->q_full, 0, err);
-      for (int j = max(0, k_issued - KST); j < k_issued; ++j) mbar_wait(&bars->k_full[j % KST], (j / KST) & 1, err);
-      for (int j = max(0, v_issued - VST); j < v_issued; ++j) mbar_wait(&bars->v_full[j % VST], (j / VST) & 1, err);
+      // Never leave a copy in flight (also after giving up on a wait).
+      mbar_wait_drain(&bars->q_full, 0, err);
+      for (int j = max(0, k_issued - KST); j < k_issued; ++j)
+        mbar_wait_drain(&bars->k_full[j % KST], (j / KST) & 1, err);
+      for (int j = max(0, v_issued - VST); j < v_issued; ++j)
+        mbar_wait_drain(&bars->v_full[j % VST], (j / VST) & 1, err);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer: S, dP
@@ -234,6 +240,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         tc_fence_after();
         issue_dp(j + 1);
       }
+      // Never leave an MMA in flight when the block frees TMEM and exits (also after
+      // giving up on a wait).
+      mma_commit(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, err);
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ MMA issuer: dQ
@@ -261,8 +271,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         mma_commit(&bars->k_empty[j % KST]);
       }
       // Every MMA of the item is complete once the last dQ is: the other issuer's S and
-      // dP of the last tile completed before its dS was written.
+      // dP of the last tile completed before its dS was written.  Wait for it here too, so
+      // that no MMA of this thread is in flight when the block frees TMEM.
       mma_commit(&bars->acc_done);
+      mbar_wait_drain(&bars->acc_done, 0, err);
     }
   } else {
     // ------------------------------------------------------------ P, dS (thread = row)
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     const int c0 = 64 * w;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!(ok = mbar_wait(&bars->s_full, j & 1, err))) break;
+      if (!(ok = mbar_wait_warp_all(&bars->s_full, j & 1, err))) break;
       tc_fence_after();
       const uint32_t ts = tmem + lane_off + T_S + c0;
       const uint32_t tdp = tmem + lane_off + T_DP + (j & 1) * 128 + c0;
@@ -318,7 +330,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
           sv[c >> 5][c & 31] = __float_as_uint(v ? e : 0.f);
         }
       }
-      if (!(ok = mbar_wait(&bars->dp_full[j & 1], (j >> 1) & 1, err))) break;
+      if (!(ok = mbar_wait_warp_all(&bars->dp_full[j & 1], (j >> 1) & 1, err))) break;
       tc_fence_after();
       uint32_t pk[2][16];  // dS as bf16 pairs
 #pragma unroll
@@ -347,7 +359,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       mbar_arrive(&bars->ds_ready[j & 1]);
     }
     // dQ rows: warpgroup w writes dims [64w, 64w + 64) of its rows.
-    if (ok && mbar_wait(&bars->acc_done, 0, err)) {
+    if (ok && mbar_wait_warp_all(&bars->acc_done, 0, err)) {
       tc_fence_after();
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {

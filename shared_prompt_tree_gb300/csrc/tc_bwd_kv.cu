@@ -115,8 +115,11 @@ struct KvBars {
   uint64_t acc_done;
   uint64_t flush_ready;  // dK/dV accumulators complete up to a flush point
   uint64_t flushed;      // compute warps have moved them to the slot
+  uint64_t drain;        // every S^T / dP^T MMA of the first issuer has completed
   uint32_t tmem_base;
 };
+
+static_assert(sizeof(KvBars) <= 512, "barrier area");
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -178,18 +181,20 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   asm("mov.u32 %0, %%smid;" : "=r"(smid));
   const bool flush_on = n_iter > kFlush && (int)smid < n_slots;
   if (n_iter > kFlush && (int)smid >= n_slots && threadIdx.x == 0) atomicOr(err, 2u);
-  // Iteration i: query head kvh*r + i / nph; within a head the primary tiles b - 1 down
-  // to a, then the secondary tiles qb2 - 1 down to qa2.  Tiles are walked from the last
-  // one down, so blocks that start together (largest first) and share a KV head meet the
-  // same query rows at about the same time: their Q/dO reads then hit the same L2 lines.
+  // Iteration i: query tile l = i / r of the walk, query head kvh*r + i % r (the r heads
+  // of one tile back to back); the walk takes the primary tiles b - 1 down to a, then
+  // the secondary tiles qb2 - 1 down to qa2.  Every item of a (group, KV head) thus walks
+  // the same sequence of Q/dO tiles from the same first tile and only stops at its own
+  // last one: blocks of one (group, KV head) that run side by side stay in step and read
+  // each tile from L2 once for all of them (the work queue keeps such items together).
   struct QTile {
     int h, qt;
     bool sec;
   };
   auto qtile = [&](int i) {
     QTile t;
-    const int l = i % nph;
-    t.h = kvh * r + i / nph;
+    const int l = i / r;
+    t.h = kvh * r + i % r;
     t.sec = l >= nqt;
     t.qt = t.sec ? qb2 - 1 - (l - nqt) : it.b - 1 - l;
     return t;
@@ -212,6 +217,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->flush_ready, 1);
     mbar_init(&bars->flushed, 128 * NWG);
+    mbar_init(&bars->drain, 1);
     fence_mbar_init();
   }
   {
@@ -290,9 +296,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
           bulk_prefetch(ap + kStatRows * 16, AUG_ROWS);
         }
       }
-      // Never leave a copy in flight.
-      mbar_wait(&bars->kv_full, 0, err);
-      for (int i = max(0, issued - NQ); i < issued; ++i) mbar_wait(&bars->q_full[i % NQ], (i / NQ) & 1, err);
+      // Never leave a copy in flight (also after giving up on a wait).
+      mbar_wait_drain(&bars->kv_full, 0, err);
+      for (int i = max(0, issued - NQ); i < issued; ++i) mbar_wait_drain(&bars->q_full[i % NQ], (i / NQ) & 1, err);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer: S^T, dP^T
@@ -346,6 +352,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         tc_fence_after();
         issue_dp(i + 1);
       }
+      // Never leave an MMA in flight when the block frees TMEM and exits (also after
+      // giving up on a wait).
+      mma_commit(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, err);
     }
   } else if (warp == MMA2_WARP) {
     // ------------------------------------------------------------ MMA issuer: dV, dK
@@ -395,8 +405,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         mma_commit(&bars->q_empty[stage]);
         if (flush_on && i % kFlush == kFlush - 1 && more) mma_commit(&bars->flush_ready);
       }
-      // All MMAs of the item are complete once the last dK is.
+      // All MMAs of the item are complete once the last dK is.  Wait for that here too,
+      // so that no MMA of this thread is in flight when the block frees TMEM (also after
+      // giving up on a wait).
       mma_commit(&bars->acc_done);
+      mbar_wait_drain(&bars->acc_done, 0, err);
     }
   } else {
     // ------------------------------------------------------------ P^T and dS^T
@@ -425,13 +438,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     const uint32_t acc_col = (po < 128 ? T_DK : T_DV) + (po & 127);
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
-      const int l = i % nph;
+      const int l = i / r;
       const bool sec = l >= nqt;
       const int64_t row0 = sec ? (int64_t)G.p0 + (int64_t)(qb2 - 1 - (l - nqt)) * bm : qbase + (int64_t)(it.b - 1 - l) * bm;
       const int64_t v_lo = sec ? q_lo2 : q_lo, v_hi = sec ? q_hi2 : q_hi;
       const int b = kv_buf(i);
       const uint32_t ts = tmem + lane_off + T_ST + b * 64 + c0, tdp = tmem + lane_off + T_DPT + b * 64 + c0;
-      if (!(ok = mbar_wait(&bars->s_full[b], kv_phase(i), err))) break;
+      if (!(ok = mbar_wait_warp_all(&bars->s_full[b], kv_phase(i), err))) break;
       tc_fence_after();
       uint32_t sraw[COLS / 32][32];
 #pragma unroll
@@ -470,7 +483,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       tc_fence_before();
       mbar_arrive(&bars->p_ready[b]);
       // dS^T = P^T (dP^T - Delta), with the same bf16 P the dV product uses
-      if (!(ok = mbar_wait(&bars->dp_full[b], kv_phase(i), err))) break;
+      if (!(ok = mbar_wait_warp_all(&bars->dp_full[b], kv_phase(i), err))) break;
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < COLS / 32; ++k) tmem_ld32(tdp + 32 * k, sraw[k]);
@@ -491,7 +504,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       if (flush_on && i % kFlush == kFlush - 1 && i + 1 < n_iter) {
         // Move this warpgroup's share of dK/dV to this block's slot (the first flush
         // stores, later ones add).
-        if (!(ok = mbar_wait(&bars->flush_ready, (i / kFlush) & 1, err))) break;
+        if (!(ok = mbar_wait_warp_all(&bars->flush_ready, (i / kFlush) & 1, err))) break;
         tc_fence_after();
         float* slot = slots + ((int64_t)smid * 128 + t) * 256 + po;
         const bool first = i == kFlush - 1;
@@ -517,7 +530,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       }
     }
     // This warpgroup's share of the key's dK (scaled by s) / dV row
-    if (ok && mbar_wait(&bars->acc_done, 0, err) && n_iter > 0) {
+    if (ok && mbar_wait_warp_all(&bars->acc_done, 0, err) && n_iter > 0) {
       tc_fence_after();
       const bool is_dk = po < 128;
       const int col0 = po & 127;

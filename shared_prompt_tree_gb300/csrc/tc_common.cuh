@@ -11,12 +11,15 @@
 namespace augtree {
 namespace tc {
 
-// Error word bits written by a kernel that gave up on a wait.
+// The plan's error block (16 bytes of device memory): word 0 holds error bits written
+// by kernels (bit 0: a bounded wait gave up), word 1 is reserved, words 2-3 hold the
+// limit in nanoseconds of a wait on another warp's work (augtree_plan_set_wait_limit,
+// 2 s by default).
 constexpr uint32_t kErrTimeout = 1u;
-// A wait gives up after this many nanoseconds of %globaltimer (about 2 s): no wait in
-// these kernels legitimately lasts longer than a kernel.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
+// Limit of a drain wait: a wait for this block's own bulk copies or MMAs to finish
+// before it frees TMEM and exits.  Copies and MMAs always complete on their own, so
+// these waits never take the (possibly very short) runtime limit.
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -52,19 +55,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity.  Returns false (and sets the error
-// word) if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* err) {
+  return *reinterpret_cast<const volatile uint64_t*>(err + 2);
+}
+// Polls until the phase completes or lim_ns have passed since the first failed poll;
+// returns false (and sets the error bit) if it gave up.
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* err, uint64_t lim_ns) {
   const uint64_t t0 = globaltimer();
   while (true) {
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 4; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > lim_ns) {
       atomicOr(err, kErrTimeout);
       return false;
     }
   }
+}
+// Bounded wait for the phase with the given parity (another warp's work): the plan's
+// runtime limit, read only once the first poll has failed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err, wait_limit_ns(err));
+}
+// Wait for this thread's own copies or MMAs to land (fixed limit, see kDrainLimitNs).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err, kDrainLimitNs);
 }
 
 // mbar_wait for a whole warp that must stay converged (the MMA-issuing warp): lane 0
@@ -77,9 +93,14 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, u
 }
 
 // Same, every lane polling: measured faster for the forward's issuing warp, whose waits
-// are few per MMA.
+// are few per MMA.  Code that every lane of a warp runs (softmax and compute warps,
+// which go on to warp-collective tcgen05.ld/st and votes) waits with this form, so
+// that a wait that gives up does so for the whole warp, never for some lanes only.
 __device__ __forceinline__ bool mbar_wait_warp_all(uint64_t* bar, uint32_t parity, uint32_t* err) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+__device__ __forceinline__ bool mbar_wait_drain_warp_all(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  return __all_sync(0xffffffffu, mbar_wait_drain(bar, parity, err));
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {

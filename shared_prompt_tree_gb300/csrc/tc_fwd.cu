@@ -44,12 +44,11 @@ using namespace tc;
 #define AUGTREE_FWD_PINGPONG 1
 #endif
 constexpr bool kFwdPingPong = AUGTREE_FWD_PINGPONG != 0;
-// One query head per block with a double-buffered S (tc_fwd1.cu) instead of two heads
-// per block.
-#ifndef AUGTREE_FWD_ONE_HEAD
-#define AUGTREE_FWD_ONE_HEAD 0
+// Paired queues (two heads of one KV head per unit) run on SM pairs (tc_fwdp.cu).
+#ifndef AUGTREE_FWD_PAIR
+#define AUGTREE_FWD_PAIR 0
 #endif
-constexpr bool kOneHeadForward = AUGTREE_FWD_ONE_HEAD != 0;
+constexpr bool kFwdPair = AUGTREE_FWD_PAIR != 0;
 constexpr int FWD_THREADS = 352;  // 8 softmax warps, producer, one MMA issuer per head
 constexpr int NST = 2;                  // K/V ring stages
 constexpr int TILE_BYTES = 128 * 128;   // one 128-row x 64-column bf16 block = 16 KB
@@ -67,8 +66,11 @@ struct FwdBars {
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t turn[2];  // softmax hand-off: turn[s] completes when head s may run its exponentials
+  uint64_t drain[2];  // issuer s: all of its MMAs have completed (before TMEM is freed)
   uint32_t tmem_base;
 };
+
+static_assert(sizeof(FwdBars) <= 256, "barrier area");
 
 __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
@@ -107,6 +109,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
       mbar_init(&bars->p_full[i], 128);
       mbar_init(&bars->o_done[i], 1);
       mbar_init(&bars->turn[i], 4);
+      mbar_init(&bars->drain[i], 1);
     }
     fence_mbar_init();
   }
@@ -144,9 +147,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
         }
         issued = j + 1;
       }
-      // Never leave a copy in flight: wait for the last fill of every stage used.
-      mbar_wait(&bars->q_full, 0, err);
-      for (int j = max(0, issued - NST); j < issued; ++j) mbar_wait(&bars->kv_full[j % NST], (j / NST) & 1, err);
+      // Never leave a copy in flight (also after giving up on a wait): wait for the last
+      // fill of every stage used.
+      mbar_wait_drain(&bars->q_full, 0, err);
+      for (int j = max(0, issued - NST); j < issued; ++j)
+        mbar_wait_drain(&bars->kv_full[j % NST], (j / NST) & 1, err);
     }
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
@@ -188,6 +193,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
         mma_commit_w(&bars->o_done[s]);
         mma_commit_w(&bars->kv_empty[stage]);
       }
+      // Never leave an MMA in flight when the block frees TMEM and exits (also after
+      // giving up on a wait).
+      mma_commit_w(&bars->drain[s]);
+      mbar_wait_drain_warp_all(&bars->drain[s], 0, err);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -275,11 +284,11 @@ bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int he
 
 cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
                    const void* vr, void* o, float* lse, cudaStream_t st) {
+  if (kFwdPair && p->paired[op]) return tc_fwdp(p, op, q, kp, vp, kr, vr, o, lse, st);
   const bool prefill = op == AUGTREE_OP_PREFILL_FWD;
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
   CUtensorMap mq, mkp, mvp, mkr, mvr;
   if (!encode_rows_map(&mq, q, q_rows, p->cfg.hq, 128)) return cudaErrorInvalidValue;
-  if (p->quad[op]) return tc_fwd2(p, op, mq, kp, vp, kr, vr, o, lse, q_rows, st);
   const bool have_p = p->total_prompt > 0 && kp && vp;
   const bool have_r = !prefill && p->total_resp > 0 && kr && vr;
   if (have_p) {
@@ -299,7 +308,6 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
     mkr = mkp;
     mvr = mvp;
   }
-  if (kOneHeadForward) return tc_fwd1(p, op, mq, mkp, mvp, mkr, mvr, o, lse, q_rows, st);
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;
   const int paired = p->paired[op];

@@ -1,5 +1,6 @@
 // The softmax warpgroup of the tensor-core forward kernels (one and two CTAs per MMA):
-// one thread per query row (TMEM lane), shared by tc_fwd.cu and tc_fwd2.cu.
+// one thread per query row (TMEM lane), shared by the forward kernel and the
+// query side of the backward (its row geometry).
 //
 // AugTree paper, Sec. 2.2 (online softmax over Q-KV tiles), Sec. 3.2 Eq. 1 (the row's
 // valid keys: the whole prompt of its group, then its own branch up to itself; causal
@@ -89,7 +90,7 @@ struct PingPong {
   int first;
   __device__ __forceinline__ bool wait(int j, uint32_t* err) const {
     const int n = j - first;
-    return n < 0 || mbar_wait(mine, n & 1, err);
+    return n < 0 || mbar_wait_warp_all(mine, n & 1, err);
   }
   __device__ __forceinline__ void pass() const {
     __syncwarp();
@@ -111,7 +112,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
   float m = -INFINITY, l = 0.f;
   bool ok = true;
   for (int j = 0; j < n_tiles; ++j) {
-    if (!(ok = mbar_wait(s_full, j & 1, err))) break;
+    if (!(ok = mbar_wait_warp_all(s_full, j & 1, err))) break;
     tc_fence_after();
     uint32_t raw[4][32];  // S row, reinterpreted as fp32 in place (no second copy)
 #pragma unroll
@@ -177,7 +178,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     if (__any_sync(0xffffffffu, need)) {
       // O += P(j-1) V must be complete before O is rescaled; PV(j) is issued only
       // after this row's warpgroup signals P(j).
-      if (!(ok = mbar_wait(o_done, (j - 1) & 1, err))) break;
+      if (!(ok = mbar_wait_warp_all(o_done, (j - 1) & 1, err))) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -193,7 +194,7 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     tc_fence_before();
     signal_p();
   }
-  if (ok && mbar_wait(o_done, (n_tiles - 1) & 1, err)) {
+  if (ok && mbar_wait_warp_all(o_done, (n_tiles - 1) & 1, err)) {
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1

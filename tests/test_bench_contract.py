@@ -86,3 +86,18 @@ def test_launch_count_of_one_step():
     assert bench.count_launches(_FakePlan(tree, True), _Ops, fused=True) == 2 + 6
     # two calls: replay 4 (preprocess, key side, split reduce, query side), prefill 3
     assert bench.count_launches(_FakePlan(tree, False), _Ops, fused=False) == 2 + 4 + 3
+
+
+def test_gpus_flag_launches_that_many_ranks():
+    """`bench.py --gpus 2` without a launcher re-runs itself under torch.distributed.run
+    with two ranks (CPU here: the reference arm, whose rank 0 alone works and prints)."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.strip().splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2

@@ -36,7 +36,42 @@ def valid_pairs(tree):
 
 
 def check_order(q):
+    """Forward queues: largest first, ties by (group, tile, kind, split, head)."""
     keys = [(-int(it[5]), int(it[1]), int(it[2]), int(it[0]), int(it[4]), int(it[3])) for it in q]
+    assert keys == sorted(keys)
+
+
+def key_side_stream(tree, bn, it):
+    """The Q/dO stream a key-side item walks, from the tree alone: (group, KV head, -1)
+    for prompt keys (the group's query tiles), (group, KV head, branch) for response
+    keys (the branch holding the tile's first key, empty branches skipped)."""
+    kind, g, tile = int(it[0]), int(it[1]), int(it[2])
+    if kind != S.RESP_KV:
+        return (g, int(it[3]), -1)
+    key = tile * bn
+    pos = 0
+    for i, li in enumerate(tree.branch_lens[g]):
+        if pos <= key < pos + li:
+            return (g, int(it[3]), i)
+        pos += li
+    raise AssertionError("tile outside its group's branches")
+
+
+def check_key_side_order(q, tree, bn):
+    """Key-side queues: the items of one stream are contiguous; streams come in order of
+    decreasing total cost (ties by group, KV head, branch); within a stream items come
+    largest first (ties by tile, kind, split)."""
+    streams = [key_side_stream(tree, bn, it) for it in q]
+    total = {}
+    for s_, it in zip(streams, q):
+        total[s_] = total.get(s_, 0) + int(it[5])
+    seen, prev = set(), None
+    for s_ in streams:
+        if s_ != prev:
+            assert s_ not in seen, "a stream's items are split apart"
+            seen.add(s_)
+            prev = s_
+    keys = [(-total[s_], s_, -int(it[5]), int(it[2]), int(it[0]), int(it[4])) for s_, it in zip(streams, q)]
     assert keys == sorted(keys)
 
 
@@ -115,7 +150,7 @@ def test_backward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv, sms):
     r = hq // hkv
     for op in (S.OP_REPLAY_BWD, S.OP_PREFILL_BWD):
         q = S.build(offs, hq, hkv, op, bm, bn, num_sms=sms)
-        check_order(q)
+        check_key_side_order(q, tree, bn)
         covered = set()
         split_ranges = {}
         for it in q:
@@ -171,7 +206,7 @@ def test_fused_backward_queue_covers_every_pair_once(ti, bm, bn, hq, hkv, sms):
     offs = tree.offsets()
     r = hq // hkv
     q = S.build(offs, hq, hkv, S.OP_TREE_BWD, bm, bn, num_sms=sms)
-    check_order(q)
+    check_key_side_order(q, tree, bn)
     rb = S.build(offs, hq, hkv, S.OP_REPLAY_BWD, bm, bn, num_sms=sms)
     nsplit = {}
     for it in rb:
@@ -219,15 +254,19 @@ def test_fused_backward_queue_covers_every_pair_once(ti, bm, bn, hq, hkv, sms):
 
 
 def test_lpt_order_meets_the_list_scheduling_bound():
-    """Items are taken largest first (Sec. 3.4).  Any list schedule on m lanes has
-    makespan <= total/m + largest item; LPT order must also be non-increasing."""
+    """Items are taken largest first (Sec. 3.4): globally in the forward queues, within
+    each stream in the key-side ones.  Any list schedule on m lanes has makespan <=
+    total/m + largest item."""
     import heapq
     tree = W.Tree([300, 20], [[37, 200, 5, 90], [400, 3]])
     offs = tree.offsets()
     for op in (S.OP_PREFILL_FWD, S.OP_REPLAY_FWD, S.OP_REPLAY_BWD, S.OP_PREFILL_BWD, S.OP_TREE_BWD):
         q = S.build(offs, 4, 2, op, 16, 16, num_sms=4)
         costs = [int(c) for c in q[:, 5]]
-        assert costs == sorted(costs, reverse=True)
+        if op in (S.OP_PREFILL_FWD, S.OP_REPLAY_FWD):
+            assert costs == sorted(costs, reverse=True)
+        else:
+            check_key_side_order(q, tree, 16)
         m = 8
         lanes = [0] * m
         for c in costs:
