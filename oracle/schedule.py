@@ -13,14 +13,14 @@ tile interactions, and blocks take items in order of decreasing weight.
 The item encoding, split rule and tie-break order are the library contract written
 out below in plain Python loops; the comparison with the library is bit for bit.
 
-Order.  Forward queues: largest first, ties by (group, tile, kind, split, head).
-Key-side backward queues: every item walks the Q/dO tiles of one stream - the group's
-query tiles for its KV head (prompt-key items) or its own branch's (response-key
-items).  The items of a stream form a chunk; chunks go largest first by their total
-cost (ties by group, KV head, branch, with -1 for the group-wide stream), and items
-within a chunk largest first (ties by tile, kind, split).  This keeps largest-first
-balancing within a chunk and makes the blocks that run side by side share one stream
-(cache locality of the on-chip scheduling; the pages' balancing is across lanes of a
+Order.  Every item walks the tiles of one stream: a forward item the K/V of its
+group's KV head (query head h uses KV head h // r); a key-side item the Q/dO tiles of
+its group for its KV head (prompt keys) or of its own branch (response keys).  The
+items of a stream form a chunk; chunks go largest first by their total cost (ties by
+group, KV head, branch, with -1 for a group-wide stream), and items within a chunk
+largest first (ties by tile, kind, split, head).  This keeps largest-first balancing
+within a chunk and makes the blocks that run side by side share one stream (cache
+locality of the on-chip scheduling; the pages' balancing is across lanes of a
 multi-node cluster and says nothing about it).
 """
 from __future__ import annotations
@@ -136,17 +136,15 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
                     items.append((PREFILL_KV, g, j, h, 0, (nq - qa) * r, qa, nq))
     else:
         raise ValueError(op)
-    if op in (OP_PREFILL_FWD, OP_REPLAY_FWD):
-        # Largest first; ties by (group, tile, kind, split, head).
-        items.sort(key=lambda it: (-it[5], it[1], it[2], it[0], it[4], it[3]))
-        return np.array(items, dtype=np.int32).reshape(-1, 8)
-    # Key side: chunks of one stream (group, KV head, branch or -1), largest chunk first.
-    chunk = [(it[1], it[3], branch_of_item.get(i, -1)) for i, it in enumerate(items)]
+    # Chunks of one stream: (group, KV head, branch or -1), largest chunk first; items
+    # within a chunk largest first, ties by (tile, kind, split, head).
+    fwd = op in (OP_PREFILL_FWD, OP_REPLAY_FWD)
+    chunk = [(it[1], it[3] // r if fwd else it[3], branch_of_item.get(i, -1)) for i, it in enumerate(items)]
     total = {}
     for c, it in zip(chunk, items):
         total[c] = total.get(c, 0) + it[5]
     order = sorted(range(len(items)), key=lambda i: (-total[chunk[i]], chunk[i], -items[i][5], items[i][2],
-                                                     items[i][0], items[i][4]))
+                                                     items[i][0], items[i][4], items[i][3]))
     return np.array([items[i] for i in order], dtype=np.int32).reshape(-1, 8)
 
 

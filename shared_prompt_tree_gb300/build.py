@@ -44,8 +44,8 @@ def is_stale() -> bool:
     return any(os.path.getmtime(f) > t for f in sources() + headers() + [os.path.abspath(__file__)])
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra, build_dir: str = None) -> str:
+    obj = os.path.join(build_dir or BUILD, os.path.basename(src) + ".o")
     cmd = [nvcc(), "-c", src, "-o", obj, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
            "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")] + ARCH + list(extra)
     if src.endswith(".cpp"):
@@ -73,6 +73,22 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
+
+
+def build_variant(defines, out_dir: str) -> str:
+    """Builds the library with extra preprocessor definitions (for example
+    "-DAUGTREE_CHECKED=1", the checked build) into out_dir/libaugtree.so; objects go to
+    out_dir as well.  Returns the library's path."""
+    os.makedirs(out_dir, exist_ok=True)
+    srcs = sources()
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+        objs = list(ex.map(lambda s: _compile(s, list(defines), out_dir), srcs))
+    lib = os.path.join(out_dir, "libaugtree.so")
+    r = subprocess.run([nvcc(), "-shared", "-o", lib] + objs + ARCH + ["-Xcompiler", "-fPIC"], capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return lib
 
 
 if __name__ == "__main__":

@@ -47,4 +47,62 @@ __device__ __forceinline__ WorkItem load_item(const int32_t* q, int64_t i) {
   return WorkItem{x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 }
 
+// ---- Checked build (-DAUGTREE_CHECKED=1) ------------------------------------------
+// Every kernel validates its work item against the plan's geometry before it uses any
+// row or key index the item implies.  A failing item sets kErrCheck in the plan's error
+// word (augtree_plan_check then returns AUGTREE_ERR_DEVICE_CHECK) and is skipped: the
+// kernel does no work for it and writes nothing, so no access leaves the tensors.  No
+// trap is ever raised.  The default build compiles the checks out.
+#ifndef AUGTREE_CHECKED
+#define AUGTREE_CHECKED 0
+#endif
+constexpr bool kChecked = AUGTREE_CHECKED != 0;
+constexpr uint32_t kErrCheck = 4u;
+
+__device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// A query-side item (PREFILL_Q or REPLAY_Q; forward and query-side backward): group and
+// head in range, its query tile inside its group, its KV tile counts those of the
+// encoding, its first row's branch start inside the group and not after the row.
+__device__ __forceinline__ bool query_item_ok(const WorkItem& it, const Geometry& geo, int bm, int bn) {
+  const bool prefill = it.kind == K_PREFILL_Q;
+  if (!prefill && it.kind != K_REPLAY_Q) return false;
+  if (it.group < 0 || it.group >= geo.n_groups || it.head < 0 || it.head >= geo.hq) return false;
+  const GroupInfo G = geo.groups[it.group];
+  const int64_t base = prefill ? G.p0 : G.r0, len = prefill ? G.lp : G.lr;
+  const int64_t total = prefill ? geo.total_prompt : geo.total_resp;
+  if (G.p0 < 0 || G.lp < 0 || G.r0 < 0 || G.lr < 0 || base + len > total) return false;
+  if (it.tile < 0 || (int64_t)it.tile * bm >= len) return false;
+  const int64_t row0 = base + (int64_t)it.tile * bm;
+  const int64_t row_end = min(row0 + (int64_t)bm, base + len);
+  if (prefill) return it.a == ceil_div64(row_end - G.p0, bn) && it.b == 0;
+  if (it.a != ceil_div64(G.lp, bn) || (int64_t)G.p0 + G.lp > geo.total_prompt) return false;
+  const int64_t own0 = geo.row_bstart[row0];
+  if (own0 < G.r0 || own0 > row0) return false;
+  return it.b == ceil_div64(row_end - own0, bn);
+}
+
+// A key-side item (PROMPT_KV, RESP_KV, PREFILL_KV, TREE_PROMPT_KV): group and KV head in
+// range, its KV tile inside its group's keys, its query tiles [a, b) inside the query
+// side it walks, its split below the group's split count.
+__device__ __forceinline__ bool key_item_ok(const WorkItem& it, const Geometry& geo, int bm, int bn) {
+  if (it.kind != K_PROMPT_KV && it.kind != K_RESP_KV && it.kind != K_PREFILL_KV && it.kind != K_TREE_PROMPT_KV)
+    return false;
+  if (it.group < 0 || it.group >= geo.n_groups || it.head < 0 || it.head >= geo.hkv) return false;
+  const GroupInfo G = geo.groups[it.group];
+  if (G.p0 < 0 || G.lp < 0 || G.r0 < 0 || G.lr < 0) return false;
+  if ((int64_t)G.p0 + G.lp > geo.total_prompt || (int64_t)G.r0 + G.lr > geo.total_resp) return false;
+  const bool resp_keys = it.kind == K_RESP_KV;
+  if (it.tile < 0 || (int64_t)it.tile * bn >= (resp_keys ? G.lr : G.lp)) return false;
+  const int64_t nq = ceil_div64(it.kind == K_PREFILL_KV ? G.lp : G.lr, bm);
+  if (it.a < 0 || it.a > it.b || it.b > nq) return false;
+  if (it.kind == K_PROMPT_KV || it.kind == K_TREE_PROMPT_KV) {
+    const int nsplit = geo.splits ? geo.splits[it.group].nsplit : 1;
+    if (it.split < 0 || it.split >= (nsplit > 1 ? nsplit : 1)) return false;
+  } else if (it.split != 0) {
+    return false;
+  }
+  return true;
+}
+
 }  // namespace augtree

@@ -212,68 +212,59 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   } else {
     return AUGTREE_ERR_INVALID_ARG;
   }
-  if (op == AUGTREE_OP_PREFILL_FWD || op == AUGTREE_OP_REPLAY_FWD) {
-    // Largest first; ties by (group, tile, kind, split, head).  The key is unique per
-    // item, so the order is fully determined.
-    std::sort(items.begin(), items.end(), [](const Item& x, const Item& y) {
-      if (x.w[5] != y.w[5]) return x.w[5] > y.w[5];
-      if (x.w[1] != y.w[1]) return x.w[1] < y.w[1];
-      if (x.w[2] != y.w[2]) return x.w[2] < y.w[2];
-      if (x.w[0] != y.w[0]) return x.w[0] < y.w[0];
-      if (x.w[4] != y.w[4]) return x.w[4] < y.w[4];
-      return x.w[3] < y.w[3];
-    });
-  } else {
-    // Key side: items walk the Q/dO tiles of a stream - the group's query tiles for a
-    // KV head (prompt keys), or one branch's (response keys).  Items of one stream form
-    // a chunk; chunks run largest first (by total cost; ties by group, KV head, branch)
-    // and within a chunk items run largest first (ties by tile, kind, split).  Blocks
-    // that run side by side then mostly share one stream, which L2 holds once for all.
-    struct Key {
-      int64_t chunk_cost;
-      int32_t g, h, br;
-      size_t idx;
-    };
-    std::vector<Key> keys(items.size());
-    std::vector<std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>> totals;
-    {
-      std::vector<std::tuple<int32_t, int32_t, int32_t, int64_t>> cs(items.size());
-      for (size_t i = 0; i < items.size(); ++i)
-        cs[i] = std::make_tuple(items[i].w[1], items[i].w[3], walk_branch[i], (int64_t)items[i].w[5]);
-      std::sort(cs.begin(), cs.end());
-      for (size_t i = 0; i < cs.size();) {
-        size_t k = i;
-        int64_t tot = 0;
-        while (k < cs.size() && std::get<0>(cs[k]) == std::get<0>(cs[i]) && std::get<1>(cs[k]) == std::get<1>(cs[i]) &&
-               std::get<2>(cs[k]) == std::get<2>(cs[i]))
-          tot += std::get<3>(cs[k++]);
-        totals.push_back({std::make_tuple(std::get<0>(cs[i]), std::get<1>(cs[i]), std::get<2>(cs[i])), tot});
-        i = k;
-      }
+  // Every item walks the K/V or Q/dO tiles of one stream: a forward item the K/V of its
+  // group's KV head, a key-side item the query tiles of its group for its KV head or,
+  // for response keys, of one branch.  Items of one stream form a chunk; chunks run
+  // largest first (by total cost; ties by group, KV head, branch with -1 for a
+  // group-wide stream), and items within a chunk largest first (ties by tile, kind,
+  // split, head).  Blocks that run side by side then mostly share one stream, which L2
+  // holds once for all of them; the queues stay balanced (largest first within chunks).
+  const bool fwd = op == AUGTREE_OP_PREFILL_FWD || op == AUGTREE_OP_REPLAY_FWD;
+  struct Key {
+    int64_t chunk_cost;
+    int32_t g, h, br;
+    size_t idx;
+  };
+  auto chunk_of = [&](size_t i) {
+    return std::make_tuple(items[i].w[1], fwd ? items[i].w[3] / r : items[i].w[3], walk_branch[i]);
+  };
+  std::vector<std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>> totals;
+  {
+    std::vector<std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>> cs(items.size());
+    for (size_t i = 0; i < items.size(); ++i) cs[i] = {chunk_of(i), (int64_t)items[i].w[5]};
+    std::sort(cs.begin(), cs.end());
+    for (size_t i = 0; i < cs.size();) {
+      size_t k = i;
+      int64_t tot = 0;
+      while (k < cs.size() && cs[k].first == cs[i].first) tot += cs[k++].second;
+      totals.push_back({cs[i].first, tot});
+      i = k;
     }
-    for (size_t i = 0; i < items.size(); ++i) {
-      const auto c = std::make_tuple(items[i].w[1], items[i].w[3], walk_branch[i]);
-      auto pos = std::lower_bound(totals.begin(), totals.end(), c,
-                                  [](const std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>& e,
-                                     const std::tuple<int32_t, int32_t, int32_t>& v) { return e.first < v; });
-      keys[i] = Key{pos->second, items[i].w[1], items[i].w[3], walk_branch[i], i};
-    }
-    std::sort(keys.begin(), keys.end(), [&](const Key& x, const Key& y) {
-      if (x.chunk_cost != y.chunk_cost) return x.chunk_cost > y.chunk_cost;
-      if (x.g != y.g) return x.g < y.g;
-      if (x.h != y.h) return x.h < y.h;
-      if (x.br != y.br) return x.br < y.br;
-      const Item& a = items[x.idx];
-      const Item& b = items[y.idx];
-      if (a.w[5] != b.w[5]) return a.w[5] > b.w[5];
-      if (a.w[2] != b.w[2]) return a.w[2] < b.w[2];
-      if (a.w[0] != b.w[0]) return a.w[0] < b.w[0];
-      return a.w[4] < b.w[4];
-    });
-    std::vector<Item> sorted(items.size());
-    for (size_t i = 0; i < keys.size(); ++i) sorted[i] = items[keys[i].idx];
-    items.swap(sorted);
   }
+  std::vector<Key> keys(items.size());
+  for (size_t i = 0; i < items.size(); ++i) {
+    const auto c = chunk_of(i);
+    auto pos = std::lower_bound(totals.begin(), totals.end(), c,
+                                [](const std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>& e,
+                                   const std::tuple<int32_t, int32_t, int32_t>& v) { return e.first < v; });
+    keys[i] = Key{pos->second, std::get<0>(c), std::get<1>(c), std::get<2>(c), i};
+  }
+  std::sort(keys.begin(), keys.end(), [&](const Key& x, const Key& y) {
+    if (x.chunk_cost != y.chunk_cost) return x.chunk_cost > y.chunk_cost;
+    if (x.g != y.g) return x.g < y.g;
+    if (x.h != y.h) return x.h < y.h;
+    if (x.br != y.br) return x.br < y.br;
+    const Item& a = items[x.idx];
+    const Item& b = items[y.idx];
+    if (a.w[5] != b.w[5]) return a.w[5] > b.w[5];
+    if (a.w[2] != b.w[2]) return a.w[2] < b.w[2];
+    if (a.w[0] != b.w[0]) return a.w[0] < b.w[0];
+    if (a.w[4] != b.w[4]) return a.w[4] < b.w[4];
+    return a.w[3] < b.w[3];
+  });
+  std::vector<Item> sorted(items.size());
+  for (size_t i = 0; i < keys.size(); ++i) sorted[i] = items[keys[i].idx];
+  items.swap(sorted);
   out.resize(items.size() * AUGTREE_ITEM_WORDS);
   if (!items.empty()) std::memcpy(out.data(), items.data(), items.size() * sizeof(Item));
   return AUGTREE_OK;
@@ -348,6 +339,7 @@ Geometry geometry(const augtree_plan* p) {
   g.d = p->cfg.head_dim;
   g.total_prompt = p->total_prompt;
   g.total_resp = p->total_resp;
+  g.n_groups = p->n_groups;
   g.scale = p->cfg.softmax_scale > 0.f ? p->cfg.softmax_scale : 1.0f / std::sqrt((float)p->cfg.head_dim);
   g.scale_log2 = g.scale * 1.4426950408889634f;
   return g;

@@ -43,6 +43,7 @@ struct Geometry {
   const SplitInfo* splits;    // [n_groups] (replay backward only)
   int32_t hq, hkv, d;
   int32_t total_prompt, total_resp;
+  int32_t n_groups;
   float scale;                // softmax scale s
   float scale_log2;           // s * log2(e)
 };
@@ -135,9 +136,6 @@ bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads,
 bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int heads, int box_rows);
 
 // ---- launchers (return cudaGetLastError() of their launches) ---------------------
-// Forward on SM pairs (2-CTA clusters, one query head per CTA) for paired queues.
-cudaError_t tc_fwdp(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                    const void* vr, void* o, float* lse, cudaStream_t st);
 // SIMT family (any dtype).
 cudaError_t simt_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
                      const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);

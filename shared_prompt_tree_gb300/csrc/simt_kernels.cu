@@ -47,10 +47,14 @@ template <typename T, int D>
 __global__ void __launch_bounds__(SIMT_THREADS) simt_fwd_kernel(
     Geometry geo, const int32_t* __restrict__ queue, int bm, int bn, const T* __restrict__ q,
     const T* __restrict__ kp, const T* __restrict__ vp, const T* __restrict__ kr, const T* __restrict__ vr,
-    T* __restrict__ o, float* __restrict__ lse, int64_t lse_rows) {
+    T* __restrict__ o, float* __restrict__ lse, int64_t lse_rows, uint32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtFwdSmem<D>& sm = *reinterpret_cast<SimtFwdSmem<D>*>(smem_raw);
   const WorkItem it = load_item(queue, blockIdx.x);
+  if (kChecked && !query_item_ok(it, geo, bm, bn)) {  // checked build only; block-uniform
+    if (threadIdx.x == 0) atomicOr(err, kErrCheck);
+    return;
+  }
   const GroupInfo G = geo.groups[it.group];
   const int r = geo.hq / geo.hkv;
   const int h = it.head, kvh = h / r;
@@ -161,10 +165,14 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_bwd_kernel(
     const float* __restrict__ lse, const T* __restrict__ dO, const float* __restrict__ delta,
     float* __restrict__ dq_acc, T* __restrict__ dk_out, T* __restrict__ dv_out, float* __restrict__ dk_part,
     float* __restrict__ dv_part, float* __restrict__ dk_sum, float* __restrict__ dv_sum,
-    const float* __restrict__ dk_add, const float* __restrict__ dv_add) {
+    const float* __restrict__ dk_add, const float* __restrict__ dv_add, uint32_t* __restrict__ err) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtBwdSmem<D>& sm = *reinterpret_cast<SimtBwdSmem<D>*>(smem_raw);
   const WorkItem it = load_item(queue, blockIdx.x);
+  if (kChecked && !key_item_ok(it, geo, bm, bn)) {  // checked build only; block-uniform
+    if (threadIdx.x == 0) atomicOr(err, kErrCheck);
+    return;
+  }
   const GroupInfo G = geo.groups[it.group];
   const int r = geo.hq / geo.hkv;
   const int kvh = it.head;
@@ -299,7 +307,7 @@ cudaError_t fwd_launch(const augtree_plan* p, int op, const void* q, const void*
   const int64_t rows = op == AUGTREE_OP_PREFILL_FWD ? p->total_prompt : p->total_resp;
   simt_fwd_kernel<T, D><<<(unsigned)p->n_items[op], SIMT_THREADS, smem, st>>>(
       geometry(p), p->queue_d[op], p->bm[op], p->bn[op], (const T*)q, (const T*)kp, (const T*)vp, (const T*)kr,
-      (const T*)vr, (T*)o, lse, rows);
+      (const T*)vr, (T*)o, lse, rows, p->err_d);
   return cudaGetLastError();
 }
 
@@ -314,7 +322,7 @@ cudaError_t bwd_launch(const augtree_plan* p, int op, const void* q, const void*
   simt_bwd_kernel<T, D><<<(unsigned)p->n_items[op], SIMT_THREADS, smem, st>>>(
       geometry(p), p->queue_d[op], p->bm[op], p->bn[op], (const T*)q, (const T*)kp, (const T*)vp, (const T*)kr,
       (const T*)vr, lse, (const T*)dO, delta, dq_acc, (T*)dk_out, (T*)dv_out, dk_part, dv_part, dk_sum, dv_sum,
-      dk_add, dv_add);
+      dk_add, dv_add, p->err_d);
   return cudaGetLastError();
 }
 

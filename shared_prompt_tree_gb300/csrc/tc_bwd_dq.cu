@@ -83,12 +83,6 @@ struct DqBars {
 
 static_assert(sizeof(DqBars) <= 256, "barrier area");
 
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
 
 __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -102,16 +96,18 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const WorkItem it = load_item(queue, blockIdx.x);
-  const int h = it.head;
-  const GroupInfo G = geo.groups[it.group];
+  const bool item_ok = !kChecked || query_item_ok(it, geo, bm, bn);  // checked build only
+  if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
+  const int h = item_ok ? it.head : 0;
+  const GroupInfo G = geo.groups[item_ok ? it.group : 0];
   const bool prefill = it.kind == K_PREFILL_Q;
   const int64_t base = prefill ? G.p0 : G.r0;
   const int64_t len = prefill ? G.lp : G.lr;
-  const int64_t row0 = base + (int64_t)it.tile * bm;
-  const int64_t row_end = min(row0 + (int64_t)bm, base + len);
-  const int n_a = it.a;
-  const int n_tiles = n_a + (prefill ? 0 : it.b);
-  const int64_t own0 = prefill ? 0 : geo.row_bstart[row0];
+  const int64_t row0 = item_ok ? base + (int64_t)it.tile * bm : 0;
+  const int64_t row_end = item_ok ? min(row0 + (int64_t)bm, base + len) : 0;
+  const int n_a = item_ok ? it.a : 0;
+  const int n_tiles = item_ok ? n_a + (prefill ? 0 : it.b) : 0;
+  const int64_t own0 = (prefill || !item_ok) ? 0 : geo.row_bstart[row0];
   const int kvh = h / (geo.hq / geo.hkv);
 
   if (threadIdx.x == 0) {
@@ -293,7 +289,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     g.n_a = n_a;
     g.bn = bn;
     const int tile_base = prefill ? G.tp0 : G.tr0;
-    const float* st = stats + ((int64_t)h * ntiles + tile_base + it.tile) * 2 * kStatRows;
+    const float* st = stats + (item_ok ? ((int64_t)h * ntiles + tile_base + it.tile) * 2 * kStatRows : 0);
     const float lse2 = st[r_local];
     const float delta = st[kStatRows + r_local];
     const float sl2 = geo.scale_log2;

@@ -127,12 +127,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                : "memory");
@@ -155,14 +149,16 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const WorkItem it = load_item(queue, blockIdx.x);
-  const GroupInfo G = geo.groups[it.group];
+  const bool item_ok = !kChecked || key_item_ok(it, geo, bm, bn);  // checked build only
+  if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
+  const GroupInfo G = geo.groups[item_ok ? it.group : 0];
   const int r = geo.hq / geo.hkv;
-  const int kvh = it.head;
+  const int kvh = item_ok ? it.head : 0;
   const bool resp_keys = it.kind == K_RESP_KV;
   const bool prefill = it.kind == K_PREFILL_KV;
   const bool tree_p = it.kind == K_TREE_PROMPT_KV;
   const int64_t kbase = resp_keys ? G.r0 : G.p0;
-  const int64_t key0 = kbase + (int64_t)it.tile * bn;
+  const int64_t key0 = kbase + (item_ok ? (int64_t)it.tile * bn : 0);
   const int64_t key_end = min(key0 + (int64_t)bn, kbase + (int64_t)(resp_keys ? G.lr : G.lp));
   // Primary query tiles [a, b): prompt rows for PREFILL_KV, response rows otherwise.
   const int64_t qbase = prefill ? G.p0 : G.r0;
@@ -174,7 +170,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   const int qa2 = (int)(((int64_t)it.tile * bn) / bm);
   const int nqt2 = (tree_p && it.split == 0) ? qb2 - qa2 : 0;
   const int nph = nqt + nqt2;  // query tiles per query head
-  const int n_iter = nph * r;
+  const int n_iter = item_ok ? nph * r : 0;
   // One block per SM at a time (shared memory and TMEM), so the SM id names a private
   // flush slot.
   uint32_t smid;

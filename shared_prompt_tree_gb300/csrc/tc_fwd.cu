@@ -44,13 +44,17 @@ using namespace tc;
 #define AUGTREE_FWD_PINGPONG 1
 #endif
 constexpr bool kFwdPingPong = AUGTREE_FWD_PINGPONG != 0;
-// Paired queues (two heads of one KV head per unit) run on SM pairs (tc_fwdp.cu).
-#ifndef AUGTREE_FWD_PAIR
-#define AUGTREE_FWD_PAIR 0
-#endif
-constexpr bool kFwdPair = AUGTREE_FWD_PAIR != 0;
+
 constexpr int FWD_THREADS = 352;  // 8 softmax warps, producer, one MMA issuer per head
 constexpr int NST = 2;                  // K/V ring stages
+// K/V tiles this many ahead of the one being filled are prefetched into L2, so that a
+// refill (issued only once the stage frees) waits on L2 rather than DRAM latency.
+// Measured neutral on prompt-heavy (1,278 against 1,285 TFLOP/s without): the kernel
+// is not bound by load latency; kept off.
+#ifndef AUGTREE_FWD_PREFETCH
+#define AUGTREE_FWD_PREFETCH 0
+#endif
+constexpr int kFwdPrefetch = AUGTREE_FWD_PREFETCH;
 constexpr int TILE_BYTES = 128 * 128;   // one 128-row x 64-column bf16 block = 16 KB
 constexpr int Q_OFF = 0;                                  // [2 heads][2 blocks]
 constexpr int K_OFF = Q_OFF + 4 * TILE_BYTES;             // [NST][2 blocks]
@@ -84,18 +88,24 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
 
   const int n_sub = paired ? 2 : 1;
   const WorkItem it0 = load_item(queue, (int64_t)blockIdx.x * n_sub);
+  const WorkItem it1 = paired ? load_item(queue, (int64_t)blockIdx.x * 2 + 1) : it0;
+  // Checked build: both items valid, and the same query tile (heads of one KV head).
+  const bool item_ok = !kChecked || (query_item_ok(it0, geo, bm, bn) && query_item_ok(it1, geo, bm, bn) &&
+                                     it1.kind == it0.kind && it1.group == it0.group && it1.tile == it0.tile &&
+                                     it1.head / (geo.hq / geo.hkv) == it0.head / (geo.hq / geo.hkv));
+  if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
   int heads[2];
-  heads[0] = it0.head;
-  heads[1] = paired ? load_item(queue, (int64_t)blockIdx.x * 2 + 1).head : it0.head;
-  const GroupInfo G = geo.groups[it0.group];
+  heads[0] = item_ok ? it0.head : 0;
+  heads[1] = item_ok ? it1.head : 0;
+  const GroupInfo G = geo.groups[item_ok ? it0.group : 0];
   const bool prefill = it0.kind == K_PREFILL_Q;
   const int64_t base = prefill ? G.p0 : G.r0;
   const int64_t len = prefill ? G.lp : G.lr;
-  const int64_t row0 = base + (int64_t)it0.tile * bm;
-  const int64_t row_end = min(row0 + (int64_t)bm, base + len);
-  const int n_a = it0.a;
-  const int n_tiles = n_a + (prefill ? 0 : it0.b);
-  const int64_t own0 = prefill ? 0 : geo.row_bstart[row0];
+  const int64_t row0 = item_ok ? base + (int64_t)it0.tile * bm : 0;
+  const int64_t row_end = item_ok ? min(row0 + (int64_t)bm, base + len) : 0;
+  const int n_a = item_ok ? it0.a : 0;
+  const int n_tiles = item_ok ? n_a + (prefill ? 0 : it0.b) : 0;
+  const int64_t own0 = (prefill || !item_ok) ? 0 : geo.row_bstart[row0];
   const int kvh = heads[0] / (geo.hq / geo.hkv);
 
   if (threadIdx.x == 0) {
@@ -146,6 +156,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
           tma_load_3d(smem + V_OFF + (stage * 2 + kb) * TILE_BYTES, vm, &bars->kv_full[stage], kb * 64, kvh, krow);
         }
         issued = j + 1;
+        if (kFwdPrefetch > 0) {
+          // At the start, the first few tiles after the ring's; then one tile per fill.
+          const int jp0 = j == 0 ? NST : j + kFwdPrefetch;
+          for (int jp = jp0; jp <= j + kFwdPrefetch && jp < n_tiles; ++jp) {
+            const bool own_p = jp >= n_a;
+            const int rp = own_p ? (int)(own0 + (int64_t)(jp - n_a) * bn) : (int)(G.p0 + (int64_t)jp * bn);
+            for (int kb = 0; kb < 2; ++kb) {
+              tma_prefetch_3d(own_p ? &tm_kr : &tm_kp, kb * 64, kvh, rp);
+              tma_prefetch_3d(own_p ? &tm_vr : &tm_vp, kb * 64, kvh, rp);
+            }
+          }
+        }
       }
       // Never leave a copy in flight (also after giving up on a wait): wait for the last
       // fill of every stage used.
@@ -284,7 +306,6 @@ bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int he
 
 cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
                    const void* vr, void* o, float* lse, cudaStream_t st) {
-  if (kFwdPair && p->paired[op]) return tc_fwdp(p, op, q, kp, vp, kr, vr, o, lse, st);
   const bool prefill = op == AUGTREE_OP_PREFILL_FWD;
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
   CUtensorMap mq, mkp, mvp, mkr, mvr;
