@@ -242,12 +242,12 @@ class Run:
     (prefill fwd, replay fwd, then one augtree_tree_bwd call, or replay_bwd +
     prefill_bwd)."""
 
-    def __init__(self, w, at, dev, kernel, fused=True):
+    def __init__(self, w, at, dev, kernel, fused=True, schedule=0):
         import torch
         import workloads as W
         self.w, self.at, self.dev, self.fused = w, at, dev, fused
         dt = at.BF16 if w.dtype == "bf16" else at.FP32
-        self.plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt, kernel=kernel)
+        self.plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=dt, kernel=kernel, schedule=schedule)
         self.t = {n: W.tensor_torch(w, n, dev) for n in W.TENSORS}
         t = self.t
         f32 = torch.float32
@@ -413,7 +413,8 @@ def run_ours(args):
         w = scaled_down(w, args.scale_down)
     kernel = {"auto": at.KERNEL_AUTO, "simt": at.KERNEL_SIMT, "tc": at.KERNEL_TC}[args.kernel]
     fused = args.bwd == "fused"
-    run = Run(w, at, dev, kernel, fused)
+    sched = {"queue": at.SCHED_QUEUE, "persistent": at.SCHED_PERSISTENT}[args.schedule]
+    run = Run(w, at, dev, kernel, fused, sched)
     m = measure(run, args.steps, args.warmup, world, local)
     ms_step = m["ms"]
 
@@ -428,7 +429,7 @@ def run_ours(args):
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in run.outputs())
     e_steps = max(2, min(args.steps, 10))
-    runs = [run, Run(w, at, dev, kernel, fused)]
+    runs = [run, Run(w, at, dev, kernel, fused, sched)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
     in_done, comp_done, out_done = [ev() for _ in range(e_steps)], [ev() for _ in range(e_steps)], \
@@ -499,6 +500,7 @@ def run_ours(args):
                    "total_resp": w.tree.total_resp, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
                    "parallelism": f"replicas x{world}", "kernel_family": args.kernel,
                    "backward": "one augtree_tree_bwd call" if fused else "augtree_replay_bwd + augtree_prefill_bwd",
+                   "schedule": args.schedule,
                    "l2": "inputs larger than L2 (no flush)"},
         "tokens_per_s": round(w.tokens * world / (ms_step * 1e-3), 1),
         "flattened_tokens_per_s": round(w.tree.flattened_tokens() * world / (ms_step * 1e-3), 1),
@@ -519,7 +521,7 @@ def run_ours(args):
         # shared-prompt tree over flattening, measured with the same kernels and the same
         # fused backward.
         wf = flattened(w)
-        rf = Run(wf, at, dev, kernel, fused)
+        rf = Run(wf, at, dev, kernel, fused, sched)
         mf = measure(rf, max(1, min(args.steps, 3)), 1, world, local, sample_clocks=False)
         rf.close()
         result["flattened_per_pair"] = {
@@ -533,7 +535,7 @@ def run_ours(args):
         for name in [n for n in ("prompt_heavy", "response_heavy", "mixed", "long") if n != w.name]:
             wo = W.workload(name)
             st, wu = (2, 1) if name == "long" else (args.steps, args.warmup)
-            ro = Run(wo, at, dev, kernel, fused)
+            ro = Run(wo, at, dev, kernel, fused, sched)
             mo = measure(ro, st, wu, world, local)
             ro.close()
             tf = useful_flops(wo) * world / (mo["ms"] * 1e-3) / 1e12
@@ -648,6 +650,8 @@ def main():
     ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
     ap.add_argument("--bwd", choices=["fused", "two-call"], default="fused",
                     help="backward as one augtree_tree_bwd call, or replay_bwd then prefill_bwd")
+    ap.add_argument("--schedule", choices=["queue", "persistent"], default="queue",
+                    help="one block per work unit (queue) or persistent blocks on AssignGrid lanes")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scale-down", type=int, default=1, help="divide every length by this (profiling only)")

@@ -63,6 +63,20 @@ typedef enum { AUGTREE_FP32 = 0, AUGTREE_BF16 = 1 } augtree_dtype;
  * cores for bf16 with head_dim 128, SIMT otherwise. */
 typedef enum { AUGTREE_KERNEL_AUTO = 0, AUGTREE_KERNEL_SIMT = 1, AUGTREE_KERNEL_TC = 2 } augtree_kernel;
 
+/* Scheduling of the tensor-core kernels' work units (augtree_config.schedule).
+ *   QUEUE       one thread block per unit, taken in queue order by the hardware block
+ *               scheduler as SMs free up (the default; the dynamic largest-first greedy).
+ *   PERSISTENT  the backward's key-side and query-side kernels run one persistent thread
+ *               block per lane (num_sms lanes), each walking a fixed list of units:
+ *               AssignGrid (Sec. 3.4, Eq. 6; augtree_assign_grid) places the queue's
+ *               units on lanes, exactly when a queue has at most
+ *               AUGTREE_LANES_EXACT_UNITS units, by the largest-first greedy otherwise
+ *               (augtree_schedule_lanes exports the placement).  The forward keeps one
+ *               block per unit, and the SIMT kernels ignore it.  Measured slower than
+ *               QUEUE on every configuration; an option, not the default. */
+typedef enum { AUGTREE_SCHED_QUEUE = 0, AUGTREE_SCHED_PERSISTENT = 1 } augtree_schedule;
+#define AUGTREE_LANES_EXACT_UNITS 12
+
 /* Operations, used to select a work queue or a workspace size. */
 typedef enum {
   AUGTREE_OP_PREFILL_FWD = 0,
@@ -97,7 +111,7 @@ typedef struct {
   float softmax_scale;   /* 0 => 1/sqrt(head_dim) (Sec. 2.2)                    */
   int32_t num_sms;       /* balancing width of the work queues; 0 => device SMs */
   int32_t kernel;        /* augtree_kernel                                      */
-  int32_t reserved;      /* must be 0                                           */
+  int32_t schedule;      /* augtree_schedule (0: one block per unit)             */
 } augtree_config;
 
 typedef struct augtree_plan augtree_plan;
@@ -162,6 +176,20 @@ augtree_status augtree_tile_sizes(const augtree_config* cfg, int32_t op, int32_t
 augtree_status augtree_schedule_build(const augtree_desc* desc, const augtree_config* cfg,
                                       int32_t op, int32_t* out, size_t cap_items,
                                       size_t* n_items);
+
+/* Host-only, no GPU needed: the persistent schedule's placement of a kernel's work
+ * units on lanes (cfg->schedule is ignored; cfg->num_sms lanes, must be > 0).
+ * kernel_id selects the kernel: AUGTREE_KID_BWD_QUERY_SIDE (op 0 or 1, the forward queue
+ * the query side walks) or AUGTREE_KID_BWD_KEY_SIDE (op 2, 3 or 4); a unit is one queue
+ * item.  Unit weights are the items' costs; AssignGrid
+ * places U units on L = min(num_sms, U) lanes of ceil(U / L) rounds, exactly when U <=
+ * AUGTREE_LANES_EXACT_UNITS, else by its largest-first greedy.  Out (CSR): lane l runs
+ * units[lane_off[l] .. lane_off[l+1]) in round order; lane_off needs n_lanes + 1 entries
+ * (cap_lanes), units n_units (cap_units).  AUGTREE_ERR_CAPACITY (with *n_lanes, *n_units
+ * set) when a buffer is too small. */
+augtree_status augtree_schedule_lanes(const augtree_desc* desc, const augtree_config* cfg, int32_t op,
+                                      int32_t kernel_id, int32_t* lane_off, size_t cap_lanes, int32_t* units,
+                                      size_t cap_units, size_t* n_lanes, size_t* n_units);
 
 /* AssignGrid (Sec. 3.4, Eq. 6), host only, no GPU needed: places n_units replay units
  * with work estimates w[n_units] (>= 0) on a grid of `rounds` x `lanes` cells, at most

@@ -28,6 +28,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEV
     ERR_CAPACITY = range(8)
 FP32, BF16 = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC = 0, 1, 2
+SCHED_QUEUE, SCHED_PERSISTENT = 0, 1
+LANES_EXACT_UNITS = 12
+KID_FWD_TC, KID_BWD_KEY_SIDE, KID_BWD_QUERY_SIDE = 1, 4, 6
 OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD, OP_TREE_BWD = 0, 1, 2, 3, 4
 # augtree_kernel_id: kinds reported by augtree_plan_kernel_times
 KERNEL_IDS = {1: "fwd_tc", 2: "fwd_simt", 3: "preprocess", 4: "bwd_key_side", 5: "split_reduce",
@@ -53,7 +56,7 @@ class Desc(ctypes.Structure):
 class Config(ctypes.Structure):
     _fields_ = [("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float), ("num_sms", ctypes.c_int32),
-                ("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("kernel", ctypes.c_int32), ("schedule", ctypes.c_int32)]
 
 
 _lib = None
@@ -66,6 +69,8 @@ _SIGS = {
                            ctypes.POINTER(ctypes.c_int32)],
     "augtree_schedule_build": [ctypes.POINTER(Desc), ctypes.POINTER(Config), ctypes.c_int32, _P, _SZ,
                                ctypes.POINTER(_SZ)],
+    "augtree_schedule_lanes": [ctypes.POINTER(Desc), ctypes.POINTER(Config), ctypes.c_int32, ctypes.c_int32, _P, _SZ,
+                               _P, _SZ, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)],
     "augtree_assign_grid": [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
                             ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)],
     "augtree_plan_create": [ctypes.POINTER(Desc), ctypes.POINTER(Config), ctypes.POINTER(_P)],
@@ -131,8 +136,9 @@ def make_desc(prompt_off, branch_begin, resp_off):
     return d, (po, bb, ro)
 
 
-def make_config(hq, hkv, head_dim, dtype=BF16, softmax_scale=0.0, num_sms=0, kernel=KERNEL_AUTO):
-    return Config(hq, hkv, head_dim, dtype, softmax_scale, num_sms, kernel, 0)
+def make_config(hq, hkv, head_dim, dtype=BF16, softmax_scale=0.0, num_sms=0, kernel=KERNEL_AUTO,
+                schedule=SCHED_QUEUE):
+    return Config(hq, hkv, head_dim, dtype, softmax_scale, num_sms, kernel, schedule)
 
 
 def tile_sizes(cfg: Config, op: int):
@@ -152,6 +158,24 @@ def schedule_build(offsets, cfg: Config, op: int) -> np.ndarray:
     _check(lib().augtree_schedule_build(ctypes.byref(d), ctypes.byref(cfg), op, out.ctypes.data, n.value,
                                         ctypes.byref(n)), "augtree_schedule_build")
     return out[:n.value]
+
+
+def schedule_lanes(offsets, cfg: Config, op: int, kernel_id: int):
+    """Host-only persistent-schedule placement of a kernel's work units on lanes
+    (AssignGrid over the queue's unit costs).  Returns (lane_off int32 [n_lanes+1],
+    units int32 [n_units]): lane l runs units[lane_off[l]:lane_off[l+1]] in order."""
+    d, keep = make_desc(*offsets)
+    nl, nu = _SZ(), _SZ()
+    st = lib().augtree_schedule_lanes(ctypes.byref(d), ctypes.byref(cfg), op, kernel_id, None, 0, None, 0,
+                                      ctypes.byref(nl), ctypes.byref(nu))
+    if st not in (OK, ERR_CAPACITY):
+        _check(st, "augtree_schedule_lanes")
+    off = np.zeros(nl.value + 1, dtype=np.int32)
+    units = np.zeros(max(1, nu.value), dtype=np.int32)
+    _check(lib().augtree_schedule_lanes(ctypes.byref(d), ctypes.byref(cfg), op, kernel_id, off.ctypes.data,
+                                        off.size, units.ctypes.data, units.size, ctypes.byref(nl),
+                                        ctypes.byref(nu)), "augtree_schedule_lanes")
+    return off, units[:nu.value]
 
 
 ASSIGN_GRID_MAX_EXACT = 16
@@ -178,8 +202,8 @@ class Plan:
     Must be created with the target CUDA device current."""
 
     def __init__(self, prompt_off, branch_begin, resp_off, hq, hkv, head_dim, dtype=BF16, softmax_scale=0.0,
-                 num_sms=0, kernel=KERNEL_AUTO):
-        self.cfg = make_config(hq, hkv, head_dim, dtype, softmax_scale, num_sms, kernel)
+                 num_sms=0, kernel=KERNEL_AUTO, schedule=SCHED_QUEUE):
+        self.cfg = make_config(hq, hkv, head_dim, dtype, softmax_scale, num_sms, kernel, schedule)
         d, (po, bb, ro) = make_desc(prompt_off, branch_begin, resp_off)
         self.prompt_off, self.branch_begin, self.resp_off = po, bb, ro
         self.total_prompt, self.total_resp = int(po[-1]), int(ro[-1])

@@ -76,7 +76,8 @@ augtree_status validate_desc(const augtree_desc* d, std::vector<int32_t>& po, st
 
 augtree_status validate_cfg(const augtree_config* c, bool need_sms) {
   if (!c) return AUGTREE_ERR_INVALID_ARG;
-  if (c->hq <= 0 || c->hkv <= 0 || c->reserved != 0) return AUGTREE_ERR_INVALID_ARG;
+  if (c->hq <= 0 || c->hkv <= 0) return AUGTREE_ERR_INVALID_ARG;
+  if (c->schedule != AUGTREE_SCHED_QUEUE && c->schedule != AUGTREE_SCHED_PERSISTENT) return AUGTREE_ERR_INVALID_ARG;
   if (c->num_sms < 0 || (need_sms && c->num_sms == 0)) return AUGTREE_ERR_INVALID_ARG;
   if (!(c->softmax_scale >= 0.0f) || std::isinf(c->softmax_scale)) return AUGTREE_ERR_INVALID_ARG;
   if (c->hq % c->hkv != 0) return AUGTREE_ERR_UNSUPPORTED;
@@ -270,6 +271,45 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   return AUGTREE_OK;
 }
 
+bool queue_pairs(const std::vector<int32_t>& q, int hq, int hkv) {
+  // Consecutive items 2i, 2i+1: the same kind, group and query tile, heads h and h + 1
+  // with h even; they then share a KV head when Hq / Hkv is even.
+  const size_t n = q.size() / AUGTREE_ITEM_WORDS;
+  const int r = hq / hkv;
+  bool ok = (hq % 2 == 0) && (r % 2 == 0) && (n % 2 == 0);
+  for (size_t i = 0; ok && i + 1 < n; i += 2) {
+    const int32_t* a = &q[i * AUGTREE_ITEM_WORDS];
+    const int32_t* b = a + AUGTREE_ITEM_WORDS;
+    ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 2 == 0 && b[3] == a[3] + 1;
+  }
+  return ok;
+}
+
+augtree_status build_lanes(const std::vector<int32_t>& q, int unit_items, int lanes, LaneSet& out) {
+  out.off.clear();
+  out.units.clear();
+  const int64_t n_units = (int64_t)(q.size() / AUGTREE_ITEM_WORDS) / unit_items;
+  if (n_units > INT32_MAX || lanes < 1) return AUGTREE_ERR_INVALID_ARG;
+  const int L = (int)std::min<int64_t>(lanes, n_units);
+  out.n_lanes = L;
+  out.off.assign((size_t)L + 1, 0);
+  if (n_units == 0) return AUGTREE_OK;
+  // Unit weight: its items' cost (the items of a unit share one tile, hence one cost).
+  std::vector<int64_t> w((size_t)n_units);
+  for (int64_t u = 0; u < n_units; ++u) w[u] = (int64_t)q[(size_t)u * unit_items * AUGTREE_ITEM_WORDS + 5] * unit_items;
+  const int rounds = (int)((n_units + L - 1) / L);
+  std::vector<int32_t> rnd((size_t)n_units), lane((size_t)n_units);
+  int64_t makespan = 0;
+  augtree_status st = augtree_assign_grid(w.data(), (int32_t)n_units, rounds, L, AUGTREE_LANES_EXACT_UNITS,
+                                          rnd.data(), lane.data(), &makespan, nullptr);
+  if (st != AUGTREE_OK) return st;
+  for (int64_t u = 0; u < n_units; ++u) out.off[lane[u] + 1] += 1;
+  for (int l = 0; l < L; ++l) out.off[l + 1] += out.off[l];
+  out.units.assign((size_t)n_units, 0);
+  for (int64_t u = 0; u < n_units; ++u) out.units[out.off[lane[u]] + rnd[u]] = (int32_t)u;
+  return AUGTREE_OK;
+}
+
 // Row statistics of the backward: SIMT kernels read Delta [Hq, rows]; tensor-core
 // kernels read tiles of {lse * log2(e), Delta} [Hq, tiles, 2 x 64] (one bulk copy each).
 static size_t stats_bytes(const augtree_plan* p, bool prompt_side) {
@@ -419,6 +459,37 @@ augtree_status augtree_schedule_build(const augtree_desc* desc, const augtree_co
   return AUGTREE_OK;
 }
 
+augtree_status augtree_schedule_lanes(const augtree_desc* desc, const augtree_config* cfg, int32_t op,
+                                      int32_t kernel_id, int32_t* lane_off, size_t cap_lanes, int32_t* units,
+                                      size_t cap_units, size_t* n_lanes, size_t* n_units) {
+  std::vector<int32_t> po, bb, ro;
+  augtree_status st = validate_desc(desc, po, bb, ro);
+  if (st != AUGTREE_OK) return st;
+  if ((st = validate_cfg(cfg, true)) != AUGTREE_OK) return st;
+  if (!n_lanes || !n_units || op < 0 || op >= kNumOps) return AUGTREE_ERR_INVALID_ARG;
+  const bool fwd_op = op <= AUGTREE_OP_REPLAY_FWD;
+  if (kernel_id != AUGTREE_KID_BWD_QUERY_SIDE && kernel_id != AUGTREE_KID_BWD_KEY_SIDE) return AUGTREE_ERR_INVALID_ARG;
+  if ((kernel_id == AUGTREE_KID_BWD_QUERY_SIDE) != fwd_op) return AUGTREE_ERR_INVALID_ARG;
+  int bm, bn;
+  tiles_for(resolve_family(cfg), op, &bm, &bn);
+  std::vector<int32_t> q;
+  LaneSet l;
+  try {
+    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, bm, bn, cfg->num_sms, q);
+    if (st != AUGTREE_OK) return st;
+    st = build_lanes(q, 1, cfg->num_sms, l);
+  } catch (const std::bad_alloc&) {
+    return AUGTREE_ERR_CAPACITY;
+  }
+  if (st != AUGTREE_OK) return st;
+  *n_lanes = (size_t)l.n_lanes;
+  *n_units = l.units.size();
+  if (*n_lanes + 1 > cap_lanes || *n_units > cap_units) return AUGTREE_ERR_CAPACITY;
+  if (lane_off) std::memcpy(lane_off, l.off.data(), l.off.size() * sizeof(int32_t));
+  if (units && !l.units.empty()) std::memcpy(units, l.units.data(), l.units.size() * sizeof(int32_t));
+  return AUGTREE_OK;
+}
+
 augtree_status augtree_plan_destroy(augtree_plan* p) {
   if (!p) return AUGTREE_ERR_INVALID_ARG;
   int cur = -1;
@@ -430,6 +501,14 @@ augtree_status augtree_plan_destroy(augtree_plan* p) {
   cudaFree(p->splits_d);
   cudaFree(p->err_d);
   for (int i = 0; i < kNumOps; ++i) cudaFree(p->queue_d[i]);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(p->lanes_dq[i].off_d);
+    cudaFree(p->lanes_dq[i].units_d);
+  }
+  for (int i = 0; i < kNumOps; ++i) {
+    cudaFree(p->lanes_kv[i].off_d);
+    cudaFree(p->lanes_kv[i].units_d);
+  }
   if (p->timing.created)
     for (int op = 0; op < kNumOps; ++op)
       for (int c = 0; c < AUGTREE_TIMING_RING; ++c)
@@ -507,14 +586,21 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   for (int op = 0; op < kNumOps; ++op) {
     p->paired[op] = 0;
     if (p->family != AUGTREE_KERNEL_TC || op > AUGTREE_OP_REPLAY_FWD) continue;
-    const int r = cfg->hq / cfg->hkv;
-    bool ok = (cfg->hq % 2 == 0) && (r % 2 == 0) && (p->n_items[op] % 2 == 0);
-    for (size_t i = 0; ok && i + 1 < p->n_items[op]; i += 2) {
-      const int32_t* a = &p->queue_h[op][i * AUGTREE_ITEM_WORDS];
-      const int32_t* b = a + AUGTREE_ITEM_WORDS;
-      ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 2 == 0 && b[3] == a[3] + 1;
+    p->paired[op] = queue_pairs(p->queue_h[op], cfg->hq, cfg->hkv) ? 1 : 0;
+  }
+  // Persistent schedule: AssignGrid's placement of every tensor-core kernel's units.
+  if (p->family == AUGTREE_KERNEL_TC && cfg->schedule == AUGTREE_SCHED_PERSISTENT) {
+    for (int op = 0; op < kNumOps && st == AUGTREE_OK; ++op) {
+      if (op <= AUGTREE_OP_REPLAY_FWD) {
+        st = build_lanes(p->queue_h[op], 1, p->cfg.num_sms, p->lanes_dq[op]);
+      } else {
+        st = build_lanes(p->queue_h[op], 1, p->cfg.num_sms, p->lanes_kv[op]);
+      }
     }
-    p->paired[op] = ok ? 1 : 0;
+    if (st != AUGTREE_OK) {
+      delete p;
+      return st;
+    }
   }
   // Split-K bookkeeping from the replay backward queue.
   p->splits_h.assign(std::max(1, p->n_groups), SplitInfo{0, 0, 0});
@@ -548,6 +634,14 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   for (int op = 0; op < kNumOps && ok; ++op)
     ok = up((void**)&p->queue_d[op], p->queue_h[op].empty() ? (const void*)pad.data() : p->queue_h[op].data(),
             p->queue_h[op].size() * sizeof(int32_t));
+  auto up_lanes = [&](LaneSet& l) -> bool {
+    if (l.off.empty()) return true;
+    return up((void**)&l.off_d, l.off.data(), l.off.size() * sizeof(int32_t)) &&
+           up((void**)&l.units_d, l.units.empty() ? (const void*)pad.data() : l.units.data(),
+              l.units.size() * sizeof(int32_t));
+  };
+  for (int op = 0; op < 2 && ok; ++op) ok = up_lanes(p->lanes_dq[op]);
+  for (int op = 0; op < kNumOps && ok; ++op) ok = up_lanes(p->lanes_kv[op]);
   if (!ok) {
     cudaGetLastError();
     augtree_plan_destroy(p);

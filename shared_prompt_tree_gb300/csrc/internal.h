@@ -48,6 +48,13 @@ struct Geometry {
   float scale_log2;           // s * log2(e)
 };
 
+// Persistent schedule: a kernel's units placed on lanes (one persistent block each).
+struct LaneSet {
+  std::vector<int32_t> off, units;  // CSR on the host: lane l runs units[off[l] .. off[l+1])
+  int32_t* off_d = nullptr;
+  int32_t* units_d = nullptr;
+  int32_t n_lanes = 0;
+};
 }  // namespace augtree
 
 struct augtree_plan {
@@ -70,6 +77,10 @@ struct augtree_plan {
   int paired[augtree::kNumOps];      // forward tensor-core units take two items (two heads of one KV head)
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error block: word 0 error bits written by kernels, words 2-3 the wait limit (ns)
+  // Persistent schedule (cfg.schedule == AUGTREE_SCHED_PERSISTENT, tensor-core family):
+  // lanes of the query-side backward (over the forward queues) and of the key-side
+  // backward, per op.
+  augtree::LaneSet lanes_dq[2], lanes_kv[augtree::kNumOps];
   // Device address of the library's fixed scratch array (augtree_prefill_bwd_static),
   // looked up at plan creation on the plan's device; null if that lookup failed.
   void* static_scratch;
@@ -89,6 +100,12 @@ struct augtree_plan {
 };
 
 namespace augtree {
+
+// Persistent schedule: places the units of `queue` (unit_items consecutive items each)
+// on min(lanes, U) lanes with augtree_assign_grid.
+augtree_status build_lanes(const std::vector<int32_t>& queue, int unit_items, int lanes, LaneSet& out);
+// Whether a forward queue pairs consecutive items (two heads of one KV head, one tile).
+bool queue_pairs(const std::vector<int32_t>& queue, int hq, int hkv);
 
 // Work-queue build shared by augtree_schedule_build and augtree_plan_create.
 augtree_status build_queue(const std::vector<int32_t>& prompt_off, const std::vector<int32_t>& branch_begin,

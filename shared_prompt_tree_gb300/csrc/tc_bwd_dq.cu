@@ -84,18 +84,27 @@ struct DqBars {
 static_assert(sizeof(DqBars) <= 256, "barrier area");
 
 
+template <bool kPersistent>
 __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
     const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
     const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr, Geometry geo,
     const int32_t* __restrict__ queue, int bm, int bn, const float* __restrict__ stats, int ntiles,
-    __nv_bfloat16* __restrict__ dq_out, uint32_t* __restrict__ err) {
+    __nv_bfloat16* __restrict__ dq_out, uint32_t* __restrict__ err,
+    const int32_t* __restrict__ sched_off, const int32_t* __restrict__ sched_units) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DqBars* bars = reinterpret_cast<DqBars*>(smem + DQ_BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // TMEM: allocated once for every unit of the lane (persistent schedule) or, as the
+  // block's first step, for its one unit (queue schedule, below).
+  if (kPersistent && warp == 9) tmem_alloc(&bars->tmem_base, 512);
+  // The queue schedule's instantiation runs exactly one unit (the loop folds away).
+  const int n_units = kPersistent ? sched_off[blockIdx.x + 1] - sched_off[blockIdx.x] : 1;
+  for (int u_i = 0; u_i < n_units; ++u_i) {
+  const int64_t unit = kPersistent ? (int64_t)sched_units[sched_off[blockIdx.x] + u_i] : (int64_t)blockIdx.x;
 
-  const WorkItem it = load_item(queue, blockIdx.x);
+  const WorkItem it = load_item(queue, unit);
   const bool item_ok = !kChecked || query_item_ok(it, geo, bm, bn);  // checked build only
   if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
   const int h = item_ok ? it.head : 0;
@@ -111,6 +120,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
   const int kvh = h / (geo.hq / geo.hkv);
 
   if (threadIdx.x == 0) {
+    if (kPersistent && u_i > 0) {
+      // Every wait, copy and MMA of the previous unit has ended (drains, then the
+      // block-wide barrier at its end): its barriers are idle and may be reused.
+      for (uint64_t* b = &bars->q_full; b < reinterpret_cast<uint64_t*>(&bars->tmem_base); ++b) mbar_inval(b);
+    }
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < KST; ++i) {
       mbar_init(&bars->k_full[i], 1);
@@ -131,7 +145,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     mbar_init(&bars->drain, 1);
     fence_mbar_init();
   }
-  if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
+  if (!kPersistent && warp == 9) tmem_alloc(&bars->tmem_base, 512);
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_do);
@@ -378,9 +392,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
   }
   tc_fence_before();
   __syncthreads();
+  }  // units of the lane
+  if (kPersistent) __syncthreads();  // an empty lane: the address is visible before it is freed
   if (warp == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(bars->tmem_base, 512);
   }
 }
 
@@ -414,11 +430,17 @@ cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* 
     mkr = mkp;
     mvr = mvp;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
+  // Persistent schedule: one block per lane, each walking its units.
+  const LaneSet& ls = p->lanes_dq[fop];
+  const bool persistent = ls.off_d != nullptr;
+  auto kern = persistent ? tc_bwd_dq_kernel<true> : tc_bwd_dq_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
   if (e != cudaSuccess) return e;
-  tc_bwd_dq_kernel<<<(unsigned)p->n_items[fop], DQ_THREADS, DQ_SMEM, st>>>(
+  const unsigned grid = persistent ? (unsigned)ls.n_lanes : (unsigned)p->n_items[fop];
+  kern<<<grid, DQ_THREADS, DQ_SMEM, st>>>(
       mq, mdo, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[fop], p->bm[fop], p->bn[fop], stats,
-      prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dq, p->err_d);
+      prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dq, p->err_d, persistent ? ls.off_d : nullptr,
+      persistent ? ls.units_d : nullptr);
   return cudaGetLastError();
 }
 

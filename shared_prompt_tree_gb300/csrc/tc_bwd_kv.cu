@@ -132,6 +132,7 @@ __device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
                : "memory");
 }
 
+template <bool kPersistent>
 __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -142,13 +143,21 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     __nv_bfloat16* __restrict__ dk_out, __nv_bfloat16* __restrict__ dv_out, __nv_bfloat16* __restrict__ dk2_out,
     __nv_bfloat16* __restrict__ dv2_out, float* __restrict__ dk_part, float* __restrict__ dv_part,
     float* __restrict__ dk_sum, float* __restrict__ dv_sum, const float* __restrict__ dk_add,
-    const float* __restrict__ dv_add, float* __restrict__ slots, int n_slots, uint32_t* __restrict__ err) {
+    const float* __restrict__ dv_add, float* __restrict__ slots, int n_slots, uint32_t* __restrict__ err,
+    const int32_t* __restrict__ sched_off, const int32_t* __restrict__ sched_units) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   KvBars* bars = reinterpret_cast<KvBars*>(smem + BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // TMEM: allocated once for every unit of the lane (persistent schedule) or, as the
+  // block's first step, for its one unit (queue schedule, below).
+  if (kPersistent && warp == MMA_WARP) tmem_alloc(&bars->tmem_base, 512);
+  // The queue schedule's instantiation runs exactly one unit (the loop folds away).
+  const int n_units = kPersistent ? sched_off[blockIdx.x + 1] - sched_off[blockIdx.x] : 1;
+  for (int u_i = 0; u_i < n_units; ++u_i) {
+  const int64_t unit = kPersistent ? (int64_t)sched_units[sched_off[blockIdx.x] + u_i] : (int64_t)blockIdx.x;
 
-  const WorkItem it = load_item(queue, blockIdx.x);
+  const WorkItem it = load_item(queue, unit);
   const bool item_ok = !kChecked || key_item_ok(it, geo, bm, bn);  // checked build only
   if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
   const GroupInfo G = geo.groups[item_ok ? it.group : 0];
@@ -197,6 +206,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   };
 
   if (threadIdx.x == 0) {
+    if (kPersistent && u_i > 0) {
+      // Every wait, copy and MMA of the previous unit has ended (drains, then the
+      // block-wide barrier at its end): its barriers are idle and may be reused.
+      for (uint64_t* b = &bars->kv_full; b < reinterpret_cast<uint64_t*>(&bars->tmem_base); ++b) mbar_inval(b);
+    }
     mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < NQ; ++i) {
       mbar_init(&bars->q_full[i], 1);
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == MMA_WARP) tmem_alloc(&bars->tmem_base, 512);
+  if (!kPersistent && warp == MMA_WARP) tmem_alloc(&bars->tmem_base, 512);
   if (warp == PRODUCER_WARP && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_do);
@@ -591,9 +605,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
   }
   tc_fence_before();
   __syncthreads();
+  }  // units of the lane
+  if (kPersistent) __syncthreads();  // an empty lane: the address is visible before it is freed
   if (warp == MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(bars->tmem_base, 512);
   }
 }
 
@@ -650,13 +666,19 @@ cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* 
     mk2 = mk;
     mv2 = mv;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
+  // Persistent schedule: one block per lane, each walking its units.
+  const LaneSet& ls = p->lanes_kv[op];
+  const bool persistent = ls.off_d != nullptr;
+  auto kern = persistent ? tc_bwd_kv_kernel<true> : tc_bwd_kv_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
   if (e != cudaSuccess) return e;
-  tc_bwd_kv_kernel<<<(unsigned)p->n_items[op], KV_THREADS, KV_SMEM, st>>>(
+  const unsigned grid = persistent ? (unsigned)ls.n_lanes : (unsigned)p->n_items[op];
+  kern<<<grid, KV_THREADS, KV_SMEM, st>>>(
       mq, mdo, mk, mv, mk2, mv2, mq2, mdo2, geometry(p), p->queue_d[op], p->row_bend_d, p->bm[op], p->bn[op],
       (const uint8_t*)aug, prefill ? p->ntiles_p : p->ntiles_r, (const uint8_t*)(aug2 ? aug2 : aug), p->ntiles_p,
       (__nv_bfloat16*)dk_out, (__nv_bfloat16*)dv_out, (__nv_bfloat16*)dk2_out, (__nv_bfloat16*)dv2_out, dk_part,
-      dv_part, dk_sum, dv_sum, dk_add, dv_add, slots, kFlushSlots, p->err_d);
+      dv_part, dk_sum, dv_sum, dk_add, dv_add, slots, kFlushSlots, p->err_d, persistent ? ls.off_d : nullptr,
+      persistent ? ls.units_d : nullptr);
   return cudaGetLastError();
 }
 
