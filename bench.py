@@ -257,6 +257,8 @@ class Run:
         self.dq_p, self.dk_p, self.dv_p = (torch.empty_like(t[n]) for n in ("q_p", "k_p", "v_p"))
         self.dq_r, self.dk_r, self.dv_r = (torch.empty_like(t[n]) for n in ("q_r", "k_r", "v_r"))
         plan = self.plan
+        n_fws = plan.workspace_bytes(at.OP_REPLAY_FWD)  # split-KV partials (short queues only)
+        self.ws_f = torch.empty(n_fws, dtype=torch.uint8, device=dev) if n_fws else None
         if fused:
             self.ws_t = torch.empty(max(1, plan.workspace_bytes(at.OP_TREE_BWD)), dtype=torch.uint8, device=dev)
         else:
@@ -277,7 +279,8 @@ class Run:
         rec(0)
         at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], self.o_p, self.lse_p, stream=s)
         rec(1)
-        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], self.o_r, self.lse_r, stream=s)
+        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], self.o_r, self.lse_r, self.ws_f,
+                              stream=s)
         rec(2)
         if self.fused:
             at.augtree_tree_bwd(plan, t["q_p"], t["k_p"], t["v_p"], self.o_p, self.lse_p, t["do_p"], t["q_r"],

@@ -130,7 +130,20 @@ typedef struct augtree_plan augtree_plan;
  *    branches, rows [r0 + tile*BM, min(r0 + (tile+1)*BM, r0 + L_R)) (a tile may span
  *    branches), query head `head`.  a = ceil(L_P / BN) prompt KV tiles (dense);
  *    b = ceil((row_end - branch_start(first row)) / BN) own KV tiles starting at the
- *    first row's branch start; cost = a + b.
+ *    first row's branch start; the tile's KV walk is the a prompt tiles, then the b
+ *    own tiles.  Unsplit: split = 0, cost = a + b.  Split-KV (tensor-core kernels,
+ *    rule below): the tile has s items per head; item `split` = k walks tiles
+ *    [k*C, min((k+1)*C, a + b)) of the walk, C = ceil((a + b) / s), cost = that count.
+ *
+ * Split-KV rule (replay_fwd with the tensor-core kernels; Sec. 3.3: partial softmax
+ * states over disjoint key ranges merge exactly): let n = (number of replay query
+ * tiles) * Hq.  If n >= 2 * num_sms nothing is split.  Otherwise, with U = Hq * sum of
+ * the tiles' a + b and T = max(4, ceil(U / (4 * num_sms))), a tile of cost c gets
+ * s = min(64, max(1, ceil(c / T))) splits (then s = ceil(c / ceil(c / s))); T doubles
+ * until the split tiles (s > 1) hold at most 4096 partial states (tiles x Hq x s).
+ * The replay forward then needs a workspace for the partial states and merges them in
+ * split order; the replay query-side backward (same items) writes fp32 dQ partials and
+ * sums them in split order.  The SIMT kernels never split.
  *  kind 2 PROMPT_KV (replay_bwd): prompt KV tile `tile` (keys [p0 + tile*BN, ...)),
  *    KV head `head`, split `split`: response query tiles [a, b) of the group, each
  *    for the r query heads of the KV head.  cost = (b - a) * r.
@@ -217,7 +230,10 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
                                    augtree_plan** out);
 augtree_status augtree_plan_destroy(augtree_plan* plan);
 
-/* Workspace bytes each compute call needs (0 allowed: pass ws = NULL). */
+/* Workspace bytes each compute call needs (0 allowed: pass ws = NULL).  The prefill
+ * forward needs none; the replay forward needs one only when its queue is split-KV
+ * (n_parts partial states: 64 KiB of fp32 O plus 512 bytes of lse each, 256-byte
+ * aligned); the replay and fused backward add 64 KiB of fp32 dQ per partial state. */
 augtree_status augtree_plan_workspace_bytes(const augtree_plan* plan, int32_t op, size_t* bytes);
 
 /* Copy of the plan's work queue for `op` to host memory (for bit-exact checks). */
@@ -234,7 +250,12 @@ augtree_status augtree_prefill_fwd(const augtree_plan* plan, const void* qp, con
 
 /* Response replay (Sec. 3.2-3.3, Eq. 1): each response row attends to all prompt keys
  * of its group (dense) and to its own branch's keys up to itself (causal); the two
- * partial states are merged in one online softmax.
+ * partial states are merged in one online softmax.  With a split-KV queue (a queue
+ * with too few blocks for the GPU, rule above) each split writes its partial state
+ * (O / l in fp32, lse) to ws, and a second kernel merges a row's states in split order
+ * (the n-way form of augtree_lse_merge) into or_ and lse_r: ws_bytes must then be at
+ * least augtree_plan_workspace_bytes(AUGTREE_OP_REPLAY_FWD), else
+ * AUGTREE_ERR_WORKSPACE_TOO_SMALL.
  * In: qr [R,Hq,D], kp/vp [P,Hkv,D], kr/vr [R,Hkv,D].  Out: or_ [R,Hq,D], lse_r [Hq,R]. */
 augtree_status augtree_replay_fwd(const augtree_plan* plan, const void* qr, const void* kp,
                                   const void* vp, const void* kr, const void* vr, void* or_,
@@ -350,7 +371,7 @@ augtree_status augtree_plan_check(const augtree_plan* plan, void* stream);
  * its stream before each kernel it launches and after the last one, in a ring that
  * keeps the last AUGTREE_TIMING_RING calls of each op.  The cost is a few event
  * records per call; nothing else changes.  A call launches at most seven kernels
- * (augtree_tree_bwd); with the SIMT family, augtree_tree_bwd records its two internal
+ * (augtree_tree_bwd with split-K and split-KV); with the SIMT family, augtree_tree_bwd records its two internal
  * calls under AUGTREE_OP_REPLAY_BWD and AUGTREE_OP_PREFILL_BWD.  Kernel kinds
  * (augtree_plan_kernel_times): */
 typedef enum {
@@ -361,7 +382,9 @@ typedef enum {
   AUGTREE_KID_SPLIT_REDUCE = 5,  /* fixed-order reduction of prompt dK/dV partials      */
   AUGTREE_KID_BWD_QUERY_SIDE = 6,/* tensor-core backward, query side (dQ)               */
   AUGTREE_KID_DQ_CONVERT = 7,    /* fp32 dQ accumulator to the output dtype (SIMT)      */
-  AUGTREE_KID_BWD_SIMT = 8       /* SIMT backward                                       */
+  AUGTREE_KID_BWD_SIMT = 8,      /* SIMT backward                                       */
+  AUGTREE_KID_FWD_MERGE = 9,     /* merge of the replay forward's split-KV partials     */
+  AUGTREE_KID_DQ_REDUCE = 10     /* sum of the replay query side's split-KV dQ partials */
 } augtree_kernel_id;
 #define AUGTREE_TIMING_RING 64
 

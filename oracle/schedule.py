@@ -32,6 +32,8 @@ import numpy as np
 PREFILL_Q, REPLAY_Q, PROMPT_KV, RESP_KV, PREFILL_KV, TREE_PROMPT_KV = 0, 1, 2, 3, 4, 5
 OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD, OP_TREE_BWD = 0, 1, 2, 3, 4
 MAX_SPLIT = 64
+FWD_MIN_CHUNK = 4      # KV tiles per split of a replay query tile, at least
+MAX_FWD_PARTS = 4096   # partial states (query tile x head x split) of one plan, at most
 
 
 def _cdiv(a: int, b: int) -> int:
@@ -60,9 +62,48 @@ def _branch_of(grp, row: int) -> int:
     raise ValueError("row outside the group's branches")
 
 
-def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -> np.ndarray:
+def _fwd_split_count(cost: int, target: int) -> int:
+    """Splits of one replay query tile walking `cost` KV tiles, at about `target` tiles
+    each (at most MAX_SPLIT; equal chunks of ceil(cost / s) tiles, the last shorter)."""
+    s = min(MAX_SPLIT, max(1, _cdiv(cost, target)))
+    return _cdiv(cost, _cdiv(cost, s)) if cost > 0 else 1
+
+
+def replay_fwd_splits(costs: List[int], hq: int, num_sms: int) -> List[int]:
+    """Split-KV rule of the replay forward (tensor-core kernels), per replay query tile
+    with `costs[i]` KV tiles (prompt tiles, then own-branch tiles).
+
+    AugTree paper, Sec. 3.3: a query's attention over disjoint key ranges gives partial
+    online-softmax states that merge associatively into the exact result (MoveQ's
+    global reduction of partial states).  Splitting a long query tile's KV walk over
+    several blocks is worth it only when the queue has too few blocks for the GPU: with
+    fewer than 2 * num_sms items (query tile x head), each tile is cut into chunks of
+    about T = max(FWD_MIN_CHUNK, ceil(U / (4 * num_sms))) KV tiles, U the total cost of
+    the queue (so that about four items per SM result), T doubling until the number of
+    partial states (tiles x heads x splits, split tiles only) is at most MAX_FWD_PARTS.
+    Otherwise every tile keeps one item."""
+    n_items = len(costs) * hq
+    if n_items == 0 or n_items >= 2 * num_sms:
+        return [1] * len(costs)
+    total = sum(costs) * hq
+    target = max(FWD_MIN_CHUNK, _cdiv(total, 4 * num_sms))
+    while True:
+        splits = [_fwd_split_count(c, target) for c in costs]
+        if sum(s * hq for s in splits if s > 1) <= MAX_FWD_PARTS:
+            return splits
+        target *= 2
+
+
+def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int,
+          split_replay_fwd: bool = False) -> np.ndarray:
     """Work queue of `op` as an int32 array [n_items, 8]:
-    kind, group, tile, head, split, cost, a, b."""
+    kind, group, tile, head, split, cost, a, b.
+
+    split_replay_fwd: apply the split-KV rule (replay_fwd_splits) to the replay forward
+    queue, as the tensor-core kernels do.  A split item k of a tile with s splits walks
+    the tile's KV tiles [k C, min((k + 1) C, a + b)), C = ceil((a + b) / s), in the
+    order prompt tiles then own-branch tiles; its cost is that count; a and b stay the
+    tile's own."""
     r = hq // hkv
     groups = _groups(offsets)
     items: List[Tuple[int, ...]] = []
@@ -75,6 +116,7 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
                 for h in range(hq):
                     items.append((PREFILL_Q, g, t, h, 0, a, a, 0))
     elif op == OP_REPLAY_FWD:
+        tiles = []
         for g, grp in enumerate(groups):
             a = _cdiv(grp["lp"], bn)
             for t in range(_cdiv(grp["lr"], bm)):
@@ -82,8 +124,16 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int) -
                 row_end = min(row_begin + bm, grp["r0"] + grp["lr"])
                 bstart = grp["starts"][_branch_of(grp, row_begin)]
                 b = _cdiv(row_end - bstart, bn)
+                tiles.append((g, t, a, b))
+        splits = replay_fwd_splits([a + b for (_, _, a, b) in tiles], hq, num_sms) if split_replay_fwd \
+            else [1] * len(tiles)
+        for (g, t, a, b), s in zip(tiles, splits):
+            cost = a + b
+            c = _cdiv(cost, s)
+            for k in range(s):
+                kc = cost if s == 1 else min(c, cost - k * c)
                 for h in range(hq):
-                    items.append((REPLAY_Q, g, t, h, 0, a + b, a, b))
+                    items.append((REPLAY_Q, g, t, h, k, kc, a, b))
     elif op in (OP_REPLAY_BWD, OP_TREE_BWD):
         # Unsplit costs first, to fix the split target.  The fused backward (all of the
         # backward in one call) uses the replay backward's split rule; split 0 of a

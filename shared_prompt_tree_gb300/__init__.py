@@ -34,7 +34,7 @@ KID_FWD_TC, KID_BWD_KEY_SIDE, KID_BWD_QUERY_SIDE = 1, 4, 6
 OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD, OP_TREE_BWD = 0, 1, 2, 3, 4
 # augtree_kernel_id: kinds reported by augtree_plan_kernel_times
 KERNEL_IDS = {1: "fwd_tc", 2: "fwd_simt", 3: "preprocess", 4: "bwd_key_side", 5: "split_reduce",
-              6: "bwd_query_side", 7: "dq_convert", 8: "bwd_simt"}
+              6: "bwd_query_side", 7: "dq_convert", 8: "bwd_simt", 9: "fwd_split_merge", 10: "dq_split_reduce"}
 TIMING_RING = 64
 ITEM_WORDS = 8
 
@@ -362,7 +362,10 @@ def forward(plan: Plan, q_p, k_p, v_p, q_r, k_r, v_r):
     lse_p = _empty((plan.hq, plan.total_prompt), plan, dev, torch.float32)
     lse_r = _empty((plan.hq, plan.total_resp), plan, dev, torch.float32)
     augtree_prefill_fwd(plan, q_p, k_p, v_p, o_p, lse_p)
-    augtree_replay_fwd(plan, q_r, k_p, v_p, k_r, v_r, o_r, lse_r)
+    # Split-KV partial states of the replay forward (only when its queue is split).
+    n_ws = plan.workspace_bytes(OP_REPLAY_FWD)
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev) if n_ws else None
+    augtree_replay_fwd(plan, q_r, k_p, v_p, k_r, v_r, o_r, lse_r, ws)
     return o_p, lse_p, o_r, lse_r
 
 

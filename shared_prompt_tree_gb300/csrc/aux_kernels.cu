@@ -1,7 +1,8 @@
 // Memory-bound kernels of the path: the backward preprocess (Delta, the SIMT family's
 // zeroed fp32 dQ accumulator, the tensor-core family's tiled row statistics), the dQ
 // conversion, the merge's backward, the fixed-order split-K reduction of the prompt
-// K/V gradient (Eq. 2), and the partial-state merge of Sec. 3.3.
+// K/V gradient (Eq. 2), the partial-state merge of Sec. 3.3 (standalone, and the
+// n-way merge of the replay forward's split-KV partials) and the split-KV dQ sum.
 //
 // AugTree paper, Sec. 3.2 (Eq. 2: the prompt K/V gradient is the sum over branches,
 // "exact many-to-one gradient aggregation") and Sec. 3.3 (partial online-softmax
@@ -167,6 +168,89 @@ __global__ void split_reduce_kernel(const GroupInfo* __restrict__ groups, const 
   }
 }
 
+// Replay forward split-KV, one block per (split query tile, head), one warp per row,
+// four head dimensions per lane (D = 128).  The tile's nsplit partial states
+// (O_k = O over the chunk's keys / l_k, lse_k) merge as the n-way form of the state
+// merge (+) of Sec. 3.3: lse = log sum_k exp(lse_k), O = sum_k exp(lse_k - lse) O_k,
+// summed in ascending split order (deterministic).  A row whose splits all saw no valid
+// key gets O = 0 and lse = -inf.
+__global__ void fwd_split_merge_kernel(const GroupInfo* __restrict__ groups, const FwdSplit* __restrict__ fsplit,
+                                       const int32_t* __restrict__ tiles, int hq, const float* __restrict__ part_o,
+                                       const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ o,
+                                       float* __restrict__ lse, int64_t total_resp) {
+  const GroupInfo G = groups[tiles[2 * blockIdx.x]];
+  const int t = tiles[2 * blockIdx.x + 1];
+  const FwdSplit fs = fsplit[G.tr0 + t];
+  const int h = blockIdx.y;
+  const int64_t row0 = (int64_t)G.r0 + (int64_t)t * kFwdPartRows;
+  const int rows = (int)min((int64_t)kFwdPartRows, (int64_t)G.r0 + G.lr - row0);
+  const int64_t slot0 = fs.slot0 + (int64_t)h * fs.nsplit;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < rows; r += blockDim.x >> 5) {
+    float m = -INFINITY;
+    for (int k = 0; k < fs.nsplit; ++k) m = fmaxf(m, part_lse[(slot0 + k) * kFwdPartRows + r]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float out_lse = -INFINITY;
+    if (m != -INFINITY) {
+      float sum = 0.f;
+      for (int k = 0; k < fs.nsplit; ++k) {
+        const float lk = part_lse[(slot0 + k) * kFwdPartRows + r];
+        sum += lk == -INFINITY ? 0.f : expf(lk - m);
+      }
+      out_lse = m + logf(sum);
+      for (int k = 0; k < fs.nsplit; ++k) {
+        const float lk = part_lse[(slot0 + k) * kFwdPartRows + r];
+        if (lk == -INFINITY) continue;
+        const float w = expf(lk - out_lse);
+        const float4 x = *reinterpret_cast<const float4*>(part_o + ((slot0 + k) * kFwdPartRows + r) * 128 + lane * 4);
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+    }
+    const int64_t row = row0 + r;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(o + (row * hq + h) * 128 + lane * 4) = pk;
+    if (lane == 0) lse[(int64_t)h * total_resp + row] = out_lse;
+  }
+}
+
+// Replay query-side backward split-KV: dQ of a split tile's rows is the sum of its
+// splits' fp32 partials, in ascending split order; one block per (split tile, head),
+// one warp per row.
+__global__ void dq_split_reduce_kernel(const GroupInfo* __restrict__ groups, const FwdSplit* __restrict__ fsplit,
+                                       const int32_t* __restrict__ tiles, int hq, const float* __restrict__ dq_part,
+                                       __nv_bfloat16* __restrict__ dq) {
+  const GroupInfo G = groups[tiles[2 * blockIdx.x]];
+  const int t = tiles[2 * blockIdx.x + 1];
+  const FwdSplit fs = fsplit[G.tr0 + t];
+  const int h = blockIdx.y;
+  const int64_t row0 = (int64_t)G.r0 + (int64_t)t * kFwdPartRows;
+  const int rows = (int)min((int64_t)kFwdPartRows, (int64_t)G.r0 + G.lr - row0);
+  const int64_t slot0 = fs.slot0 + (int64_t)h * fs.nsplit;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < rows; r += blockDim.x >> 5) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < fs.nsplit; ++k) {
+      const float4 x = *reinterpret_cast<const float4*>(dq_part + ((slot0 + k) * kFwdPartRows + r) * 128 + lane * 4);
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    const int64_t row = row0 + r;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dq + (row * hq + h) * 128 + lane * 4) = pk;
+  }
+}
+
 // (O, lse) merge, one thread per (row, head) pair looping over d.
 __global__ void lse_merge_kernel(int64_t rows, int h, int d, const float* __restrict__ oa,
                                  const float* __restrict__ la, const float* __restrict__ ob,
@@ -297,6 +381,27 @@ cudaError_t launch_split_reduce_final(const augtree_plan* p, const float* dk_par
   split_reduce_kernel<__nv_bfloat16><<<p->total_prompt, 256, 0, st>>>(
       p->groups_d, p->splits_d, p->n_groups, cols, dk_part, dv_part, (__nv_bfloat16*)dkp, (__nv_bfloat16*)dvp,
       p->total_prompt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_split_merge(const augtree_plan* p, const float* part_o, const float* part_lse, void* o,
+                                   float* lse, cudaStream_t st) {
+  const size_t n_tiles = p->fsplit_tiles_h.size() / 2;
+  if (n_tiles == 0) return cudaSuccess;
+  if (p->cfg.head_dim != 128 || !part_o || !part_lse) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)n_tiles, p->cfg.hq);
+  fwd_split_merge_kernel<<<grid, 256, 0, st>>>(p->groups_d, p->fsplit_d, p->fsplit_tiles_d, p->cfg.hq, part_o,
+                                               part_lse, (__nv_bfloat16*)o, lse, p->total_resp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_split_reduce(const augtree_plan* p, const float* dq_part, void* dq, cudaStream_t st) {
+  const size_t n_tiles = p->fsplit_tiles_h.size() / 2;
+  if (n_tiles == 0) return cudaSuccess;
+  if (p->cfg.head_dim != 128 || !dq_part) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)n_tiles, p->cfg.hq);
+  dq_split_reduce_kernel<<<grid, 256, 0, st>>>(p->groups_d, p->fsplit_d, p->fsplit_tiles_d, p->cfg.hq, dq_part,
+                                               (__nv_bfloat16*)dq);
   return cudaGetLastError();
 }
 

@@ -82,6 +82,16 @@ __device__ __forceinline__ bool query_item_ok(const WorkItem& it, const Geometry
   return it.b == ceil_div64(row_end - own0, bn);
 }
 
+// The split of a query-side item (after query_item_ok): 0 unless the item is a replay
+// item of a split-KV tile, then below the tile's split count with a non-empty chunk.
+__device__ __forceinline__ bool split_item_ok(const WorkItem& it, const Geometry& geo) {
+  if (it.kind != K_REPLAY_Q || geo.fsplit == nullptr) return it.split == 0;
+  const FwdSplit fs = geo.fsplit[geo.groups[it.group].tr0 + it.tile];
+  if (fs.nsplit <= 1) return it.split == 0;
+  return it.split >= 0 && it.split < fs.nsplit && fs.chunk > 0 && (int64_t)it.split * fs.chunk < (int64_t)it.a + it.b &&
+         fs.slot0 >= 0;
+}
+
 // A key-side item (PROMPT_KV, RESP_KV, PREFILL_KV, TREE_PROMPT_KV): group and KV head in
 // range, its KV tile inside its group's keys, its query tiles [a, b) inside the query
 // side it walks, its split below the group's split count.

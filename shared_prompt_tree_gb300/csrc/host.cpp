@@ -113,9 +113,35 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 namespace augtree {
 
+void replay_fwd_splits(const std::vector<int64_t>& costs, int hq, int num_sms, std::vector<int64_t>& splits) {
+  // Split-KV of the replay forward (Sec. 3.3: partial states over disjoint key ranges
+  // merge exactly).  Only a queue with fewer than 2 * num_sms items (too few blocks for
+  // the GPU) is split: each query tile into chunks of about T KV tiles, T = max(4,
+  // ceil(U / (4 * num_sms))) for a queue of total cost U (about four items per SM),
+  // doubled until the split tiles hold at most kMaxFwdParts partial states.
+  splits.assign(costs.size(), 1);
+  const int64_t n_items = (int64_t)costs.size() * hq;
+  if (n_items == 0 || n_items >= 2 * (int64_t)num_sms) return;
+  int64_t total = 0;
+  for (int64_t c : costs) total += c * hq;
+  int64_t target = std::max<int64_t>(kFwdMinChunk, cdiv(total, 4 * (int64_t)num_sms));
+  for (;;) {
+    int64_t parts = 0;
+    for (size_t i = 0; i < costs.size(); ++i) {
+      const int64_t c = costs[i];
+      int64_t s = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, cdiv(c, target)));
+      s = c > 0 ? cdiv(c, cdiv(c, s)) : 1;
+      splits[i] = s;
+      if (s > 1) parts += s * hq;
+    }
+    if (parts <= kMaxFwdParts) return;
+    target *= 2;
+  }
+}
+
 augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int32_t>& bb,
                            const std::vector<int32_t>& ro, int hq, int hkv, int op, int bm, int bn,
-                           int num_sms, std::vector<int32_t>& out) {
+                           int num_sms, bool split_fwd, std::vector<int32_t>& out) {
   std::vector<Grp> groups;
   read_groups(po, bb, ro, groups);
   const int r = hq / hkv;
@@ -142,6 +168,9 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
       }
     }
   } else if (op == AUGTREE_OP_REPLAY_FWD) {
+    struct RT { int g; int64_t t, a, b; };
+    std::vector<RT> tiles;
+    std::vector<int64_t> costs;
     for (int g = 0; g < ng; ++g) {
       const Grp& G = groups[g];
       int64_t a = cdiv(G.lp, bn);
@@ -150,7 +179,18 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
         int64_t row_end = std::min(row_begin + bm, G.r0 + G.lr);
         int64_t bstart = G.starts[branch_of(G, row_begin)];
         int64_t b = cdiv(row_end - bstart, bn);
-        for (int h = 0; h < hq; ++h) push(K_REPLAY_Q, g, t, h, 0, a + b, a, b);
+        tiles.push_back({g, t, a, b});
+        costs.push_back(a + b);
+      }
+    }
+    std::vector<int64_t> splits(tiles.size(), 1);
+    if (split_fwd) replay_fwd_splits(costs, hq, num_sms, splits);
+    for (size_t i = 0; i < tiles.size(); ++i) {
+      const RT& x = tiles[i];
+      const int64_t cost = x.a + x.b, s = splits[i], c = cdiv(cost, s);
+      for (int64_t k = 0; k < s; ++k) {
+        const int64_t kc = s == 1 ? cost : std::min(c, cost - k * c);
+        for (int h = 0; h < hq; ++h) push(K_REPLAY_Q, x.g, x.t, h, (int)k, kc, x.a, x.b);
       }
     }
   } else if (op == AUGTREE_OP_REPLAY_BWD || op == AUGTREE_OP_TREE_BWD) {
@@ -272,15 +312,15 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
 }
 
 bool queue_pairs(const std::vector<int32_t>& q, int hq, int hkv) {
-  // Consecutive items 2i, 2i+1: the same kind, group and query tile, heads h and h + 1
-  // with h even; they then share a KV head when Hq / Hkv is even.
+  // Consecutive items 2i, 2i+1: the same kind, group, query tile and split, heads h and
+  // h + 1 with h even; they then share a KV head when Hq / Hkv is even.
   const size_t n = q.size() / AUGTREE_ITEM_WORDS;
   const int r = hq / hkv;
   bool ok = (hq % 2 == 0) && (r % 2 == 0) && (n % 2 == 0);
   for (size_t i = 0; ok && i + 1 < n; i += 2) {
     const int32_t* a = &q[i * AUGTREE_ITEM_WORDS];
     const int32_t* b = a + AUGTREE_ITEM_WORDS;
-    ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[3] % 2 == 0 && b[3] == a[3] + 1;
+    ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[4] == b[4] && a[3] % 2 == 0 && b[3] == a[3] + 1;
   }
   return ok;
 }
@@ -330,6 +370,15 @@ static size_t aug_bytes(const augtree_plan* p, bool prompt_side) {
   return align256((size_t)p->cfg.hq * (prompt_side ? p->ntiles_p : p->ntiles_r) * kAugTileBytes);
 }
 
+FwdWorkspace replay_fwd_ws(const augtree_plan* p) {
+  FwdWorkspace w;
+  const size_t n = (size_t)p->n_fwd_parts;
+  w.o_off = 0;
+  w.lse_off = align256(n * kFwdPartRows * p->cfg.head_dim * 4);
+  w.total = n ? w.lse_off + align256(n * kFwdPartRows * 4) : 0;
+  return w;
+}
+
 BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
   BwdWorkspace w;
   const size_t hkv = p->cfg.hkv, d = p->cfg.head_dim, R = p->total_resp;
@@ -338,7 +387,8 @@ BwdWorkspace replay_bwd_ws(const augtree_plan* p) {
   w.dq_off = w.aug_off + aug_bytes(p, false);
   w.dkpart_off = w.dq_off + dq_acc_bytes(p, R);
   w.dvpart_off = w.dkpart_off + align256((size_t)p->part_rows * hkv * d * 4);
-  w.slots_off = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
+  w.dqpart_off = w.dvpart_off + align256((size_t)p->part_rows * hkv * d * 4);
+  w.slots_off = w.dqpart_off + align256((size_t)p->n_fwd_parts * kFwdPartRows * d * 4);
   w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
   return w;
 }
@@ -364,7 +414,7 @@ BwdWorkspace prefill_bwd_ws(const augtree_plan* p) {
   w.delta_off = 0;
   w.aug_off = align256(stats_bytes(p, true));
   w.dq_off = w.aug_off + aug_bytes(p, true);
-  w.dkpart_off = w.dvpart_off = w.slots_off = w.dq_off + dq_acc_bytes(p, P);
+  w.dkpart_off = w.dvpart_off = w.dqpart_off = w.slots_off = w.dq_off + dq_acc_bytes(p, P);
   w.total = w.slots_off + (p->family == AUGTREE_KERNEL_TC ? kFlushSlots * kFlushSlotBytes : 0);
   return w;
 }
@@ -374,6 +424,7 @@ Geometry geometry(const augtree_plan* p) {
   g.groups = p->groups_d;
   g.row_bstart = p->row_bstart_d;
   g.splits = p->splits_d;
+  g.fsplit = p->fsplit_d;
   g.hq = p->cfg.hq;
   g.hkv = p->cfg.hkv;
   g.d = p->cfg.head_dim;
@@ -448,7 +499,8 @@ augtree_status augtree_schedule_build(const augtree_desc* desc, const augtree_co
   tiles_for(resolve_family(cfg), op, &bm, &bn);
   std::vector<int32_t> q;
   try {
-    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, bm, bn, cfg->num_sms, q);
+    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, bm, bn, cfg->num_sms,
+                     resolve_family(cfg) == AUGTREE_KERNEL_TC, q);
   } catch (const std::bad_alloc&) {
     return AUGTREE_ERR_CAPACITY;
   }
@@ -475,7 +527,8 @@ augtree_status augtree_schedule_lanes(const augtree_desc* desc, const augtree_co
   std::vector<int32_t> q;
   LaneSet l;
   try {
-    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, bm, bn, cfg->num_sms, q);
+    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, bm, bn, cfg->num_sms,
+                     resolve_family(cfg) == AUGTREE_KERNEL_TC, q);
     if (st != AUGTREE_OK) return st;
     st = build_lanes(q, 1, cfg->num_sms, l);
   } catch (const std::bad_alloc&) {
@@ -499,6 +552,8 @@ augtree_status augtree_plan_destroy(augtree_plan* p) {
   cudaFree(p->row_bstart_d);
   cudaFree(p->row_bend_d);
   cudaFree(p->splits_d);
+  cudaFree(p->fsplit_d);
+  cudaFree(p->fsplit_tiles_d);
   cudaFree(p->err_d);
   for (int i = 0; i < kNumOps; ++i) cudaFree(p->queue_d[i]);
   for (int i = 0; i < 2; ++i) {
@@ -533,6 +588,9 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   p->row_bstart_d = nullptr;
   p->row_bend_d = nullptr;
   p->splits_d = nullptr;
+  p->fsplit_d = nullptr;
+  p->fsplit_tiles_d = nullptr;
+  p->n_fwd_parts = 0;
   p->static_scratch = nullptr;
   for (int i = 0; i < kNumOps; ++i) p->queue_d[i] = nullptr;
   if (cudaGetDevice(&p->device) != cudaSuccess) {
@@ -573,7 +631,8 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
     }
   for (int op = 0; op < kNumOps; ++op) {
     tiles_for(p->family, op, &p->bm[op], &p->bn[op]);
-    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, p->bm[op], p->bn[op], p->cfg.num_sms, p->queue_h[op]);
+    st = build_queue(po, bb, ro, cfg->hq, cfg->hkv, op, p->bm[op], p->bn[op], p->cfg.num_sms,
+                     p->family == AUGTREE_KERNEL_TC, p->queue_h[op]);
     if (st != AUGTREE_OK) {
       delete p;
       return st;
@@ -614,6 +673,28 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
     s.part_row0 = p->part_rows;
     if (s.nsplit > 1) p->part_rows += (int64_t)s.nsplit * p->groups_h[g].lp;
   }
+  // Replay forward split-KV: per response query tile, its split count and chunk (the
+  // cost of its split 0) from the queue, and the first of its Hq * nsplit partial slots.
+  // (Tensor-core family only: its replay query tiles are the 128-row statistics tiles.)
+  p->fsplit_h.assign(std::max(1, p->ntiles_r), FwdSplit{1, 0, 0});
+  const size_t n_fwd_items = p->family == AUGTREE_KERNEL_TC ? p->n_items[AUGTREE_OP_REPLAY_FWD] : 0;
+  for (size_t i = 0; i < n_fwd_items; ++i) {
+    const int32_t* it = &p->queue_h[AUGTREE_OP_REPLAY_FWD][i * AUGTREE_ITEM_WORDS];
+    FwdSplit& f = p->fsplit_h[p->groups_h[it[1]].tr0 + it[2]];
+    f.nsplit = std::max(f.nsplit, it[4] + 1);
+    if (it[4] == 0) f.chunk = it[5];
+  }
+  bool any_split = false;
+  for (int g = 0; g < p->n_groups && n_fwd_items > 0; ++g)
+    for (int32_t t = 0; t < (int32_t)cdiv(p->groups_h[g].lr, kFwdPartRows); ++t) {
+      FwdSplit& f = p->fsplit_h[p->groups_h[g].tr0 + t];
+      if (f.nsplit <= 1) continue;
+      any_split = true;
+      f.slot0 = p->n_fwd_parts;
+      p->n_fwd_parts += (int64_t)cfg->hq * f.nsplit;
+      p->fsplit_tiles_h.push_back(g);
+      p->fsplit_tiles_h.push_back(t);
+    }
   // Device copies.
   auto up = [&](void** dst, const void* src, size_t bytes) -> bool {
     if (bytes == 0) bytes = 16;
@@ -631,6 +712,10 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   const uint32_t err_init[4] = {0u, 0u, (uint32_t)lim, (uint32_t)(lim >> 32)};
   ok = ok && up((void**)&p->err_d, err_init, sizeof(err_init));
   ok = ok && up((void**)&p->splits_d, p->splits_h.data(), p->splits_h.size() * sizeof(SplitInfo));
+  if (any_split) {
+    ok = ok && up((void**)&p->fsplit_d, p->fsplit_h.data(), p->fsplit_h.size() * sizeof(FwdSplit));
+    ok = ok && up((void**)&p->fsplit_tiles_d, p->fsplit_tiles_h.data(), p->fsplit_tiles_h.size() * sizeof(int32_t));
+  }
   for (int op = 0; op < kNumOps && ok; ++op)
     ok = up((void**)&p->queue_d[op], p->queue_h[op].empty() ? (const void*)pad.data() : p->queue_h[op].data(),
             p->queue_h[op].size() * sizeof(int32_t));
@@ -661,8 +746,8 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
 augtree_status augtree_plan_workspace_bytes(const augtree_plan* p, int32_t op, size_t* bytes) {
   if (!p || !bytes) return AUGTREE_ERR_INVALID_ARG;
   switch (op) {
-    case AUGTREE_OP_PREFILL_FWD:
-    case AUGTREE_OP_REPLAY_FWD: *bytes = 0; return AUGTREE_OK;
+    case AUGTREE_OP_PREFILL_FWD: *bytes = 0; return AUGTREE_OK;
+    case AUGTREE_OP_REPLAY_FWD: *bytes = replay_fwd_ws(p).total; return AUGTREE_OK;
     case AUGTREE_OP_REPLAY_BWD: *bytes = replay_bwd_ws(p).total; return AUGTREE_OK;
     case AUGTREE_OP_PREFILL_BWD: *bytes = prefill_bwd_ws(p).total; return AUGTREE_OK;
     case AUGTREE_OP_TREE_BWD: *bytes = tree_bwd_ws(p).total; return AUGTREE_OK;
@@ -714,7 +799,7 @@ augtree_status augtree_prefill_fwd(const augtree_plan* p, const void* qp, const 
   cudaError_t e;
   if (p->family == AUGTREE_KERNEL_TC) {
     tm.mark(AUGTREE_KID_FWD_TC);
-    e = tc_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s);
+    e = tc_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, nullptr, nullptr, s);
   } else {
     tm.mark(AUGTREE_KID_FWD_SIMT);
     e = simt_fwd(p, AUGTREE_OP_PREFILL_FWD, qp, kp, vp, nullptr, nullptr, op, lse_p, s);
@@ -726,11 +811,12 @@ augtree_status augtree_prefill_fwd(const augtree_plan* p, const void* qp, const 
 augtree_status augtree_replay_fwd(const augtree_plan* p, const void* qr, const void* kp, const void* vp,
                                   const void* kr, const void* vr, void* or_, float* lse_r, void* ws,
                                   size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (!p) return AUGTREE_ERR_INVALID_ARG;
   if (p->total_resp > 0 && (!qr || !kr || !vr || !or_ || !lse_r)) return AUGTREE_ERR_INVALID_ARG;
   if (p->total_resp > 0 && p->total_prompt > 0 && (!kp || !vp)) return AUGTREE_ERR_INVALID_ARG;
+  const FwdWorkspace w = replay_fwd_ws(p);
+  if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
+  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
   augtree_status st = check_device(p);
   if (st != AUGTREE_OK) return st;
   if (p->n_items[AUGTREE_OP_REPLAY_FWD] == 0) return AUGTREE_OK;
@@ -738,8 +824,16 @@ augtree_status augtree_replay_fwd(const augtree_plan* p, const void* qr, const v
   CallTimer tm(p, AUGTREE_OP_REPLAY_FWD, s);
   cudaError_t e;
   if (p->family == AUGTREE_KERNEL_TC) {
+    // Split-KV (a queue too short for the GPU): the split tiles' partial states go to
+    // the workspace and are merged in split order (Sec. 3.3).
+    float* part_o = w.total ? (float*)((char*)ws + w.o_off) : nullptr;
+    float* part_lse = w.total ? (float*)((char*)ws + w.lse_off) : nullptr;
     tm.mark(AUGTREE_KID_FWD_TC);
-    e = tc_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s);
+    e = tc_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, part_o, part_lse, s);
+    if (e == cudaSuccess && p->n_fwd_parts > 0) {
+      tm.mark(AUGTREE_KID_FWD_MERGE);
+      e = launch_fwd_split_merge(p, part_o, part_lse, or_, lse_r, s);
+    }
   } else {
     tm.mark(AUGTREE_KID_FWD_SIMT);
     e = simt_fwd(p, AUGTREE_OP_REPLAY_FWD, qr, kp, vp, kr, vr, or_, lse_r, s);
@@ -791,8 +885,13 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
       e = launch_split_reduce(p, dk_part, dv_part, dkp_sum, dvp_sum, s);
     }
     if (e == cudaSuccess && p->total_resp > 0) {
+      float* dq_part = (float*)(base + w.dqpart_off);
       tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
-      e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dqr, s);
+      e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta, dor, dqr, dq_part, s);
+      if (e == cudaSuccess && p->n_fwd_parts > 0) {
+        tm.mark(AUGTREE_KID_DQ_REDUCE);
+        e = launch_dq_split_reduce(p, dq_part, dqr, s);
+      }
     }
     tm.finish();
     return from_cuda(e);
@@ -851,7 +950,7 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
     }
     if (e == cudaSuccess) {
       tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
-      e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dqp, s);
+      e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta, dop, dqp, nullptr, s);
     }
     tm.finish();
     return from_cuda(e);
@@ -928,11 +1027,16 @@ augtree_status augtree_tree_bwd(const augtree_plan* p, const void* qp, const voi
   }
   if (e == cudaSuccess && p->total_prompt > 0) {
     tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
-    e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta_p, dop, dqp, s);
+    e = tc_bwd_dq(p, AUGTREE_OP_PREFILL_BWD, qp, kp, vp, nullptr, nullptr, delta_p, dop, dqp, nullptr, s);
   }
   if (e == cudaSuccess && p->total_resp > 0) {
+    float* dq_part = (float*)(base + w.r.dqpart_off);
     tm.mark(AUGTREE_KID_BWD_QUERY_SIDE);
-    e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta_r, dor, dqr, s);
+    e = tc_bwd_dq(p, AUGTREE_OP_REPLAY_BWD, qr, kp, vp, kr, vr, delta_r, dor, dqr, dq_part, s);
+    if (e == cudaSuccess && p->n_fwd_parts > 0) {
+      tm.mark(AUGTREE_KID_DQ_REDUCE);
+      e = launch_dq_split_reduce(p, dq_part, dqr, s);
+    }
   }
   tm.finish();
   return from_cuda(e);

@@ -14,6 +14,10 @@ namespace augtree {
 enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3, K_PREFILL_KV = 4, K_TREE_PROMPT_KV = 5 };
 constexpr int kNumOps = 5;  // queues per plan: the four calls' ops and the fused backward
 constexpr int kMaxSplit = 64;
+// Split-KV of the replay forward: KV tiles per split at least, partial states per plan
+// at most.
+constexpr int kFwdMinChunk = 4;
+constexpr int64_t kMaxFwdParts = 4096;
 // Limit of a device-side wait on another warp's work: default and largest settable.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 constexpr uint64_t kMaxWaitLimitNs = 60000000000ull;
@@ -36,11 +40,24 @@ struct SplitInfo {
   int64_t part_row0;  // first row of the group's partial block in the workspace
 };
 
+// Split-KV of the replay forward, per 128-row response query tile (numbered like the
+// row statistics, GroupInfo::tr0 + tile): split k of the tile walks its KV tiles
+// [k * chunk, min((k + 1) * chunk, a + b)); a tile with nsplit > 1 writes partial states
+// (forward: fp32 O / l and lse; query-side backward: fp32 dQ) to slots
+// slot0 + head * nsplit + k.
+struct FwdSplit {
+  int32_t nsplit;
+  int32_t chunk;
+  int64_t slot0;
+};
+constexpr int kFwdPartRows = 128;  // rows of one partial slot (the forward query tile)
+
 // Pointers a kernel needs to interpret queue items.
 struct Geometry {
   const GroupInfo* groups;    // [n_groups]
   const int32_t* row_bstart;  // [total_resp] first response row of each row's branch
   const SplitInfo* splits;    // [n_groups] (replay backward only)
+  const FwdSplit* fsplit;     // [ntiles_r] replay forward split-KV, null if no tile splits
   int32_t hq, hkv, d;
   int32_t total_prompt, total_resp;
   int32_t n_groups;
@@ -66,6 +83,11 @@ struct augtree_plan {
   std::vector<augtree::GroupInfo> groups_h;
   std::vector<augtree::SplitInfo> splits_h;
   int64_t part_rows;  // rows of split partials (per dK and per dV), over all groups
+  // Replay forward split-KV (tensor-core family): per response query tile its split
+  // info; the (group, tile) pairs of the split tiles; the number of partial slots.
+  std::vector<augtree::FwdSplit> fsplit_h;
+  std::vector<int32_t> fsplit_tiles_h;
+  int64_t n_fwd_parts;
   std::vector<int32_t> queue_h[augtree::kNumOps];
   size_t n_items[augtree::kNumOps];
   // device copies
@@ -73,6 +95,8 @@ struct augtree_plan {
   int32_t* row_bstart_d;
   int32_t* row_bend_d;  // [total_resp] one past the last response row of each row's branch
   augtree::SplitInfo* splits_d;
+  augtree::FwdSplit* fsplit_d;      // null when no replay query tile is split
+  int32_t* fsplit_tiles_d;
   int32_t* queue_d[augtree::kNumOps];
   int paired[augtree::kNumOps];      // forward tensor-core units take two items (two heads of one KV head)
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
@@ -108,13 +132,24 @@ augtree_status build_lanes(const std::vector<int32_t>& queue, int unit_items, in
 bool queue_pairs(const std::vector<int32_t>& queue, int hq, int hkv);
 
 // Work-queue build shared by augtree_schedule_build and augtree_plan_create.
+// split_fwd: apply the replay forward's split-KV rule (tensor-core family).
 augtree_status build_queue(const std::vector<int32_t>& prompt_off, const std::vector<int32_t>& branch_begin,
                            const std::vector<int32_t>& resp_off, int hq, int hkv, int op, int bm, int bn,
-                           int num_sms, std::vector<int32_t>& out);
+                           int num_sms, bool split_fwd, std::vector<int32_t>& out);
+// Split counts of the replay query tiles with the given KV-tile costs.
+void replay_fwd_splits(const std::vector<int64_t>& costs, int hq, int num_sms, std::vector<int64_t>& splits);
 
-// Workspace layout of the backward calls.
+// Workspace of the replay forward with split-KV: fp32 O partials [n_parts][128][D],
+// then fp32 lse partials [n_parts][128].
+struct FwdWorkspace {
+  size_t o_off, lse_off, total;
+};
+FwdWorkspace replay_fwd_ws(const augtree_plan* p);
+
+// Workspace layout of the backward calls.  dqpart: fp32 dQ partials of the split replay
+// query tiles [n_fwd_parts][128][D] (tensor-core family).
 struct BwdWorkspace {
-  size_t delta_off, aug_off, dq_off, dkpart_off, dvpart_off, slots_off, total;
+  size_t delta_off, aug_off, dq_off, dkpart_off, dvpart_off, dqpart_off, slots_off, total;
 };
 constexpr int kAugTileBytes = 2 * kStatRows * 16;  // {L, D} rows of one query tile
 // fp32 flush slots of the tensor-core backward: one per SM id, 128 keys x 256 floats.
@@ -162,8 +197,11 @@ cudaError_t simt_bwd(const augtree_plan* p, int op, const void* q, const void* k
                      float* dk_part, float* dv_part, float* dk_sum, float* dv_sum,
                      const float* dk_add, const float* dv_add, cudaStream_t st);
 // Tensor-core family (bf16).
+// part_o / part_lse: the replay forward's split-KV partial states (null without split
+// tiles); their merge is launch_fwd_split_merge.
 cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp,
-                   const void* kr, const void* vr, void* o, float* lse, cudaStream_t st);
+                   const void* kr, const void* vr, void* o, float* lse, float* part_o, float* part_lse,
+                   cudaStream_t st);
 // Backward, key side (dK, dV; prompt dK/dV summed over the branches, split-K partials
 // reduced afterwards) and query side (dQ, written once per query tile and head).
 // Key side of the tensor-core backward.  Primary query rows q / dO / aug: the prompt for
@@ -176,7 +214,8 @@ cudaError_t tc_bwd_kv(const augtree_plan* p, int op, const void* q, const void* 
                       float* dk_sum, float* dv_sum, const float* dk_add, const float* dv_add, float* slots,
                       cudaStream_t st);
 cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                      const void* vr, const float* stats, const void* dO, void* dq, cudaStream_t st);
+                      const void* vr, const float* stats, const void* dO, void* dq, float* dq_part,
+                      cudaStream_t st);
 
 // Fixed scratch array of augtree_prefill_bwd_static (static_scratch.cu): its size, and
 // the lookup of its device address on the current device.
@@ -197,6 +236,12 @@ cudaError_t launch_split_reduce(const augtree_plan* p, const float* dk_part, con
 // Fused backward: bf16 prompt dK/dV of the split groups from their partials, in split order.
 cudaError_t launch_split_reduce_final(const augtree_plan* p, const float* dk_part, const float* dv_part, void* dkp,
                                       void* dvp, cudaStream_t st);
+// Replay forward split-KV: merges each split tile's partial states in split order into
+// bf16 O and lse (Sec. 3.3); and sums each split tile's fp32 dQ partials in split order
+// into bf16 dQ.
+cudaError_t launch_fwd_split_merge(const augtree_plan* p, const float* part_o, const float* part_lse, void* o,
+                                   float* lse, cudaStream_t st);
+cudaError_t launch_dq_split_reduce(const augtree_plan* p, const float* dq_part, void* dq, cudaStream_t st);
 cudaError_t launch_lse_merge(int64_t rows, int h, int d, const float* oa, const float* la,
                              const float* ob, const float* lb, float* o, float* l, cudaStream_t st);
 cudaError_t launch_lse_merge_bwd(int64_t rows, int h, int d, const float* oa, const float* la, const float* ob,

@@ -84,14 +84,16 @@ struct DqBars {
 static_assert(sizeof(DqBars) <= 256, "barrier area");
 
 
-template <bool kPersistent>
+// kSplit: the replay queue holds split-KV items, whose dQ over their chunk of KV tiles
+// goes to an fp32 partial slot (summed afterwards in split order).
+template <bool kPersistent, bool kSplit>
 __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
     const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
     const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr, Geometry geo,
     const int32_t* __restrict__ queue, int bm, int bn, const float* __restrict__ stats, int ntiles,
     __nv_bfloat16* __restrict__ dq_out, uint32_t* __restrict__ err,
-    const int32_t* __restrict__ sched_off, const int32_t* __restrict__ sched_units) {
+    const int32_t* __restrict__ sched_off, const int32_t* __restrict__ sched_units, float* __restrict__ dq_part) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DqBars* bars = reinterpret_cast<DqBars*>(smem + DQ_BAR_OFF);
@@ -105,7 +107,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
   const int64_t unit = kPersistent ? (int64_t)sched_units[sched_off[blockIdx.x] + u_i] : (int64_t)blockIdx.x;
 
   const WorkItem it = load_item(queue, unit);
-  const bool item_ok = !kChecked || query_item_ok(it, geo, bm, bn);  // checked build only
+  const bool item_ok = !kChecked || (query_item_ok(it, geo, bm, bn) &&  // checked build only
+                                     (kSplit ? split_item_ok(it, geo) : it.split == 0));
   if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
   const int h = item_ok ? it.head : 0;
   const GroupInfo G = geo.groups[item_ok ? it.group : 0];
@@ -115,9 +118,20 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
   const int64_t row0 = item_ok ? base + (int64_t)it.tile * bm : 0;
   const int64_t row_end = item_ok ? min(row0 + (int64_t)bm, base + len) : 0;
   const int n_a = item_ok ? it.a : 0;
-  const int n_tiles = item_ok ? n_a + (prefill ? 0 : it.b) : 0;
+  int n_tiles = item_ok ? n_a + (prefill ? 0 : it.b) : 0;
   const int64_t own0 = (prefill || !item_ok) ? 0 : geo.row_bstart[row0];
   const int kvh = h / (geo.hq / geo.hkv);
+  // Split-KV item: KV tiles [j0, j0 + n_tiles) of the walk, dQ to partial slot `slot`.
+  int j0 = 0;
+  int64_t slot = -1;
+  if (kSplit && item_ok && !prefill) {
+    const FwdSplit fs = geo.fsplit[G.tr0 + it.tile];
+    if (fs.nsplit > 1) {
+      j0 = it.split * fs.chunk;
+      n_tiles = min(fs.chunk, n_tiles - j0);
+      slot = fs.slot0 + (int64_t)h * fs.nsplit + it.split;
+    }
+  }
 
   if (threadIdx.x == 0) {
     if (kPersistent && u_i > 0) {
@@ -166,12 +180,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         tma_load_3d(smem + DQ_Q_OFF + kb * BLK, &tm_q, &bars->q_full, kb * 64, h, (int)row0);
         tma_load_3d(smem + DQ_DO_OFF + kb * BLK, &tm_do, &bars->q_full, kb * 64, h, (int)row0);
       }
+      // First key row of the item's j-th KV tile (tile j0 + j of the row's walk).
       auto krow_of = [&](int j) {
-        return j >= n_a ? (int)(own0 + (int64_t)(j - n_a) * bn) : (int)(G.p0 + (int64_t)j * bn);
+        const int jt = j0 + j;
+        return jt >= n_a ? (int)(own0 + (int64_t)(jt - n_a) * bn) : (int)(G.p0 + (int64_t)jt * bn);
       };
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
-        const bool own = j >= n_a;
+        const bool own = j0 + j >= n_a;
         const int krow = krow_of(j);
         const CUtensorMap* km = own ? &tm_kr : &tm_kp;
         const CUtensorMap* vm = own ? &tm_vr : &tm_vp;
@@ -189,8 +205,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         // Warm L2 with the K/V tiles a few steps ahead.
         const int jp = j + kPrefetchTiles;
         if (jp < n_tiles) {
-          const CUtensorMap* kmp = jp >= n_a ? &tm_kr : &tm_kp;
-          const CUtensorMap* vmp = jp >= n_a ? &tm_vr : &tm_vp;
+          const CUtensorMap* kmp = j0 + jp >= n_a ? &tm_kr : &tm_kp;
+          const CUtensorMap* vmp = j0 + jp >= n_a ? &tm_vr : &tm_vp;
           const int rp = krow_of(jp);
           for (int kb = 0; kb < 2; ++kb) {
             tma_prefetch_3d(kmp, kb * 64, kvh, rp);
@@ -302,6 +318,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     g.own0 = own0;
     g.n_a = n_a;
     g.bn = bn;
+    g.j0 = j0;
     const int tile_base = prefill ? G.tp0 : G.tr0;
     const float* st = stats + (item_ok ? ((int64_t)h * ntiles + tile_base + it.tile) * 2 * kStatRows : 0);
     const float lse2 = st[r_local];
@@ -376,7 +393,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + T_DQ + c0 + half * 32, v);
         tmem_ld_wait();
-        if (g.row_ok) {
+        if (kSplit && slot >= 0) {
+          // Split-KV item: the fp32 partial (times the scale) of its chunk.
+          if (g.row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dq_part + (slot * kFwdPartRows + r_local) * 128 + c0 + half * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(v[4 * i]) * geo.scale, __uint_as_float(v[4 * i + 1]) * geo.scale,
+                                  __uint_as_float(v[4 * i + 2]) * geo.scale, __uint_as_float(v[4 * i + 3]) * geo.scale);
+          }
+        } else if (g.row_ok) {
           const bool any = n_tiles > 0;
           uint32_t o[16];
 #pragma unroll
@@ -403,7 +429,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
 }  // namespace
 
 cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                      const void* vr, const float* stats, const void* dO, void* dq, cudaStream_t st) {
+                      const void* vr, const float* stats, const void* dO, void* dq, float* dq_part,
+                      cudaStream_t st) {
   // The query-side items of the backward are those of the matching forward op.
   const bool prefill = op == AUGTREE_OP_PREFILL_BWD;
   const int fop = prefill ? AUGTREE_OP_PREFILL_FWD : AUGTREE_OP_REPLAY_FWD;
@@ -433,14 +460,18 @@ cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* 
   // Persistent schedule: one block per lane, each walking its units.
   const LaneSet& ls = p->lanes_dq[fop];
   const bool persistent = ls.off_d != nullptr;
-  auto kern = persistent ? tc_bwd_dq_kernel<true> : tc_bwd_dq_kernel<false>;
+  // The split-KV instantiation only where the replay queue has split items.
+  const bool split = !prefill && p->n_fwd_parts > 0;
+  if (split && !dq_part) return cudaErrorInvalidValue;
+  auto kern = persistent ? (split ? tc_bwd_dq_kernel<true, true> : tc_bwd_dq_kernel<true, false>)
+                         : (split ? tc_bwd_dq_kernel<false, true> : tc_bwd_dq_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = persistent ? (unsigned)ls.n_lanes : (unsigned)p->n_items[fop];
   kern<<<grid, DQ_THREADS, DQ_SMEM, st>>>(
       mq, mdo, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[fop], p->bm[fop], p->bn[fop], stats,
       prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dq, p->err_d, persistent ? ls.off_d : nullptr,
-      persistent ? ls.units_d : nullptr);
+      persistent ? ls.units_d : nullptr, dq_part);
   return cudaGetLastError();
 }
 

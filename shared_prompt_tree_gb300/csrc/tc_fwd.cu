@@ -76,11 +76,15 @@ struct FwdBars {
 
 static_assert(sizeof(FwdBars) <= 256, "barrier area");
 
+// kSplit: the replay queue holds split-KV items (a tile's KV walk cut into chunks,
+// partial states to the workspace); the instantiation without it is the plain kernel.
+template <bool kSplit>
 __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
     const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kr,
     const __grid_constant__ CUtensorMap tm_vr, Geometry geo, const int32_t* __restrict__ queue, int paired, int bm,
-    int bn, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int64_t lse_rows, uint32_t* __restrict__ err) {
+    int bn, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int64_t lse_rows, uint32_t* __restrict__ err,
+    float* __restrict__ part_o, float* __restrict__ part_lse) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + BAR_OFF);
@@ -89,10 +93,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
   const int n_sub = paired ? 2 : 1;
   const WorkItem it0 = load_item(queue, (int64_t)blockIdx.x * n_sub);
   const WorkItem it1 = paired ? load_item(queue, (int64_t)blockIdx.x * 2 + 1) : it0;
-  // Checked build: both items valid, and the same query tile (heads of one KV head).
+  // Checked build: both items valid, and the same query tile and split (heads of one KV
+  // head).
   const bool item_ok = !kChecked || (query_item_ok(it0, geo, bm, bn) && query_item_ok(it1, geo, bm, bn) &&
                                      it1.kind == it0.kind && it1.group == it0.group && it1.tile == it0.tile &&
-                                     it1.head / (geo.hq / geo.hkv) == it0.head / (geo.hq / geo.hkv));
+                                     it1.split == it0.split &&
+                                     it1.head / (geo.hq / geo.hkv) == it0.head / (geo.hq / geo.hkv) &&
+                                     (kSplit ? split_item_ok(it0, geo) : it0.split == 0));
   if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
   int heads[2];
   heads[0] = item_ok ? it0.head : 0;
@@ -104,9 +111,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
   const int64_t row0 = item_ok ? base + (int64_t)it0.tile * bm : 0;
   const int64_t row_end = item_ok ? min(row0 + (int64_t)bm, base + len) : 0;
   const int n_a = item_ok ? it0.a : 0;
-  const int n_tiles = item_ok ? n_a + (prefill ? 0 : it0.b) : 0;
+  int n_tiles = item_ok ? n_a + (prefill ? 0 : it0.b) : 0;
   const int64_t own0 = (prefill || !item_ok) ? 0 : geo.row_bstart[row0];
   const int kvh = heads[0] / (geo.hq / geo.hkv);
+  // Split-KV item: KV tiles [j0, j0 + n_tiles) of the walk; partial-state slot of head s
+  // = slot0 + heads[s] * nsplit + split.
+  int j0 = 0;
+  int64_t slot_base = -1, slot_stride = 0;
+  if (kSplit && item_ok && !prefill) {
+    const FwdSplit fs = geo.fsplit[G.tr0 + it0.tile];
+    if (fs.nsplit > 1) {
+      j0 = it0.split * fs.chunk;
+      n_tiles = min(fs.chunk, n_tiles - j0);
+      slot_base = fs.slot0 + it0.split;
+      slot_stride = fs.nsplit;
+    }
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -147,8 +167,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
         const int stage = j % NST, use = j / NST;
         if (!mbar_wait(&bars->kv_empty[stage], (use & 1) ^ 1, err)) break;
         mbar_expect_tx(&bars->kv_full[stage], 4 * TILE_BYTES);
-        const bool own = j >= n_a;
-        const int krow = own ? (int)(own0 + (int64_t)(j - n_a) * bn) : (int)(G.p0 + (int64_t)j * bn);
+        const int jt = j0 + j;  // tile of the row's walk
+        const bool own = jt >= n_a;
+        const int krow = own ? (int)(own0 + (int64_t)(jt - n_a) * bn) : (int)(G.p0 + (int64_t)jt * bn);
         const CUtensorMap* km = own ? &tm_kr : &tm_kp;
         const CUtensorMap* vm = own ? &tm_vr : &tm_vp;
         for (int kb = 0; kb < 2; ++kb) {
@@ -160,8 +181,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
           // At the start, the first few tiles after the ring's; then one tile per fill.
           const int jp0 = j == 0 ? NST : j + kFwdPrefetch;
           for (int jp = jp0; jp <= j + kFwdPrefetch && jp < n_tiles; ++jp) {
-            const bool own_p = jp >= n_a;
-            const int rp = own_p ? (int)(own0 + (int64_t)(jp - n_a) * bn) : (int)(G.p0 + (int64_t)jp * bn);
+            const int jpt = j0 + jp;
+            const bool own_p = jpt >= n_a;
+            const int rp = own_p ? (int)(own0 + (int64_t)(jpt - n_a) * bn) : (int)(G.p0 + (int64_t)jpt * bn);
             for (int kb = 0; kb < 2; ++kb) {
               tma_prefetch_3d(own_p ? &tm_kr : &tm_kp, kb * 64, kvh, rp);
               tma_prefetch_3d(own_p ? &tm_vr : &tm_vp, kb * 64, kvh, rp);
@@ -237,18 +259,28 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
       g.own0 = own0;
       g.n_a = n_a;
       g.bn = bn;
+      g.j0 = j0;
       const int h = heads[s];
       uint64_t* p_full = &bars->p_full[s];
       auto signal = [p_full]() { mbar_arrive(p_full); };
       __nv_bfloat16* orow = out + (g.row * geo.hq + h) * 128;
       float* lrow = lse + (int64_t)h * lse_rows + g.row;
+      float* prow = nullptr;
+      float* plse = nullptr;
+      if (kSplit && slot_base >= 0) {
+        const int64_t slot = slot_base + (int64_t)h * slot_stride;
+        prow = part_o + (slot * kFwdPartRows + r_local) * 128;
+        plse = part_lse + slot * kFwdPartRows + r_local;
+      }
       if (kFwdPingPong && n_sub == 2) {
         const PingPong turn{&bars->turn[s], &bars->turn[s ^ 1], s == 0 ? 1 : 0};
-        fwd_softmax_row(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles, geo.scale_log2,
-                        &bars->s_full[s], &bars->o_done[s], signal, orow, lrow, err, turn);
+        fwd_softmax_row<kSplit>(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles,
+                                geo.scale_log2, &bars->s_full[s], &bars->o_done[s], signal, orow, lrow, err, turn,
+                                prow, plse);
       } else {
-        fwd_softmax_row(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles, geo.scale_log2,
-                        &bars->s_full[s], &bars->o_done[s], signal, orow, lrow, err);
+        fwd_softmax_row<kSplit>(tmem + s * 128 + lane_off, tmem + 256 + s * 128 + lane_off, g, n_tiles,
+                                geo.scale_log2, &bars->s_full[s], &bars->o_done[s], signal, orow, lrow, err, NoTurn(),
+                                prow, plse);
       }
     }
   }
@@ -305,7 +337,7 @@ bool encode_f32_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int he
 }
 
 cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp, const void* vp, const void* kr,
-                   const void* vr, void* o, float* lse, cudaStream_t st) {
+                   const void* vr, void* o, float* lse, float* part_o, float* part_lse, cudaStream_t st) {
   const bool prefill = op == AUGTREE_OP_PREFILL_FWD;
   const int64_t q_rows = prefill ? p->total_prompt : p->total_resp;
   CUtensorMap mq, mkp, mvp, mkr, mvr;
@@ -329,13 +361,17 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
     mkr = mkp;
     mvr = mvp;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
+  // The split-KV instantiation only where the replay queue has split items.
+  const bool split = !prefill && p->n_fwd_parts > 0;
+  if (split && (!part_o || !part_lse)) return cudaErrorInvalidValue;
+  auto kern = split ? tc_fwd_kernel<true> : tc_fwd_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;
   const int paired = p->paired[op];
   const size_t units = paired ? p->n_items[op] / 2 : p->n_items[op];
-  tc_fwd_kernel<<<(unsigned)units, FWD_THREADS, FWD_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op],
-                                                                paired, p->bm[op], p->bn[op], (__nv_bfloat16*)o, lse,
-                                                                q_rows, p->err_d);
+  kern<<<(unsigned)units, FWD_THREADS, FWD_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op], paired,
+                                                       p->bm[op], p->bn[op], (__nv_bfloat16*)o, lse, q_rows, p->err_d,
+                                                       part_o, part_lse);
   return cudaGetLastError();
 }
 

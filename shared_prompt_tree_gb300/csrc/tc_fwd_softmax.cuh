@@ -49,9 +49,12 @@ struct FwdRowGeom {
   int64_t own0;     // first key of the own-branch tiles
   int n_a;          // number of prompt tiles
   int bn;           // keys per tile
+  int j0;           // first KV tile of the item (a split item's chunk; 0 otherwise)
 };
 
-__device__ __forceinline__ void fwd_valid_cols(const FwdRowGeom& g, int j, int& lo_i, int& hi_i) {
+// Valid columns of the item's j-th KV tile (tile j0 + j of the row's walk).
+__device__ __forceinline__ void fwd_valid_cols(const FwdRowGeom& g, int j_local, int& lo_i, int& hi_i) {
+  const int j = j_local + g.j0;
   const bool own = j >= g.n_a;
   const int64_t key0 = own ? g.own0 + (int64_t)(j - g.n_a) * g.bn : g.p0 + (int64_t)j * g.bn;
   int64_t lo, hi;
@@ -103,12 +106,15 @@ struct PingPong {
 // (only when the max grows by more than 2^8; exact, every term shares the offset),
 // writes P = exp2(s*log2e*S - m) as bf16 over S (one value in 64 from the FMA-pipe
 // exponential), adds the bf16 values to the row sum, and calls signal_p() once its
-// warpgroup may hand P to the MMA issuer.  At the end writes O / l (bf16) and lse.
-template <typename SignalP, typename Turn = NoTurn>
+// warpgroup may hand P to the MMA issuer.  At the end writes O / l (bf16) and lse; or,
+// with kMayPart and a non-null part_row (a split-KV item), the partial state O / l as
+// fp32 to part_row[128] and its lse to *part_lse (-inf and zeros if no key was valid).
+template <bool kMayPart = false, typename SignalP, typename Turn = NoTurn>
 __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const FwdRowGeom& g, int n_tiles, float sl2,
                                                 uint64_t* s_full, uint64_t* o_done, SignalP signal_p,
                                                 __nv_bfloat16* out_row, float* lse_ptr, uint32_t* err,
-                                                Turn turn = Turn()) {
+                                                Turn turn = Turn(), float* part_row = nullptr,
+                                                float* part_lse = nullptr) {
   float m = -INFINITY, l = 0.f;
   bool ok = true;
   for (int j = 0; j < n_tiles; ++j) {
@@ -197,6 +203,23 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
   if (ok && mbar_wait_warp_all(o_done, (n_tiles - 1) & 1, err)) {
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (kMayPart && part_row != nullptr) {
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait();
+        if (g.row_ok) {
+          float4* d4 = reinterpret_cast<float4*>(part_row + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        }
+      }
+      if (g.row_ok) *part_lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      return;
+    }
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];

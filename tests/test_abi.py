@@ -48,7 +48,7 @@ def test_schedule_bit_exact_with_reference_builder(augtree_lib, ti, kernel, dtyp
     for op in range(5):
         bm, bn = at.tile_sizes(cfg, op)
         got = at.schedule_build(tree.offsets(), cfg, op)
-        want = S.build(tree.offsets(), hq, hkv, op, bm, bn, sms)
+        want = S.build(tree.offsets(), hq, hkv, op, bm, bn, sms, split_replay_fwd=kernel == at.KERNEL_TC)
         assert got.shape == want.shape and np.array_equal(got, want), (op, bm, bn)
 
 
@@ -59,7 +59,7 @@ def test_schedule_bit_exact_on_the_benchmark_shapes(augtree_lib):
         for op in range(5):
             bm, bn = at.tile_sizes(cfg, op)
             got = at.schedule_build(w.tree.offsets(), cfg, op)
-            want = S.build(w.tree.offsets(), w.hq, w.hkv, op, bm, bn, 152)
+            want = S.build(w.tree.offsets(), w.hq, w.hkv, op, bm, bn, 152, split_replay_fwd=True)
             assert np.array_equal(got, want), (name, op)
 
 

@@ -86,17 +86,30 @@ TILES = [(4, 4), (8, 4), (4, 8), (16, 16), (8, 16)]
 @pytest.mark.parametrize("ti", range(len(TREES)))
 @pytest.mark.parametrize("bm,bn", TILES)
 @pytest.mark.parametrize("hq,hkv", [(4, 2), (2, 2)])
-def test_forward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv):
+@pytest.mark.parametrize("split", [False, True])
+def test_forward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv, split):
+    """Every valid (row, key) pair of every head exactly once; with the split-KV rule
+    (many SMs, so that the short replay queues split), split k of a tile walks the
+    chunk [k C, k C + cost) of the tile's KV walk, C the cost of its split 0."""
     tree = TREES[ti]
     groups = valid_pairs(tree)
     offs = tree.offsets()
+    sms = 1000 if split else 3
     for op, kind, side in ((S.OP_PREFILL_FWD, S.PREFILL_Q, "pp"), (S.OP_REPLAY_FWD, S.REPLAY_Q, None)):
-        q = S.build(offs, hq, hkv, op, bm, bn, num_sms=3)
+        q = S.build(offs, hq, hkv, op, bm, bn, num_sms=sms, split_replay_fwd=split)
         check_key_side_order(q, tree, bn, hq // hkv)
+        chunk, nsplit = {}, {}
+        for it in q:
+            k, g, tile, h, sp, cost, a, b = map(int, it)
+            if sp == 0:
+                chunk[(g, tile, h)] = cost
+            nsplit[(g, tile, h)] = max(nsplit.get((g, tile, h), 0), sp + 1)
+        walked = {}
         covered = {}
         for it in q:
-            k, g, tile, h, split, cost, a, b = map(int, it)
-            assert k == kind and split == 0
+            k, g, tile, h, sp, cost, a, b = map(int, it)
+            assert k == kind and (sp == 0 or (split and op == S.OP_REPLAY_FWD))
+            walked[(g, tile, h)] = walked.get((g, tile, h), 0) + cost
             grp = groups[g]
             if op == S.OP_PREFILL_FWD:
                 rows = range(grp["p0"] + tile * bm, min(grp["p0"] + (tile + 1) * bm, grp["p0"] + grp["lp"]))
@@ -109,7 +122,13 @@ def test_forward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv):
                 bstart = min(y for (rr, y) in grp["rr"] if rr == first)
                 tiles = [("p", grp["p0"] + j * bn) for j in range(a)] + \
                         [("r", bstart + j * bn) for j in range(b)]
-                assert cost == a + b
+                if nsplit[(g, tile, h)] == 1:
+                    assert cost == a + b
+                else:
+                    c = chunk[(g, tile, h)]
+                    assert nsplit[(g, tile, h)] == -(-(a + b) // c) and 0 < cost <= c
+                    assert cost == min(c, a + b - sp * c)
+                    tiles = tiles[sp * c: sp * c + cost]
             assert len(rows) > 0
             for (side_k, k0) in tiles:
                 keys = range(k0, k0 + bn)
@@ -125,6 +144,10 @@ def test_forward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv):
                             covered[(side_k, row, key, h)] = 1
                             hit += 1
                 assert hit > 0, "empty KV tile in an item"
+        if op == S.OP_REPLAY_FWD:
+            for (g, tile, h), n in walked.items():
+                it = [x for x in q if x[1] == g and x[2] == tile and x[3] == h][0]
+                assert n == int(it[6]) + int(it[7])  # the splits walk a + b tiles in all
         # every valid pair, every head
         for grp in groups:
             for h in range(hq):

@@ -24,7 +24,7 @@ def test_random_trees_bit_exact(augtree_lib, seed):
         for op in range(5):
             bm, bn = at.tile_sizes(cfg, op)
             got = at.schedule_build(tree.offsets(), cfg, op)
-            want = S.build(tree.offsets(), hq, hkv, op, bm, bn, sms)
+            want = S.build(tree.offsets(), hq, hkv, op, bm, bn, sms, split_replay_fwd=kernel == at.KERNEL_TC)
             assert got.shape == want.shape and np.array_equal(got, want), (seed, kernel, op)
 
 

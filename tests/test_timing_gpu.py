@@ -28,11 +28,15 @@ def test_kernel_times_cover_each_call(cuda_device):
     ev[2].record(stream)
     torch.cuda.synchronize()
     plan.check()
+    # This queue is short for the GPU: the replay forward splits its KV walks, and its
+    # partial states and dQ partials are merged and summed by two more kernels.
+    fsplit = bool((plan.schedule(at.OP_REPLAY_FWD)[:, 4] > 0).any())
+    assert fsplit
     assert [k for k, _ in plan.kernel_times(at.OP_PREFILL_FWD)] == ["fwd_tc"]
-    assert [k for k, _ in plan.kernel_times(at.OP_REPLAY_FWD)] == ["fwd_tc"]
+    assert [k for k, _ in plan.kernel_times(at.OP_REPLAY_FWD)] == ["fwd_tc", "fwd_split_merge"]
     rb = plan.kernel_times(at.OP_REPLAY_BWD)
     pb = plan.kernel_times(at.OP_PREFILL_BWD)
-    assert [k for k, _ in rb] == ["preprocess", "bwd_key_side", "split_reduce", "bwd_query_side"]
+    assert [k for k, _ in rb] == ["preprocess", "bwd_key_side", "split_reduce", "bwd_query_side", "dq_split_reduce"]
     assert [k for k, _ in pb] == ["preprocess", "bwd_key_side", "bwd_query_side"]
     fwd_ms = sum(m for op in (at.OP_PREFILL_FWD, at.OP_REPLAY_FWD) for _, m in plan.kernel_times(op))
     bwd_ms = sum(m for _, m in rb + pb)
@@ -59,8 +63,9 @@ def test_kernel_times_of_the_fused_backward(cuda_device):
     plan.check()
     tb = plan.kernel_times(at.OP_TREE_BWD)
     split = bool((plan.schedule(at.OP_TREE_BWD)[:, 4] > 0).any())
+    fsplit = bool((plan.schedule(at.OP_REPLAY_FWD)[:, 4] > 0).any())
     want = ["preprocess", "preprocess", "bwd_key_side"] + (["split_reduce"] if split else []) + \
-        ["bwd_query_side", "bwd_query_side"]
+        ["bwd_query_side", "bwd_query_side"] + (["dq_split_reduce"] if fsplit else [])
     assert [k for k, _ in tb] == want
     part = sum(m for _, m in tb)
     assert 0.0 < part <= e0.elapsed_time(e1) * 1.02 + 0.02

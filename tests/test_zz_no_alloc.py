@@ -17,6 +17,8 @@ and that a plan needing more scratch than the array holds is rejected before any
 is queued.  It is named to run last, and passes alone in a fresh process as well as
 after the other tests.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -59,13 +61,23 @@ def test_static_scratch_prefill_backward_matches_workspace_version(cuda_device, 
     outs = [[e(t["q_p"]), e(t["k_p"]), e(t["v_p"])] for _ in range(2)]
     torch.cuda.synchronize()
     for call in range(2):
-        alloc0 = torch.cuda.memory_allocated(cuda_device)
-        free0 = torch.cuda.mem_get_info(cuda_device)[0]
-        at.augtree_prefill_bwd_static(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], dk_acc, dv_acc,
-                                      *outs[call])
-        plan.check()
-        assert torch.cuda.memory_allocated(cuda_device) == alloc0, call
-        assert torch.cuda.mem_get_info(cuda_device)[0] == free0, call
+        # Tensors of earlier tests held in reference cycles (an exception's traceback,
+        # say) are freed whenever Python's cycle collector runs: collect them first and
+        # keep the collector off while the call is measured.
+        gc.collect()
+        gc.disable()
+        try:
+            alloc0 = torch.cuda.memory_allocated(cuda_device)
+            free0 = torch.cuda.mem_get_info(cuda_device)[0]
+            at.augtree_prefill_bwd_static(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], dk_acc,
+                                          dv_acc, *outs[call])
+            plan.check()
+            alloc1 = torch.cuda.memory_allocated(cuda_device)
+            free1 = torch.cuda.mem_get_info(cuda_device)[0]
+        finally:
+            gc.enable()
+        assert alloc1 == alloc0, call
+        assert free1 == free0, call
         for name, a, b in zip(("dq_p", "dk_p", "dv_p"), outs[call], ref):
             if kernel == at.KERNEL_SIMT and name == "dq_p":
                 err = rel_frob(a.double().cpu().numpy(), b.double().cpu().numpy())
