@@ -34,6 +34,7 @@ OP_PREFILL_FWD, OP_REPLAY_FWD, OP_REPLAY_BWD, OP_PREFILL_BWD, OP_TREE_BWD = 0, 1
 MAX_SPLIT = 64
 FWD_MIN_CHUNK = 4      # KV tiles per split of a replay query tile, at least
 MAX_FWD_PARTS = 4096   # partial states (query tile x head x split) of one plan, at most
+FWD_BLOCK_OVERHEAD = 2  # a block's fixed cost in KV tiles, for the choice of the chunk
 
 
 def _cdiv(a: int, b: int) -> int:
@@ -69,7 +70,7 @@ def _fwd_split_count(cost: int, target: int) -> int:
     return _cdiv(cost, _cdiv(cost, s)) if cost > 0 else 1
 
 
-def replay_fwd_splits(costs: List[int], hq: int, num_sms: int) -> List[int]:
+def replay_fwd_splits(costs: List[int], hq: int, hkv: int, num_sms: int) -> List[int]:
     """Split-KV rule of the replay forward (tensor-core kernels), per replay query tile
     with `costs[i]` KV tiles (prompt tiles, then own-branch tiles).
 
@@ -77,21 +78,33 @@ def replay_fwd_splits(costs: List[int], hq: int, num_sms: int) -> List[int]:
     online-softmax states that merge associatively into the exact result (MoveQ's
     global reduction of partial states).  Splitting a long query tile's KV walk over
     several blocks is worth it only when the queue has too few blocks for the GPU: with
-    fewer than 2 * num_sms items (query tile x head), each tile is cut into chunks of
-    about T = max(FWD_MIN_CHUNK, ceil(U / (4 * num_sms))) KV tiles, U the total cost of
-    the queue (so that about four items per SM result), T doubling until the number of
-    partial states (tiles x heads x splits, split tiles only) is at most MAX_FWD_PARTS.
-    Otherwise every tile keeps one item."""
+    fewer than 2 * num_sms items (query tile x head) the tiles are cut into chunks of
+    about T KV tiles; otherwise every tile keeps one item.  T is chosen among
+    ceil(c_max / s), s = 1..64 (c_max the largest cost; T >= FWD_MIN_CHUNK when s > 1;
+    at most MAX_FWD_PARTS partial states, tiles x heads x splits over split tiles), as
+    the one with the least estimated time
+        ceil(blocks / num_sms) * (largest chunk + FWD_BLOCK_OVERHEAD),
+    the first (largest T) on ties.  A block is one split of a tile for Hq / 2 head pairs
+    when the forward pairs heads (Hq and Hq / Hkv even), else for one head."""
     n_items = len(costs) * hq
     if n_items == 0 or n_items >= 2 * num_sms:
         return [1] * len(costs)
-    total = sum(costs) * hq
-    target = max(FWD_MIN_CHUNK, _cdiv(total, 4 * num_sms))
-    while True:
-        splits = [_fwd_split_count(c, target) for c in costs]
-        if sum(s * hq for s in splits if s > 1) <= MAX_FWD_PARTS:
-            return splits
-        target *= 2
+    per_tile = hq // 2 if hq % 2 == 0 and (hq // hkv) % 2 == 0 else hq
+    cmax = max(costs)
+    best_t, best_time = cmax, None
+    for sc in range(1, MAX_SPLIT + 1):
+        t = _cdiv(cmax, sc)
+        if sc > 1 and t < FWD_MIN_CHUNK:
+            break
+        splits = [_fwd_split_count(c, t) for c in costs]
+        if sum(s * hq for s in splits if s > 1) > MAX_FWD_PARTS:
+            continue
+        blocks = sum(per_tile * s for s in splits)
+        chunk_max = max(_cdiv(c, s) for c, s in zip(costs, splits))
+        time = _cdiv(blocks, num_sms) * (chunk_max + FWD_BLOCK_OVERHEAD)
+        if best_time is None or time < best_time:
+            best_t, best_time = t, time
+    return [_fwd_split_count(c, best_t) for c in costs]
 
 
 def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int,
@@ -125,7 +138,7 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int,
                 bstart = grp["starts"][_branch_of(grp, row_begin)]
                 b = _cdiv(row_end - bstart, bn)
                 tiles.append((g, t, a, b))
-        splits = replay_fwd_splits([a + b for (_, _, a, b) in tiles], hq, num_sms) if split_replay_fwd \
+        splits = replay_fwd_splits([a + b for (_, _, a, b) in tiles], hq, hkv, num_sms) if split_replay_fwd \
             else [1] * len(tiles)
         for (g, t, a, b), s in zip(tiles, splits):
             cost = a + b

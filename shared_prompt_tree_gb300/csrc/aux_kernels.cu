@@ -168,12 +168,13 @@ __global__ void split_reduce_kernel(const GroupInfo* __restrict__ groups, const 
   }
 }
 
-// Replay forward split-KV, one block per (split query tile, head), one warp per row,
-// four head dimensions per lane (D = 128).  The tile's nsplit partial states
-// (O_k = O over the chunk's keys / l_k, lse_k) merge as the n-way form of the state
-// merge (+) of Sec. 3.3: lse = log sum_k exp(lse_k), O = sum_k exp(lse_k - lse) O_k,
-// summed in ascending split order (deterministic).  A row whose splits all saw no valid
-// key gets O = 0 and lse = -inf.
+// Replay forward split-KV: one warp per (row, head) of a split query tile (block
+// (tile, head, group of 8 rows)), four head dimensions per lane (D = 128).  The tile's
+// nsplit <= 64 partial states (O_k = O over the chunk's keys / l_k, lse_k) merge as the
+// n-way form of the state merge (+) of Sec. 3.3: lse = log sum_k exp(lse_k),
+// O = sum_k exp(lse_k - lse) O_k, summed in ascending split order (deterministic).
+// Lane k holds lse_k and lse_{k+32}; the weights reach every lane by shuffles.  A row
+// whose splits all saw no valid key gets O = 0 and lse = -inf.
 __global__ void fwd_split_merge_kernel(const GroupInfo* __restrict__ groups, const FwdSplit* __restrict__ fsplit,
                                        const int32_t* __restrict__ tiles, int hq, const float* __restrict__ part_o,
                                        const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ o,
@@ -182,46 +183,46 @@ __global__ void fwd_split_merge_kernel(const GroupInfo* __restrict__ groups, con
   const int t = tiles[2 * blockIdx.x + 1];
   const FwdSplit fs = fsplit[G.tr0 + t];
   const int h = blockIdx.y;
-  const int64_t row0 = (int64_t)G.r0 + (int64_t)t * kFwdPartRows;
-  const int rows = (int)min((int64_t)kFwdPartRows, (int64_t)G.r0 + G.lr - row0);
-  const int64_t slot0 = fs.slot0 + (int64_t)h * fs.nsplit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < rows; r += blockDim.x >> 5) {
-    float m = -INFINITY;
-    for (int k = 0; k < fs.nsplit; ++k) m = fmaxf(m, part_lse[(slot0 + k) * kFwdPartRows + r]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float out_lse = -INFINITY;
-    if (m != -INFINITY) {
-      float sum = 0.f;
-      for (int k = 0; k < fs.nsplit; ++k) {
-        const float lk = part_lse[(slot0 + k) * kFwdPartRows + r];
-        sum += lk == -INFINITY ? 0.f : expf(lk - m);
-      }
-      out_lse = m + logf(sum);
-      for (int k = 0; k < fs.nsplit; ++k) {
-        const float lk = part_lse[(slot0 + k) * kFwdPartRows + r];
-        if (lk == -INFINITY) continue;
-        const float w = expf(lk - out_lse);
-        const float4 x = *reinterpret_cast<const float4*>(part_o + ((slot0 + k) * kFwdPartRows + r) * 128 + lane * 4);
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
-      }
+  const int r = blockIdx.z * (blockDim.x >> 5) + warp;
+  const int64_t row0 = (int64_t)G.r0 + (int64_t)t * kFwdPartRows;
+  if (r >= kFwdPartRows || row0 + r >= (int64_t)G.r0 + G.lr) return;
+  const int64_t slot0 = fs.slot0 + (int64_t)h * fs.nsplit;
+  const int n = fs.nsplit;
+  const float l0 = lane < n ? part_lse[(slot0 + lane) * kFwdPartRows + r] : -INFINITY;
+  const float l1 = lane + 32 < n ? part_lse[(slot0 + lane + 32) * kFwdPartRows + r] : -INFINITY;
+  const float m = warp_max(fmaxf(l0, l1));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float out_lse = -INFINITY;
+  if (m != -INFINITY) {
+    const float s = warp_sum((l0 == -INFINITY ? 0.f : expf(l0 - m)) + (l1 == -INFINITY ? 0.f : expf(l1 - m)));
+    out_lse = m + logf(s);
+    const float w0 = l0 == -INFINITY ? 0.f : expf(l0 - out_lse);
+    const float w1 = l1 == -INFINITY ? 0.f : expf(l1 - out_lse);
+    const float* src = part_o + (slot0 * kFwdPartRows + r) * 128 + lane * 4;
+    const int64_t step = (int64_t)kFwdPartRows * 128;
+#pragma unroll 4
+    for (int k = 0; k < n; ++k) {
+      const float w = __shfl_sync(0xffffffffu, k < 32 ? w0 : w1, k & 31);
+      const float4 x = *reinterpret_cast<const float4*>(src + k * step);
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
     }
-    const int64_t row = row0 + r;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(o + (row * hq + h) * 128 + lane * 4) = pk;
-    if (lane == 0) lse[(int64_t)h * total_resp + row] = out_lse;
   }
+  const int64_t row = row0 + r;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(o + (row * hq + h) * 128 + lane * 4) = pk;
+  if (lane == 0) lse[(int64_t)h * total_resp + row] = out_lse;
 }
 
-// Replay query-side backward split-KV: dQ of a split tile's rows is the sum of its
-// splits' fp32 partials, in ascending split order; one block per (split tile, head),
-// one warp per row.
+// Replay query-side backward split-KV: dQ of a split tile's row is the sum of its
+// splits' fp32 partials, in ascending split order; one warp per (row, head), blocks as
+// in the merge.
 __global__ void dq_split_reduce_kernel(const GroupInfo* __restrict__ groups, const FwdSplit* __restrict__ fsplit,
                                        const int32_t* __restrict__ tiles, int hq, const float* __restrict__ dq_part,
                                        __nv_bfloat16* __restrict__ dq) {
@@ -229,26 +230,28 @@ __global__ void dq_split_reduce_kernel(const GroupInfo* __restrict__ groups, con
   const int t = tiles[2 * blockIdx.x + 1];
   const FwdSplit fs = fsplit[G.tr0 + t];
   const int h = blockIdx.y;
-  const int64_t row0 = (int64_t)G.r0 + (int64_t)t * kFwdPartRows;
-  const int rows = (int)min((int64_t)kFwdPartRows, (int64_t)G.r0 + G.lr - row0);
-  const int64_t slot0 = fs.slot0 + (int64_t)h * fs.nsplit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < rows; r += blockDim.x >> 5) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < fs.nsplit; ++k) {
-      const float4 x = *reinterpret_cast<const float4*>(dq_part + ((slot0 + k) * kFwdPartRows + r) * 128 + lane * 4);
-      acc.x += x.x;
-      acc.y += x.y;
-      acc.z += x.z;
-      acc.w += x.w;
-    }
-    const int64_t row = row0 + r;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dq + (row * hq + h) * 128 + lane * 4) = pk;
+  const int r = blockIdx.z * (blockDim.x >> 5) + warp;
+  const int64_t row0 = (int64_t)G.r0 + (int64_t)t * kFwdPartRows;
+  if (r >= kFwdPartRows || row0 + r >= (int64_t)G.r0 + G.lr) return;
+  const int64_t slot0 = fs.slot0 + (int64_t)h * fs.nsplit;
+  const float* src = dq_part + (slot0 * kFwdPartRows + r) * 128 + lane * 4;
+  const int64_t step = (int64_t)kFwdPartRows * 128;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int k = 0; k < fs.nsplit; ++k) {
+    const float4 x = *reinterpret_cast<const float4*>(src + k * step);
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
   }
+  const int64_t row = row0 + r;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dq + (row * hq + h) * 128 + lane * 4) = pk;
 }
 
 // (O, lse) merge, one thread per (row, head) pair looping over d.
@@ -389,7 +392,7 @@ cudaError_t launch_fwd_split_merge(const augtree_plan* p, const float* part_o, c
   const size_t n_tiles = p->fsplit_tiles_h.size() / 2;
   if (n_tiles == 0) return cudaSuccess;
   if (p->cfg.head_dim != 128 || !part_o || !part_lse) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)n_tiles, p->cfg.hq);
+  dim3 grid((unsigned)n_tiles, p->cfg.hq, kFwdPartRows / 8);
   fwd_split_merge_kernel<<<grid, 256, 0, st>>>(p->groups_d, p->fsplit_d, p->fsplit_tiles_d, p->cfg.hq, part_o,
                                                part_lse, (__nv_bfloat16*)o, lse, p->total_resp);
   return cudaGetLastError();
@@ -399,7 +402,7 @@ cudaError_t launch_dq_split_reduce(const augtree_plan* p, const float* dq_part, 
   const size_t n_tiles = p->fsplit_tiles_h.size() / 2;
   if (n_tiles == 0) return cudaSuccess;
   if (p->cfg.head_dim != 128 || !dq_part) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)n_tiles, p->cfg.hq);
+  dim3 grid((unsigned)n_tiles, p->cfg.hq, kFwdPartRows / 8);
   dq_split_reduce_kernel<<<grid, 256, 0, st>>>(p->groups_d, p->fsplit_d, p->fsplit_tiles_d, p->cfg.hq, dq_part,
                                                (__nv_bfloat16*)dq);
   return cudaGetLastError();

@@ -113,30 +113,48 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 namespace augtree {
 
-void replay_fwd_splits(const std::vector<int64_t>& costs, int hq, int num_sms, std::vector<int64_t>& splits) {
+namespace {
+// Splits of a replay query tile walking c KV tiles at about T tiles per split.
+int64_t fwd_split_count(int64_t c, int64_t T) {
+  const int64_t s = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, cdiv(c, T)));
+  return c > 0 ? cdiv(c, cdiv(c, s)) : 1;
+}
+}  // namespace
+
+void replay_fwd_splits(const std::vector<int64_t>& costs, int hq, int hkv, int num_sms, std::vector<int64_t>& splits) {
   // Split-KV of the replay forward (Sec. 3.3: partial states over disjoint key ranges
   // merge exactly).  Only a queue with fewer than 2 * num_sms items (too few blocks for
-  // the GPU) is split: each query tile into chunks of about T KV tiles, T = max(4,
-  // ceil(U / (4 * num_sms))) for a queue of total cost U (about four items per SM),
-  // doubled until the split tiles hold at most kMaxFwdParts partial states.
+  // the GPU) is split.  The chunk T is the one of the candidates ceil(c_max / s),
+  // s = 1..64 (c_max the largest tile cost, T >= kFwdMinChunk for s > 1, at most
+  // kMaxFwdParts partial states) that minimises the estimated time
+  //   ceil(blocks / num_sms) * (largest chunk + kFwdBlockOverhead)
+  // (waves of blocks times the longest block; a block is one split of a tile for two
+  // query heads when the forward pairs heads, else one); ties keep the larger T.
   splits.assign(costs.size(), 1);
   const int64_t n_items = (int64_t)costs.size() * hq;
   if (n_items == 0 || n_items >= 2 * (int64_t)num_sms) return;
-  int64_t total = 0;
-  for (int64_t c : costs) total += c * hq;
-  int64_t target = std::max<int64_t>(kFwdMinChunk, cdiv(total, 4 * (int64_t)num_sms));
-  for (;;) {
-    int64_t parts = 0;
-    for (size_t i = 0; i < costs.size(); ++i) {
-      const int64_t c = costs[i];
-      int64_t s = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, cdiv(c, target)));
-      s = c > 0 ? cdiv(c, cdiv(c, s)) : 1;
-      splits[i] = s;
-      if (s > 1) parts += s * hq;
+  const int64_t per_tile = (hq % 2 == 0 && (hq / hkv) % 2 == 0) ? hq / 2 : hq;
+  int64_t cmax = 0;
+  for (int64_t c : costs) cmax = std::max(cmax, c);
+  int64_t best_t = cmax, best_time = -1;
+  for (int64_t sc = 1; sc <= kMaxSplit; ++sc) {
+    const int64_t T = cdiv(cmax, sc);
+    if (sc > 1 && T < kFwdMinChunk) break;
+    int64_t blocks = 0, parts = 0, chunk_max = 0;
+    for (int64_t c : costs) {
+      const int64_t st = fwd_split_count(c, T);
+      blocks += per_tile * st;
+      if (st > 1) parts += (int64_t)hq * st;
+      chunk_max = std::max(chunk_max, cdiv(c, st));
     }
-    if (parts <= kMaxFwdParts) return;
-    target *= 2;
+    if (parts > kMaxFwdParts) continue;
+    const int64_t time = cdiv(blocks, num_sms) * (chunk_max + kFwdBlockOverhead);
+    if (best_time < 0 || time < best_time) {
+      best_time = time;
+      best_t = T;
+    }
   }
+  for (size_t i = 0; i < costs.size(); ++i) splits[i] = fwd_split_count(costs[i], best_t);
 }
 
 augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int32_t>& bb,
@@ -184,7 +202,7 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
       }
     }
     std::vector<int64_t> splits(tiles.size(), 1);
-    if (split_fwd) replay_fwd_splits(costs, hq, num_sms, splits);
+    if (split_fwd) replay_fwd_splits(costs, hq, hkv, num_sms, splits);
     for (size_t i = 0; i < tiles.size(); ++i) {
       const RT& x = tiles[i];
       const int64_t cost = x.a + x.b, s = splits[i], c = cdiv(cost, s);

@@ -15,9 +15,11 @@ enum ItemKind { K_PREFILL_Q = 0, K_REPLAY_Q = 1, K_PROMPT_KV = 2, K_RESP_KV = 3,
 constexpr int kNumOps = 5;  // queues per plan: the four calls' ops and the fused backward
 constexpr int kMaxSplit = 64;
 // Split-KV of the replay forward: KV tiles per split at least, partial states per plan
-// at most.
+// at most, and a block's fixed cost (prologue, partial write) in KV tiles for the
+// choice of the chunk.
 constexpr int kFwdMinChunk = 4;
 constexpr int64_t kMaxFwdParts = 4096;
+constexpr int kFwdBlockOverhead = 2;
 // Limit of a device-side wait on another warp's work: default and largest settable.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 constexpr uint64_t kMaxWaitLimitNs = 60000000000ull;
@@ -137,7 +139,7 @@ augtree_status build_queue(const std::vector<int32_t>& prompt_off, const std::ve
                            const std::vector<int32_t>& resp_off, int hq, int hkv, int op, int bm, int bn,
                            int num_sms, bool split_fwd, std::vector<int32_t>& out);
 // Split counts of the replay query tiles with the given KV-tile costs.
-void replay_fwd_splits(const std::vector<int64_t>& costs, int hq, int num_sms, std::vector<int64_t>& splits);
+void replay_fwd_splits(const std::vector<int64_t>& costs, int hq, int hkv, int num_sms, std::vector<int64_t>& splits);
 
 // Workspace of the replay forward with split-KV: fp32 O partials [n_parts][128][D],
 // then fp32 lse partials [n_parts][128].

@@ -294,5 +294,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Largest of three values in one instruction (three-input max, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// acc + lo + hi for the two bf16 values packed in x (low half first), each widened
+// exactly and added in fp32 round-to-nearest by the mixed-precision add (sm_100 and
+// later): two instructions instead of two unpacks and two adds.
+__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t x) {
+  asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\nadd.rn.f32.bf16 %0, lo, %0;\nadd.rn.f32.bf16 %0, hi, %0;\n}"
+      : "+f"(acc)
+      : "r"(x));
+  return acc;
+}
+
 }  // namespace tc
 }  // namespace augtree

@@ -37,6 +37,13 @@ constexpr int kFwdFmaOffset = AUGTREE_FWD_FMA_OFFSET;
 #define AUGTREE_FWD_TURN_POS 0
 #endif
 constexpr int kFwdTurnPos = AUGTREE_FWD_TURN_POS;
+// Row max with three-input max instructions and row sum with mixed-precision bf16 adds
+// (about 190 instead of about 380 instructions per row and tile); 0: two-input max,
+// unpack-and-add.
+#ifndef AUGTREE_FWD_MIXED_OPS
+#define AUGTREE_FWD_MIXED_OPS 1
+#endif
+constexpr bool kFwdMixedOps = AUGTREE_FWD_MIXED_OPS != 0;
 
 // Where the row's keys come from in KV tile j: prompt tiles first, then the own-branch
 // tiles, and the valid columns [lo, hi] of the row in that tile.
@@ -137,11 +144,27 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     // Row max with 8 independent partial maxima (a single 127-long dependent chain
     // would dominate the latency of the warpgroup's turn).
     float pm[8];
+    float tmax;
+    if (kFwdMixedOps) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(AUGTREE_X(k));
+      for (int k = 0; k < 8; ++k)
+        pm[k] = fmax3(__uint_as_float(AUGTREE_X(k)), __uint_as_float(AUGTREE_X(k + 8)),
+                      __uint_as_float(AUGTREE_X(k + 16)));
 #pragma unroll
-    for (int c = 8; c < 128; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(AUGTREE_X(c)));
-    const float tmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      for (int c = 24; c < 120; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          pm[k] = fmax3(pm[k], __uint_as_float(AUGTREE_X(c + k)), __uint_as_float(AUGTREE_X(c + 8 + k)));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], __uint_as_float(AUGTREE_X(120 + k)));
+      tmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(AUGTREE_X(k));
+#pragma unroll
+      for (int c = 8; c < 128; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(AUGTREE_X(c)));
+      tmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+    }
     const float mx = tmax * sl2;  // -inf stays -inf
     const bool need = (m != -INFINITY) && (mx > m + 8.0f);
     const float m_new = (m == -INFINITY) ? mx : (need ? mx : m);
@@ -171,7 +194,10 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
         pk[i] = pack_bf16x2(p0, p1);
         // The denominator sums the bf16 values the PV product uses, so numerator and
         // denominator carry the same rounded weights.
-        ps[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+        if (kFwdMixedOps)
+          ps[i & 3] = add_bf16x2_f32(ps[i & 3], pk[i]);
+        else
+          ps[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
       }
       tmem_st32(tS + c * 32, pk);
       if (kFwdTurnPos == 1 && c == 0) turn.pass();

@@ -89,8 +89,9 @@ TILES = [(4, 4), (8, 4), (4, 8), (16, 16), (8, 16)]
 @pytest.mark.parametrize("split", [False, True])
 def test_forward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv, split):
     """Every valid (row, key) pair of every head exactly once; with the split-KV rule
-    (many SMs, so that the short replay queues split), split k of a tile walks the
-    chunk [k C, k C + cost) of the tile's KV walk, C the cost of its split 0."""
+    (1000 SMs, so that the short replay queues split into small chunks), split k of a
+    tile walks the chunk [k C, k C + cost) of the tile's KV walk, C the cost of its
+    split 0."""
     tree = TREES[ti]
     groups = valid_pairs(tree)
     offs = tree.offsets()
