@@ -46,12 +46,6 @@ using namespace tc;
 #define AUGTREE_DQ_EXP_FMA 0
 #endif
 constexpr int kDqExpFma = AUGTREE_DQ_EXP_FMA;  // 0, or N: one exponential in N via exp2_fma
-// TMEM loads of S and dP: one 64-column load each (1), or 32-column loads with dP's two
-// halves loaded and waited for one after the other (0).
-#ifndef AUGTREE_DQ_LD64
-#define AUGTREE_DQ_LD64 0
-#endif
-constexpr bool kDqLd64 = AUGTREE_DQ_LD64 != 0;
 constexpr int DQ_THREADS = 352;  // 8 compute warps, producer, two MMA issuers
 // K tiles are read by S(j) and dQ(j), V tiles only by dP(j), so the two rings are
 // separate: a V stage frees as soon as dP(j) is done, and the K ring has one stage more
@@ -338,12 +332,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       const uint32_t ts = tmem + lane_off + T_S + c0;
       const uint32_t tdp = tmem + lane_off + T_DP + (j & 1) * 128 + c0;
       uint32_t sv[2][32];  // S, then P in place (fp32)
-      if (kDqLd64) {
-        tmem_ld64(ts, &sv[0][0]);
-      } else {
-        tmem_ld32(ts, sv[0]);
-        tmem_ld32(ts + 32, sv[1]);
-      }
+      tmem_ld32(ts, sv[0]);
+      tmem_ld32(ts + 32, sv[1]);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars->s_free);
@@ -370,21 +360,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
       if (!(ok = mbar_wait_warp_all(&bars->dp_full[j & 1], (j >> 1) & 1, err))) break;
       tc_fence_after();
       uint32_t pk[2][16];  // dS as bf16 pairs
-      uint32_t dp_all[kDqLd64 ? 64 : 1];
-      if (kDqLd64) {
-        tmem_ld64(tdp, dp_all);
-        tmem_ld_wait();
-      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t dp[32];
-        if (kDqLd64) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) dp[i] = dp_all[kDqLd64 ? half * 32 + i : 0];
-        } else {
-          tmem_ld32(tdp + half * 32, dp);
-          tmem_ld_wait();
-        }
+        tmem_ld32(tdp + half * 32, dp);
+        tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float d0 = __uint_as_float(sv[half][2 * i]) * (__uint_as_float(dp[2 * i]) - delta);

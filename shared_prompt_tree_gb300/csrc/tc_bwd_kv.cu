@@ -64,11 +64,6 @@ constexpr bool DB = BMQ == 64;
 #endif
 constexpr int kKvExpFma = AUGTREE_KV_EXP_FMA;           // 0, or N: one exponential in N via exp2_fma
 static_assert(kKvExpFma == 0 || (kKvExpFma >= 2 && kKvExpFma % 2 == 0), "exp2_fma fraction");
-// TMEM loads of S^T and dP^T: one 64-column load per phase (1) or 32-column loads (0).
-#ifndef AUGTREE_KV_LD64
-#define AUGTREE_KV_LD64 0
-#endif
-constexpr bool kKvLd64 = AUGTREE_KV_LD64 != 0;
 constexpr int NWG = 2;                                  // compute warpgroups
 constexpr int COLS = BMQ / NWG;                         // query columns per warpgroup
 constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1, MMA2_WARP = 4 * NWG + 2;
@@ -463,12 +458,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       tc_fence_after();
       uint32_t sraw[COLS / 32][32];
 #pragma unroll
-      if (kKvLd64 && COLS == 64) {
-        tmem_ld64(ts, &sraw[0][0]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < COLS / 32; ++k) tmem_ld32(ts + 32 * k, sraw[k]);
-      }
+      for (int k = 0; k < COLS / 32; ++k) tmem_ld32(ts + 32 * k, sraw[k]);
       tmem_ld_wait();
       // this warpgroup's valid columns: [lo, hi) relative to c0
       const int64_t lo64 = v_lo - row0 - c0, hi64 = v_hi - row0 - c0;
@@ -506,12 +496,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       if (!(ok = mbar_wait_warp_all(&bars->dp_full[b], kv_phase(i), err))) break;
       tc_fence_after();
 #pragma unroll
-      if (kKvLd64 && COLS == 64) {
-        tmem_ld64(tdp, &sraw[0][0]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < COLS / 32; ++k) tmem_ld32(tdp + 32 * k, sraw[k]);
-      }
+      for (int k = 0; k < COLS / 32; ++k) tmem_ld32(tdp + 32 * k, sraw[k]);
       tmem_ld_wait();
       // the accumulator holds dP^T - Delta
 #pragma unroll

@@ -44,17 +44,6 @@ constexpr int kFwdTurnPos = AUGTREE_FWD_TURN_POS;
 #define AUGTREE_FWD_MIXED_OPS 1
 #endif
 constexpr bool kFwdMixedOps = AUGTREE_FWD_MIXED_OPS != 0;
-// TMEM access shapes of the softmax: S loaded in loads of kFwdLdCols columns (32, 64 or
-// 128); P stored per half of the row (0) or in one 64-column store at the end (1).
-#ifndef AUGTREE_FWD_LD_COLS
-#define AUGTREE_FWD_LD_COLS 32
-#endif
-#ifndef AUGTREE_FWD_P_ONE_STORE
-#define AUGTREE_FWD_P_ONE_STORE 0
-#endif
-constexpr int kFwdLdCols = AUGTREE_FWD_LD_COLS;
-constexpr bool kFwdPOneStore = AUGTREE_FWD_P_ONE_STORE != 0;
-static_assert(kFwdLdCols == 32 || kFwdLdCols == 64 || kFwdLdCols == 128, "load shape");
 
 // Where the row's keys come from in KV tile j: prompt tiles first, then the own-branch
 // tiles, and the valid columns [lo, hi] of the row in that tile.
@@ -139,15 +128,8 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     if (!(ok = mbar_wait_warp_all(s_full, j & 1, err))) break;
     tc_fence_after();
     uint32_t raw[4][32];  // S row, reinterpreted as fp32 in place (no second copy)
-    if (kFwdLdCols == 128) {
-      tmem_ld128(tS, &raw[0][0]);
-    } else if (kFwdLdCols == 64) {
-      tmem_ld64(tS, &raw[0][0]);
-      tmem_ld64(tS + 64, &raw[2][0]);
-    } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, raw[c]);
-    }
+    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, raw[c]);
     tmem_ld_wait();
 #define AUGTREE_X(c) raw[(c) >> 5][(c) & 31]
     if (kFwdTurnPos == 2 && !(ok = turn.wait(j, err))) break;
@@ -191,7 +173,6 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
     const float mu = (m == -INFINITY) ? 0.f : m;
     if (kFwdTurnPos != 2 && !(ok = turn.wait(j, err))) break;
     float ps[4] = {0.f, 0.f, 0.f, 0.f};  // 4 independent partial sums
-    uint32_t pk_all[kFwdPOneStore ? 64 : 1];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       uint32_t pk[32];
@@ -218,15 +199,9 @@ __device__ __forceinline__ void fwd_softmax_row(uint32_t tS, uint32_t tO, const 
         else
           ps[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
       }
-      if (kFwdPOneStore) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk_all[(kFwdPOneStore ? c * 32 + i : 0)] = pk[i];
-      } else {
-        tmem_st32(tS + c * 32, pk);
-      }
+      tmem_st32(tS + c * 32, pk);
       if (kFwdTurnPos == 1 && c == 0) turn.pass();
     }
-    if (kFwdPOneStore) tmem_st64(tS, pk_all);
 #undef AUGTREE_X
     if (kFwdTurnPos != 1) turn.pass();
     tmem_st_wait();
