@@ -18,13 +18,15 @@ from tests.gpu_util import compare, device_inputs, rel_frob, run_cuda, run_oracl
 pytestmark = pytest.mark.gpu
 
 # (tree, hq, hkv): 1-3-token branches under 4k-8k prompts; a single response row; chunk
-# boundaries inside the own-branch tiles; an empty prompt.
+# boundaries inside the own-branch tiles; an empty prompt; a 16k prompt whose one query
+# tile splits 33 ways (the merge's second group of 32 splits).
 CASES = [
     (W.Tree([8192], [[3] * 32]), 32, 8),
     (W.Tree([4000, 8000], [[1, 2, 3, 1], [3, 3, 2]]), 4, 2),
     (W.Tree([8192], [[1]]), 4, 1),
     (W.Tree([300], [[600]]), 2, 2),
     (W.Tree([0], [[1000]]), 2, 1),
+    (W.Tree([16384], [[1]]), 2, 1),
 ]
 
 
@@ -39,6 +41,8 @@ def test_split_kv_matches_oracle(cuda_device, ci):
     w = W.custom(tree, hq=hq, hkv=hkv, d=128, dtype="bf16", seed=900 + ci)
     plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=at.BF16, kernel=at.KERNEL_TC)
     assert _split_items(plan) > 0 and plan.workspace_bytes(at.OP_REPLAY_FWD) > 0
+    if ci == len(CASES) - 1:
+        assert int(plan.schedule(at.OP_REPLAY_FWD)[:, 4].max()) + 1 == 33
     compare(run_cuda(w, plan=plan), run_oracle(w), "bf16")
 
 
