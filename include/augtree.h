@@ -232,7 +232,9 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
                                    augtree_plan** out);
 augtree_status augtree_plan_destroy(augtree_plan* plan);
 
-/* Workspace bytes each compute call needs (0 allowed: pass ws = NULL).  The prefill
+/* Workspace bytes each compute call needs (0 allowed: pass ws = NULL).  A workspace is
+ * device memory owned by the caller, 16-byte aligned (AUGTREE_ERR_INVALID_ARG
+ * otherwise), and its contents on entry do not matter.  The prefill
  * forward needs none; the replay forward needs one only when its queue is split-KV
  * (n_parts partial states: 64 KiB of fp32 O plus 512 bytes of lse each, 256-byte
  * aligned); the replay and fused backward add 64 KiB of fp32 dQ per partial state. */

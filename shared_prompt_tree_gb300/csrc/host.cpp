@@ -10,6 +10,7 @@
 //                   balancing (the work queues built here; thread blocks are the lanes).
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <tuple>
@@ -834,7 +835,7 @@ augtree_status augtree_replay_fwd(const augtree_plan* p, const void* qr, const v
   if (p->total_resp > 0 && p->total_prompt > 0 && (!kp || !vp)) return AUGTREE_ERR_INVALID_ARG;
   const FwdWorkspace w = replay_fwd_ws(p);
   if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
-  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
+  if (w.total > 0 && (!ws || ((uintptr_t)ws & 15u))) return AUGTREE_ERR_INVALID_ARG;
   augtree_status st = check_device(p);
   if (st != AUGTREE_OK) return st;
   if (p->n_items[AUGTREE_OP_REPLAY_FWD] == 0) return AUGTREE_OK;
@@ -871,7 +872,7 @@ augtree_status augtree_replay_bwd(const augtree_plan* p, const void* qr, const v
   if (p->total_resp > 0 && p->total_prompt > 0 && (!kp || !vp)) return AUGTREE_ERR_INVALID_ARG;
   BwdWorkspace w = replay_bwd_ws(p);
   if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
-  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
+  if (w.total > 0 && (!ws || ((uintptr_t)ws & 15u))) return AUGTREE_ERR_INVALID_ARG;
   augtree_status st = check_device(p);
   if (st != AUGTREE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
@@ -945,7 +946,7 @@ augtree_status augtree_prefill_bwd(const augtree_plan* p, const void* qp, const 
   if ((dkp_acc == nullptr) != (dvp_acc == nullptr)) return AUGTREE_ERR_INVALID_ARG;
   BwdWorkspace w = prefill_bwd_ws(p);
   if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
-  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
+  if (w.total > 0 && (!ws || ((uintptr_t)ws & 15u))) return AUGTREE_ERR_INVALID_ARG;
   augtree_status st = check_device(p);
   if (st != AUGTREE_OK) return st;
   if (p->total_prompt == 0) return AUGTREE_OK;
@@ -999,7 +1000,7 @@ augtree_status augtree_tree_bwd(const augtree_plan* p, const void* qp, const voi
     return AUGTREE_ERR_INVALID_ARG;
   const TreeWorkspace w = tree_bwd_ws(p);
   if (ws_bytes < w.total) return AUGTREE_ERR_WORKSPACE_TOO_SMALL;
-  if (w.total > 0 && !ws) return AUGTREE_ERR_INVALID_ARG;
+  if (w.total > 0 && (!ws || ((uintptr_t)ws & 15u))) return AUGTREE_ERR_INVALID_ARG;
   augtree_status st = check_device(p);
   if (st != AUGTREE_OK) return st;
   char* base = (char*)ws;

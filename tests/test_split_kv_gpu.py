@@ -110,3 +110,10 @@ def test_split_kv_forward_rejects_a_small_workspace(cuda_device):
         with pytest.raises(at.AugtreeError) as e:
             at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, ws)
         assert e.value.status in (at.ERR_WORKSPACE_TOO_SMALL, at.ERR_INVALID_ARG)
+    # A workspace must start on a 16-byte boundary (its partial states are written in
+    # 16-byte vectors).
+    big = torch.empty(need + 16, dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(at.AugtreeError) as e:
+        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, big[8:])
+    assert e.value.status == at.ERR_INVALID_ARG
+    del e
