@@ -531,6 +531,8 @@ def run_ours(args):
             "ms_per_step": round(mf["ms"], 3), "pairs": wf.tree.pair_count(), "tree_pairs": w.tree.pair_count(),
             "speedup_of_tree": round(mf["ms"] / ms_step, 3), "steps": max(1, min(args.steps, 3)),
             "backward": result["config"]["backward"]}
+    if not args.no_split_kv and args.scale_down == 1 and w.dtype == "bf16" and kernel != at.KERNEL_SIMT:
+        result["split_kv_replay_fwd"] = split_kv_probe(at, dev)
     if not args.no_per_workload and args.scale_down == 1:
         # The other bf16 configurations, each timed the same way (fewer steps for the
         # long one, whose step takes seconds).
@@ -556,6 +558,49 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def split_kv_probe(at, dev, reps=20):
+    """Replay forward of a queue too short for the GPU: one 8,192-token prompt under 32
+    branches of 3 tokens (Hq 32, Hkv 8, one 128-row query tile, 16 two-head blocks when
+    whole).  The split-KV queue (the device's SM count as balancing width) against the
+    same tile unsplit (balancing width 1), CUDA events around `reps` calls each; the
+    split call's kernels (forward and the merge of the partial states) from the plan's
+    kernel timing."""
+    import torch
+    import workloads as W
+    w = W.custom(W.Tree([8192], [[3] * 32]), hq=32, hkv=8, d=128, dtype="bf16", seed=5)
+    t = {n: W.tensor_torch(w, n, dev) for n in ("q_r", "k_p", "v_p", "k_r", "v_r")}
+    out = {"tree": "prompt 8192, 32 branches x 3 tokens, Hq 32, Hkv 8, D 128, bf16"}
+    for label, sms in (("split", 0), ("whole", 1)):
+        plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=at.BF16, kernel=at.KERNEL_TC, num_sms=sms)
+        o = torch.empty_like(t["q_r"])
+        lse = torch.empty(w.hq, w.tree.total_resp, dtype=torch.float32, device=dev)
+        nb = plan.workspace_bytes(at.OP_REPLAY_FWD)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        call = lambda: at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o, lse, ws)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        q = plan.schedule(at.OP_REPLAY_FWD)
+        row = {"ms": round(e0.elapsed_time(e1) / reps, 4), "items": int(len(q)),
+               "splits_per_tile": int(q[:, 4].max()) + 1, "workspace_bytes": int(nb)}
+        if label == "split":
+            plan.set_timing(True)
+            call()
+            torch.cuda.synchronize()
+            row["kernels_ms"] = {k: round(m, 4) for k, m in plan.kernel_times(at.OP_REPLAY_FWD)}
+        plan.check()
+        plan.close()
+        out[label] = row
+    out["speedup"] = round(out["whole"]["ms"] / out["split"]["ms"], 3)
+    return out
 
 
 def flattened(w):
@@ -661,6 +706,8 @@ def main():
     ap.add_argument("--no-flattened", action="store_true",
                     help="skip timing the flattened-per-pair structure (no prompt reuse)")
     ap.add_argument("--no-per-workload", action="store_true", help="skip timing the other configurations")
+    ap.add_argument("--no-split-kv", action="store_true",
+                    help="skip timing the split-KV replay forward of a short-response tree")
     args = ap.parse_args()
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(spawn_replicas(args.gpus))
