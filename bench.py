@@ -627,19 +627,23 @@ def scaled_down(w, k):
 
 
 def count_launches(plan, at, fused=False):
-    """Kernels one step launches: prefill fwd 1, replay fwd 1; then either the fused
-    backward (preprocess per side, key side, split reduce when a group is split, query
-    side per side) or replay bwd 4 (preprocess, key side, split reduce, query side) and
-    prefill bwd 3."""
+    """Kernels one step launches: prefill fwd 1, replay fwd 1 (plus the split-KV merge
+    when the replay queue is split); then either the fused backward (preprocess per
+    side, key side, split reduce when a group is split, query side per side, the
+    split-KV dQ sum) or replay bwd 4 (preprocess, key side, split reduce, query side;
+    plus the dQ sum) and prefill bwd 3."""
     n = 0
     n += 1 if plan.schedule(at.OP_PREFILL_FWD).shape[0] else 0
-    n += 1 if plan.schedule(at.OP_REPLAY_FWD).shape[0] else 0
+    qf = plan.schedule(at.OP_REPLAY_FWD)
+    fsplit = bool(qf.shape[0]) and bool((qf[:, 4] > 0).any())
+    n += (1 if qf.shape[0] else 0) + (1 if fsplit else 0)
     if fused:
         q = plan.schedule(at.OP_TREE_BWD)
         split = bool(q.shape[0]) and bool((q[:, 4] > 0).any())
         n += 2 * (1 if plan.total_resp else 0) + 2 * (1 if plan.total_prompt else 0)
-        n += (1 if q.shape[0] else 0) + (1 if split else 0)
+        n += (1 if q.shape[0] else 0) + (1 if split else 0) + (1 if fsplit else 0)
         return n
+    n += 1 if fsplit else 0
     n += (1 if plan.total_resp else 0) + (1 if plan.schedule(at.OP_REPLAY_BWD).shape[0] else 0) \
         + (1 if plan.total_prompt else 0) + (1 if plan.total_resp else 0)
     n += 3 if plan.total_prompt else 0
