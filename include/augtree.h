@@ -141,8 +141,8 @@ typedef struct augtree_plan augtree_plan;
  * s(c, T) = ceil(c / ceil(c / min(64, max(1, ceil(c / T))))) splits for the chunk T
  * chosen among ceil(c_max / k), k = 1..64 (c_max the largest tile cost; T >= 4 for
  * k > 1; the split tiles, s > 1, holding at most 4096 partial states, tiles x Hq x s)
- * with the least ceil(B / num_sms) * (max_tile ceil(c / s) + 2), B = sum over tiles of
- * s times Hq/2 (heads paired: Hq and Hq/Hkv even) or Hq; the largest T on ties.
+ * with the least ceil(B / num_sms) * (max_tile ceil(c / s) + 2), B = Hq times the sum
+ * over tiles of s (one thread block per split and head); the largest T on ties.
  * The replay forward then needs a workspace for the partial states and merges them in
  * split order; the replay query-side backward (same items) writes fp32 dQ partials and
  * sums them in split order.  The SIMT kernels never split.

@@ -84,12 +84,12 @@ def replay_fwd_splits(costs: List[int], hq: int, hkv: int, num_sms: int) -> List
     at most MAX_FWD_PARTS partial states, tiles x heads x splits over split tiles), as
     the one with the least estimated time
         ceil(blocks / num_sms) * (largest chunk + FWD_BLOCK_OVERHEAD),
-    the first (largest T) on ties.  A block is one split of a tile for Hq / 2 head pairs
-    when the forward pairs heads (Hq and Hq / Hkv even), else for one head."""
+    the first (largest T) on ties.  A block is one split of a tile for one query head
+    (Hq blocks per split of a tile); hkv does not enter."""
     n_items = len(costs) * hq
     if n_items == 0 or n_items >= 2 * num_sms:
         return [1] * len(costs)
-    per_tile = hq // 2 if hq % 2 == 0 and (hq // hkv) % 2 == 0 else hq
+    per_tile = hq
     cmax = max(costs)
     best_t, best_time = cmax, None
     for sc in range(1, MAX_SPLIT + 1):

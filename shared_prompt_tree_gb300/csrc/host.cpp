@@ -129,12 +129,13 @@ void replay_fwd_splits(const std::vector<int64_t>& costs, int hq, int hkv, int n
   // s = 1..64 (c_max the largest tile cost, T >= kFwdMinChunk for s > 1, at most
   // kMaxFwdParts partial states) that minimises the estimated time
   //   ceil(blocks / num_sms) * (largest chunk + kFwdBlockOverhead)
-  // (waves of blocks times the longest block; a block is one split of a tile for two
-  // query heads when the forward pairs heads, else one); ties keep the larger T.
+  // (waves of blocks times the longest block; a block is one split of a tile for one
+  // query head); ties keep the larger T.
+  (void)hkv;
   splits.assign(costs.size(), 1);
   const int64_t n_items = (int64_t)costs.size() * hq;
   if (n_items == 0 || n_items >= 2 * (int64_t)num_sms) return;
-  const int64_t per_tile = (hq % 2 == 0 && (hq / hkv) % 2 == 0) ? hq / 2 : hq;
+  const int64_t per_tile = hq;
   int64_t cmax = 0;
   for (int64_t c : costs) cmax = std::max(cmax, c);
   int64_t best_t = cmax, best_time = -1;
@@ -328,20 +329,6 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   out.resize(items.size() * AUGTREE_ITEM_WORDS);
   if (!items.empty()) std::memcpy(out.data(), items.data(), items.size() * sizeof(Item));
   return AUGTREE_OK;
-}
-
-bool queue_pairs(const std::vector<int32_t>& q, int hq, int hkv) {
-  // Consecutive items 2i, 2i+1: the same kind, group, query tile and split, heads h and
-  // h + 1 with h even; they then share a KV head when Hq / Hkv is even.
-  const size_t n = q.size() / AUGTREE_ITEM_WORDS;
-  const int r = hq / hkv;
-  bool ok = (hq % 2 == 0) && (r % 2 == 0) && (n % 2 == 0);
-  for (size_t i = 0; ok && i + 1 < n; i += 2) {
-    const int32_t* a = &q[i * AUGTREE_ITEM_WORDS];
-    const int32_t* b = a + AUGTREE_ITEM_WORDS;
-    ok = a[1] == b[1] && a[2] == b[2] && a[0] == b[0] && a[4] == b[4] && a[3] % 2 == 0 && b[3] == a[3] + 1;
-  }
-  return ok;
 }
 
 augtree_status build_lanes(const std::vector<int32_t>& q, int unit_items, int lanes, LaneSet& out) {
@@ -657,14 +644,6 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
       return st;
     }
     p->n_items[op] = p->queue_h[op].size() / AUGTREE_ITEM_WORDS;
-  }
-  // Forward tensor-core units pair consecutive items: heads h, h+1 (h even) of one
-  // query tile share their KV head when Hq/Hkv is even.  The sort order puts the Hq
-  // items of a (group, tile) next to each other, so pairs are checked, not assumed.
-  for (int op = 0; op < kNumOps; ++op) {
-    p->paired[op] = 0;
-    if (p->family != AUGTREE_KERNEL_TC || op > AUGTREE_OP_REPLAY_FWD) continue;
-    p->paired[op] = queue_pairs(p->queue_h[op], cfg->hq, cfg->hkv) ? 1 : 0;
   }
   // Persistent schedule: AssignGrid's placement of every tensor-core kernel's units.
   if (p->family == AUGTREE_KERNEL_TC && cfg->schedule == AUGTREE_SCHED_PERSISTENT) {

@@ -100,7 +100,6 @@ struct augtree_plan {
   augtree::FwdSplit* fsplit_d;      // null when no replay query tile is split
   int32_t* fsplit_tiles_d;
   int32_t* queue_d[augtree::kNumOps];
-  int paired[augtree::kNumOps];      // forward tensor-core units take two items (two heads of one KV head)
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
   uint32_t* err_d;    // error block: word 0 error bits written by kernels, words 2-3 the wait limit (ns)
   // Persistent schedule (cfg.schedule == AUGTREE_SCHED_PERSISTENT, tensor-core family):
@@ -130,8 +129,6 @@ namespace augtree {
 // Persistent schedule: places the units of `queue` (unit_items consecutive items each)
 // on min(lanes, U) lanes with augtree_assign_grid.
 augtree_status build_lanes(const std::vector<int32_t>& queue, int unit_items, int lanes, LaneSet& out);
-// Whether a forward queue pairs consecutive items (two heads of one KV head, one tile).
-bool queue_pairs(const std::vector<int32_t>& queue, int hq, int hkv);
 
 // Work-queue build shared by augtree_schedule_build and augtree_plan_create.
 // split_fwd: apply the replay forward's split-KV rule (tensor-core family).

@@ -32,7 +32,7 @@
 
 #include "common.cuh"
 #include "tc_common.cuh"
-#include "tc_fwd_softmax.cuh"
+#include "tc_rows.cuh"
 
 namespace augtree {
 namespace {

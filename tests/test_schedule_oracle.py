@@ -294,23 +294,22 @@ def test_lpt_order_meets_the_list_scheduling_bound():
 
 def test_replay_split_rule_worked_examples():
     """The split-KV rule on hand-worked cases (one replay query tile of 65 KV tiles:
-    a 8,192-token prompt is 64 tiles, 32 three-token branches one own tile; 32 query
-    heads in 16 head pairs; 152 SMs).  Candidates T = ceil(65 / s): s = 8 gives T = 9,
-    8 splits of 9 tiles, 128 blocks, one wave, time 9 + 2 = 11; s = 9 gives T = 8, 9
-    splits (8 x 8 + 1), 144 blocks, one wave, time 10; s = 10 gives 160 blocks, two
-    waves, time 2 x 9 = 18; fewer splits take longer.  So 9 splits."""
-    assert S.replay_fwd_splits([65], 32, 8, 152) == [9]
+    an 8,192-token prompt is 64 tiles, 32 three-token branches one own tile; 32 query
+    heads, one block per head and split; 152 SMs).  Candidates T = ceil(65 / s): s = 3
+    gives T = 22, 96 blocks, one wave, time 22 + 2 = 24; s = 4 gives T = 17, 128
+    blocks, one wave, time 19; s = 5 gives T = 13, 160 blocks, two waves, time
+    2 x 15 = 30; s = 9 gives T = 8, 288 blocks, two waves, time 20.  So 4 splits
+    (17 + 17 + 17 + 14 tiles)."""
+    assert S.replay_fwd_splits([65], 32, 8, 152) == [4]
     # Enough items (2 * 152 or more) for the GPU: nothing splits.
     assert S.replay_fwd_splits([65] * 10, 32, 8, 152) == [1] * 10
-    # Four such tiles: 64 blocks unsplit; s = 2 (T = 33) gives 128 blocks in one wave,
-    # time 33 + 2 = 35, against 2 x (22 + 2) = 48 for s = 3 and 2 x (17 + 2) = 38 for
-    # s = 4.
-    assert S.replay_fwd_splits([65] * 4, 32, 8, 152) == [2] * 4
-    # Unpaired heads (Hq / Hkv = 3): one block per head, 3 per split; every candidate
-    # down to T = 4 (17 splits of 4 tiles, 51 blocks) fits in one wave, and the smallest
-    # chunk is then the fastest: time 4 + 2.
+    # Four such tiles: 128 blocks whole, one wave, time 65 + 2 = 67; two splits give
+    # 256 blocks in two waves, time 2 x 35 = 70, and more splits longer still.
+    assert S.replay_fwd_splits([65] * 4, 32, 8, 152) == [1] * 4
+    # Three heads: every candidate down to T = 4 (17 splits of 4 tiles, 51 blocks) fits
+    # in one wave, and the smallest chunk is then the fastest: time 4 + 2.
     assert S.replay_fwd_splits([65], 3, 1, 152) == [17]
     q = S.build(W.Tree([8192], [[3] * 32]).offsets(), 32, 8, S.OP_REPLAY_FWD, 128, 128, 152,
                 split_replay_fwd=True)
-    assert len(q) == 9 * 32
-    assert sorted(set(int(c) for c in q[:, 5])) == [1, 8]
+    assert len(q) == 4 * 32
+    assert sorted(set(int(c) for c in q[:, 5])) == [14, 17]
