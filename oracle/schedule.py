@@ -5,7 +5,7 @@ TEST INFRASTRUCTURE ONLY: imported by tests, never by the library.
 AugTree paper, Sec. 3.4: the response paths of a tree become bounded replay units,
 each with a work estimate from its query length and its valid Q-KV tile count, and
 units are assigned to lanes so that the most loaded lane is as light as possible
-("largest-first greedy balancing" when the exact subset DP is not used).  On one GPU
+(by largest-first greedy balancing when the exact subset DP is not used).  On one GPU
 a lane is a thread block: a unit is a (query tile, head) item in the forward and a
 (KV tile, KV head, split) item in the backward, its weight is its number of valid
 tile interactions, and blocks take items in order of decreasing weight.

@@ -5,7 +5,7 @@
 // n-way merge of the replay forward's split-KV partials) and the split-KV dQ sum.
 //
 // AugTree paper, Sec. 3.2 (Eq. 2: the prompt K/V gradient is the sum over branches,
-// "exact many-to-one gradient aggregation") and Sec. 3.3 (partial online-softmax
+// aggregated exactly from all of them into the one prompt) and Sec. 3.3 (partial online-softmax
 // states S = (m, l, O_acc) merge associatively; here in (O, lse) form).
 #include <cmath>
 #include <type_traits>
