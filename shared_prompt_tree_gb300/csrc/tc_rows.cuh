@@ -26,28 +26,30 @@ struct FwdRowGeom {
   int j0;           // first KV tile of the item (a split item's chunk; 0 otherwise)
 };
 
-// Valid columns of the item's j-th KV tile (tile j0 + j of the row's walk).
+// Valid columns of the item's j-th KV tile (tile j0 + j of the row's walk), clamped to
+// [-1, 128].  Rows and keys are int32 offsets (the descriptors are int32), so every
+// difference below fits in 32 bits; 32-bit arithmetic measured 1.4 % faster in the
+// forward than 64-bit.
 __device__ __forceinline__ void fwd_valid_cols(const FwdRowGeom& g, int j_local, int& lo_i, int& hi_i) {
   const int j = j_local + g.j0;
   const bool own = j >= g.n_a;
-  const int64_t key0 = own ? g.own0 + (int64_t)(j - g.n_a) * g.bn : g.p0 + (int64_t)j * g.bn;
-  int64_t lo, hi;
+  const int key0 = own ? (int)g.own0 + (j - g.n_a) * g.bn : (int)g.p0 + j * g.bn;
+  const int row = (int)g.row;
+  int lo = 0, hi;
   if (g.prefill) {
-    lo = 0;
-    hi = g.row - key0;
+    hi = row - key0;
   } else if (!own) {
-    lo = 0;
-    hi = g.p_end - 1 - key0;
+    hi = (int)g.p_end - 1 - key0;
   } else {
-    lo = g.bs - key0;
-    hi = g.row - key0;
+    lo = (int)g.bs - key0;
+    hi = row - key0;
   }
   if (!g.row_ok) {
     lo = 1;
     hi = 0;
   }
-  lo_i = lo < -1 ? -1 : (lo > 128 ? 128 : (int)lo);
-  hi_i = hi < -1 ? -1 : (hi > 128 ? 128 : (int)hi);
+  lo_i = min(max(lo, -1), 128);
+  hi_i = min(max(hi, -1), 128);
 }
 
 }  // namespace tc
