@@ -447,11 +447,16 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
     const int po = w * SHARE;
     const uint32_t acc_col = (po < 128 ? T_DK : T_DV) + (po & 127);
     bool ok = true;
+    // Rows and keys are int32 offsets (the descriptors are int32), so the per-iteration
+    // geometry runs in 32-bit arithmetic, and the walk position advances by counters
+    // instead of a division by r.
+    const int q_lo_i = (int)q_lo, q_hi_i = (int)q_hi, q_lo2_i = (int)q_lo2, q_hi2_i = (int)q_hi2;
+    const int qbase_i = (int)qbase;
+    int l = 0, lh = 0;  // iteration i = l * r + lh: query tile l of the walk, head lh
     for (int i = 0; i < n_iter; ++i) {
-      const int l = i / r;
       const bool sec = l >= nqt;
-      const int64_t row0 = sec ? (int64_t)G.p0 + (int64_t)(qb2 - 1 - (l - nqt)) * bm : qbase + (int64_t)(it.b - 1 - l) * bm;
-      const int64_t v_lo = sec ? q_lo2 : q_lo, v_hi = sec ? q_hi2 : q_hi;
+      const int row0 = sec ? G.p0 + (qb2 - 1 - (l - nqt)) * bm : qbase_i + (it.b - 1 - l) * bm;
+      const int v_lo = sec ? q_lo2_i : q_lo_i, v_hi = sec ? q_hi2_i : q_hi_i;
       const int b = kv_buf(i);
       const uint32_t ts = tmem + lane_off + T_ST + b * 64 + c0, tdp = tmem + lane_off + T_DPT + b * 64 + c0;
       if (!(ok = mbar_wait_warp_all(&bars->s_full[b], kv_phase(i), err))) break;
@@ -461,9 +466,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
       for (int k = 0; k < COLS / 32; ++k) tmem_ld32(ts + 32 * k, sraw[k]);
       tmem_ld_wait();
       // this warpgroup's valid columns: [lo, hi) relative to c0
-      const int64_t lo64 = v_lo - row0 - c0, hi64 = v_hi - row0 - c0;
-      const int lo = lo64 < 0 ? 0 : (lo64 > COLS ? COLS : (int)lo64);
-      const int hi = hi64 < 0 ? 0 : (hi64 > COLS ? COLS : (int)hi64);
+      const int lo = min(max(v_lo - row0 - c0, 0), COLS);
+      const int hi = min(max(v_hi - row0 - c0, 0), COLS);
       // P^T as bf16 pairs (A operand of dV and the P factor of dS): the accumulator
       // already holds S^T - lse/s, so P = exp2(s log2e (S^T - lse/s)).
       uint32_t pk[COLS / 2];
@@ -537,6 +541,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         }
         tc_fence_before();
         mbar_arrive(&bars->flushed);
+      }
+      if (++lh == r) {
+        lh = 0;
+        ++l;
       }
     }
     // This warpgroup's share of the key's dK (scaled by s) / dV row
