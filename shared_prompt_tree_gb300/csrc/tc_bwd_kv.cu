@@ -284,12 +284,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1) tc_bwd_kv_kernel(
         const CUtensorMap* qm = t.sec ? &tm_q2 : &tm_q;
         const CUtensorMap* om = t.sec ? &tm_do2 : &tm_do;
         mbar_expect_tx(&bars->q_full[stage], 4 * QBLK + 2 * AUG_ROWS);
-        for (int kb = 0; kb < 2; ++kb) {
-          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * QBLK, qm, &bars->q_full[stage], kb * 64, t.h, (int)row0);
-          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * QBLK, om, &bars->q_full[stage], kb * 64, t.h, (int)row0);
-        }
+        // Q and its -lse/s rows first (S^T needs them first), then dO and its -Delta rows.
         const uint8_t* src = aug_src(t);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_3d(smem + Q_OFF + (stage * 2 + kb) * QBLK, qm, &bars->q_full[stage], kb * 64, t.h, (int)row0);
         bulk_load(smem + AUG_OFF + stage * AUG_STAGE, src, AUG_ROWS, &bars->q_full[stage]);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_3d(smem + DO_OFF + (stage * 2 + kb) * QBLK, om, &bars->q_full[stage], kb * 64, t.h, (int)row0);
         bulk_load(smem + AUG_OFF + stage * AUG_STAGE + AUG_ROWS, src + kStatRows * 16, AUG_ROWS, &bars->q_full[stage]);
         issued = i + 1;
         // Warm L2 with the tiles a few iterations ahead.
