@@ -32,7 +32,10 @@
  * Execution: compute calls are asynchronous on the given stream (0 = legacy default
  * stream) of the plan's device.  They validate arguments on the host and return an
  * error code; no exception, abort or device trap is ever raised.  A CUDA launch
- * failure is reported as AUGTREE_ERR_CUDA.
+ * failure is reported as AUGTREE_ERR_CUDA.  Calls that use one plan must be ordered on
+ * the GPU (one stream, or events between streams): the plan's device memory holds its
+ * error word and the work counters of the forward kernels, which take their items in
+ * queue order through a counter that each launch leaves at zero.
  */
 #ifndef AUGTREE_H
 #define AUGTREE_H

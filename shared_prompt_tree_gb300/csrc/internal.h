@@ -23,6 +23,12 @@ constexpr int kFwdBlockOverhead = 2;
 // Limit of a device-side wait on another warp's work: default and largest settable.
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 constexpr uint64_t kMaxWaitLimitNs = 60000000000ull;
+// The plan's error block, 32 bytes of device memory: word 0 error bits, word 1
+// reserved, words 2-3 the wait limit (ns), then per forward op (prefill, replay) the two
+// work counters of the persistent forward (next item, finished blocks), zero between
+// launches.
+constexpr int kErrBlockWords = 8;
+constexpr int kErrFwdCounter = 4;
 
 // Per-group geometry on the device: first prompt row, prompt length, first response
 // row, total response length of the group's branches, and the group's first 128-row
@@ -101,7 +107,7 @@ struct augtree_plan {
   int32_t* fsplit_tiles_d;
   int32_t* queue_d[augtree::kNumOps];
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
-  uint32_t* err_d;    // error block: word 0 error bits written by kernels, words 2-3 the wait limit (ns)
+  uint32_t* err_d;    // error block (kErrBlockWords): error bits, the wait limit (ns), forward work counters
   // Persistent schedule (cfg.schedule == AUGTREE_SCHED_PERSISTENT, tensor-core family):
   // lanes of the query-side backward (over the forward queues) and of the key-side
   // backward, per op.

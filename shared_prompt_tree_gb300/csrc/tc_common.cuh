@@ -11,10 +11,10 @@
 namespace augtree {
 namespace tc {
 
-// The plan's error block (16 bytes of device memory): word 0 holds error bits written
+// The plan's error block (32 bytes of device memory): word 0 holds error bits written
 // by kernels (bit 0: a bounded wait gave up), word 1 is reserved, words 2-3 hold the
 // limit in nanoseconds of a wait on another warp's work (augtree_plan_set_wait_limit,
-// 2 s by default).
+// 2 s by default), words 4-7 the persistent forward's work counters.
 constexpr uint32_t kErrTimeout = 1u;
 // Limit of a drain wait: a wait for this block's own bulk copies or MMAs to finish
 // before it frees TMEM and exits.  Copies and MMAs always complete on their own, so

@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -424,6 +425,527 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
   }
 }
 
+// ---------------------------------------------------------------- persistent form
+// One block per SM; each block takes work items from the queue in queue order through
+// a counter in device memory (so the queue's largest-first, stream-ordered order is
+// kept, as with one block per item), and the items of a block overlap: the next item's
+// query tile is warmed in L2 as soon as the item is taken, loaded once the current
+// item's last S product has read Q, and its first score tiles are computed while the
+// softmax warps finish the current item (last tile, merge of the two warpgroups' states,
+// output).  Barrier phases, the K/V ring and the score buffers run on across items
+// (counters of the block's items and K/V tiles), so nothing is re-initialised between
+// items.
+#ifndef AUGTREE_FWD_PERSISTENT
+#define AUGTREE_FWD_PERSISTENT 1
+#endif
+constexpr bool kFwdPersistent = AUGTREE_FWD_PERSISTENT != 0;
+constexpr int FWD_XCH_OFF = FWD_BAR_OFF + 256;   // [128 rows] float2: row-state exchange
+constexpr int FWD_SLOT_OFF = FWD_XCH_OFF + 1024;  // 2 decoded items
+constexpr int FWDP_SMEM = FWD_SLOT_OFF + 128 + 1024;
+static_assert(FWDP_SMEM <= 232448, "shared memory per block");
+constexpr int FWD_CONSUMER_WARPS = 10;  // S issuer, PV issuer, 8 softmax warps
+
+struct FwdPBars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[FWD_NST];
+  uint64_t v_full[FWD_NST];
+  uint64_t kv_empty[FWD_NST];
+  uint64_t s_full[2];
+  uint64_t p_full[2][2];
+  uint64_t pv_done[2];
+  uint64_t item_full[2];   // a decoded item is in slot i
+  uint64_t item_empty[2];  // every consumer warp has read slot i
+  uint64_t xch_m;          // warpgroup 1 has published (m, l) of its rows
+  uint64_t xch_s;          // warpgroup 0 has published the merge factors
+  uint64_t drain[2];
+  uint32_t tmem_base;
+};
+static_assert(sizeof(FwdPBars) <= 256, "barrier area");
+
+// A work item decoded once by the producer for every warp of the block.
+struct FwdSlot {
+  int32_t stop;             // 1: the queue is exhausted
+  int32_t h;                // query head
+  int32_t prefill;
+  int32_t n_a;              // prompt KV tiles of the rows' walk
+  int32_t n_tiles;          // KV tiles this item walks
+  int32_t j0;               // first KV tile of the walk (split item), else 0
+  int32_t row0, row_end;    // query rows [row0, row_end)
+  int32_t own0;             // first key of the own-branch tiles
+  int32_t p0, lp;           // the group's prompt keys
+  int32_t pad;
+  int64_t slot;             // partial-state slot of a split item, else -1
+};
+static_assert(sizeof(FwdSlot) <= 64, "item slot");
+
+template <bool kSplit>
+__device__ __forceinline__ FwdSlot decode_fwd_item(const int32_t* __restrict__ queue, int idx, const Geometry& geo,
+                                                   int bm, int bn, uint32_t* err) {
+  FwdSlot s;
+  const WorkItem it = load_item(queue, idx);
+  // Checked build: the item and its split are valid for the plan's geometry.
+  const bool item_ok = !kChecked || (query_item_ok(it, geo, bm, bn) &&
+                                     (kSplit ? split_item_ok(it, geo) : it.split == 0));
+  if (kChecked && !item_ok) atomicOr(err, kErrCheck);
+  const GroupInfo G = geo.groups[item_ok ? it.group : 0];
+  s.stop = 0;
+  s.h = item_ok ? it.head : 0;
+  s.prefill = it.kind == K_PREFILL_Q ? 1 : 0;
+  const int base = s.prefill ? G.p0 : G.r0, len = s.prefill ? G.lp : G.lr;
+  s.row0 = item_ok ? base + it.tile * bm : 0;
+  s.row_end = item_ok ? min(s.row0 + bm, base + len) : 0;
+  s.n_a = item_ok ? it.a : 0;
+  s.n_tiles = item_ok ? s.n_a + (s.prefill ? 0 : it.b) : 0;
+  s.own0 = (s.prefill || !item_ok) ? 0 : geo.row_bstart[s.row0];
+  s.p0 = G.p0;
+  s.lp = G.lp;
+  s.pad = 0;
+  s.j0 = 0;
+  s.slot = -1;
+  if (kSplit && item_ok && !s.prefill) {
+    const FwdSplit fs = geo.fsplit[G.tr0 + it.tile];
+    if (fs.nsplit > 1) {
+      s.j0 = it.split * fs.chunk;
+      s.n_tiles = min(fs.chunk, s.n_tiles - s.j0);
+      s.slot = fs.slot0 + (int64_t)s.h * fs.nsplit + it.split;
+    }
+  }
+  return s;
+}
+
+// ctr: two words of the plan's device memory, zero between launches: the next item to
+// take, and the blocks that have finished taking items.
+template <bool kSplit>
+__global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
+    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kr,
+    const __grid_constant__ CUtensorMap tm_vr, Geometry geo, const int32_t* __restrict__ queue,
+    unsigned n_items, int bm, int bn, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int64_t lse_rows,
+    uint32_t* __restrict__ err, unsigned* __restrict__ ctr, float* __restrict__ part_o,
+    float* __restrict__ part_lse) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdPBars* bars = reinterpret_cast<FwdPBars*>(smem + FWD_BAR_OFF);
+  float2* xch = reinterpret_cast<float2*>(smem + FWD_XCH_OFF);
+  FwdSlot* slots = reinterpret_cast<FwdSlot*>(smem + FWD_SLOT_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < FWD_NST; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b][0], 128);
+      mbar_init(&bars->p_full[b][1], 128);
+      mbar_init(&bars->pv_done[b], 1);
+      mbar_init(&bars->item_full[b], 1);
+      mbar_init(&bars->item_empty[b], FWD_CONSUMER_WARPS);
+      mbar_init(&bars->drain[b], 1);
+    }
+    mbar_init(&bars->xch_m, 128);
+    mbar_init(&bars->xch_s, 128);
+    fence_mbar_init();
+  }
+  if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_kp);
+    prefetch_tmap(&tm_vp);
+    prefetch_tmap(&tm_kr);
+    prefetch_tmap(&tm_vr);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int r = geo.hq / geo.hkv;
+      bool ok = true;
+      int n = 0;         // items of this block so far
+      int n_q = 0;       // query tiles loaded
+      int jg = 0;        // K/V tiles loaded
+      FwdSlot stop_slot{};
+      stop_slot.stop = 1;
+      unsigned taken = atomicAdd(ctr, 1u);
+      FwdSlot cur = taken < n_items ? decode_fwd_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
+      slots[0] = cur;
+      mbar_arrive(&bars->item_full[0]);
+      if (!cur.stop) {
+        tma_prefetch_3d(&tm_q, 0, cur.h, cur.row0);
+        tma_prefetch_3d(&tm_q, 64, cur.h, cur.row0);
+      }
+      while (!cur.stop) {
+        // Take the next item now and publish it, so that every warp can prepare it.
+        taken = atomicAdd(ctr, 1u);
+        const FwdSlot nxt = taken < n_items ? decode_fwd_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
+        const int sn = (n + 1) & 1;
+        if (n + 1 >= 2 && !(ok = mbar_wait(&bars->item_empty[sn], (((n + 1) >> 1) - 1) & 1, err))) break;
+        slots[sn] = nxt;
+        mbar_arrive(&bars->item_full[sn]);
+        if (!nxt.stop) {
+          tma_prefetch_3d(&tm_q, 0, nxt.h, nxt.row0);
+          tma_prefetch_3d(&tm_q, 64, nxt.h, nxt.row0);
+        }
+        // The current item's query tile, once the previous item's S products have read Q.
+        if (n >= 1 && !(ok = mbar_wait(&bars->q_empty, (n - 1) & 1, err))) break;
+        mbar_expect_tx(&bars->q_full, 2 * FWD_TILE);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_3d(smem + FWD_Q_OFF + kb * FWD_TILE, &tm_q, &bars->q_full, kb * 64, cur.h, cur.row0);
+        ++n_q;
+        const int kvh = cur.h / r;
+        for (int j = 0; j < cur.n_tiles; ++j) {
+          const int stage = (int)(jg % FWD_NST);
+          const uint32_t use = (uint32_t)(jg / FWD_NST);
+          if (!(ok = mbar_wait(&bars->kv_empty[stage], (use & 1) ^ 1, err))) break;
+          mbar_expect_tx(&bars->kv_full[stage], (kFwdVBar ? 2 : 4) * FWD_TILE);
+          if (kFwdVBar) mbar_expect_tx(&bars->v_full[stage], 2 * FWD_TILE);
+          const int jt = cur.j0 + j;  // tile of the rows' walk
+          const bool own = jt >= cur.n_a;
+          const int krow = own ? cur.own0 + (jt - cur.n_a) * bn : cur.p0 + jt * bn;
+          const CUtensorMap* km = own ? &tm_kr : &tm_kp;
+          const CUtensorMap* vm = own ? &tm_vr : &tm_vp;
+          uint64_t* vbar = kFwdVBar ? &bars->v_full[stage] : &bars->kv_full[stage];
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_3d(smem + FWD_K_OFF + (stage * 2 + kb) * FWD_TILE, km, &bars->kv_full[stage], kb * 64, kvh, krow);
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_3d(smem + FWD_V_OFF + (stage * 2 + kb) * FWD_TILE, vm, vbar, kb * 64, kvh, krow);
+          ++jg;
+        }
+        if (!ok) break;
+        ++n;
+        cur = nxt;
+      }
+      // This thread's copies in flight land before the block frees its memory.
+      if (n_q > 0) mbar_wait_drain(&bars->q_full, (n_q - 1) & 1, err);
+      for (int t = jg > FWD_NST ? jg - FWD_NST : 0; t < jg; ++t) {
+        mbar_wait_drain(&bars->kv_full[t % FWD_NST], (uint32_t)(t / FWD_NST) & 1, err);
+        if (kFwdVBar) mbar_wait_drain(&bars->v_full[t % FWD_NST], (uint32_t)(t / FWD_NST) & 1, err);
+      }
+      // A block that gave up takes the rest of the queue unprocessed, so that the counter
+      // always passes the end; the last block to finish zeroes both words for the next
+      // launch (launches on one plan are ordered on the GPU).
+      while (taken < n_items) taken = atomicAdd(ctr, 1u);
+      __threadfence();
+      if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+        atomicExch(ctr, 0u);
+        atomicExch(ctr + 1, 0u);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer: S
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+    const uint64_t dq = smem_desc_sw128(smem_u32(smem + FWD_Q_OFF), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + FWD_K_OFF), 16, 1024);
+    constexpr uint64_t kStage = (2 * FWD_TILE) >> 4;
+    auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * FWD_TILE + (kk & 3) * 32) >> 4); };
+    bool ok = true;
+    int jg = 0;
+    for (int n = 0; ok; ++n) {
+      const int sn = n & 1;
+      if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n >> 1) & 1, err))) break;
+      const int stop = slots[sn].stop, n_tiles = slots[sn].n_tiles;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
+      if (stop) break;
+      if (!(ok = mbar_wait_warp_all(&bars->q_full, n & 1, err))) break;
+      tc_fence_after();
+      for (int j = 0; j < n_tiles; ++j) {
+        const int stage = (int)(jg % FWD_NST), b = (int)(jg & 1);
+        if (!(ok = mbar_wait_warp_all(&bars->kv_full[stage], (uint32_t)(jg / FWD_NST) & 1, err))) break;
+        // S overwrites the P of the tile two before in buffer b (possibly the previous
+        // item's): both PV products of that tile must be done.
+        if (jg >= 2 && !(ok = mbar_wait_warp_all(&bars->pv_done[b], (uint32_t)((jg >> 1) - 1) & 1, err))) break;
+        tc_fence_after();
+        const uint64_t dk = dk0 + stage * kStage;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_w(tmem + b * 128, dq + koff(kk), dk + koff(kk), idesc_qk, kk > 0 ? 1u : 0u);
+        mma_commit_w(&bars->s_full[b]);
+        ++jg;
+      }
+      if (!ok) break;
+      mma_commit_w(&bars->q_empty);  // Q is free once these products complete
+    }
+    mma_commit_w(&bars->drain[0]);
+    mbar_wait_drain_warp_all(&bars->drain[0], 0, err);
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ MMA issuer: PV
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+    const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + FWD_V_OFF), FWD_TILE, 1024);
+    constexpr uint64_t kStage = (2 * FWD_TILE) >> 4;
+    bool ok = true;
+    int jg = 0;
+    for (int n = 0; ok; ++n) {
+      const int sn = n & 1;
+      if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n >> 1) & 1, err))) break;
+      const int stop = slots[sn].stop, n_tiles = slots[sn].n_tiles;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
+      if (stop) break;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int stage = (int)(jg % FWD_NST), b = (int)(jg & 1);
+        const uint32_t par = (uint32_t)(jg >> 1) & 1;
+        if (kFwdVBar && !(ok = mbar_wait_warp_all(&bars->v_full[stage], (uint32_t)(jg / FWD_NST) & 1, err))) break;
+        // An item's first products overwrite O_0 and O_1, which both warpgroups read out
+        // for the previous item; a warpgroup signals P of this tile only after that.
+        if (j == 0 && !(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
+        if (!kFwdPvEarly) {
+          if (!(ok = mbar_wait_warp_all(&bars->p_full[b][0], par, err))) break;
+          if (!(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
+          tc_fence_after();
+        }
+        const uint64_t dv = dv0 + stage * kStage;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          if (kFwdPvEarly) {
+            if (!(ok = mbar_wait_warp_all(&bars->p_full[b][w], par, err))) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_w(tmem + 256 + w * 128, tmem + b * 128 + w * 64 + kk * 8, dv + (4 * w + kk) * (2048 >> 4),
+                     idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit_w(&bars->pv_done[b]);
+        mma_commit_w(&bars->kv_empty[stage]);
+        ++jg;
+      }
+    }
+    mma_commit_w(&bars->drain[1]);
+    mbar_wait_drain_warp_all(&bars->drain[1], 0, err);
+  } else {
+    // ------------------------------------------------------------ softmax (half tiles)
+    const int w = warp >> 2;        // keys [64w, 64w + 64) of every tile
+    const int q4 = warp & 3;        // TMEM lane quarter
+    const int r_local = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const float sl2 = geo.scale_log2;
+    const uint32_t tO = tmem + lane_off + 256 + w * 128;
+    bool ok = mbar_wait_warp_all(&bars->item_full[0], 0, err);
+    FwdSlot cur{};
+    cur.stop = 1;
+    if (ok) {
+      cur = slots[0];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[0]);
+    }
+    int bs = (!cur.stop && !cur.prefill && cur.row0 + r_local < cur.row_end) ? geo.row_bstart[cur.row0 + r_local] : 0;
+    int jg = 0;
+    for (int n = 0; ok && !cur.stop; ++n) {
+      FwdRowGeom g;
+      g.row = cur.row0 + r_local;
+      g.row_ok = g.row < cur.row_end;
+      g.prefill = cur.prefill != 0;
+      g.bs = bs;
+      g.p0 = cur.p0;
+      g.p_end = (int64_t)cur.p0 + cur.lp;
+      g.own0 = cur.own0;
+      g.n_a = cur.n_a;
+      g.bn = bn;
+      g.j0 = cur.j0;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < cur.n_tiles; ++j) {
+        const int b = (int)(jg & 1);
+        const uint32_t tS = tmem + lane_off + b * 128 + w * 64;
+        if (!(ok = mbar_wait_warp_all(&bars->s_full[b], (uint32_t)(jg >> 1) & 1, err))) break;
+        tc_fence_after();
+        uint32_t raw[2][32];
+        tmem_ld32(tS, raw[0]);
+        tmem_ld32(tS + 32, raw[1]);
+        tmem_ld_wait();
+#define FWD_X(c) raw[(c) >> 5][(c) & 31]
+        int lo_i, hi_i;
+        fwd_valid_cols(g, j, lo_i, hi_i);
+        const int lo = lo_i - 64 * w, hi = hi_i - 64 * w;  // valid local columns [lo, hi]
+        const bool masked = lo > 0 || hi < 63;
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < lo || c > hi) FWD_X(c) = 0xFF800000u;  // -inf
+        }
+        float pm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          pm[k] = fmax3(__uint_as_float(FWD_X(k)), __uint_as_float(FWD_X(k + 8)), __uint_as_float(FWD_X(k + 16)));
+#pragma unroll
+        for (int c = 24; c < 56; c += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            pm[k] = fmax3(pm[k], __uint_as_float(FWD_X(c + k)), __uint_as_float(FWD_X(c + 8 + k)));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], __uint_as_float(FWD_X(56 + k)));
+        const float tmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7]));
+        const float mx = tmax * sl2;  // -inf stays -inf
+        // Lazy rescaling: the offset moves only when the max grows by more than 2^8
+        // (exact: every term of the state shares the offset).
+        const bool need = (m != -INFINITY) && (mx > m + 8.0f);
+        const float m_new = (m == -INFINITY) ? mx : (need ? mx : m);
+        const float alpha = need ? fast_exp2(m - m_new) : 1.f;
+        m = m_new;
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        uint32_t pk[32];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float a0 = fmaf(__uint_as_float(FWD_X(2 * i)), sl2, -mu);
+          const float a1 = fmaf(__uint_as_float(FWD_X(2 * i + 1)), sl2, -mu);
+          const float p0 = fast_exp2(a0);
+          float p1;
+          if (i % kFwdFmaPairs == kFwdFmaPairs - 1) {
+            // One exponential in 2 * kFwdFmaPairs on the FMA pipe; a masked column stays
+            // exactly zero.
+            p1 = exp2_fma(a1);
+            if (masked && a1 == -INFINITY) p1 = 0.f;
+          } else {
+            p1 = fast_exp2(a1);
+          }
+          pk[i] = pack_bf16x2(p0, p1);
+          // The row sum uses the bf16 weights the PV product uses.
+          ps[i & 3] = add_bf16x2_f32(ps[i & 3], pk[i]);
+        }
+#undef FWD_X
+        tmem_st32(tS, pk);
+        tmem_st_wait();
+        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+        if (__any_sync(0xffffffffu, need)) {
+          // O_w += P(j-1) V must be complete before O_w is rescaled; PV(j) is issued only
+          // after this warpgroup signals P(j).
+          if (!(ok = mbar_wait_warp_all(&bars->pv_done[(jg - 1) & 1], (uint32_t)((jg - 1) >> 1) & 1, err))) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[b][w]);
+        ++jg;
+      }
+      // The next item, published an item ahead: its row's branch start is fetched now and
+      // used after this item's output.
+      FwdSlot nxt{};
+      nxt.stop = 1;
+      if (ok) {
+        const int sn = (n + 1) & 1;
+        if (mbar_wait_warp_all(&bars->item_full[sn], ((n + 1) >> 1) & 1, err)) {
+          nxt = slots[sn];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
+        }
+      }
+      const int nrow = nxt.row0 + r_local;
+      const int bs_next = (!nxt.stop && !nxt.prefill && nrow < nxt.row_end) ? geo.row_bstart[nrow] : 0;
+      // Merge the two warpgroups' states of each row, (O_0, m_0, l_0) and (O_1, m_1, l_1):
+      // warpgroup 1 hands its (m, l) to warpgroup 0, which returns the two factors.
+      const int last = jg - 1;
+      if (ok && cur.n_tiles > 0) ok = mbar_wait_warp_all(&bars->pv_done[last & 1], (uint32_t)(last >> 1) & 1, err);
+      tc_fence_after();
+      float s0 = 0.f, s1 = 0.f, lse_v = -INFINITY;
+      if (w == 1) {
+        xch[r_local] = make_float2(m, l);
+        mbar_arrive(&bars->xch_m);  // also after a failed wait, so that the other warpgroup's wait ends
+        if (ok) ok = mbar_wait_warp_all(&bars->xch_s, n & 1, err);
+        if (ok) {
+          const float2 f = xch[r_local];
+          s0 = f.x;
+          s1 = f.y;
+        }
+      } else {
+        const bool got = mbar_wait_warp_all(&bars->xch_m, n & 1, err);
+        ok = ok && got;
+        if (ok) {
+          const float2 o1 = xch[r_local];
+          const float m0 = m, l0 = l, m1 = o1.x, l1 = o1.y;
+          const float M = fmaxf(m0, m1);
+          const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
+          const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
+          const float L = l0 * a0 + l1 * a1;
+          const bool any = L > 0.f && cur.n_tiles > 0;  // a row with no key writes zeros
+          const float inv = any ? 1.f / L : 0.f;
+          s0 = a0 * inv;
+          s1 = a1 * inv;
+          if (any) lse_v = (M + log2f(L)) * 0.69314718055994531f;
+          xch[r_local] = make_float2(s0, s1);
+        }
+        mbar_arrive(&bars->xch_s);
+      }
+      if (ok) {
+        // Factors are zero for a row with no key (its output is zero); at least one is
+        // positive otherwise.
+        const bool any = s0 > 0.f || s1 > 0.f;
+        const int h = cur.h;
+        if (kSplit && cur.slot >= 0) {
+          // Split-KV item: the chunk's state O / l (fp32) and its lse.
+          float* prow = part_o + (cur.slot * kFwdPartRows + r_local) * 128 + 64 * w;
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
+            tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
+            tmem_ld_wait();
+            if (g.row_ok) {
+              float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  v[e] = any ? __uint_as_float(o0[4 * i + e]) * s0 + __uint_as_float(o1[4 * i + e]) * s1 : 0.f;
+                d4[i] = make_float4(v[0], v[1], v[2], v[3]);
+              }
+            }
+          }
+          if (w == 0 && g.row_ok) part_lse[cur.slot * kFwdPartRows + r_local] = lse_v;
+        } else {
+          __nv_bfloat16* orow = out + ((int64_t)g.row * geo.hq + h) * 128 + 64 * w;
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
+            tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
+            tmem_ld_wait();
+            if (g.row_ok) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float v0 = any ? __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1 : 0.f;
+                const float v1 = any ? __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1 : 0.f;
+                pk[i] = pack_bf16x2(v0, v1);
+              }
+              uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+          if (w == 0 && g.row_ok) lse[(int64_t)h * lse_rows + g.row] = lse_v;
+        }
+      }
+      cur = nxt;
+      bs = bs_next;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -496,6 +1018,21 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
   // The split-KV instantiation only where the replay queue has split items.
   const bool split = !prefill && p->n_fwd_parts > 0;
   if (split && (!part_o || !part_lse)) return cudaErrorInvalidValue;
+  if (kFwdPersistent) {
+    // One block per SM (fewer if the queue is shorter), items taken in queue order.
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) return e;
+    const unsigned n_items = (unsigned)p->n_items[op];
+    const unsigned grid = std::min<unsigned>(n_items, (unsigned)std::max(sms, 1));
+    auto kern = split ? tc_fwd_persistent_kernel<true> : tc_fwd_persistent_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FWDP_SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, FWD_THREADS, FWDP_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op], n_items,
+                                               p->bm[op], p->bn[op], (__nv_bfloat16*)o, lse, q_rows, p->err_d,
+                                               p->err_d + kErrFwdCounter + 2 * op, part_o, part_lse);
+    return cudaGetLastError();
+  }
   auto kern = split ? tc_fwd_kernel<true> : tc_fwd_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;

@@ -50,3 +50,39 @@ def test_tc_forward_large_scores(cuda_device):
         assert np.all(err <= 1e-2 + 2.0 ** -8 * np.abs(ref[k])), (k, float(err.max()))
     for k in ("lse_p", "lse_r"):
         assert np.max(np.abs(got[k] - ref[k])) <= 1e-2, k
+
+
+def test_tc_forward_many_items_per_block(cuda_device):
+    """The forward runs one block per SM, each taking items in queue order until the
+    queue is exhausted, with consecutive items overlapped.  A queue many times the SM
+    count, of items from 1 to 15 KV tiles (short and long prompts, one- to three-tile
+    branches), matches the oracle; repeated calls into outputs filled with NaN give
+    bit-identical results, so every item is computed on every call (the work counter
+    starts from zero each launch) whichever block takes it."""
+    import torch
+    rng = np.random.default_rng(5)
+    prompts = [int(x) for x in rng.integers(0, 1500, size=24)]
+    branches = [[int(x) for x in rng.integers(1, 300, size=int(rng.integers(1, 6)))] for _ in prompts]
+    w = W.custom(W.Tree(prompts, branches), hq=8, hkv=2, d=128, dtype="bf16", seed=61)
+    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=at.BF16, kernel=at.KERNEL_TC)
+    n_sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    assert len(plan.schedule(at.OP_REPLAY_FWD)) > 4 * n_sms and len(plan.schedule(at.OP_PREFILL_FWD)) > 4 * n_sms
+    t = {n: W.tensor_torch(w, n, cuda_device) for n in ("q_p", "k_p", "v_p", "q_r", "k_r", "v_r")}
+    nb = plan.workspace_bytes(at.OP_REPLAY_FWD)
+    ws = torch.empty(nb, dtype=torch.uint8, device=cuda_device) if nb else None
+    runs = []
+    for _ in range(3):
+        o_p = torch.full_like(t["q_p"], float("nan"))
+        o_r = torch.full_like(t["q_r"], float("nan"))
+        lse_p = torch.full((w.hq, w.tree.total_prompt), float("nan"), dtype=torch.float32, device=cuda_device)
+        lse_r = torch.full((w.hq, w.tree.total_resp), float("nan"), dtype=torch.float32, device=cuda_device)
+        at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p)
+        at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, ws)
+        torch.cuda.synchronize()
+        plan.check()
+        runs.append({"o_p": o_p, "lse_p": lse_p, "o_r": o_r, "lse_r": lse_r})
+    for r in runs[1:]:
+        for k in r:
+            assert torch.equal(r[k], runs[0][k]), k
+    got = {k: v.double().cpu().numpy() for k, v in runs[0].items()}
+    compare(got, run_oracle_fwd(w), "bf16", keys=("o_p", "o_r", "lse_p", "lse_r"))
