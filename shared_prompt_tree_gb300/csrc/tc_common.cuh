@@ -16,6 +16,9 @@ namespace tc {
 // limit in nanoseconds of a wait on another warp's work (augtree_plan_set_wait_limit,
 // 2 s by default), words 4-7 the persistent forward's work counters.
 constexpr uint32_t kErrTimeout = 1u;
+// A block found its shared memory laid out other than its kernel requires (it then
+// does nothing).
+constexpr uint32_t kErrLayout = 8u;
 // Limit of a drain wait: a wait for this block's own bulk copies or MMAs to finish
 // before it frees TMEM and exits.  Copies and MMAs always complete on their own, so
 // these waits never take the (possibly very short) runtime limit.

@@ -439,11 +439,29 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
 #define AUGTREE_FWD_PERSISTENT 1
 #endif
 constexpr bool kFwdPersistent = AUGTREE_FWD_PERSISTENT != 0;
-constexpr int FWD_XCH_OFF = FWD_BAR_OFF + 256;   // [128 rows] float2: row-state exchange
-constexpr int FWD_SLOT_OFF = FWD_XCH_OFF + 1024;  // 2 decoded items
-constexpr int FWDP_SMEM = FWD_SLOT_OFF + 128 + 1024;
-static_assert(FWDP_SMEM <= 232448, "shared memory per block");
-constexpr int FWD_CONSUMER_WARPS = 10;  // S issuer, PV issuer, 8 softmax warps
+// 1: a fifth warpgroup writes each item's output (merge of the two softmax warpgroups'
+// states, O read out of TMEM, stores), so the softmax warps go on to the next item at
+// once; the next item's first PV product waits until the output has been read out.
+// 0: the softmax warps write it themselves.
+#ifndef AUGTREE_FWD_EPI_WARPS
+#define AUGTREE_FWD_EPI_WARPS 1
+#endif
+constexpr bool kFwdEpi = AUGTREE_FWD_EPI_WARPS != 0;
+constexpr int FWDP_THREADS = kFwdEpi ? 480 : 352;
+constexpr int FWDP_SLOTS = kFwdEpi ? 4 : 2;  // ring of decoded items
+constexpr int FWDP_BAR_BYTES = 288;
+// Behind the tiles: barriers, the row-state exchange ([2 warpgroups][128 rows] float2
+// with the epilogue warps, [128 rows] float2 between the two softmax warpgroups
+// otherwise) and the decoded items.
+constexpr int FWD_XCH_OFF = FWD_BAR_OFF + FWDP_BAR_BYTES;
+constexpr int FWD_SLOT_OFF = FWD_XCH_OFF + (kFwdEpi ? 2048 : 1024);
+constexpr int FWDP_END = FWD_SLOT_OFF + 64 * FWDP_SLOTS;
+// The block takes the most shared memory a block may have; the tiles start at the first
+// 1024-byte boundary of it, and a block whose allocation leaves too little room behind
+// that boundary records an error and does nothing.
+constexpr int FWDP_SMEM = 232448;
+static_assert(FWDP_END <= FWDP_SMEM, "shared memory per block");
+constexpr int FWD_CONSUMER_WARPS = kFwdEpi ? 14 : 10;  // S and PV issuers, 8 softmax warps (+ 4 epilogue)
 
 struct FwdPBars {
   uint64_t q_full, q_empty;
@@ -453,14 +471,17 @@ struct FwdPBars {
   uint64_t s_full[2];
   uint64_t p_full[2][2];
   uint64_t pv_done[2];
-  uint64_t item_full[2];   // a decoded item is in slot i
-  uint64_t item_empty[2];  // every consumer warp has read slot i
+  uint64_t item_full[FWDP_SLOTS];   // a decoded item is in slot i
+  uint64_t item_empty[FWDP_SLOTS];  // every consumer warp has read slot i
   uint64_t xch_m;          // warpgroup 1 has published (m, l) of its rows
   uint64_t xch_s;          // warpgroup 0 has published the merge factors
+  uint64_t ml_ready;       // both softmax warpgroups have published (m, l) (epilogue warps)
+  uint64_t ml_free;        // the epilogue warps have read them
+  uint64_t o_free;         // the epilogue warps have read O_0 and O_1 out of TMEM
   uint64_t drain[2];
   uint32_t tmem_base;
 };
-static_assert(sizeof(FwdPBars) <= 256, "barrier area");
+static_assert(sizeof(FwdPBars) <= FWDP_BAR_BYTES, "barrier area");
 
 // A work item decoded once by the producer for every warp of the block.
 struct FwdSlot {
@@ -516,7 +537,7 @@ __device__ __forceinline__ FwdSlot decode_fwd_item(const int32_t* __restrict__ q
 // ctr: two words of the plan's device memory, zero between launches: the next item to
 // take, and the blocks that have finished taking items.
 template <bool kSplit>
-__global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
+__global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
     const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kr,
     const __grid_constant__ CUtensorMap tm_vr, Geometry geo, const int32_t* __restrict__ queue,
@@ -525,6 +546,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
     float* __restrict__ part_lse) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if ((smem - smem_raw) + FWDP_END > FWDP_SMEM) {
+    if (threadIdx.x == 0) atomicOr(err, kErrLayout);
+    return;
+  }
   FwdPBars* bars = reinterpret_cast<FwdPBars*>(smem + FWD_BAR_OFF);
   float2* xch = reinterpret_cast<float2*>(smem + FWD_XCH_OFF);
   FwdSlot* slots = reinterpret_cast<FwdSlot*>(smem + FWD_SLOT_OFF);
@@ -543,12 +568,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
       mbar_init(&bars->p_full[b][0], 128);
       mbar_init(&bars->p_full[b][1], 128);
       mbar_init(&bars->pv_done[b], 1);
-      mbar_init(&bars->item_full[b], 1);
-      mbar_init(&bars->item_empty[b], FWD_CONSUMER_WARPS);
       mbar_init(&bars->drain[b], 1);
+    }
+    for (int i = 0; i < FWDP_SLOTS; ++i) {
+      mbar_init(&bars->item_full[i], 1);
+      mbar_init(&bars->item_empty[i], FWD_CONSUMER_WARPS);
     }
     mbar_init(&bars->xch_m, 128);
     mbar_init(&bars->xch_s, 128);
+    mbar_init(&bars->ml_ready, 256);
+    mbar_init(&bars->ml_free, 128);
+    mbar_init(&bars->o_free, 128);
     fence_mbar_init();
   }
   if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
@@ -585,8 +615,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
         // Take the next item now and publish it, so that every warp can prepare it.
         taken = atomicAdd(ctr, 1u);
         const FwdSlot nxt = taken < n_items ? decode_fwd_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
-        const int sn = (n + 1) & 1;
-        if (n + 1 >= 2 && !(ok = mbar_wait(&bars->item_empty[sn], (((n + 1) >> 1) - 1) & 1, err))) break;
+        const int u = n + 1, sn = u % FWDP_SLOTS;
+        if (u >= FWDP_SLOTS && !(ok = mbar_wait(&bars->item_empty[sn], ((u / FWDP_SLOTS) - 1) & 1, err))) break;
         slots[sn] = nxt;
         mbar_arrive(&bars->item_full[sn]);
         if (!nxt.stop) {
@@ -648,8 +678,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
     bool ok = true;
     int jg = 0;
     for (int n = 0; ok; ++n) {
-      const int sn = n & 1;
-      if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n >> 1) & 1, err))) break;
+      const int sn = n % FWDP_SLOTS;
+      if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n / FWDP_SLOTS) & 1, err))) break;
       const int stop = slots[sn].stop, n_tiles = slots[sn].n_tiles;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
@@ -683,8 +713,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
     bool ok = true;
     int jg = 0;
     for (int n = 0; ok; ++n) {
-      const int sn = n & 1;
-      if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n >> 1) & 1, err))) break;
+      const int sn = n % FWDP_SLOTS;
+      if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n / FWDP_SLOTS) & 1, err))) break;
       const int stop = slots[sn].stop, n_tiles = slots[sn].n_tiles;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
@@ -693,9 +723,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
         const int stage = (int)(jg % FWD_NST), b = (int)(jg & 1);
         const uint32_t par = (uint32_t)(jg >> 1) & 1;
         if (kFwdVBar && !(ok = mbar_wait_warp_all(&bars->v_full[stage], (uint32_t)(jg / FWD_NST) & 1, err))) break;
-        // An item's first products overwrite O_0 and O_1, which both warpgroups read out
-        // for the previous item; a warpgroup signals P of this tile only after that.
-        if (j == 0 && !(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
+        // An item's first products overwrite O_0 and O_1, read out for the previous item
+        // by the epilogue warps, or else by both softmax warpgroups (each signals P of
+        // this tile only after that).
+        if (kFwdEpi) {
+          if (j == 0 && n >= 1 && !(ok = mbar_wait_warp_all(&bars->o_free, (n - 1) & 1, err))) break;
+        } else {
+          if (j == 0 && !(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
+        }
         if (!kFwdPvEarly) {
           if (!(ok = mbar_wait_warp_all(&bars->p_full[b][0], par, err))) break;
           if (!(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
@@ -721,6 +756,91 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
     }
     mma_commit_w(&bars->drain[1]);
     mbar_wait_drain_warp_all(&bars->drain[1], 0, err);
+  } else if (kFwdEpi && warp >= 11) {
+    // ------------------------------------------------------------ epilogue warps
+    // Warp 11 + i reads TMEM lane quarter (11 + i) % 4; thread r owns row r of the tile,
+    // all 128 dims: the merge of the two softmax warpgroups' states (O_0, m_0, l_0) and
+    // (O_1, m_1, l_1), O read out of TMEM, the output (or a split item's partial state).
+    const int q4 = warp & 3;
+    const int r_local = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    bool ok = true;
+    int jg = 0;
+    for (int n = 0; ok; ++n) {
+      const int sn = n % FWDP_SLOTS;
+      if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n / FWDP_SLOTS) & 1, err))) break;
+      const FwdSlot cur = slots[sn];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
+      if (cur.stop) break;
+      jg += cur.n_tiles;
+      if (!(ok = mbar_wait_warp_all(&bars->ml_ready, n & 1, err))) break;
+      const float2 st0 = xch[r_local], st1 = xch[128 + r_local];
+      mbar_arrive(&bars->ml_free);
+      const int last = jg - 1;
+      if (cur.n_tiles > 0 && !(ok = mbar_wait_warp_all(&bars->pv_done[last & 1], (uint32_t)(last >> 1) & 1, err)))
+        break;
+      tc_fence_after();
+      const float m0 = st0.x, l0 = st0.y, m1 = st1.x, l1 = st1.y;
+      const float M = fmaxf(m0, m1);
+      const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
+      const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
+      const float L = l0 * a0 + l1 * a1;
+      const bool any = L > 0.f && cur.n_tiles > 0;  // a row with no key writes zeros
+      const float inv = any ? 1.f / L : 0.f;
+      const float s0 = a0 * inv, s1 = a1 * inv;
+      const float lse_v = any ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      const int row = cur.row0 + r_local;
+      const bool row_ok = row < cur.row_end;
+      if (kSplit && cur.slot >= 0) {
+        // Split-KV item: the chunk's state O / l (fp32) and its lse.
+        float* prow = part_o + (cur.slot * kFwdPartRows + r_local) * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tmem + lane_off + 256 + 32 * c, o0);
+          tmem_ld32(tmem + lane_off + 384 + 32 * c, o1);
+          tmem_ld_wait();
+          if (row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float v[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                v[e] = any ? __uint_as_float(o0[4 * i + e]) * s0 + __uint_as_float(o1[4 * i + e]) * s1 : 0.f;
+              d4[i] = make_float4(v[0], v[1], v[2], v[3]);
+            }
+          }
+        }
+        if (row_ok) part_lse[cur.slot * kFwdPartRows + r_local] = lse_v;
+      } else {
+        __nv_bfloat16* orow = out + ((int64_t)row * geo.hq + cur.h) * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tmem + lane_off + 256 + 32 * c, o0);
+          tmem_ld32(tmem + lane_off + 384 + 32 * c, o1);
+          tmem_ld_wait();
+          if (row_ok) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float v0 = any ? __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1 : 0.f;
+              const float v1 = any ? __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1 : 0.f;
+              pk[i] = pack_bf16x2(v0, v1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row_ok) lse[(int64_t)cur.h * lse_rows + row] = lse_v;
+      }
+      // The next item's first PV products may overwrite O_0 and O_1.
+      tc_fence_before();
+      mbar_arrive(&bars->o_free);
+    }
   } else {
     // ------------------------------------------------------------ softmax (half tiles)
     const int w = warp >> 2;        // keys [64w, 64w + 64) of every tile
@@ -835,13 +955,20 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
         mbar_arrive(&bars->p_full[b][w]);
         ++jg;
       }
+      if (kFwdEpi) {
+        // Hand the rows' states to the epilogue warps, once they have read the previous
+        // item's.
+        if (ok && n >= 1) ok = mbar_wait_warp_all(&bars->ml_free, (n - 1) & 1, err);
+        if (ok) xch[w * 128 + r_local] = make_float2(m, l);
+        mbar_arrive(&bars->ml_ready);  // also after a failed wait, so that the epilogue's wait ends
+      }
       // The next item, published an item ahead: its row's branch start is fetched now and
       // used after this item's output.
       FwdSlot nxt{};
       nxt.stop = 1;
       if (ok) {
-        const int sn = (n + 1) & 1;
-        if (mbar_wait_warp_all(&bars->item_full[sn], ((n + 1) >> 1) & 1, err)) {
+        const int sn = (n + 1) % FWDP_SLOTS;
+        if (mbar_wait_warp_all(&bars->item_full[sn], ((n + 1) / FWDP_SLOTS) & 1, err)) {
           nxt = slots[sn];
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
@@ -849,89 +976,91 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_persistent_kernel(
       }
       const int nrow = nxt.row0 + r_local;
       const int bs_next = (!nxt.stop && !nxt.prefill && nrow < nxt.row_end) ? geo.row_bstart[nrow] : 0;
-      // Merge the two warpgroups' states of each row, (O_0, m_0, l_0) and (O_1, m_1, l_1):
-      // warpgroup 1 hands its (m, l) to warpgroup 0, which returns the two factors.
-      const int last = jg - 1;
-      if (ok && cur.n_tiles > 0) ok = mbar_wait_warp_all(&bars->pv_done[last & 1], (uint32_t)(last >> 1) & 1, err);
-      tc_fence_after();
-      float s0 = 0.f, s1 = 0.f, lse_v = -INFINITY;
-      if (w == 1) {
-        xch[r_local] = make_float2(m, l);
-        mbar_arrive(&bars->xch_m);  // also after a failed wait, so that the other warpgroup's wait ends
-        if (ok) ok = mbar_wait_warp_all(&bars->xch_s, n & 1, err);
-        if (ok) {
-          const float2 f = xch[r_local];
-          s0 = f.x;
-          s1 = f.y;
-        }
-      } else {
-        const bool got = mbar_wait_warp_all(&bars->xch_m, n & 1, err);
-        ok = ok && got;
-        if (ok) {
-          const float2 o1 = xch[r_local];
-          const float m0 = m, l0 = l, m1 = o1.x, l1 = o1.y;
-          const float M = fmaxf(m0, m1);
-          const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
-          const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
-          const float L = l0 * a0 + l1 * a1;
-          const bool any = L > 0.f && cur.n_tiles > 0;  // a row with no key writes zeros
-          const float inv = any ? 1.f / L : 0.f;
-          s0 = a0 * inv;
-          s1 = a1 * inv;
-          if (any) lse_v = (M + log2f(L)) * 0.69314718055994531f;
-          xch[r_local] = make_float2(s0, s1);
-        }
-        mbar_arrive(&bars->xch_s);
-      }
-      if (ok) {
-        // Factors are zero for a row with no key (its output is zero); at least one is
-        // positive otherwise.
-        const bool any = s0 > 0.f || s1 > 0.f;
-        const int h = cur.h;
-        if (kSplit && cur.slot >= 0) {
-          // Split-KV item: the chunk's state O / l (fp32) and its lse.
-          float* prow = part_o + (cur.slot * kFwdPartRows + r_local) * 128 + 64 * w;
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o0[32], o1[32];
-            tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
-            tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
-            tmem_ld_wait();
-            if (g.row_ok) {
-              float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                float v[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  v[e] = any ? __uint_as_float(o0[4 * i + e]) * s0 + __uint_as_float(o1[4 * i + e]) * s1 : 0.f;
-                d4[i] = make_float4(v[0], v[1], v[2], v[3]);
-              }
-            }
+      if constexpr (!kFwdEpi) {
+        // Merge the two warpgroups' states of each row, (O_0, m_0, l_0) and (O_1, m_1, l_1):
+        // warpgroup 1 hands its (m, l) to warpgroup 0, which returns the two factors.
+        const int last = jg - 1;
+        if (ok && cur.n_tiles > 0) ok = mbar_wait_warp_all(&bars->pv_done[last & 1], (uint32_t)(last >> 1) & 1, err);
+        tc_fence_after();
+        float s0 = 0.f, s1 = 0.f, lse_v = -INFINITY;
+        if (w == 1) {
+          xch[r_local] = make_float2(m, l);
+          mbar_arrive(&bars->xch_m);  // also after a failed wait, so that the other warpgroup's wait ends
+          if (ok) ok = mbar_wait_warp_all(&bars->xch_s, n & 1, err);
+          if (ok) {
+            const float2 f = xch[r_local];
+            s0 = f.x;
+            s1 = f.y;
           }
-          if (w == 0 && g.row_ok) part_lse[cur.slot * kFwdPartRows + r_local] = lse_v;
         } else {
-          __nv_bfloat16* orow = out + ((int64_t)g.row * geo.hq + h) * 128 + 64 * w;
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o0[32], o1[32];
-            tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
-            tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
-            tmem_ld_wait();
-            if (g.row_ok) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float v0 = any ? __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1 : 0.f;
-                const float v1 = any ? __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1 : 0.f;
-                pk[i] = pack_bf16x2(v0, v1);
-              }
-              uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+          const bool got = mbar_wait_warp_all(&bars->xch_m, n & 1, err);
+          ok = ok && got;
+          if (ok) {
+            const float2 o1 = xch[r_local];
+            const float m0 = m, l0 = l, m1 = o1.x, l1 = o1.y;
+            const float M = fmaxf(m0, m1);
+            const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
+            const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
+            const float L = l0 * a0 + l1 * a1;
+            const bool any = L > 0.f && cur.n_tiles > 0;  // a row with no key writes zeros
+            const float inv = any ? 1.f / L : 0.f;
+            s0 = a0 * inv;
+            s1 = a1 * inv;
+            if (any) lse_v = (M + log2f(L)) * 0.69314718055994531f;
+            xch[r_local] = make_float2(s0, s1);
           }
-          if (w == 0 && g.row_ok) lse[(int64_t)h * lse_rows + g.row] = lse_v;
+          mbar_arrive(&bars->xch_s);
+        }
+        if (ok) {
+          // Factors are zero for a row with no key (its output is zero); at least one is
+          // positive otherwise.
+          const bool any = s0 > 0.f || s1 > 0.f;
+          const int h = cur.h;
+          if (kSplit && cur.slot >= 0) {
+            // Split-KV item: the chunk's state O / l (fp32) and its lse.
+            float* prow = part_o + (cur.slot * kFwdPartRows + r_local) * 128 + 64 * w;
+  #pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o0[32], o1[32];
+              tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
+              tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
+              tmem_ld_wait();
+              if (g.row_ok) {
+                float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
+  #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  float v[4];
+  #pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    v[e] = any ? __uint_as_float(o0[4 * i + e]) * s0 + __uint_as_float(o1[4 * i + e]) * s1 : 0.f;
+                  d4[i] = make_float4(v[0], v[1], v[2], v[3]);
+                }
+              }
+            }
+            if (w == 0 && g.row_ok) part_lse[cur.slot * kFwdPartRows + r_local] = lse_v;
+          } else {
+            __nv_bfloat16* orow = out + ((int64_t)g.row * geo.hq + h) * 128 + 64 * w;
+  #pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o0[32], o1[32];
+              tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
+              tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
+              tmem_ld_wait();
+              if (g.row_ok) {
+                uint32_t pk[16];
+  #pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float v0 = any ? __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1 : 0.f;
+                  const float v1 = any ? __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1 : 0.f;
+                  pk[i] = pack_bf16x2(v0, v1);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
+  #pragma unroll
+                for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              }
+            }
+            if (w == 0 && g.row_ok) lse[(int64_t)h * lse_rows + g.row] = lse_v;
+          }
         }
       }
       cur = nxt;
@@ -1028,7 +1157,7 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
     auto kern = split ? tc_fwd_persistent_kernel<true> : tc_fwd_persistent_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FWDP_SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, FWD_THREADS, FWDP_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op], n_items,
+    kern<<<grid, FWDP_THREADS, FWDP_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op], n_items,
                                                p->bm[op], p->bn[op], (__nv_bfloat16*)o, lse, q_rows, p->err_d,
                                                p->err_d + kErrFwdCounter + 2 * op, part_o, part_lse);
     return cudaGetLastError();
