@@ -67,16 +67,18 @@ typedef enum { AUGTREE_FP32 = 0, AUGTREE_BF16 = 1 } augtree_dtype;
 typedef enum { AUGTREE_KERNEL_AUTO = 0, AUGTREE_KERNEL_SIMT = 1, AUGTREE_KERNEL_TC = 2 } augtree_kernel;
 
 /* Scheduling of the tensor-core kernels' work units (augtree_config.schedule).
- *   QUEUE       one thread block per unit, taken in queue order by the hardware block
- *               scheduler as SMs free up (the default; the dynamic largest-first greedy).
- *   PERSISTENT  the backward's key-side and query-side kernels run one persistent thread
- *               block per lane (num_sms lanes), each walking a fixed list of units:
- *               AssignGrid (Sec. 3.4, Eq. 6; augtree_assign_grid) places the queue's
- *               units on lanes, exactly when a queue has at most
- *               AUGTREE_LANES_EXACT_UNITS units, by the largest-first greedy otherwise
- *               (augtree_schedule_lanes exports the placement).  The forward keeps one
- *               block per unit, and the SIMT kernels ignore it.  Measured slower than
- *               QUEUE on every configuration; an option, not the default. */
+ *   QUEUE       units taken in queue order as SMs free up (the dynamic largest-first
+ *               greedy; the default): the forward runs one persistent thread block per
+ *               SM that takes units one after the other through a counter in the plan's
+ *               device memory and overlaps consecutive units; the backward kernels run
+ *               one thread block per unit, dispatched by the hardware in queue order.
+ *   PERSISTENT  every tensor-core kernel runs one persistent thread block per lane
+ *               (num_sms lanes), each walking a fixed list of units: AssignGrid (Sec.
+ *               3.4, Eq. 6; augtree_assign_grid) places the queue's units on lanes,
+ *               exactly when a queue has at most AUGTREE_LANES_EXACT_UNITS units, by the
+ *               largest-first greedy otherwise (augtree_schedule_lanes exports the
+ *               placement).  The SIMT kernels ignore it.  Measured slower than QUEUE on
+ *               every configuration; an option, not the default. */
 typedef enum { AUGTREE_SCHED_QUEUE = 0, AUGTREE_SCHED_PERSISTENT = 1 } augtree_schedule;
 #define AUGTREE_LANES_EXACT_UNITS 12
 

@@ -706,9 +706,11 @@ augtree_status augtree_plan_create(const augtree_desc* desc, const augtree_confi
   ok = ok && up((void**)&p->row_bstart_d, bstart.data(), bstart.size() * sizeof(int32_t));
   ok = ok && up((void**)&p->row_bend_d, bend.data(), bend.size() * sizeof(int32_t));
   // Error block: word 0 error bits, word 1 reserved, words 2-3 the wait limit (ns),
-  // words 4-7 the persistent forward's work counters.
+  // words 4-7 the persistent forward's work counters (zero).
   const uint64_t lim = kDefaultWaitLimitNs;
-  const uint32_t err_init[kErrBlockWords] = {0u, 0u, (uint32_t)lim, (uint32_t)(lim >> 32), 0u, 0u, 0u, 0u};
+  uint32_t err_init[kErrBlockWords] = {};
+  err_init[2] = (uint32_t)lim;
+  err_init[3] = (uint32_t)(lim >> 32);
   ok = ok && up((void**)&p->err_d, err_init, sizeof(err_init));
   ok = ok && up((void**)&p->splits_d, p->splits_h.data(), p->splits_h.size() * sizeof(SplitInfo));
   if (any_split) {

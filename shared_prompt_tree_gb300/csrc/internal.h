@@ -107,7 +107,7 @@ struct augtree_plan {
   int32_t* fsplit_tiles_d;
   int32_t* queue_d[augtree::kNumOps];
   int32_t ntiles_p, ntiles_r;  // 128-row query tiles per side (row-statistics buffer)
-  uint32_t* err_d;    // error block (kErrBlockWords): error bits, the wait limit (ns), forward work counters
+  uint32_t* err_d;    // error block (kErrBlockWords): error bits, the wait limit (ns), work counters
   // Persistent schedule (cfg.schedule == AUGTREE_SCHED_PERSISTENT, tensor-core family):
   // lanes of the query-side backward (over the forward queues) and of the key-side
   // backward, per op.

@@ -1,5 +1,5 @@
-// Tensor-core forward of tree attention on sm_103a: one query head per thread block,
-// with a double-buffered score tile.
+// Tensor-core forward of tree attention on sm_103a: persistent blocks, one query head
+// per work item, with a double-buffered score tile.
 //
 // AugTree paper, "Splitting Prompt Prefill from Response Replay ...":
 //   Sec. 2.2  attention as Q-KV tile interactions with an online softmax;
@@ -8,20 +8,33 @@
 //   Sec. 3.3  partial softmax states merge associatively: here the two halves of every
 //             key tile keep separate running states, merged once per row at the end
 //             (and, for a split-KV item, its chunk's state goes to the workspace for the
-//             merge across chunks).
+//             merge across chunks);
+//   Sec. 3.4  replay units placed on lanes: here a lane is a persistent block.
 //
-// One block per work item: one 128-row query tile of one query head.
-//   warp 8      TMA producer: Q, then a 3-stage ring of K/V tiles (128 keys x 128 dims)
-//   warp 9      TMEM allocator and issuer of S(j) = Q K^T into buffer j % 2
-//   warp 10     issuer of O_w += P_w(j) V_w(j), w = 0, 1 (V_w: the tile's keys
-//               [64w, 64w + 64))
-//   warps 0-7   two softmax warpgroups; warpgroup w owns keys [64w, 64w + 64) of every
-//               tile and its own running max, sum of rounded weights and accumulator
-//               O_w; thread i of each warpgroup owns row i (TMEM lane i)
+// A work item is one 128-row query tile of one query head.  One block per SM (fewer for
+// a short queue) takes items one after the other: in queue order through a counter in
+// the plan's device memory (the largest-first, stream-ordered order of the queue, as
+// the hardware would hand out one block per item), or from its lane of AssignGrid's
+// placement (persistent schedule).  Consecutive items of a block overlap: the next
+// item's query tile is warmed in L2 as soon as it is taken and loaded once the current
+// item's last S product has read Q, its first score tiles are computed while the
+// softmax warps finish the current item, and a separate warpgroup writes the output.
+// Barrier phases, the K/V ring and the score buffers run on across items (counters of
+// the block's items and K/V tiles); nothing is re-initialised between items.
+//   warp 8       TMA producer: takes and decodes the items (a ring of 4), loads Q, then a
+//                3-stage ring of K/V tiles (128 keys x 128 dims)
+//   warp 9       TMEM allocator and issuer of S(j) = Q K^T into buffer j % 2
+//   warp 10      issuer of O_w += P_w(j) V_w(j), w = 0, 1 (V_w: the tile's keys
+//                [64w, 64w + 64))
+//   warps 0-7    two softmax warpgroups; warpgroup w owns keys [64w, 64w + 64) of every
+//                tile and its own running max, sum of rounded weights and accumulator
+//                O_w; thread i of each warpgroup owns row i (TMEM lane i)
+//   warps 11-14  epilogue: the merge of the two warpgroups' states of a row, O read out
+//                of TMEM, the output rows (or a split item's partial state)
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O_0 [256,384), O_1 [384,512).
 // S(j+1) goes to the other buffer and waits only for the PV products of tile j-1, so
-// the softmax of tile j+1 can start as soon as that of tile j ends: the per-head chain
-// PV(j) -> S(j+1) of a shared score buffer is gone.
+// the softmax of tile j+1 can start as soon as that of tile j ends.  An item's first PV
+// products wait until the epilogue warps have read O out for the previous item.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -58,410 +71,28 @@ static_assert(kFwdFmaPairs >= 1 && 32 % kFwdFmaPairs == 0, "FMA exponential spac
 #define AUGTREE_FWD_VBAR 1
 #endif
 constexpr bool kFwdVBar = AUGTREE_FWD_VBAR != 0;
-constexpr int FWD_THREADS = 352;
 constexpr int FWD_NST = 3;                     // K/V ring stages
 constexpr int FWD_TILE = 128 * 128;            // 128 rows x 64 bf16 columns = 16 KB
 constexpr int FWD_Q_OFF = 0;                   // 2 blocks
 constexpr int FWD_K_OFF = FWD_Q_OFF + 2 * FWD_TILE;            // [NST][2 blocks]
 constexpr int FWD_V_OFF = FWD_K_OFF + FWD_NST * 2 * FWD_TILE;   // [NST][2 blocks]
 constexpr int FWD_BAR_OFF = FWD_V_OFF + FWD_NST * 2 * FWD_TILE;
-constexpr int FWD_SMEM = FWD_BAR_OFF + 256 + 1024;  // + barriers + alignment slack
-static_assert(FWD_SMEM <= 232448, "shared memory per block");
 
-struct FwdBars {
-  uint64_t q_full;
-  uint64_t kv_full[FWD_NST];   // K landed (and V too unless kFwdVBar)
-  uint64_t v_full[FWD_NST];    // V landed (kFwdVBar)
-  uint64_t kv_empty[FWD_NST];
-  uint64_t s_full[2];      // per S buffer
-  uint64_t p_full[2][2];   // per S buffer and warpgroup
-  uint64_t pv_done[2];     // per S buffer: both PV products of the tile have completed
-  uint64_t xch;            // both warpgroups have published their row states
-  uint64_t drain[2];
-  uint32_t tmem_base;
-};
-static_assert(sizeof(FwdBars) <= 256, "barrier area");
-
-// kSplit: the replay queue holds split-KV items (a chunk of a tile's KV walk, partial
-// state to the workspace); the instantiation without it is the plain kernel.
-template <bool kSplit>
-__global__ void __launch_bounds__(FWD_THREADS, 1) tc_fwd_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
-    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kr,
-    const __grid_constant__ CUtensorMap tm_vr, Geometry geo, const int32_t* __restrict__ queue, int bm, int bn,
-    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int64_t lse_rows, uint32_t* __restrict__ err,
-    float* __restrict__ part_o, float* __restrict__ part_lse) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + FWD_BAR_OFF);
-  // Row-state exchange at the end, [2 warpgroups][128 rows][m, l]: it reuses the Q tile,
-  // free once the last S product (implied complete by the last PV product) has read it.
-  float* xch = reinterpret_cast<float*>(smem + FWD_Q_OFF);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const WorkItem it = load_item(queue, blockIdx.x);
-  // Checked build: the item and its split are valid for the plan's geometry.
-  const bool item_ok = !kChecked || (query_item_ok(it, geo, bm, bn) &&
-                                     (kSplit ? split_item_ok(it, geo) : it.split == 0));
-  if (kChecked && !item_ok && threadIdx.x == 0) atomicOr(err, kErrCheck);
-  const int h = item_ok ? it.head : 0;
-  const GroupInfo G = geo.groups[item_ok ? it.group : 0];
-  const bool prefill = it.kind == K_PREFILL_Q;
-  const int64_t base = prefill ? G.p0 : G.r0;
-  const int64_t len = prefill ? G.lp : G.lr;
-  const int64_t row0 = item_ok ? base + (int64_t)it.tile * bm : 0;
-  const int64_t row_end = item_ok ? min(row0 + (int64_t)bm, base + len) : 0;
-  const int n_a = item_ok ? it.a : 0;
-  int n_tiles = item_ok ? n_a + (prefill ? 0 : it.b) : 0;
-  const int64_t own0 = (prefill || !item_ok) ? 0 : geo.row_bstart[row0];
-  const int kvh = h / (geo.hq / geo.hkv);
-  // Split-KV item: KV tiles [j0, j0 + n_tiles) of the walk, partial state to `slot`.
-  int j0 = 0;
-  int64_t slot = -1;
-  if (kSplit && item_ok && !prefill) {
-    const FwdSplit fs = geo.fsplit[G.tr0 + it.tile];
-    if (fs.nsplit > 1) {
-      j0 = it.split * fs.chunk;
-      n_tiles = min(fs.chunk, n_tiles - j0);
-      slot = fs.slot0 + (int64_t)h * fs.nsplit + it.split;
-    }
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < FWD_NST; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b][0], 128);
-      mbar_init(&bars->p_full[b][1], 128);
-      mbar_init(&bars->pv_done[b], 1);
-    }
-    mbar_init(&bars->xch, 256);
-    mbar_init(&bars->drain[0], 1);
-    mbar_init(&bars->drain[1], 1);
-    fence_mbar_init();
-  }
-  if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
-  if (warp == 8 && lane == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_kp);
-    prefetch_tmap(&tm_vp);
-    prefetch_tmap(&tm_kr);
-    prefetch_tmap(&tm_vr);
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      mbar_expect_tx(&bars->q_full, 2 * FWD_TILE);
-      for (int kb = 0; kb < 2; ++kb)
-        tma_load_3d(smem + FWD_Q_OFF + kb * FWD_TILE, &tm_q, &bars->q_full, kb * 64, h, (int)row0);
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int stage = j % FWD_NST, use = j / FWD_NST;
-        if (!mbar_wait(&bars->kv_empty[stage], (use & 1) ^ 1, err)) break;
-        mbar_expect_tx(&bars->kv_full[stage], (kFwdVBar ? 2 : 4) * FWD_TILE);
-        if (kFwdVBar) mbar_expect_tx(&bars->v_full[stage], 2 * FWD_TILE);
-        const int jt = j0 + j;  // tile of the row's walk
-        const bool own = jt >= n_a;
-        const int krow = own ? (int)(own0 + (int64_t)(jt - n_a) * bn) : (int)(G.p0 + (int64_t)jt * bn);
-        const CUtensorMap* km = own ? &tm_kr : &tm_kp;
-        const CUtensorMap* vm = own ? &tm_vr : &tm_vp;
-        uint64_t* vbar = kFwdVBar ? &bars->v_full[stage] : &bars->kv_full[stage];
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(smem + FWD_K_OFF + (stage * 2 + kb) * FWD_TILE, km, &bars->kv_full[stage], kb * 64, kvh, krow);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(smem + FWD_V_OFF + (stage * 2 + kb) * FWD_TILE, vm, vbar, kb * 64, kvh, krow);
-        issued = j + 1;
-      }
-      mbar_wait_drain(&bars->q_full, 0, err);
-      for (int j = max(0, issued - FWD_NST); j < issued; ++j) {
-        mbar_wait_drain(&bars->kv_full[j % FWD_NST], (j / FWD_NST) & 1, err);
-        if (kFwdVBar) mbar_wait_drain(&bars->v_full[j % FWD_NST], (j / FWD_NST) & 1, err);
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer: S
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-    const uint64_t dq = smem_desc_sw128(smem_u32(smem + FWD_Q_OFF), 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + FWD_K_OFF), 16, 1024);
-    constexpr uint64_t kStage = (2 * FWD_TILE) >> 4;
-    auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * FWD_TILE + (kk & 3) * 32) >> 4); };
-    bool ok = mbar_wait_warp_all(&bars->q_full, 0, err);
-    tc_fence_after();
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int stage = j % FWD_NST, b = j & 1;
-      if (!(ok = mbar_wait_warp_all(&bars->kv_full[stage], (j / FWD_NST) & 1, err))) break;
-      // S(j) overwrites P(j-2) in buffer b: both PV products of tile j-2 must be done.
-      if (j >= 2 && !(ok = mbar_wait_warp_all(&bars->pv_done[b], ((j >> 1) - 1) & 1, err))) break;
-      tc_fence_after();
-      const uint64_t dk = dk0 + stage * kStage;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ss_w(tmem + b * 128, dq + koff(kk), dk + koff(kk), idesc_qk, kk > 0 ? 1u : 0u);
-      mma_commit_w(&bars->s_full[b]);
-    }
-    mma_commit_w(&bars->drain[0]);
-    mbar_wait_drain_warp_all(&bars->drain[0], 0, err);
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ MMA issuer: PV
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
-    const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + FWD_V_OFF), FWD_TILE, 1024);
-    constexpr uint64_t kStage = (2 * FWD_TILE) >> 4;
-    bool ok = true;
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int stage = j % FWD_NST, b = j & 1;
-      const uint32_t par = (j >> 1) & 1;
-      if (kFwdVBar && !(ok = mbar_wait_warp_all(&bars->v_full[stage], (j / FWD_NST) & 1, err))) break;
-      if (!kFwdPvEarly) {
-        if (!(ok = mbar_wait_warp_all(&bars->p_full[b][0], par, err))) break;
-        if (!(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
-        tc_fence_after();
-      }
-      const uint64_t dv = dv0 + stage * kStage;
-      // 16 keys per step: 16 swizzled 128-byte rows of V = 2048 bytes; P packs two keys
-      // per TMEM column.  Warpgroup w's keys [64w, 64w + 64) sit in columns
-      // [64w, 64w + 32) of the buffer.
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        if (kFwdPvEarly) {
-          // O_w's product goes as soon as warpgroup w's P is ready.
-          if (!(ok = mbar_wait_warp_all(&bars->p_full[b][w], par, err))) break;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts_w(tmem + 256 + w * 128, tmem + b * 128 + w * 64 + kk * 8, dv + (4 * w + kk) * (2048 >> 4), idesc_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      if (!ok) break;
-      mma_commit_w(&bars->pv_done[b]);
-      mma_commit_w(&bars->kv_empty[stage]);
-    }
-    mma_commit_w(&bars->drain[1]);
-    mbar_wait_drain_warp_all(&bars->drain[1], 0, err);
-  } else {
-    // ------------------------------------------------------------ softmax (half tiles)
-    const int w = warp >> 2;        // keys [64w, 64w + 64) of every tile
-    const int q4 = warp & 3;        // TMEM lane quarter
-    const int r_local = q4 * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    FwdRowGeom g;
-    g.row = row0 + r_local;
-    g.row_ok = g.row < row_end;
-    g.prefill = prefill;
-    g.bs = (!prefill && g.row_ok) ? geo.row_bstart[g.row] : 0;
-    g.p0 = G.p0;
-    g.p_end = (int64_t)G.p0 + G.lp;
-    g.own0 = own0;
-    g.n_a = n_a;
-    g.bn = bn;
-    g.j0 = j0;
-    const float sl2 = geo.scale_log2;
-    const uint32_t tO = tmem + lane_off + 256 + w * 128;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      const uint32_t tS = tmem + lane_off + b * 128 + w * 64;
-      if (!(ok = mbar_wait_warp_all(&bars->s_full[b], (j >> 1) & 1, err))) break;
-      tc_fence_after();
-      uint32_t raw[2][32];
-      tmem_ld32(tS, raw[0]);
-      tmem_ld32(tS + 32, raw[1]);
-      tmem_ld_wait();
-#define FWD_X(c) raw[(c) >> 5][(c) & 31]
-      int lo_i, hi_i;
-      fwd_valid_cols(g, j, lo_i, hi_i);
-      const int lo = lo_i - 64 * w, hi = hi_i - 64 * w;  // valid local columns [lo, hi]
-      const bool masked = lo > 0 || hi < 63;
-      if (masked) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < lo || c > hi) FWD_X(c) = 0xFF800000u;  // -inf
-      }
-      float pm[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        pm[k] = fmax3(__uint_as_float(FWD_X(k)), __uint_as_float(FWD_X(k + 8)), __uint_as_float(FWD_X(k + 16)));
-#pragma unroll
-      for (int c = 24; c < 56; c += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], __uint_as_float(FWD_X(c + k)), __uint_as_float(FWD_X(c + 8 + k)));
-#pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], __uint_as_float(FWD_X(56 + k)));
-      const float tmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7]));
-      const float mx = tmax * sl2;  // -inf stays -inf
-      // Lazy rescaling: the offset moves only when the max grows by more than 2^8
-      // (exact: every term of the state shares the offset).
-      const bool need = (m != -INFINITY) && (mx > m + 8.0f);
-      const float m_new = (m == -INFINITY) ? mx : (need ? mx : m);
-      const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-      m = m_new;
-      const float mu = (m == -INFINITY) ? 0.f : m;
-      uint32_t pk[32];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a0 = fmaf(__uint_as_float(FWD_X(2 * i)), sl2, -mu);
-        const float a1 = fmaf(__uint_as_float(FWD_X(2 * i + 1)), sl2, -mu);
-        const float p0 = fast_exp2(a0);
-        float p1;
-        if (i % kFwdFmaPairs == kFwdFmaPairs - 1) {
-          // One exponential in 2 * kFwdFmaPairs on the FMA pipe; a masked column stays
-          // exactly zero.
-          p1 = exp2_fma(a1);
-          if (masked && a1 == -INFINITY) p1 = 0.f;
-        } else {
-          p1 = fast_exp2(a1);
-        }
-        pk[i] = pack_bf16x2(p0, p1);
-        // The row sum uses the bf16 weights the PV product uses.
-        ps[i & 3] = add_bf16x2_f32(ps[i & 3], pk[i]);
-      }
-#undef FWD_X
-      tmem_st32(tS, pk);
-      tmem_st_wait();
-      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      if (__any_sync(0xffffffffu, need)) {
-        // O_w += P(j-1) V must be complete before O_w is rescaled; PV(j) is issued only
-        // after this warpgroup signals P(j).
-        if (!(ok = mbar_wait_warp_all(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err))) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c * 32, o);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[b][w]);
-    }
-    // Merge the two warpgroups' states of each row: (O_0, m_0, l_0) and (O_1, m_1, l_1).
-    const int last = n_tiles - 1;
-    if (ok && n_tiles > 0) ok = mbar_wait_warp_all(&bars->pv_done[last & 1], (last >> 1) & 1, err);
-    tc_fence_after();
-    float* mine = xch + (w * 128 + r_local) * 2;
-    mine[0] = m;
-    mine[1] = l;
-    mbar_arrive(&bars->xch);  // also on a failed wait, so the other warpgroup's wait ends
-    if (ok) ok = mbar_wait_warp_all(&bars->xch, 0, err);
-    if (ok) {
-      const float m0 = xch[r_local * 2], l0 = xch[r_local * 2 + 1];
-      const float m1 = xch[(128 + r_local) * 2], l1 = xch[(128 + r_local) * 2 + 1];
-      const float M = fmaxf(m0, m1);
-      const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
-      const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
-      const float L = l0 * a0 + l1 * a1;
-      const bool any = L > 0.f && n_tiles > 0;  // a row with no key writes zeros
-      const float inv = any ? 1.f / L : 0.f;
-      const float s0 = a0 * inv, s1 = a1 * inv;
-      // Warpgroup w writes dims [64w, 64w + 64) of its rows.
-      __nv_bfloat16* orow = out + (g.row * geo.hq + h) * 128 + 64 * w;
-      if (kSplit && slot >= 0) {
-        // Split-KV item: the chunk's state O / l (fp32) and its lse.
-        float* prow = part_o + (slot * kFwdPartRows + r_local) * 128 + 64 * w;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
-          tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
-          tmem_ld_wait();
-          if (g.row_ok) {
-            float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float v[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                v[e] = any ? __uint_as_float(o0[4 * i + e]) * s0 + __uint_as_float(o1[4 * i + e]) * s1 : 0.f;
-              d4[i] = make_float4(v[0], v[1], v[2], v[3]);
-            }
-          }
-        }
-        if (w == 0 && g.row_ok)
-          part_lse[slot * kFwdPartRows + r_local] = any ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-      } else {
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o0[32], o1[32];
-        tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
-        tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
-        tmem_ld_wait();
-        if (g.row_ok) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float v0 = any ? __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1 : 0.f;
-            const float v1 = any ? __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1 : 0.f;
-            pk[i] = pack_bf16x2(v0, v1);
-          }
-          uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
-      }
-      if (w == 0 && g.row_ok) lse[(int64_t)h * lse_rows + g.row] = any ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ---------------------------------------------------------------- persistent form
-// One block per SM; each block takes work items from the queue in queue order through
-// a counter in device memory (so the queue's largest-first, stream-ordered order is
-// kept, as with one block per item), and the items of a block overlap: the next item's
-// query tile is warmed in L2 as soon as the item is taken, loaded once the current
-// item's last S product has read Q, and its first score tiles are computed while the
-// softmax warps finish the current item (last tile, merge of the two warpgroups' states,
-// output).  Barrier phases, the K/V ring and the score buffers run on across items
-// (counters of the block's items and K/V tiles), so nothing is re-initialised between
-// items.
-#ifndef AUGTREE_FWD_PERSISTENT
-#define AUGTREE_FWD_PERSISTENT 1
-#endif
-constexpr bool kFwdPersistent = AUGTREE_FWD_PERSISTENT != 0;
-// 1: a fifth warpgroup writes each item's output (merge of the two softmax warpgroups'
-// states, O read out of TMEM, stores), so the softmax warps go on to the next item at
-// once; the next item's first PV product waits until the output has been read out.
-// 0: the softmax warps write it themselves.
-#ifndef AUGTREE_FWD_EPI_WARPS
-#define AUGTREE_FWD_EPI_WARPS 1
-#endif
-constexpr bool kFwdEpi = AUGTREE_FWD_EPI_WARPS != 0;
-constexpr int FWDP_THREADS = kFwdEpi ? 480 : 352;
-constexpr int FWDP_SLOTS = kFwdEpi ? 4 : 2;  // ring of decoded items
+// ---------------------------------------------------------------- kernel
+constexpr int FWDP_SLOTS = 4;  // ring of decoded items
+constexpr int FWDP_THREADS = 480;
 constexpr int FWDP_BAR_BYTES = 288;
-// Behind the tiles: barriers, the row-state exchange ([2 warpgroups][128 rows] float2
-// with the epilogue warps, [128 rows] float2 between the two softmax warpgroups
-// otherwise) and the decoded items.
+// Behind the tiles: barriers, the row states handed to the epilogue warps ([2
+// warpgroups][128 rows] float2) and the decoded items.
 constexpr int FWD_XCH_OFF = FWD_BAR_OFF + FWDP_BAR_BYTES;
-constexpr int FWD_SLOT_OFF = FWD_XCH_OFF + (kFwdEpi ? 2048 : 1024);
+constexpr int FWD_SLOT_OFF = FWD_XCH_OFF + 2048;
 constexpr int FWDP_END = FWD_SLOT_OFF + 64 * FWDP_SLOTS;
 // The block takes the most shared memory a block may have; the tiles start at the first
 // 1024-byte boundary of it, and a block whose allocation leaves too little room behind
 // that boundary records an error and does nothing.
 constexpr int FWDP_SMEM = 232448;
 static_assert(FWDP_END <= FWDP_SMEM, "shared memory per block");
-constexpr int FWD_CONSUMER_WARPS = kFwdEpi ? 14 : 10;  // S and PV issuers, 8 softmax warps (+ 4 epilogue)
+constexpr int FWD_CONSUMER_WARPS = 14;  // S and PV issuers, 8 softmax warps, 4 epilogue warps
 
 struct FwdPBars {
   uint64_t q_full, q_empty;
@@ -473,9 +104,7 @@ struct FwdPBars {
   uint64_t pv_done[2];
   uint64_t item_full[FWDP_SLOTS];   // a decoded item is in slot i
   uint64_t item_empty[FWDP_SLOTS];  // every consumer warp has read slot i
-  uint64_t xch_m;          // warpgroup 1 has published (m, l) of its rows
-  uint64_t xch_s;          // warpgroup 0 has published the merge factors
-  uint64_t ml_ready;       // both softmax warpgroups have published (m, l) (epilogue warps)
+  uint64_t ml_ready;       // both softmax warpgroups have published (m, l)
   uint64_t ml_free;        // the epilogue warps have read them
   uint64_t o_free;         // the epilogue warps have read O_0 and O_1 out of TMEM
   uint64_t drain[2];
@@ -483,67 +112,16 @@ struct FwdPBars {
 };
 static_assert(sizeof(FwdPBars) <= FWDP_BAR_BYTES, "barrier area");
 
-// A work item decoded once by the producer for every warp of the block.
-struct FwdSlot {
-  int32_t stop;             // 1: the queue is exhausted
-  int32_t h;                // query head
-  int32_t prefill;
-  int32_t n_a;              // prompt KV tiles of the rows' walk
-  int32_t n_tiles;          // KV tiles this item walks
-  int32_t j0;               // first KV tile of the walk (split item), else 0
-  int32_t row0, row_end;    // query rows [row0, row_end)
-  int32_t own0;             // first key of the own-branch tiles
-  int32_t p0, lp;           // the group's prompt keys
-  int32_t pad;
-  int64_t slot;             // partial-state slot of a split item, else -1
-};
-static_assert(sizeof(FwdSlot) <= 64, "item slot");
-
-template <bool kSplit>
-__device__ __forceinline__ FwdSlot decode_fwd_item(const int32_t* __restrict__ queue, int idx, const Geometry& geo,
-                                                   int bm, int bn, uint32_t* err) {
-  FwdSlot s;
-  const WorkItem it = load_item(queue, idx);
-  // Checked build: the item and its split are valid for the plan's geometry.
-  const bool item_ok = !kChecked || (query_item_ok(it, geo, bm, bn) &&
-                                     (kSplit ? split_item_ok(it, geo) : it.split == 0));
-  if (kChecked && !item_ok) atomicOr(err, kErrCheck);
-  const GroupInfo G = geo.groups[item_ok ? it.group : 0];
-  s.stop = 0;
-  s.h = item_ok ? it.head : 0;
-  s.prefill = it.kind == K_PREFILL_Q ? 1 : 0;
-  const int base = s.prefill ? G.p0 : G.r0, len = s.prefill ? G.lp : G.lr;
-  s.row0 = item_ok ? base + it.tile * bm : 0;
-  s.row_end = item_ok ? min(s.row0 + bm, base + len) : 0;
-  s.n_a = item_ok ? it.a : 0;
-  s.n_tiles = item_ok ? s.n_a + (s.prefill ? 0 : it.b) : 0;
-  s.own0 = (s.prefill || !item_ok) ? 0 : geo.row_bstart[s.row0];
-  s.p0 = G.p0;
-  s.lp = G.lp;
-  s.pad = 0;
-  s.j0 = 0;
-  s.slot = -1;
-  if (kSplit && item_ok && !s.prefill) {
-    const FwdSplit fs = geo.fsplit[G.tr0 + it.tile];
-    if (fs.nsplit > 1) {
-      s.j0 = it.split * fs.chunk;
-      s.n_tiles = min(fs.chunk, s.n_tiles - s.j0);
-      s.slot = fs.slot0 + (int64_t)s.h * fs.nsplit + it.split;
-    }
-  }
-  return s;
-}
-
-// ctr: two words of the plan's device memory, zero between launches: the next item to
-// take, and the blocks that have finished taking items.
-template <bool kSplit>
-__global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
+// kLanes: items from the block's lane (lane_off / lane_units) instead of the counter pair
+// ctr.  kSplit: the replay queue holds split-KV items.
+template <bool kLanes, bool kSplit>
+__global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
     const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kr,
     const __grid_constant__ CUtensorMap tm_vr, Geometry geo, const int32_t* __restrict__ queue,
     unsigned n_items, int bm, int bn, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int64_t lse_rows,
-    uint32_t* __restrict__ err, unsigned* __restrict__ ctr, float* __restrict__ part_o,
-    float* __restrict__ part_lse) {
+    uint32_t* __restrict__ err, unsigned* __restrict__ ctr, const int32_t* __restrict__ lane_off,
+    const int32_t* __restrict__ lane_units, float* __restrict__ part_o, float* __restrict__ part_lse) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if ((smem - smem_raw) + FWDP_END > FWDP_SMEM) {
@@ -552,7 +130,7 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
   }
   FwdPBars* bars = reinterpret_cast<FwdPBars*>(smem + FWD_BAR_OFF);
   float2* xch = reinterpret_cast<float2*>(smem + FWD_XCH_OFF);
-  FwdSlot* slots = reinterpret_cast<FwdSlot*>(smem + FWD_SLOT_OFF);
+  QuerySlot* slots = reinterpret_cast<QuerySlot*>(smem + FWD_SLOT_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -574,8 +152,6 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
       mbar_init(&bars->item_full[i], 1);
       mbar_init(&bars->item_empty[i], FWD_CONSUMER_WARPS);
     }
-    mbar_init(&bars->xch_m, 128);
-    mbar_init(&bars->xch_s, 128);
     mbar_init(&bars->ml_ready, 256);
     mbar_init(&bars->ml_free, 128);
     mbar_init(&bars->o_free, 128);
@@ -601,10 +177,11 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
       int n = 0;         // items of this block so far
       int n_q = 0;       // query tiles loaded
       int jg = 0;        // K/V tiles loaded
-      FwdSlot stop_slot{};
+      QuerySlot stop_slot{};
       stop_slot.stop = 1;
-      unsigned taken = atomicAdd(ctr, 1u);
-      FwdSlot cur = taken < n_items ? decode_fwd_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
+      ItemSource<kLanes> src = item_source<kLanes>(ctr, lane_off, lane_units, n_items);
+      unsigned taken = src.next();
+      QuerySlot cur = taken < n_items ? decode_query_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
       slots[0] = cur;
       mbar_arrive(&bars->item_full[0]);
       if (!cur.stop) {
@@ -613,8 +190,8 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
       }
       while (!cur.stop) {
         // Take the next item now and publish it, so that every warp can prepare it.
-        taken = atomicAdd(ctr, 1u);
-        const FwdSlot nxt = taken < n_items ? decode_fwd_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
+        taken = src.next();
+        const QuerySlot nxt = taken < n_items ? decode_query_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
         const int u = n + 1, sn = u % FWDP_SLOTS;
         if (u >= FWDP_SLOTS && !(ok = mbar_wait(&bars->item_empty[sn], ((u / FWDP_SLOTS) - 1) & 1, err))) break;
         slots[sn] = nxt;
@@ -658,15 +235,7 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
         mbar_wait_drain(&bars->kv_full[t % FWD_NST], (uint32_t)(t / FWD_NST) & 1, err);
         if (kFwdVBar) mbar_wait_drain(&bars->v_full[t % FWD_NST], (uint32_t)(t / FWD_NST) & 1, err);
       }
-      // A block that gave up takes the rest of the queue unprocessed, so that the counter
-      // always passes the end; the last block to finish zeroes both words for the next
-      // launch (launches on one plan are ordered on the GPU).
-      while (taken < n_items) taken = atomicAdd(ctr, 1u);
-      __threadfence();
-      if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
-        atomicExch(ctr, 0u);
-        atomicExch(ctr + 1, 0u);
-      }
+      src.finish(taken);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer: S
@@ -680,7 +249,8 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
     for (int n = 0; ok; ++n) {
       const int sn = n % FWDP_SLOTS;
       if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n / FWDP_SLOTS) & 1, err))) break;
-      const int stop = slots[sn].stop, n_tiles = slots[sn].n_tiles;
+      const QuerySlot it = warp_uniform(slots[sn]);
+      const int stop = it.stop, n_tiles = it.n_tiles;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
       if (stop) break;
@@ -715,7 +285,8 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
     for (int n = 0; ok; ++n) {
       const int sn = n % FWDP_SLOTS;
       if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n / FWDP_SLOTS) & 1, err))) break;
-      const int stop = slots[sn].stop, n_tiles = slots[sn].n_tiles;
+      const QuerySlot it = warp_uniform(slots[sn]);
+      const int stop = it.stop, n_tiles = it.n_tiles;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
       if (stop) break;
@@ -723,14 +294,9 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
         const int stage = (int)(jg % FWD_NST), b = (int)(jg & 1);
         const uint32_t par = (uint32_t)(jg >> 1) & 1;
         if (kFwdVBar && !(ok = mbar_wait_warp_all(&bars->v_full[stage], (uint32_t)(jg / FWD_NST) & 1, err))) break;
-        // An item's first products overwrite O_0 and O_1, read out for the previous item
-        // by the epilogue warps, or else by both softmax warpgroups (each signals P of
-        // this tile only after that).
-        if (kFwdEpi) {
-          if (j == 0 && n >= 1 && !(ok = mbar_wait_warp_all(&bars->o_free, (n - 1) & 1, err))) break;
-        } else {
-          if (j == 0 && !(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
-        }
+        // An item's first products overwrite O_0 and O_1, which the epilogue warps read
+        // out for the previous item.
+        if (j == 0 && n >= 1 && !(ok = mbar_wait_warp_all(&bars->o_free, (n - 1) & 1, err))) break;
         if (!kFwdPvEarly) {
           if (!(ok = mbar_wait_warp_all(&bars->p_full[b][0], par, err))) break;
           if (!(ok = mbar_wait_warp_all(&bars->p_full[b][1], par, err))) break;
@@ -756,7 +322,7 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
     }
     mma_commit_w(&bars->drain[1]);
     mbar_wait_drain_warp_all(&bars->drain[1], 0, err);
-  } else if (kFwdEpi && warp >= 11) {
+  } else if (warp >= 11) {
     // ------------------------------------------------------------ epilogue warps
     // Warp 11 + i reads TMEM lane quarter (11 + i) % 4; thread r owns row r of the tile,
     // all 128 dims: the merge of the two softmax warpgroups' states (O_0, m_0, l_0) and
@@ -769,7 +335,7 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
     for (int n = 0; ok; ++n) {
       const int sn = n % FWDP_SLOTS;
       if (!(ok = mbar_wait_warp_all(&bars->item_full[sn], (n / FWDP_SLOTS) & 1, err))) break;
-      const FwdSlot cur = slots[sn];
+      const QuerySlot cur = warp_uniform(slots[sn]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
       if (cur.stop) break;
@@ -850,10 +416,10 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
     const float sl2 = geo.scale_log2;
     const uint32_t tO = tmem + lane_off + 256 + w * 128;
     bool ok = mbar_wait_warp_all(&bars->item_full[0], 0, err);
-    FwdSlot cur{};
+    QuerySlot cur{};
     cur.stop = 1;
     if (ok) {
-      cur = slots[0];
+      cur = warp_uniform(slots[0]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[0]);
     }
@@ -955,114 +521,24 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_persistent_kernel(
         mbar_arrive(&bars->p_full[b][w]);
         ++jg;
       }
-      if (kFwdEpi) {
-        // Hand the rows' states to the epilogue warps, once they have read the previous
-        // item's.
-        if (ok && n >= 1) ok = mbar_wait_warp_all(&bars->ml_free, (n - 1) & 1, err);
-        if (ok) xch[w * 128 + r_local] = make_float2(m, l);
-        mbar_arrive(&bars->ml_ready);  // also after a failed wait, so that the epilogue's wait ends
-      }
-      // The next item, published an item ahead: its row's branch start is fetched now and
-      // used after this item's output.
-      FwdSlot nxt{};
+      // Hand the rows' states to the epilogue warps, once they have read the previous
+      // item's.
+      if (ok && n >= 1) ok = mbar_wait_warp_all(&bars->ml_free, (n - 1) & 1, err);
+      if (ok) xch[w * 128 + r_local] = make_float2(m, l);
+      mbar_arrive(&bars->ml_ready);  // also after a failed wait, so that the epilogue's wait ends
+      // The next item, published an item ahead: its row's branch start is fetched now.
+      QuerySlot nxt{};
       nxt.stop = 1;
       if (ok) {
         const int sn = (n + 1) % FWDP_SLOTS;
         if (mbar_wait_warp_all(&bars->item_full[sn], ((n + 1) / FWDP_SLOTS) & 1, err)) {
-          nxt = slots[sn];
+          nxt = warp_uniform(slots[sn]);
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->item_empty[sn]);
         }
       }
       const int nrow = nxt.row0 + r_local;
       const int bs_next = (!nxt.stop && !nxt.prefill && nrow < nxt.row_end) ? geo.row_bstart[nrow] : 0;
-      if constexpr (!kFwdEpi) {
-        // Merge the two warpgroups' states of each row, (O_0, m_0, l_0) and (O_1, m_1, l_1):
-        // warpgroup 1 hands its (m, l) to warpgroup 0, which returns the two factors.
-        const int last = jg - 1;
-        if (ok && cur.n_tiles > 0) ok = mbar_wait_warp_all(&bars->pv_done[last & 1], (uint32_t)(last >> 1) & 1, err);
-        tc_fence_after();
-        float s0 = 0.f, s1 = 0.f, lse_v = -INFINITY;
-        if (w == 1) {
-          xch[r_local] = make_float2(m, l);
-          mbar_arrive(&bars->xch_m);  // also after a failed wait, so that the other warpgroup's wait ends
-          if (ok) ok = mbar_wait_warp_all(&bars->xch_s, n & 1, err);
-          if (ok) {
-            const float2 f = xch[r_local];
-            s0 = f.x;
-            s1 = f.y;
-          }
-        } else {
-          const bool got = mbar_wait_warp_all(&bars->xch_m, n & 1, err);
-          ok = ok && got;
-          if (ok) {
-            const float2 o1 = xch[r_local];
-            const float m0 = m, l0 = l, m1 = o1.x, l1 = o1.y;
-            const float M = fmaxf(m0, m1);
-            const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - M);
-            const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
-            const float L = l0 * a0 + l1 * a1;
-            const bool any = L > 0.f && cur.n_tiles > 0;  // a row with no key writes zeros
-            const float inv = any ? 1.f / L : 0.f;
-            s0 = a0 * inv;
-            s1 = a1 * inv;
-            if (any) lse_v = (M + log2f(L)) * 0.69314718055994531f;
-            xch[r_local] = make_float2(s0, s1);
-          }
-          mbar_arrive(&bars->xch_s);
-        }
-        if (ok) {
-          // Factors are zero for a row with no key (its output is zero); at least one is
-          // positive otherwise.
-          const bool any = s0 > 0.f || s1 > 0.f;
-          const int h = cur.h;
-          if (kSplit && cur.slot >= 0) {
-            // Split-KV item: the chunk's state O / l (fp32) and its lse.
-            float* prow = part_o + (cur.slot * kFwdPartRows + r_local) * 128 + 64 * w;
-  #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-              uint32_t o0[32], o1[32];
-              tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
-              tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
-              tmem_ld_wait();
-              if (g.row_ok) {
-                float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
-  #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  float v[4];
-  #pragma unroll
-                  for (int e = 0; e < 4; ++e)
-                    v[e] = any ? __uint_as_float(o0[4 * i + e]) * s0 + __uint_as_float(o1[4 * i + e]) * s1 : 0.f;
-                  d4[i] = make_float4(v[0], v[1], v[2], v[3]);
-                }
-              }
-            }
-            if (w == 0 && g.row_ok) part_lse[cur.slot * kFwdPartRows + r_local] = lse_v;
-          } else {
-            __nv_bfloat16* orow = out + ((int64_t)g.row * geo.hq + h) * 128 + 64 * w;
-  #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-              uint32_t o0[32], o1[32];
-              tmem_ld32(tmem + lane_off + 256 + 64 * w + 32 * c, o0);
-              tmem_ld32(tmem + lane_off + 384 + 64 * w + 32 * c, o1);
-              tmem_ld_wait();
-              if (g.row_ok) {
-                uint32_t pk[16];
-  #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const float v0 = any ? __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1 : 0.f;
-                  const float v1 = any ? __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1 : 0.f;
-                  pk[i] = pack_bf16x2(v0, v1);
-                }
-                uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
-  #pragma unroll
-                for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-              }
-            }
-            if (w == 0 && g.row_ok) lse[(int64_t)h * lse_rows + g.row] = lse_v;
-          }
-        }
-      }
       cur = nxt;
       bs = bs_next;
     }
@@ -1147,27 +623,26 @@ cudaError_t tc_fwd(const augtree_plan* p, int op, const void* q, const void* kp,
   // The split-KV instantiation only where the replay queue has split items.
   const bool split = !prefill && p->n_fwd_parts > 0;
   if (split && (!part_o || !part_lse)) return cudaErrorInvalidValue;
-  if (kFwdPersistent) {
-    // One block per SM (fewer if the queue is shorter), items taken in queue order.
+  const unsigned n_items = (unsigned)p->n_items[op];
+  // Persistent schedule: one block per lane of AssignGrid's placement; else one block
+  // per SM (fewer for a short queue) taking items in queue order.
+  const LaneSet& ls = p->lanes_dq[op];
+  const bool lanes = ls.off_d != nullptr;
+  unsigned grid = (unsigned)ls.n_lanes;
+  if (!lanes) {
     int sms = 0;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) return e;
-    const unsigned n_items = (unsigned)p->n_items[op];
-    const unsigned grid = std::min<unsigned>(n_items, (unsigned)std::max(sms, 1));
-    auto kern = split ? tc_fwd_persistent_kernel<true> : tc_fwd_persistent_kernel<false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FWDP_SMEM);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, FWDP_THREADS, FWDP_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op], n_items,
-                                               p->bm[op], p->bn[op], (__nv_bfloat16*)o, lse, q_rows, p->err_d,
-                                               p->err_d + kErrFwdCounter + 2 * op, part_o, part_lse);
-    return cudaGetLastError();
+    grid = std::min<unsigned>(n_items, (unsigned)std::max(sms, 1));
   }
-  auto kern = split ? tc_fwd_kernel<true> : tc_fwd_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
+  auto kern = lanes ? (split ? tc_fwd_kernel<true, true> : tc_fwd_kernel<true, false>)
+                    : (split ? tc_fwd_kernel<false, true> : tc_fwd_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FWDP_SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)p->n_items[op], FWD_THREADS, FWD_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op],
-                                                                p->bm[op], p->bn[op], (__nv_bfloat16*)o, lse, q_rows,
-                                                                p->err_d, part_o, part_lse);
+  kern<<<grid, FWDP_THREADS, FWDP_SMEM, st>>>(mq, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[op], n_items, p->bm[op],
+                                             p->bn[op], (__nv_bfloat16*)o, lse, q_rows, p->err_d,
+                                             p->err_d + kErrFwdCounter + 2 * op, lanes ? ls.off_d : nullptr,
+                                             lanes ? ls.units_d : nullptr, part_o, part_lse);
   return cudaGetLastError();
 }
 
