@@ -53,6 +53,12 @@ constexpr int DQ_THREADS = 352;  // 8 compute warps, producer, two MMA issuers
 constexpr int KST = 3;                             // K ring stages
 constexpr int VST = 2;                             // V ring stages
 constexpr int kPrefetchTiles = 4;                  // L2 prefetch distance (KV tiles)
+// 1: each block warms L2 with the Q and dO tiles of the item one wave (the SM count)
+// ahead in the queue.
+#ifndef AUGTREE_DQ_NEXT_WAVE
+#define AUGTREE_DQ_NEXT_WAVE 1
+#endif
+constexpr bool kDqPrefetchNextWave = AUGTREE_DQ_NEXT_WAVE != 0;
 constexpr int BLK = 128 * 128;                     // 128 rows x 64 dims bf16 = 16 KB
 constexpr int DQ_Q_OFF = 0;                        // 2 blocks
 constexpr int DQ_DO_OFF = DQ_Q_OFF + 2 * BLK;      // 2 blocks
@@ -93,7 +99,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr, Geometry geo,
     const int32_t* __restrict__ queue, int bm, int bn, const float* __restrict__ stats, int ntiles,
     __nv_bfloat16* __restrict__ dq_out, uint32_t* __restrict__ err,
-    const int32_t* __restrict__ sched_off, const int32_t* __restrict__ sched_units, float* __restrict__ dq_part) {
+    const int32_t* __restrict__ sched_off, const int32_t* __restrict__ sched_units, float* __restrict__ dq_part,
+    int64_t n_items, int ahead) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DqBars* bars = reinterpret_cast<DqBars*>(smem + DQ_BAR_OFF);
@@ -211,6 +218,20 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
           for (int kb = 0; kb < 2; ++kb) {
             tma_prefetch_3d(kmp, kb * 64, kvh, rp);
             tma_prefetch_3d(vmp, kb * 64, kvh, rp);
+          }
+        }
+      }
+      // Warm L2 with the Q and dO tiles of the item a wave ahead in the queue (the block
+      // that will start on some SM about when this one ends), so that its first copies
+      // hit L2.
+      if (!kPersistent && ahead > 0 && unit + ahead < n_items) {
+        const WorkItem nx = load_item(queue, unit + ahead);
+        if (!kChecked || query_item_ok(nx, geo, bm, bn)) {
+          const GroupInfo NG = geo.groups[nx.group];
+          const int nrow = (nx.kind == K_PREFILL_Q ? NG.p0 : NG.r0) + nx.tile * bm;
+          for (int kb = 0; kb < 2; ++kb) {
+            tma_prefetch_3d(&tm_q, kb * 64, nx.head, nrow);
+            tma_prefetch_3d(&tm_do, kb * 64, nx.head, nrow);
           }
         }
       }
@@ -468,10 +489,14 @@ cudaError_t tc_bwd_dq(const augtree_plan* p, int op, const void* q, const void* 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = persistent ? (unsigned)ls.n_lanes : (unsigned)p->n_items[fop];
+  // One block per SM runs at a time: the item a wave ahead is the one an SM's next block
+  // is likely to take.
+  int sms = 0;
+  if (!persistent && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) sms = 0;
   kern<<<grid, DQ_THREADS, DQ_SMEM, st>>>(
       mq, mdo, mkp, mvp, mkr, mvr, geometry(p), p->queue_d[fop], p->bm[fop], p->bn[fop], stats,
       prefill ? p->ntiles_p : p->ntiles_r, (__nv_bfloat16*)dq, p->err_d, persistent ? ls.off_d : nullptr,
-      persistent ? ls.units_d : nullptr, dq_part);
+      persistent ? ls.units_d : nullptr, dq_part, (int64_t)p->n_items[fop], kDqPrefetchNextWave ? sms : 0);
   return cudaGetLastError();
 }
 
