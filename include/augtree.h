@@ -174,15 +174,19 @@ typedef struct augtree_plan augtree_plan;
  * gets s = min(64, max(1, ceil(nq*r / T))) splits of C = ceil(nq / s) query tiles
  * (then s = ceil(nq / C)); split k covers query tiles [k*C, min((k+1)*C, nq)).
  *
- * Order: thread blocks take items in queue order.  Every item walks the tiles of one
- * stream: a forward item (kinds 0, 1) the K/V of its group's KV head (head / r); a
- * key-side item the query tiles of its group for its KV head (kinds 2, 4, 5) or of the
- * branch holding the tile's first key (kind 3).  The items of a stream are contiguous;
- * streams come by total cost descending, then (group, KV head, branch) ascending with -1
- * for a group-wide stream; within a stream items come by cost descending, then (tile,
- * kind, split, head) ascending - the largest-first greedy balancing of replay units
- * (Sec. 3.4) within each stream.  Blocks that run side by side then walk the same
- * tiles, which L2 holds once for all of them.
+ * Order: items start in queue order.  Every item walks the tiles of one stream: a
+ * forward item (kinds 0, 1) the K/V of its group's KV head (head / r); a key-side item
+ * the query tiles of its group for its KV head (kinds 2, 4, 5) or of the branch holding
+ * the tile's first key (kind 3).  The items of a stream are contiguous; streams come by
+ * total cost descending, then (group, KV head, branch) ascending with -1 for a
+ * group-wide stream.  Within a stream, replay forward items (kind 1) form sub-streams by
+ * the branch of their query tile's first row (whose own-branch keys they read): the
+ * items of a sub-stream are contiguous, sub-streams come by total cost descending, then
+ * branch ascending; every other item is its stream's only sub-stream.  Within a
+ * sub-stream items come by cost descending, then (tile, kind, split, head) ascending -
+ * the largest-first greedy balancing of replay units (Sec. 3.4) within each sub-stream.
+ * Blocks that run side by side then walk the same tiles, which L2 holds once for all of
+ * them.
  */
 #define AUGTREE_ITEM_WORDS 8
 

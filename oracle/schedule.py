@@ -17,11 +17,14 @@ Order.  Every item walks the tiles of one stream: a forward item the K/V of its
 group's KV head (query head h uses KV head h // r); a key-side item the Q/dO tiles of
 its group for its KV head (prompt keys) or of its own branch (response keys).  The
 items of a stream form a chunk; chunks go largest first by their total cost (ties by
-group, KV head, branch, with -1 for a group-wide stream), and items within a chunk
-largest first (ties by tile, kind, split, head).  This keeps largest-first balancing
-within a chunk and makes the blocks that run side by side share one stream (cache
-locality of the on-chip scheduling; the pages' balancing is across lanes of a
-multi-node cluster and says nothing about it).
+group, KV head, branch, with -1 for a group-wide stream).  Within a chunk, replay
+forward items form sub-chunks by the branch of their query tile's first row (the
+branch whose keys their own-branch tiles are), largest first (ties by branch); every
+other item is its chunk's only sub-chunk.  Items within a sub-chunk go largest first
+(ties by tile, kind, split, head).  This keeps largest-first balancing within a
+sub-chunk and makes the blocks that run side by side share one stream (cache locality
+of the on-chip scheduling; the pages' balancing is across lanes of a multi-node
+cluster and says nothing about it).
 """
 from __future__ import annotations
 
@@ -121,6 +124,7 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int,
     groups = _groups(offsets)
     items: List[Tuple[int, ...]] = []
     branch_of_item = {}  # response-key items: index of the branch whose tiles they walk
+    row_branch_of_item = {}  # replay forward items: branch of the query tile's first row
     if op == OP_PREFILL_FWD:
         for g, grp in enumerate(groups):
             for t in range(_cdiv(grp["lp"], bm)):
@@ -135,18 +139,20 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int,
             for t in range(_cdiv(grp["lr"], bm)):
                 row_begin = grp["r0"] + t * bm
                 row_end = min(row_begin + bm, grp["r0"] + grp["lr"])
-                bstart = grp["starts"][_branch_of(grp, row_begin)]
+                br = _branch_of(grp, row_begin)
+                bstart = grp["starts"][br]
                 b = _cdiv(row_end - bstart, bn)
-                tiles.append((g, t, a, b))
-        splits = replay_fwd_splits([a + b for (_, _, a, b) in tiles], hq, hkv, num_sms) if split_replay_fwd \
+                tiles.append((g, t, a, b, br))
+        splits = replay_fwd_splits([a + b for (_, _, a, b, _) in tiles], hq, hkv, num_sms) if split_replay_fwd \
             else [1] * len(tiles)
-        for (g, t, a, b), s in zip(tiles, splits):
+        for (g, t, a, b, br), s in zip(tiles, splits):
             cost = a + b
             c = _cdiv(cost, s)
             for k in range(s):
                 kc = cost if s == 1 else min(c, cost - k * c)
                 for h in range(hq):
                     items.append((REPLAY_Q, g, t, h, k, kc, a, b))
+                    row_branch_of_item[len(items) - 1] = br
     elif op in (OP_REPLAY_BWD, OP_TREE_BWD):
         # Unsplit costs first, to fix the split target.  The fused backward (all of the
         # backward in one call) uses the replay backward's split rule; split 0 of a
@@ -199,15 +205,20 @@ def build(offsets, hq: int, hkv: int, op: int, bm: int, bn: int, num_sms: int,
                     items.append((PREFILL_KV, g, j, h, 0, (nq - qa) * r, qa, nq))
     else:
         raise ValueError(op)
-    # Chunks of one stream: (group, KV head, branch or -1), largest chunk first; items
-    # within a chunk largest first, ties by (tile, kind, split, head).
+    # Chunks of one stream: (group, KV head, branch or -1), largest chunk first; within a
+    # chunk, sub-chunks by the branch of a replay forward item's first query row (-1 for
+    # every other item), largest first; items within a sub-chunk largest first, ties by
+    # (tile, kind, split, head).
     fwd = op in (OP_PREFILL_FWD, OP_REPLAY_FWD)
     chunk = [(it[1], it[3] // r if fwd else it[3], branch_of_item.get(i, -1)) for i, it in enumerate(items)]
-    total = {}
-    for c, it in zip(chunk, items):
+    sub = [c + (row_branch_of_item.get(i, -1),) for i, c in enumerate(chunk)]
+    total, sub_total = {}, {}
+    for c, sc, it in zip(chunk, sub, items):
         total[c] = total.get(c, 0) + it[5]
-    order = sorted(range(len(items)), key=lambda i: (-total[chunk[i]], chunk[i], -items[i][5], items[i][2],
-                                                     items[i][0], items[i][4], items[i][3]))
+        sub_total[sc] = sub_total.get(sc, 0) + it[5]
+    order = sorted(range(len(items)), key=lambda i: (-total[chunk[i]], chunk[i], -sub_total[sub[i]], sub[i][3],
+                                                     -items[i][5], items[i][2], items[i][0], items[i][4],
+                                                     items[i][3]))
     return np.array([items[i] for i in order], dtype=np.int32).reshape(-1, 8)
 
 

@@ -169,13 +169,17 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   // Key-side queues: the branch (index within the group) whose query tiles a response-key
   // item walks, -1 for prompt-key items (they walk the group's query tiles).
   std::vector<int32_t> walk_branch;
+  // Replay forward queue: the branch of the query tile's first row, whose keys the item's
+  // own-branch tiles are (-1 elsewhere).
+  std::vector<int32_t> row_branch;
   auto push = [&](int kind, int g, int64_t tile, int head, int split, int64_t cost, int64_t a, int64_t b,
-                  int branch = -1) {
+                  int branch = -1, int rbranch = -1) {
     Item it;
     it.w[0] = kind; it.w[1] = g; it.w[2] = (int32_t)tile; it.w[3] = head;
     it.w[4] = split; it.w[5] = (int32_t)cost; it.w[6] = (int32_t)a; it.w[7] = (int32_t)b;
     items.push_back(it);
     walk_branch.push_back(branch);
+    row_branch.push_back(rbranch);
   };
   const int ng = (int)groups.size();
   if (op == AUGTREE_OP_PREFILL_FWD) {
@@ -188,7 +192,7 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
       }
     }
   } else if (op == AUGTREE_OP_REPLAY_FWD) {
-    struct RT { int g; int64_t t, a, b; };
+    struct RT { int g; int64_t t, a, b; int br; };
     std::vector<RT> tiles;
     std::vector<int64_t> costs;
     for (int g = 0; g < ng; ++g) {
@@ -197,9 +201,10 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
       for (int64_t t = 0; t < cdiv(G.lr, bm); ++t) {
         int64_t row_begin = G.r0 + t * bm;
         int64_t row_end = std::min(row_begin + bm, G.r0 + G.lr);
-        int64_t bstart = G.starts[branch_of(G, row_begin)];
+        const int br = branch_of(G, row_begin);
+        int64_t bstart = G.starts[br];
         int64_t b = cdiv(row_end - bstart, bn);
-        tiles.push_back({g, t, a, b});
+        tiles.push_back({g, t, a, b, br});
         costs.push_back(a + b);
       }
     }
@@ -210,7 +215,7 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
       const int64_t cost = x.a + x.b, s = splits[i], c = cdiv(cost, s);
       for (int64_t k = 0; k < s; ++k) {
         const int64_t kc = s == 1 ? cost : std::min(c, cost - k * c);
-        for (int h = 0; h < hq; ++h) push(K_REPLAY_Q, x.g, x.t, h, (int)k, kc, x.a, x.b);
+        for (int h = 0; h < hq; ++h) push(K_REPLAY_Q, x.g, x.t, h, (int)k, kc, x.a, x.b, -1, x.br);
       }
     }
   } else if (op == AUGTREE_OP_REPLAY_BWD || op == AUGTREE_OP_TREE_BWD) {
@@ -277,44 +282,62 @@ augtree_status build_queue(const std::vector<int32_t>& po, const std::vector<int
   // group's KV head, a key-side item the query tiles of its group for its KV head or,
   // for response keys, of one branch.  Items of one stream form a chunk; chunks run
   // largest first (by total cost; ties by group, KV head, branch with -1 for a
-  // group-wide stream), and items within a chunk largest first (ties by tile, kind,
-  // split, head).  Blocks that run side by side then mostly share one stream, which L2
-  // holds once for all of them; the queues stay balanced (largest first within chunks).
+  // group-wide stream).  Within a chunk, replay forward items form sub-chunks by the
+  // branch of their query tile's first row (whose own-branch K/V they read), largest
+  // first (ties by branch); every other item is its chunk's only sub-chunk.  Items
+  // within a sub-chunk run largest first (ties by tile, kind, split, head).  Blocks that
+  // run side by side then mostly share one stream, which L2 holds once for all of them;
+  // the queues stay balanced (largest first within sub-chunks).
   const bool fwd = op == AUGTREE_OP_PREFILL_FWD || op == AUGTREE_OP_REPLAY_FWD;
-  struct Key {
-    int64_t chunk_cost;
-    int32_t g, h, br;
-    size_t idx;
-  };
+  using CKey = std::tuple<int32_t, int32_t, int32_t>;
+  using SKey = std::tuple<int32_t, int32_t, int32_t, int32_t>;
   auto chunk_of = [&](size_t i) {
-    return std::make_tuple(items[i].w[1], fwd ? items[i].w[3] / r : items[i].w[3], walk_branch[i]);
+    return CKey(items[i].w[1], fwd ? items[i].w[3] / r : items[i].w[3], walk_branch[i]);
   };
-  std::vector<std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>> totals;
-  {
-    std::vector<std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>> cs(items.size());
-    for (size_t i = 0; i < items.size(); ++i) cs[i] = {chunk_of(i), (int64_t)items[i].w[5]};
+  auto sub_of = [&](size_t i) {
+    const CKey c = chunk_of(i);
+    return SKey(std::get<0>(c), std::get<1>(c), std::get<2>(c), row_branch[i]);
+  };
+  // Total cost per key, looked up by binary search in a sorted table.
+  auto totals_of = [&](auto key_of) {
+    using K = decltype(key_of(size_t(0)));
+    std::vector<std::pair<K, int64_t>> cs(items.size()), tot;
+    for (size_t i = 0; i < items.size(); ++i) cs[i] = {key_of(i), (int64_t)items[i].w[5]};
     std::sort(cs.begin(), cs.end());
     for (size_t i = 0; i < cs.size();) {
       size_t k = i;
-      int64_t tot = 0;
-      while (k < cs.size() && cs[k].first == cs[i].first) tot += cs[k++].second;
-      totals.push_back({cs[i].first, tot});
+      int64_t t = 0;
+      while (k < cs.size() && cs[k].first == cs[i].first) t += cs[k++].second;
+      tot.push_back({cs[i].first, t});
       i = k;
     }
-  }
+    return tot;
+  };
+  const auto chunk_tot = totals_of(chunk_of);
+  const auto sub_tot = totals_of(sub_of);
+  auto lookup = [](const auto& tab, const auto& key) {
+    auto pos = std::lower_bound(tab.begin(), tab.end(), key,
+                                [](const auto& e, const auto& v) { return e.first < v; });
+    return pos->second;
+  };
+  struct Key {
+    int64_t chunk_cost, sub_cost;
+    int32_t g, h, br, sb;
+    size_t idx;
+  };
   std::vector<Key> keys(items.size());
   for (size_t i = 0; i < items.size(); ++i) {
-    const auto c = chunk_of(i);
-    auto pos = std::lower_bound(totals.begin(), totals.end(), c,
-                                [](const std::pair<std::tuple<int32_t, int32_t, int32_t>, int64_t>& e,
-                                   const std::tuple<int32_t, int32_t, int32_t>& v) { return e.first < v; });
-    keys[i] = Key{pos->second, std::get<0>(c), std::get<1>(c), std::get<2>(c), i};
+    const CKey c = chunk_of(i);
+    keys[i] = Key{lookup(chunk_tot, c), lookup(sub_tot, sub_of(i)), std::get<0>(c), std::get<1>(c), std::get<2>(c),
+                  row_branch[i], i};
   }
   std::sort(keys.begin(), keys.end(), [&](const Key& x, const Key& y) {
     if (x.chunk_cost != y.chunk_cost) return x.chunk_cost > y.chunk_cost;
     if (x.g != y.g) return x.g < y.g;
     if (x.h != y.h) return x.h < y.h;
     if (x.br != y.br) return x.br < y.br;
+    if (x.sub_cost != y.sub_cost) return x.sub_cost > y.sub_cost;
+    if (x.sb != y.sb) return x.sb < y.sb;
     const Item& a = items[x.idx];
     const Item& b = items[y.idx];
     if (a.w[5] != b.w[5]) return a.w[5] > b.w[5];

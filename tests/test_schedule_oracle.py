@@ -54,22 +54,41 @@ def key_side_stream(tree, bn, it, r=1):
     raise AssertionError("tile outside its group's branches")
 
 
-def check_key_side_order(q, tree, bn, r=1):
+def first_row_branch(tree, bm, it):
+    """Replay forward item: the branch (index within its group) of its query tile's
+    first row; -1 for every other item."""
+    if int(it[0]) != S.REPLAY_Q:
+        return -1
+    g, row = int(it[1]), int(it[2]) * bm
+    pos = 0
+    for i, li in enumerate(tree.branch_lens[g]):
+        if pos <= row < pos + li:
+            return i
+        pos += li
+    raise AssertionError("query tile outside its group's branches")
+
+
+def check_key_side_order(q, tree, bn, r=1, bm=None):
     """Every queue: the items of one stream are contiguous; streams come in order of
-    decreasing total cost (ties by group, KV head, branch); within a stream items come
-    largest first (ties by tile, kind, split, head)."""
+    decreasing total cost (ties by group, KV head, branch); within a stream, the replay
+    forward items of one first-row branch are contiguous, those sub-streams come by
+    decreasing total cost (ties by branch), and items within a sub-stream come largest
+    first (ties by tile, kind, split, head)."""
     streams = [key_side_stream(tree, bn, it, r) for it in q]
-    total = {}
-    for s_, it in zip(streams, q):
+    subs = [s_ + (first_row_branch(tree, bm if bm is not None else bn, it),) for s_, it in zip(streams, q)]
+    total, sub_total = {}, {}
+    for s_, sb, it in zip(streams, subs, q):
         total[s_] = total.get(s_, 0) + int(it[5])
-    seen, prev = set(), None
-    for s_ in streams:
-        if s_ != prev:
-            assert s_ not in seen, "a stream's items are split apart"
-            seen.add(s_)
-            prev = s_
-    keys = [(-total[s_], s_, -int(it[5]), int(it[2]), int(it[0]), int(it[4]), int(it[3]))
-            for s_, it in zip(streams, q)]
+        sub_total[sb] = sub_total.get(sb, 0) + int(it[5])
+    for seq in (streams, subs):
+        seen, prev = set(), None
+        for s_ in seq:
+            if s_ != prev:
+                assert s_ not in seen, "a stream's items are split apart"
+                seen.add(s_)
+                prev = s_
+    keys = [(-total[s_], s_, -sub_total[sb], sb[3], -int(it[5]), int(it[2]), int(it[0]), int(it[4]), int(it[3]))
+            for s_, sb, it in zip(streams, subs, q)]
     assert keys == sorted(keys)
 
 
@@ -98,7 +117,7 @@ def test_forward_queues_cover_valid_pairs_once(ti, bm, bn, hq, hkv, split):
     sms = 1000 if split else 3
     for op, kind, side in ((S.OP_PREFILL_FWD, S.PREFILL_Q, "pp"), (S.OP_REPLAY_FWD, S.REPLAY_Q, None)):
         q = S.build(offs, hq, hkv, op, bm, bn, num_sms=sms, split_replay_fwd=split)
-        check_key_side_order(q, tree, bn, hq // hkv)
+        check_key_side_order(q, tree, bn, hq // hkv, bm)
         chunk, nsplit = {}, {}
         for it in q:
             k, g, tile, h, sp, cost, a, b = map(int, it)
@@ -284,7 +303,7 @@ def test_lpt_order_meets_the_list_scheduling_bound():
     for op in (S.OP_PREFILL_FWD, S.OP_REPLAY_FWD, S.OP_REPLAY_BWD, S.OP_PREFILL_BWD, S.OP_TREE_BWD):
         q = S.build(offs, 4, 2, op, 16, 16, num_sms=4)
         costs = [int(c) for c in q[:, 5]]
-        check_key_side_order(q, tree, 16, 2)
+        check_key_side_order(q, tree, 16, 2, 16)
         m = 8
         lanes = [0] * m
         for c in costs:
