@@ -1,10 +1,11 @@
 // Row geometry of the query-side tensor-core kernels (the forward and the backward's
-// query side): where a query row's keys lie in each KV tile of its walk.
+// query side): where a query row's keys lie in each KV tile of its walk.  Also the
+// persistent forward's decoded work items and the source its blocks take them from.
 //
 // AugTree paper, Sec. 3.2 Eq. 1 (the row's valid keys: the whole prompt of its group,
-// then its own branch up to itself; causal over the prompt for prefill rows) and Sec. 3.3
+// then its own branch up to itself; causal over the prompt for prefill rows), Sec. 3.3
 // (the prompt-part and own-part states merge associatively; one running state crosses
-// both parts).
+// both parts) and Sec. 3.4 (replay units taken by lanes: here persistent blocks).
 #pragma once
 
 #include "common.cuh"
