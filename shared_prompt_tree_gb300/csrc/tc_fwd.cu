@@ -71,6 +71,12 @@ static_assert(kFwdFmaPairs >= 1 && 32 % kFwdFmaPairs == 0, "FMA exponential spac
 #define AUGTREE_FWD_VBAR 1
 #endif
 constexpr bool kFwdVBar = AUGTREE_FWD_VBAR != 0;
+// 1: the epilogue writes each thread's row in 32-byte stores (whole sectors) where the
+// destination is 32-byte aligned; 0: 16-byte stores.
+#ifndef AUGTREE_FWD_V8_STORE
+#define AUGTREE_FWD_V8_STORE 1
+#endif
+constexpr bool kFwdV8Store = AUGTREE_FWD_V8_STORE != 0;
 constexpr int FWD_NST = 3;                     // K/V ring stages
 constexpr int FWD_TILE = 128 * 128;            // 128 rows x 64 bf16 columns = 16 KB
 constexpr int FWD_Q_OFF = 0;                   // 2 blocks
@@ -189,28 +195,13 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
         tma_prefetch_3d(&tm_q, 64, cur.h, cur.row0);
       }
       while (!cur.stop) {
-        // Take the next item now and publish it, so that every warp can prepare it.
-        taken = src.next();
-        const QuerySlot nxt = taken < n_items ? decode_query_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
-        const int u = n + 1, sn = u % FWDP_SLOTS;
-        if (u >= FWDP_SLOTS && !(ok = mbar_wait(&bars->item_empty[sn], ((u / FWDP_SLOTS) - 1) & 1, err))) break;
-        slots[sn] = nxt;
-        mbar_arrive(&bars->item_full[sn]);
-        if (!nxt.stop) {
-          tma_prefetch_3d(&tm_q, 0, nxt.h, nxt.row0);
-          tma_prefetch_3d(&tm_q, 64, nxt.h, nxt.row0);
-        }
-        // The current item's query tile, once the previous item's S products have read Q.
-        if (n >= 1 && !(ok = mbar_wait(&bars->q_empty, (n - 1) & 1, err))) break;
-        mbar_expect_tx(&bars->q_full, 2 * FWD_TILE);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(smem + FWD_Q_OFF + kb * FWD_TILE, &tm_q, &bars->q_full, kb * 64, cur.h, cur.row0);
-        ++n_q;
         const int kvh = cur.h / r;
-        for (int j = 0; j < cur.n_tiles; ++j) {
+        // K/V tile j of the current item into the next ring stage, once the PV products
+        // of the tile that held that stage are done.
+        auto load_kv = [&](int j) {
           const int stage = (int)(jg % FWD_NST);
           const uint32_t use = (uint32_t)(jg / FWD_NST);
-          if (!(ok = mbar_wait(&bars->kv_empty[stage], (use & 1) ^ 1, err))) break;
+          if (!mbar_wait(&bars->kv_empty[stage], (use & 1) ^ 1, err)) return false;
           mbar_expect_tx(&bars->kv_full[stage], (kFwdVBar ? 2 : 4) * FWD_TILE);
           if (kFwdVBar) mbar_expect_tx(&bars->v_full[stage], 2 * FWD_TILE);
           const int jt = cur.j0 + j;  // tile of the rows' walk
@@ -224,7 +215,42 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
           for (int kb = 0; kb < 2; ++kb)
             tma_load_3d(smem + FWD_V_OFF + (stage * 2 + kb) * FWD_TILE, vm, vbar, kb * 64, kvh, krow);
           ++jg;
+          return true;
+        };
+        // The item's first K/V tile goes ahead of its query tile: it needs only a free ring
+        // stage, while Q waits for the previous item's last S product, so both have landed
+        // when that wait ends and Q arrives.
+        int j = 0;
+        if (cur.n_tiles > 0) {
+          if (!(ok = load_kv(0))) break;
+          j = 1;
         }
+        // The current item's query tile, once the previous item's S products have read Q.
+        if (n >= 1 && !(ok = mbar_wait(&bars->q_empty, (n - 1) & 1, err))) break;
+        mbar_expect_tx(&bars->q_full, 2 * FWD_TILE);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_3d(smem + FWD_Q_OFF + kb * FWD_TILE, &tm_q, &bars->q_full, kb * 64, cur.h, cur.row0);
+        ++n_q;
+        if (j < cur.n_tiles) {
+          if (!(ok = load_kv(j))) break;
+          ++j;
+        }
+        // Take the next item and publish it, so that every warp can prepare it, here,
+        // with the first two K/V tiles and Q of the current item issued: taking and
+        // decoding it is a chain of dependent loads, kept out of the way from the previous
+        // item's last S product to this item's query tile.
+        taken = src.next();
+        const QuerySlot nxt = taken < n_items ? decode_query_item<kSplit>(queue, (int)taken, geo, bm, bn, err) : stop_slot;
+        const int u = n + 1, sn = u % FWDP_SLOTS;
+        if (u >= FWDP_SLOTS && !(ok = mbar_wait(&bars->item_empty[sn], ((u / FWDP_SLOTS) - 1) & 1, err))) break;
+        slots[sn] = nxt;
+        mbar_arrive(&bars->item_full[sn]);
+        if (!nxt.stop) {
+          tma_prefetch_3d(&tm_q, 0, nxt.h, nxt.row0);
+          tma_prefetch_3d(&tm_q, 64, nxt.h, nxt.row0);
+        }
+        for (; j < cur.n_tiles; ++j)
+          if (!(ok = load_kv(j))) break;
         if (!ok) break;
         ++n;
         cur = nxt;
@@ -330,6 +356,10 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
     const int q4 = warp & 3;
     const int r_local = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    // Rows start on 256-byte boundaries of the output (bf16) and 512-byte boundaries of
+    // the partial states (fp32), so 32-byte stores need only aligned base pointers.
+    const bool v8_out = kFwdV8Store && ((reinterpret_cast<uintptr_t>(out) & 31) == 0);
+    const bool v8_part = kFwdV8Store && ((reinterpret_cast<uintptr_t>(part_o) & 31) == 0);
     bool ok = true;
     int jg = 0;
     for (int n = 0; ok; ++n) {
@@ -355,6 +385,10 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
       const bool any = L > 0.f && cur.n_tiles > 0;  // a row with no key writes zeros
       const float inv = any ? 1.f / L : 0.f;
       const float s0 = a0 * inv, s1 = a1 * inv;
+      // O_0 and O_1 hold the item's products whenever it walked a tile (finite: weights
+      // in [0, 1] times finite values), so a row without a key gets 0 * O = 0 from its
+      // zero factors; an item without tiles never wrote O and writes zeros.
+      const bool live = cur.n_tiles > 0;
       const float lse_v = any ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       const int row = cur.row0 + r_local;
       const bool row_ok = row < cur.row_end;
@@ -368,14 +402,23 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
           tmem_ld32(tmem + lane_off + 384 + 32 * c, o1);
           tmem_ld_wait();
           if (row_ok) {
-            float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
+            uint32_t v[32];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float v[4];
+            for (int i = 0; i < 16; ++i) {
+              if (live)
+                f32x2_scale_add(o0[2 * i], o0[2 * i + 1], o1[2 * i], o1[2 * i + 1], s0, s1, v[2 * i], v[2 * i + 1]);
+              else
+                v[2 * i] = v[2 * i + 1] = 0u;
+            }
+            if (v8_part) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                v[e] = any ? __uint_as_float(o0[4 * i + e]) * s0 + __uint_as_float(o1[4 * i + e]) * s1 : 0.f;
-              d4[i] = make_float4(v[0], v[1], v[2], v[3]);
+              for (int i = 0; i < 4; ++i) st_global_v8(prow + 32 * c + 8 * i, v + 8 * i);
+            } else {
+              float4* d4 = reinterpret_cast<float4*>(prow + 32 * c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
             }
           }
         }
@@ -392,13 +435,18 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float v0 = any ? __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1 : 0.f;
-              const float v1 = any ? __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1 : 0.f;
-              pk[i] = pack_bf16x2(v0, v1);
+              uint32_t v0 = 0u, v1 = 0u;
+              if (live) f32x2_scale_add(o0[2 * i], o0[2 * i + 1], o1[2 * i], o1[2 * i + 1], s0, s1, v0, v1);
+              pk[i] = pack_bf16x2(__uint_as_float(v0), __uint_as_float(v1));
             }
-            uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
+            if (v8_out) {
+              st_global_v8(orow + 32 * c, pk);
+              st_global_v8(orow + 32 * c + 16, pk + 8);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
         }
         if (row_ok) lse[(int64_t)cur.h * lse_rows + row] = lse_v;

@@ -86,3 +86,36 @@ def test_tc_forward_many_items_per_block(cuda_device):
             assert torch.equal(r[k], runs[0][k]), k
     got = {k: v.double().cpu().numpy() for k, v in runs[0].items()}
     compare(got, run_oracle_fwd(w), "bf16", keys=("o_p", "o_r", "lse_p", "lse_r"))
+
+
+def test_tc_forward_output_alignment(cuda_device):
+    """The forward writes each output row in 32-byte stores when the output's base is
+    32-byte aligned and in 16-byte stores otherwise: an output that starts 16 bytes into
+    an allocation gets the same bits as an aligned one (split-KV replay included, whose
+    partial states go to a workspace at a 16-byte offset as well)."""
+    import torch
+    for tree, hq, hkv in ((TREES[4], 8, 2), (W.Tree([4096], [[2, 3, 1]]), 4, 2)):
+        w = W.custom(tree, hq=hq, hkv=hkv, d=128, dtype="bf16", seed=71)
+        plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=at.BF16, kernel=at.KERNEL_TC)
+        t = {n: W.tensor_torch(w, n, cuda_device) for n in ("q_p", "k_p", "v_p", "q_r", "k_r", "v_r")}
+        nb = plan.workspace_bytes(at.OP_REPLAY_FWD)
+        outs = []
+        for off in (0, 16):
+            def shifted(like):
+                raw = torch.empty(like.numel() * like.element_size() + 64, dtype=torch.uint8, device=cuda_device)
+                assert raw.data_ptr() % 32 == 0
+                return raw[off:off + like.numel() * like.element_size()].view(like.dtype).view(like.shape)
+            o_p, o_r = shifted(t["q_p"]), shifted(t["q_r"])
+            lse_p = torch.empty(w.hq, w.tree.total_prompt, dtype=torch.float32, device=cuda_device)
+            lse_r = torch.empty(w.hq, w.tree.total_resp, dtype=torch.float32, device=cuda_device)
+            ws = None
+            if nb:
+                raw = torch.empty(nb + 64, dtype=torch.uint8, device=cuda_device)
+                ws = raw[off:off + nb]
+            at.augtree_prefill_fwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p)
+            at.augtree_replay_fwd(plan, t["q_r"], t["k_p"], t["v_p"], t["k_r"], t["v_r"], o_r, lse_r, ws)
+            torch.cuda.synchronize()
+            plan.check()
+            outs.append([x.clone() for x in (o_p, o_r, lse_p, lse_r)])
+        for a, b in zip(*outs):
+            assert torch.equal(a, b)
