@@ -401,6 +401,11 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
           tmem_ld32(tmem + lane_off + 256 + 32 * c, o0);
           tmem_ld32(tmem + lane_off + 384 + 32 * c, o1);
           tmem_ld_wait();
+          if (c == 3) {
+            // O is read out: the next item's first PV products may overwrite it.
+            tc_fence_before();
+            mbar_arrive(&bars->o_free);
+          }
           if (row_ok) {
             uint32_t v[32];
 #pragma unroll
@@ -431,6 +436,11 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
           tmem_ld32(tmem + lane_off + 256 + 32 * c, o0);
           tmem_ld32(tmem + lane_off + 384 + 32 * c, o1);
           tmem_ld_wait();
+          if (c == 3) {
+            // O is read out: the next item's first PV products may overwrite it.
+            tc_fence_before();
+            mbar_arrive(&bars->o_free);
+          }
           if (row_ok) {
             uint32_t pk[16];
 #pragma unroll
@@ -451,9 +461,6 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
         }
         if (row_ok) lse[(int64_t)cur.h * lse_rows + row] = lse_v;
       }
-      // The next item's first PV products may overwrite O_0 and O_1.
-      tc_fence_before();
-      mbar_arrive(&bars->o_free);
     }
   } else {
     // ------------------------------------------------------------ softmax (half tiles)
