@@ -85,6 +85,27 @@ constexpr int FWD_V_OFF = FWD_K_OFF + FWD_NST * 2 * FWD_TILE;   // [NST][2 block
 constexpr int FWD_BAR_OFF = FWD_V_OFF + FWD_NST * 2 * FWD_TILE;
 
 // ---------------------------------------------------------------- kernel
+// a0 * s0 + a1 * s1 on a pair of fp32 values (word pairs x0, x1 of two accumulators),
+// in the packed two-lane fp32 arithmetic of sm_100 and later: one multiply and one fused
+// multiply-add for both lanes, each lane rounded as the scalar operations would be.
+__device__ __forceinline__ void f32x2_scale_add(uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi, float s0,
+                                                float s1, uint32_t& r_lo, uint32_t& r_hi) {
+  asm("{\n .reg .b64 a, b, s, t, r;\n"
+      " mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mov.b64 s, {%6, %6};\n mov.b64 t, {%7, %7};\n"
+      " mul.rn.f32x2 r, a, s;\n fma.rn.f32x2 r, b, t, r;\n"
+      " mov.b64 {%0, %1}, r;\n}"
+      : "=r"(r_lo), "=r"(r_hi)
+      : "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "f"(s0), "f"(s1));
+}
+
+// One 32-byte store of eight words (sm_100 and later); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* r) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]),
+               "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 constexpr int FWDP_SLOTS = 4;  // ring of decoded items
 constexpr int FWDP_THREADS = 480;
 constexpr int FWDP_BAR_BYTES = 288;
