@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "tc_common.cuh"
 #include "tc_rows.cuh"
+#include "tc_store.cuh"
 
 namespace augtree {
 namespace {
@@ -140,7 +141,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     }
   }
 
-  if (threadIdx.x == 0) {
+  // The barriers are set up by the producer thread under the queue schedule, which then
+  // starts the item's Q and dO copies at once, ahead of the block-wide barrier (measured:
+  // the block's set-up takes about 0.7 us and its first copies about 1.4 us); under the
+  // persistent schedule by thread 0, for each unit.
+  if (threadIdx.x == (kPersistent ? 0 : 256)) {
     if (kPersistent && u_i > 0) {
       // Every wait, copy and MMA of the previous unit has ended (drains, then the
       // block-wide barrier at its end): its barriers are idle and may be reused.
@@ -165,6 +170,26 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     fence_mbar_init();
+    if (!kPersistent) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+      mbar_expect_tx(&bars->q_full, 4 * BLK);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_3d(smem + DQ_Q_OFF + kb * BLK, &tm_q, &bars->q_full, kb * 64, h, (int)row0);
+        tma_load_3d(smem + DQ_DO_OFF + kb * BLK, &tm_do, &bars->q_full, kb * 64, h, (int)row0);
+      }
+      // The first K/V tile into stage 0 of both rings (free: the barriers are fresh).
+      if (n_tiles > 0) {
+        const bool own = j0 >= n_a;
+        const int krow = own ? (int)(own0 + (int64_t)(j0 - n_a) * bn) : (int)(G.p0 + (int64_t)j0 * bn);
+        mbar_expect_tx(&bars->k_full[0], 2 * BLK);
+        mbar_expect_tx(&bars->v_full[0], 2 * BLK);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_3d(smem + DQ_K_OFF + kb * BLK, own ? &tm_kr : &tm_kp, &bars->k_full[0], kb * 64, kvh, krow);
+          tma_load_3d(smem + DQ_V_OFF + kb * BLK, own ? &tm_vr : &tm_vp, &bars->v_full[0], kb * 64, kvh, krow);
+        }
+      }
+    }
   }
   if (!kPersistent && warp == 9) tmem_alloc(&bars->tmem_base, 512);
   if (warp == 8 && lane == 0) {
@@ -182,18 +207,31 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_expect_tx(&bars->q_full, 4 * BLK);
-      for (int kb = 0; kb < 2; ++kb) {
-        tma_load_3d(smem + DQ_Q_OFF + kb * BLK, &tm_q, &bars->q_full, kb * 64, h, (int)row0);
-        tma_load_3d(smem + DQ_DO_OFF + kb * BLK, &tm_do, &bars->q_full, kb * 64, h, (int)row0);
+      if (kPersistent) {
+        mbar_expect_tx(&bars->q_full, 4 * BLK);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_3d(smem + DQ_Q_OFF + kb * BLK, &tm_q, &bars->q_full, kb * 64, h, (int)row0);
+          tma_load_3d(smem + DQ_DO_OFF + kb * BLK, &tm_do, &bars->q_full, kb * 64, h, (int)row0);
+        }
       }
       // First key row of the item's j-th KV tile (tile j0 + j of the row's walk).
       auto krow_of = [&](int j) {
         const int jt = j0 + j;
         return jt >= n_a ? (int)(own0 + (int64_t)(jt - n_a) * bn) : (int)(G.p0 + (int64_t)jt * bn);
       };
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
+      // Queue schedule: tile 0 went out with Q and dO before the block-wide barrier.
+      const int first = (!kPersistent && n_tiles > 0) ? 1 : 0;
+      int k_issued = first, v_issued = first;
+      if (first && kPrefetchTiles < n_tiles) {
+        const CUtensorMap* kmp = j0 + kPrefetchTiles >= n_a ? &tm_kr : &tm_kp;
+        const CUtensorMap* vmp = j0 + kPrefetchTiles >= n_a ? &tm_vr : &tm_vp;
+        const int rp = krow_of(kPrefetchTiles);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_prefetch_3d(kmp, kb * 64, kvh, rp);
+          tma_prefetch_3d(vmp, kb * 64, kvh, rp);
+        }
+      }
+      for (int j = first; j < n_tiles; ++j) {
         const bool own = j0 + j >= n_a;
         const int krow = krow_of(j);
         const CUtensorMap* km = own ? &tm_kr : &tm_kp;
@@ -409,6 +447,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
     // dQ rows: warpgroup w writes dims [64w, 64w + 64) of its rows.
     if (ok && mbar_wait_warp_all(&bars->acc_done, 0, err)) {
       tc_fence_after();
+      // Rows start on 256-byte boundaries of dQ (bf16) and 512-byte boundaries of the
+      // partials (fp32): 32-byte stores where the base pointers allow them.
+      const bool v8_out = (reinterpret_cast<uintptr_t>(dq_out) & 31) == 0;
+      const bool v8_part = (reinterpret_cast<uintptr_t>(dq_part) & 31) == 0;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t v[32];
@@ -417,11 +459,19 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
         if (kSplit && slot >= 0) {
           // Split-KV item: the fp32 partial (times the scale) of its chunk.
           if (g.row_ok) {
-            float4* d4 = reinterpret_cast<float4*>(dq_part + (slot * kFwdPartRows + r_local) * 128 + c0 + half * 32);
+            float* prow = dq_part + (slot * kFwdPartRows + r_local) * 128 + c0 + half * 32;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(v[4 * i]) * geo.scale, __uint_as_float(v[4 * i + 1]) * geo.scale,
-                                  __uint_as_float(v[4 * i + 2]) * geo.scale, __uint_as_float(v[4 * i + 3]) * geo.scale);
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * geo.scale);
+            if (v8_part) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) st_global_v8(prow + 8 * i, v + 8 * i);
+            } else {
+              float4* d4 = reinterpret_cast<float4*>(prow);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            }
           }
         } else if (g.row_ok) {
           const bool any = n_tiles > 0;
@@ -430,9 +480,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1) tc_bwd_dq_kernel(
           for (int i = 0; i < 16; ++i)
             o[i] = any ? pack_bf16x2(__uint_as_float(v[2 * i]) * geo.scale, __uint_as_float(v[2 * i + 1]) * geo.scale)
                        : 0u;
-          uint4* d4 = reinterpret_cast<uint4*>(dq_out + (g.row * geo.hq + h) * 128 + c0 + half * 32);
+          __nv_bfloat16* orow = dq_out + (g.row * geo.hq + h) * 128 + c0 + half * 32;
+          if (v8_out) {
+            st_global_v8(orow, o);
+            st_global_v8(orow + 16, o + 8);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          }
         }
       }
     }

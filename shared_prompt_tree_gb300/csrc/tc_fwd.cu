@@ -45,6 +45,7 @@
 #include "common.cuh"
 #include "tc_common.cuh"
 #include "tc_rows.cuh"
+#include "tc_store.cuh"
 
 namespace augtree {
 namespace {
@@ -99,12 +100,6 @@ __device__ __forceinline__ void f32x2_scale_add(uint32_t a_lo, uint32_t a_hi, ui
       : "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "f"(s0), "f"(s1));
 }
 
-// One 32-byte store of eight words (sm_100 and later); p must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* r) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]),
-               "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
 
 constexpr int FWDP_SLOTS = 4;  // ring of decoded items
 constexpr int FWDP_THREADS = 480;

@@ -81,3 +81,33 @@ def test_fused_backward_rejects_small_workspace(cuda_device):
         at.augtree_tree_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], t["q_r"], t["k_r"], t["v_r"],
                             o_r, lse_r, t["do_r"], *outs, ws)
     assert e.value.status == at.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_tree_bwd_output_alignment(cuda_device):
+    """The query side writes dQ rows (and split-KV fp32 partials) in 32-byte stores when
+    the base pointers are 32-byte aligned and in 16-byte stores otherwise: gradients
+    and workspace at a 16-byte offset give the same bits as aligned ones (a tree whose
+    replay queue splits, so the partial path runs too)."""
+    import torch
+    w = W.custom(W.Tree([4096, 300], [[2, 3, 1], [200, 9]]), hq=4, hkv=2, d=128, dtype="bf16", seed=83)
+    plan = at.Plan.from_tree(w.tree, w.hq, w.hkv, w.d, dtype=at.BF16, kernel=at.KERNEL_TC)
+    assert int(plan.schedule(at.OP_REPLAY_FWD)[:, 4].max()) > 0
+    t = {n: W.tensor_torch(w, n, cuda_device) for n in W.TENSORS}
+    o_p, lse_p, o_r, lse_r = at.forward(plan, t["q_p"], t["k_p"], t["v_p"], t["q_r"], t["k_r"], t["v_r"])
+    nb = max(1, plan.workspace_bytes(at.OP_TREE_BWD))
+    outs = []
+    for off in (0, 16):
+        def shifted(like):
+            raw = torch.empty(like.numel() * like.element_size() + 64, dtype=torch.uint8, device=cuda_device)
+            assert raw.data_ptr() % 32 == 0
+            return raw[off:off + like.numel() * like.element_size()].view(like.dtype).view(like.shape)
+        g = [shifted(t[n]) for n in ("q_p", "k_p", "v_p", "q_r", "k_r", "v_r")]
+        raw = torch.empty(nb + 64, dtype=torch.uint8, device=cuda_device)
+        ws = raw[off:off + nb]
+        at.augtree_tree_bwd(plan, t["q_p"], t["k_p"], t["v_p"], o_p, lse_p, t["do_p"], t["q_r"], t["k_r"], t["v_r"],
+                            o_r, lse_r, t["do_r"], *g, ws)
+        torch.cuda.synchronize()
+        plan.check()
+        outs.append([x.clone() for x in g])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
