@@ -16,12 +16,14 @@
 // the plan's device memory (the largest-first, stream-ordered order of the queue, as
 // the hardware would hand out one block per item), or from its lane of AssignGrid's
 // placement (persistent schedule).  Consecutive items of a block overlap: the next
-// item's query tile is warmed in L2 as soon as it is taken and loaded once the current
-// item's last S product has read Q, its first score tiles are computed while the
-// softmax warps finish the current item, and a separate warpgroup writes the output.
+// item is taken once the current one's query tile and first two K/V tiles are in
+// flight, its query tile is warmed in L2 then and loaded once the current item's last S
+// product has read Q (its first K/V tile goes out before that wait), its first score
+// tiles are computed while the softmax warps finish the current item, and a separate
+// warpgroup writes the output.
 // Barrier phases, the K/V ring and the score buffers run on across items (counters of
 // the block's items and K/V tiles); nothing is re-initialised between items.
-//   warp 8       TMA producer: takes and decodes the items (a ring of 4), loads Q, then a
+//   warp 8       TMA producer: takes and decodes the items (a ring of 4), loads Q and a
 //                3-stage ring of K/V tiles (128 keys x 128 dims)
 //   warp 9       TMEM allocator and issuer of S(j) = Q K^T into buffer j % 2
 //   warp 10      issuer of O_w += P_w(j) V_w(j), w = 0, 1 (V_w: the tile's keys
@@ -597,7 +599,8 @@ __global__ void __launch_bounds__(FWDP_THREADS, 1) tc_fwd_kernel(
       if (ok && n >= 1) ok = mbar_wait_warp_all(&bars->ml_free, (n - 1) & 1, err);
       if (ok) xch[w * 128 + r_local] = make_float2(m, l);
       mbar_arrive(&bars->ml_ready);  // also after a failed wait, so that the epilogue's wait ends
-      // The next item, published an item ahead: its row's branch start is fetched now.
+      // The next item, published while this one's tiles were loaded: its row's branch
+      // start is fetched now.
       QuerySlot nxt{};
       nxt.stop = 1;
       if (ok) {
